@@ -1,0 +1,401 @@
+"""Pins for the oracle: checks against things other than the oracle itself.
+
+Each pin is a plain function that raises AssertionError on failure.  The test
+modules call every pin against the oracle build (``test_oracle_pins.py``) and
+against builds with a planted mistake (``test_oracle_mutants.py``), where at
+least one pin must fail.
+
+What pins what:
+  * number formats: hand-worked golden points (tests/golden), torch's own
+    float8_e4m3fn / bfloat16 casts, exhaustive code round trips and the
+    ties-to-even midpoints of every adjacent code pair;
+  * RMSNorm: torch.nn.functional.rms_norm in float64, exact invariance under
+    power-of-two scaling, unit RMS with unit weight;
+  * RoPE: identity at position 0, pair norms preserved, the relative-position
+    property of q.k, and the textbook complex-rotation form in float64;
+  * placement: hand-worked golden points and brute force (search, no division)
+    over tiny pools;
+  * the whole producer: Q / index-Q / K / index-K against a float64 textbook
+    composition, V against torch's fp8 cast, and the exact set of written bytes
+    (sentinels, page padding and guard bands unchanged).
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import torch
+
+import oracle
+from paged_kv_cache_msa_gb300 import workloads as wl
+from harness import (bf16_bits_to_f32, cache_cells, e4m3_ulp_distance, run_oracle)
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _read_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            rows.append(line.split())
+    return rows
+
+
+def _torch_e4m3(x: np.ndarray) -> np.ndarray:
+    """torch's float8_e4m3fn cast (round to nearest even) after clamping to the
+    largest finite magnitude, i.e. saturating."""
+    t = torch.from_numpy(np.asarray(x, dtype=np.float32)).clamp(-448.0, 448.0)
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _torch_bf16(x: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.asarray(x, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# number formats
+# ---------------------------------------------------------------------------
+
+def pin_e4m3_golden():
+    for v, code, *_ in _read_golden("e4m3_points.txt"):
+        got = oracle.e4m3_encode(float(v))
+        assert got == int(code, 16), f"e4m3({v}) = {got:#04x}, expected {code}"
+
+
+def pin_e4m3_decode_vs_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    got = np.array([oracle.e4m3_decode(int(c)) for c in codes], dtype=np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def pin_e4m3_roundtrip_and_ties():
+    finite = [c for c in range(256) if (c & 0x7F) != 0x7F]
+    for c in finite:
+        v = oracle.e4m3_decode(c)
+        assert oracle.e4m3_encode(v) == c, f"round trip of {c:#04x}"
+    # every adjacent pair of positive finite codes: the midpoint goes to the even
+    # code; one float step either side of it goes to the nearer code
+    for c in range(0, 0x7E):
+        lo, hi = oracle.e4m3_decode(c), oracle.e4m3_decode(c + 1)
+        mid = np.float32((np.float64(lo) + np.float64(hi)) / 2)
+        assert float(mid) == (lo + hi) / 2
+        even = c if c % 2 == 0 else c + 1
+        assert oracle.e4m3_encode(float(mid)) == even, f"tie between {c:#04x} and {c + 1:#04x}"
+        assert oracle.e4m3_encode(float(np.nextafter(mid, np.float32(-1)))) == c
+        assert oracle.e4m3_encode(float(np.nextafter(mid, np.float32(1e9)))) == c + 1
+        assert oracle.e4m3_encode(-float(mid)) == 0x80 | even
+
+
+def pin_e4m3_saturation():
+    for v in (448.0, 448.5, 463.99, 464.0, 465.0, 480.0, 1e4, 3e38, math.inf):
+        assert oracle.e4m3_encode(v) == 0x7E, v
+        assert oracle.e4m3_encode(-v) == 0xFE, -v
+    assert oracle.e4m3_encode(math.nan) & 0x7F == 0x7F
+
+
+def pin_e4m3_vs_torch_random():
+    rng = np.random.default_rng(7)
+    x = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32) * 30,
+        (rng.standard_normal(20000) * 1e-2).astype(np.float32),
+        rng.uniform(-448, 448, 20000).astype(np.float32),
+        rng.uniform(-2000, 2000, 5000).astype(np.float32),
+    ])
+    ref = _torch_e4m3(x)
+    got = np.array([oracle.e4m3_encode(float(v)) for v in x], dtype=np.uint8)
+    assert np.array_equal(got, ref), np.argwhere(got != ref)[:5]
+
+
+def pin_bf16_golden():
+    for v, code, *_ in _read_golden("bf16_points.txt"):
+        got = oracle.bf16_encode(float(v))
+        assert got == int(code, 16), f"bf16({v}) = {got:#06x}, expected {code}"
+
+
+def pin_bf16_vs_torch():
+    rng = np.random.default_rng(11)
+    bits = rng.integers(0, 2**32, size=60000, dtype=np.uint64).astype(np.uint32)
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x)]
+    # exact ties: low 16 bits 0x8000
+    ties = ((rng.integers(0, 2**16, 4000, dtype=np.uint32) << 16) | 0x8000).view(np.float32)
+    x = np.concatenate([x, ties[np.isfinite(ties)]])
+    ref = _torch_bf16(x)
+    got = np.array([oracle.bf16_encode(float(v)) for v in x], dtype=np.uint16)
+    assert np.array_equal(got, ref), np.argwhere(got != ref)[:5]
+    for h in (0x3F80, 0xC000, 0x0001, 0x7F7F, 0x8000):
+        assert oracle.bf16_decode(h) == float(bf16_bits_to_f32(np.array([h]))[0])
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm
+# ---------------------------------------------------------------------------
+
+def pin_rmsnorm_vs_torch():
+    rng = np.random.default_rng(3)
+    for D in (64, 128):
+        for scale in (1.0, 20.0, 1e-3):
+            x = (rng.standard_normal(D) * scale).astype(np.float32)
+            w = rng.uniform(0.5, 1.5, D).astype(np.float32)
+            got = oracle.rmsnorm(x, w, eps=1e-6)
+            ref = torch.nn.functional.rms_norm(torch.from_numpy(x).double(), (D,),
+                                               torch.from_numpy(w).double(), eps=1e-6).numpy()
+            assert np.allclose(got, ref, rtol=2e-6, atol=1e-7), (D, scale, np.abs(got - ref).max())
+
+
+def pin_rmsnorm_unit_rms_and_scaling():
+    rng = np.random.default_rng(4)
+    for D in (64, 128):
+        x = rng.standard_normal(D).astype(np.float32)
+        y = oracle.rmsnorm(x, None, eps=1e-6).astype(np.float64)
+        assert abs(math.sqrt(np.mean(y * y)) - 1.0) < 1e-5
+        # with eps = 0 the norm is exactly invariant under power-of-two scaling
+        y0 = oracle.rmsnorm(x, None, eps=0.0)
+        y1 = oracle.rmsnorm(x * np.float32(8.0), None, eps=0.0)
+        assert np.array_equal(y0, y1)
+
+
+# ---------------------------------------------------------------------------
+# RoPE
+# ---------------------------------------------------------------------------
+
+def _textbook_rope(y, rd, pos, theta, style):
+    """Rotary embedding as a complex rotation of dim pairs, in float64."""
+    y = np.array(y, dtype=np.float64)
+    if rd == 0:
+        return y
+    k = np.arange(rd // 2)
+    ang = pos * theta ** (-2.0 * k / rd)
+    if style == oracle.ROPE_NEOX:
+        iu, iv = k, k + rd // 2
+    else:
+        iu, iv = 2 * k, 2 * k + 1
+    z = (y[iu] + 1j * y[iv]) * np.exp(1j * ang)
+    y[iu], y[iv] = z.real, z.imag
+    return y
+
+
+def pin_rope_identity_and_passthrough():
+    rng = np.random.default_rng(5)
+    for style in (oracle.ROPE_NEOX, oracle.ROPE_GPTJ):
+        for D, rd in ((64, 64), (128, 128), (128, 64), (128, 32)):
+            x = rng.standard_normal(D).astype(np.float32)
+            assert np.array_equal(oracle.rope(x, rd, 0, style=style), x)
+            y = oracle.rope(x, rd, 777, style=style)
+            assert np.array_equal(y[rd:], x[rd:])
+
+
+def pin_rope_textbook():
+    rng = np.random.default_rng(6)
+    for style in (oracle.ROPE_NEOX, oracle.ROPE_GPTJ):
+        for D, rd in ((64, 64), (128, 128), (128, 64)):
+            for pos in (1, 2, 17, 511, 4097, 9215):
+                x = rng.standard_normal(D).astype(np.float32)
+                got = oracle.rope(x, rd, pos, theta=1e4, style=style)
+                ref = _textbook_rope(x, rd, pos, 1e4, style)
+                # the angle is a float32 product (relative error 2^-24), so large
+                # positions carry up to pos * 6e-8 rad of angle error
+                tol = 2e-6 + pos * 1.2e-7 * 4
+                assert np.abs(got - ref).max() < tol, (style, D, rd, pos, np.abs(got - ref).max())
+
+
+def pin_rope_norms_and_relative_position():
+    rng = np.random.default_rng(8)
+    for style in (oracle.ROPE_NEOX, oracle.ROPE_GPTJ):
+        D = rd = 128
+        q = rng.standard_normal(D).astype(np.float32)
+        k = rng.standard_normal(D).astype(np.float32)
+        qr = oracle.rope(q, rd, 300, style=style).astype(np.float64)
+        half = rd // 2
+        if style == oracle.ROPE_NEOX:
+            pairs = [(i, i + half) for i in range(half)]
+        else:
+            pairs = [(2 * i, 2 * i + 1) for i in range(half)]
+        q64 = q.astype(np.float64)
+        for a, b in pairs:
+            n0 = math.hypot(q64[a], q64[b])
+            n1 = math.hypot(qr[a], qr[b])
+            assert abs(n0 - n1) <= 1e-6 * max(1.0, n0)
+        for m, n in ((5, 3), (100, 40), (260, 7)):
+            d0 = float(np.dot(oracle.rope(q, rd, m, style=style).astype(np.float64),
+                              oracle.rope(k, rd, n, style=style).astype(np.float64)))
+            for shift in (1, 37, 150):
+                d1 = float(np.dot(oracle.rope(q, rd, m + shift, style=style).astype(np.float64),
+                                  oracle.rope(k, rd, n + shift, style=style).astype(np.float64)))
+                assert abs(d0 - d1) < 1e-4 * max(1.0, abs(d0)), (m, n, shift, d0, d1)
+
+
+# ---------------------------------------------------------------------------
+# placement
+# ---------------------------------------------------------------------------
+
+def pin_placement_golden():
+    tables = {"A": np.array([3, -1, 9, 1, 7], dtype=np.int32), "B": None}
+    for case, slot, page, off in _read_golden("placement_points.txt"):
+        got = oracle.place(int(slot), 4, tables[case], 8)
+        exp = None if page == "none" else (int(page), int(off))
+        assert got == exp, (case, slot, got, exp)
+
+
+def _brute_place(ls, P, table, num_pages):
+    """Search every (block, offset) whose slot is ls; no division."""
+    if ls < 0:
+        return None
+    nblocks = len(table) if table is not None else num_pages
+    for b in range(nblocks + 64):
+        for o in range(P):
+            if b * P + o == ls:
+                if table is None:
+                    page = b
+                elif b < len(table):
+                    page = int(table[b])
+                else:
+                    return None
+                if 0 <= page < num_pages:
+                    return (page, o)
+                return None
+    return None
+
+
+def pin_placement_brute_force():
+    rng = np.random.default_rng(9)
+    P, npages = 4, 8
+    for trial in range(20):
+        table = rng.integers(-1, npages + 3, size=10).astype(np.int32)
+        for ls in range(-2, 41):
+            assert oracle.place(ls, P, table, npages) == _brute_place(ls, P, table, npages), (table, ls)
+    for ls in range(-2, 41):
+        assert oracle.place(ls, P, None, npages) == _brute_place(ls, P, None, npages)
+    # a table whose buffer runs on past its stated length with valid pages: the
+    # entries past the length must never be read
+    buf = np.array([3, -1, 6, 1, 2, 2, 2, 2], dtype=np.int32)
+    for ls in range(-2, 41):
+        assert oracle.place(ls, P, buf, npages, table_len=4) == _brute_place(ls, P, buf[:4], npages)
+    # 64-bit slots
+    assert oracle.place(3 * 2**33 + 5, 64, None, 2**40) == (3 * 2**33 // 64, 5)
+
+
+# ---------------------------------------------------------------------------
+# the whole producer
+# ---------------------------------------------------------------------------
+
+def _tiny_pool_workload(seed, heads, rd=None, style=0, idx_k_dtype=wl.DTYPE_E4M3,
+                        kv_dtype=wl.DTYPE_E4M3, page_pad=0, row_pad=0):
+    """A small batch over tiny pools: P = 4, 8 pages, slots that cover padding,
+    table entries of -1 and at or beyond the page count."""
+    rng = np.random.default_rng(seed)
+    P, npages, max_blocks = 4, 8, 3
+    S = 4
+    seq_positions = [[int(p)] for p in rng.integers(0, max_blocks * P, size=S)]
+    seq_positions += [[0, 1, 2, 3, 4, 5]]          # a short prefill chunk
+    w = wl.make_batch(f"tinypool{seed}", seed, heads, seq_positions, max_blocks=max_blocks,
+                      num_pages=npages, rotary_dim=rd, rope_style=style, page_size=P,
+                      kv_dtype=kv_dtype, idx_k_dtype=idx_k_dtype, page_pad_bytes=page_pad,
+                      row_pad=row_pad, shuffle_pages=True)
+    # make the table hold -1 and out-of-range entries, and add padded slots
+    pt = np.array(w.page_table, copy=True)
+    pt.reshape(-1)[::5] = -1
+    pt.reshape(-1)[1::7] = npages + 2
+    w.page_table = pt
+    w.slot_mapping = np.array(w.slot_mapping, copy=True)
+    w.slot_mapping[1] = -1
+    return w
+
+
+def _textbook_forward(w):
+    """Float64 composition of the producer from library/textbook pieces:
+    torch rms_norm, complex-rotation RoPE, torch casts."""
+    s = w.shape
+    D, rd = s["head_dim"], s["rotary_dim"]
+    Hq, Hkv, Hiq, Hik = s["num_q_heads"], s["num_kv_heads"], s["num_idx_q_heads"], s["num_idx_k_heads"]
+    x = bf16_bits_to_f32(w.qkv[:, :w.width]).astype(np.float64)
+    wts = {k: bf16_bits_to_f32(v).astype(np.float64) for k, v in w.weights.items()}
+    o = np.cumsum([0, Hq * D, Hkv * D, Hkv * D, Hiq * D, Hik * D])
+    sec = {"q": (o[0], Hq), "k": (o[1], Hkv), "v": (o[2], Hkv), "idx_q": (o[3], Hiq), "idx_k": (o[4], Hik)}
+    out = {}
+    for name, (start, H) in sec.items():
+        v = x[:, start:start + H * D].reshape(-1, H, D)
+        if name != "v":
+            v = torch.nn.functional.rms_norm(torch.from_numpy(v), (D,), torch.from_numpy(wts[name]),
+                                             eps=s["rms_eps"]).numpy()
+            v = np.stack([np.stack([_textbook_rope(v[t, h], rd, int(w.positions[t]), s["rope_theta"],
+                                                   s["rope_style"]) for h in range(H)])
+                          for t in range(v.shape[0])])
+        out[name] = v
+    return out
+
+
+def _check_producer(w):
+    q, iq, pools = run_oracle(w)
+    init = wl.host_pools(w)
+    ref = _textbook_forward(w)
+    # compact outputs: one bf16 rounding of the float64 value, plus float32 noise
+    for name, got in (("q", q), ("idx_q", iq)):
+        g = bf16_bits_to_f32(got).astype(np.float64)
+        r = ref[name]
+        assert np.all(np.abs(g - r) <= 2.0 ** -8 * np.abs(r) + 2e-4), (name, np.abs(g - r).max())
+    # placement from the brute-force search, not from the oracle
+    P = w.shape["page_size"]
+    pt = None if w.page_table is None else w.page_table.reshape(-1)
+    touched = {p: np.zeros(n, dtype=bool) for p, n in w.pools.items()}
+    for key in ("k", "v", "idx_k"):
+        c = w.caches.get(key)
+        if c is None:
+            continue
+        pls = [_brute_place(int(ls), P, pt, c.num_pages) for ls in w.slot_mapping]
+        cells = cache_cells(w, key, pls)
+        tok = [t for t, pl in enumerate(pls) if pl is not None]
+        pool = pools[c.pool]
+        if cells.size:
+            assert not touched[c.pool][cells].any(), "two writes to one cell"
+            touched[c.pool][cells] = True
+        for i, t in enumerate(tok):
+            for h in range(c.num_heads):
+                got = pool[cells[i, h]]
+                if c.dtype == wl.DTYPE_E4M3:
+                    scale = np.float32(w.scales[{"k": 0, "v": 1, "idx_k": 2}[key]])
+                    inv = np.float32(1.0) / scale
+                    if key == "v":
+                        # V: no norm, no RoPE: exactly the saturating cast of x * (1/s)
+                        xv = bf16_bits_to_f32(w.qkv[t, (w.shape["num_q_heads"] + w.shape["num_kv_heads"]
+                                                        + h) * w.shape["head_dim"]:][:w.shape["head_dim"]])
+                        exp = _torch_e4m3(xv * inv)
+                        assert np.array_equal(got, exp), (key, t, h)
+                    else:
+                        exp = _torch_e4m3((ref[key][t, h] * np.float64(inv)).astype(np.float32))
+                        assert e4m3_ulp_distance(got, exp).max() <= 1, (key, t, h)
+                else:
+                    gv = bf16_bits_to_f32(got.view(np.uint16)).astype(np.float64)
+                    r = ref[key][t, h]
+                    assert np.all(np.abs(gv - r) <= 2.0 ** -8 * np.abs(r) + 2e-4), (key, t, h)
+    # every byte outside the written cells is the sentinel it started as
+    for p in pools:
+        assert np.array_equal(pools[p][~touched[p]], init[p][~touched[p]]), f"stray write in pool {p}"
+
+
+def pin_producer_tiny_shapes():
+    _check_producer(_tiny_pool_workload(21, wl.TINY, idx_k_dtype=wl.DTYPE_BF16))
+
+
+def pin_producer_big_shapes_partial_rope_strided():
+    _check_producer(_tiny_pool_workload(22, wl.BIG, rd=64, page_pad=256, row_pad=64))
+
+
+def pin_producer_gptj_bf16_caches():
+    _check_producer(_tiny_pool_workload(23, wl.TINY, style=wl.ROPE_GPTJ, kv_dtype=wl.DTYPE_BF16,
+                                       idx_k_dtype=wl.DTYPE_BF16))
+
+
+def pin_producer_config1():
+    _check_producer(wl.config1_tiny_decode())
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]
