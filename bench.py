@@ -1,0 +1,480 @@
+#!/usr/bin/env python3
+"""Benchmark of the MSA fused producer on GB300; prints one JSON line.
+
+Default workload: the prefill batch, 8 sequences x 8,192 tokens (65,536 tokens),
+64 Q / 8 K-V / 8 index-Q / 1 index-K heads of dim 128, fp8 E4M3 HND caches with a
+shuffled page table.  One step = one producer launch over the whole batch (all
+steps of the path: placement, RMSNorm, RoPE, compact Q/index-Q, three cache
+scatters).  The rows read per step (1.49 GB) are far larger than L2, so no flush
+is needed between steps.
+
+Also reported: the 60-layer decode step at batch 256 (tiny shapes, one launch per
+layer, all 60 captured in one CUDA graph; microseconds per layer and per step),
+an end-to-end figure through the same C-ABI call with pinned host buffers and the
+host<->device copies inside the timed region, the roofline of the producer kernel
+against the measured HBM copy bandwidth, and the CPU oracle timed on a bounded
+sample of the same workload on this machine's host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (under torchrun) every rank runs its own replica of the workload
+(tokens are independent; there is no exchange step), and value = tokens of all
+ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "producer tokens/s & HBM GB/s (% of peak); us/layer at decode batch 256"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCE = os.path.join(ROOT, "paged_kv_cache_msa_gb300", "csrc", "msa_producer.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash() -> str:
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """dram bytes per launch from a committed ncu capture of this exact kernel
+    source (None when the kernel has changed since)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("kernel_sha") == kernel_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda") if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reported baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+class OracleRunner:
+    """The CPU oracle over a workload, with its host pools prepared once so that
+    only the oracle's own work is timed."""
+
+    def __init__(self, w):
+        import oracle
+        from paged_kv_cache_msa_gb300 import workloads as wl
+        oracle.build()
+        self.oracle = oracle
+        self.w = w
+        self.pools = wl.host_pools(w)
+        self.ca = wl.oracle_cache_args(w, self.pools)
+        self.q, self.iq = wl.empty_outputs(w)
+        self.next = 0
+
+    def run(self, n: int) -> int:
+        """Runs the next n tokens (wrapping around); returns the tokens done."""
+        w = self.w
+        if self.next >= w.num_tokens:
+            self.next = 0
+        n = min(n, w.num_tokens - self.next)
+        self.oracle.forward(w.shape, w.qkv, w.row_stride, w.positions, w.slot_mapping,
+                            w.page_table, w.weights, self.q, self.iq, self.ca["k"], self.ca["v"],
+                            self.ca["idx_k"], w.scales, num_tokens=n, token_offset=self.next)
+        self.next += n
+        return n
+
+    def timed(self, budget_s: float, chunk: int = 256):
+        """Consecutive chunks until the budget is spent; returns (tokens, seconds)."""
+        done, t0 = 0, time.perf_counter()
+        while True:
+            done += self.run(chunk)
+            if time.perf_counter() - t0 >= budget_s or done >= self.w.num_tokens:
+                break
+        return done, time.perf_counter() - t0
+
+
+def make_workload(name: str):
+    from paged_kv_cache_msa_gb300 import workloads as wl
+    if name == "prefill":
+        return wl.config4_prefill()
+    if name == "decode64":
+        return wl.config2_decode64()
+    if name == "mixed":
+        return wl.config5_mixed()
+    if name == "tiny":
+        return wl.config1_tiny_decode()
+    raise ValueError(name)
+
+
+WORKLOAD_DESC = {
+    "prefill": "prefill 8x8192 = 65,536 tokens; Q64/KV8/idxQ8/idxK1 heads, head_dim 128, "
+               "rotary 128 NeoX; fp8 E4M3 K/V/idx-K HND caches, page 64, shuffled table",
+    "decode64": "decode batch 64; big shapes; padded HND fp8 pages; 10% padded slots",
+    "mixed": "mixed 4x2048 prefill + 192 decode; rotary 64/128; strided rows; pool > 2^31 elements",
+    "tiny": "tiny decode batch 4",
+}
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    w = make_workload(args.workload)
+    runner = OracleRunner(w)
+    cores = 1
+    sample = 64
+    for _ in range(args.warmup):
+        runner.run(sample)
+    t0 = time.perf_counter()
+    tok = 0
+    for _ in range(args.steps):
+        tok += runner.run(sample)
+    el = time.perf_counter() - t0
+    value = tok / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * el / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC[args.workload], "tokens_per_step": sample,
+                   "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{sample} consecutive tokens of the workload per step "
+                                   f"(cycling through it), single-threaded C oracle"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def decode_step_timing(replays: int, big: bool, pdl: bool):
+    """60 decode layers at batch 256 captured as 60 launches in one CUDA graph."""
+    import torch
+    from paged_kv_cache_msa_gb300 import binding as B
+    from paged_kv_cache_msa_gb300 import workloads as wl
+    from paged_kv_cache_msa_gb300.device import DeviceWorkload
+    layers = [DeviceWorkload(wl.config3_decode_step(l, big=big)) for l in range(60)]
+    flags = B.MSA_LAUNCH_PERSISTENT | (B.MSA_LAUNCH_PDL if pdl else 0)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for dw in layers:
+            dw.run(flags, stream=s)
+    with torch.cuda.stream(s):
+        for _ in range(20):
+            g.replay()
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(replays):
+            g.replay()
+        e1.record(s)
+        e1.synchronize()
+    us_step = 1e3 * e0.elapsed_time(e1) / replays
+    tokens = layers[0].w.num_tokens
+    del g, layers
+    torch.cuda.empty_cache()
+    return {"us_per_step": us_step, "us_per_layer": us_step / 60, "layers": 60,
+            "tokens_per_layer": tokens, "launches_per_step": 60,
+            "shapes": "big" if big else "tiny", "pdl": pdl, "replays": replays}
+
+
+def run_ours(args):
+    import torch
+    from paged_kv_cache_msa_gb300 import binding as B
+    from paged_kv_cache_msa_gb300 import build as build_mod
+    from paged_kv_cache_msa_gb300.device import DeviceWorkload
+
+    rank, world, local = dist_setup(args.gpus)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        build_mod.build()
+    barrier(world)
+    B.load()
+
+    t_gen = time.perf_counter()
+    w = make_workload(args.workload)
+    log(f"[bench] workload {w.name}: {w.num_tokens} tokens, generated in "
+        f"{time.perf_counter() - t_gen:.1f}s")
+    dw = DeviceWorkload(w, device=dev)
+    flags = B.MSA_LAUNCH_PERSISTENT
+    grid, block, _ = B.msa_producer_launch_shape(dw.cfg, w.num_tokens, flags)
+    stream = torch.cuda.Stream(device=dev)
+    alg_bytes = w.algorithmic_bytes()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            dw.run(flags, stream=stream)
+        stream.synchronize()
+
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local)
+        clocks.start()
+        time.sleep(0.3)
+        barrier(world)
+        torch.cuda.synchronize()
+        t_begin = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_begin.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            dw.run(flags, stream=stream)
+            ends[i].record(stream)
+        t_end.record(stream)
+        t_end.synchronize()
+        torch.cuda.synchronize()
+        barrier(world)
+        clk = clocks.stop()
+    elapsed_ms = t_begin.elapsed_time(t_end)
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kernel_avg_ms = sum(kernel_ms) / len(kernel_ms)
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
+
+    tokens_total = w.num_tokens * args.steps * world
+    value = tokens_total / (elapsed_ms / 1e3)
+    peak, peak_kind = peaks()
+    achieved = alg_bytes / (kernel_avg_ms / 1e3) / 1e9
+    traffic = ncu_traffic(args.workload)
+
+    # end to end: pinned host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(dw, w, flags, steps=min(args.steps, 20), warmup=2, world=world)
+
+    decode = None
+    if not args.no_decode_step:
+        decode = {"tiny": decode_step_timing(1000, big=False, pdl=True),
+                  "tiny_no_pdl": decode_step_timing(1000, big=False, pdl=False),
+                  "big": decode_step_timing(200, big=True, pdl=True)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        n, dt = OracleRunner(w).timed(budget_s=args.cpu_budget)
+        cpu = {"value": n / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {n} of {w.num_tokens} tokens of the same workload "
+                         f"({dt:.1f}s, single-threaded C oracle on the host)"}
+
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC[args.workload], "tokens_per_step": w.num_tokens,
+                   "global_batch": w.num_tokens * world, "launch": f"persistent grid {grid}x{block}",
+                   "l2": "inputs larger than L2 (1.49 GB of rows per step), no flush",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_gbs": achieved, "hbm_frac_of_peak": achieved / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "kernel_avg_us": kernel_avg_ms * 1e3},
+        "us_per_launch": kernel_avg_ms * 1e3,
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+        "decode_step": decode,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_e2e(dw, w, flags, steps, warmup, world):
+    """Per step: pinned host -> device copies of rows, positions, slots and page
+    table; the producer; device -> pinned host copies of compact Q and index-Q."""
+    import torch
+    dev = dw.qkv.device
+    h_qkv = torch.from_numpy(w.qkv.view(np.int16)).pin_memory()
+    h_pos = torch.from_numpy(w.positions).pin_memory()
+    h_slot = torch.from_numpy(w.slot_mapping).pin_memory()
+    h_pt = None if w.page_table is None else torch.from_numpy(w.page_table.reshape(-1)).pin_memory()
+    h_q = torch.empty(dw.q_out.shape, dtype=torch.int16).pin_memory()
+    h_iq = torch.empty(dw.idx_q_out.shape, dtype=torch.int16).pin_memory()
+    stream = torch.cuda.Stream(device=dev)
+    h2d = (h_qkv.numel() * 2 + h_pos.numel() * 4 + h_slot.numel() * 8
+           + (0 if h_pt is None else h_pt.numel() * 4))
+    d2h = h_q.numel() * 2 + h_iq.numel() * 2
+
+    def step():
+        dw.qkv.copy_(h_qkv, non_blocking=True)
+        dw.positions.copy_(h_pos, non_blocking=True)
+        dw.slots.copy_(h_slot, non_blocking=True)
+        if h_pt is not None:
+            dw.page_table.copy_(h_pt, non_blocking=True)
+        dw.run(flags, stream=stream)
+        h_q.copy_(dw.q_out, non_blocking=True)
+        h_iq.copy_(dw.idx_q_out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+        stream.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        e1.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
+    return {"value": w.num_tokens * steps * world / (ms / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": ms / steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["prefill", "decode64", "mixed", "tiny"], default="prefill")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode-step", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        log("[bench] warmup raised to 3 (timing rule)")
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,193 @@
+/*
+ * msa_producer.h -- C ABI of the MiniMax-M3 MSA per-layer fused producer and
+ * paged-cache write, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("[None][perf] Fuse MiniMax-M3 QKV and index projection",
+ * TensorRT-LLM PR 18205, Description, "AFTER" diagram and the list under "This
+ * change adds"): one fused producer takes the packed projection row
+ * [Q | K | V | index-Q | index-K] of every new token, applies per-head Q/K
+ * RMSNorm and RoPE, emits compact Q and index-Q, and writes the current K, V and
+ * index-K directly into paged head-major (HND) caches, with strided cache
+ * layouts, 64-bit element offsets, CUDA Graph replay and safe containment of
+ * padded or out-of-range cache slots.  The page and in-page offset of a token are
+ * derived once per token ("[None][perf] Fuse MiniMax-M3 MSA per-layer KV-cache
+ * writes into one kernel", PR 18614, "The fix"), from a slot that is either a
+ * physical slot or a logical slot looked up through a page table ("Wire in
+ * custom decode kernels for MinimaxM3", PR 18611, merge commit message: write
+ * slots re-derived from the staged block table).
+ *
+ * Per token t, with D = head_dim, P = page_size:
+ *   placement   ls = slot_mapping[t]; nothing is written to a cache when ls < 0.
+ *               block = ls / P, off = ls % P; page = page_table[block] when a
+ *               table is given (nothing written when block >= page_table_len),
+ *               else page = block; a cache takes the token only when
+ *               0 <= page < that cache's num_pages.
+ *   RMSNorm     y = (x * r) * w, r = 1 / sqrt(sum(x^2) / D + rms_eps), per head,
+ *               one weight vector [D] per tensor shared by its heads; applied to
+ *               Q, K, index-Q and index-K, not to V.
+ *   RoPE        after the norm, on dims [0, rotary_dim) at angle
+ *               positions[t] * rope_theta^(-2k / rotary_dim) for pair k;
+ *               NeoX pairs (k, k + rotary_dim/2), GPT-J pairs (2k, 2k + 1):
+ *               u' = u cos - v sin, v' = v cos + u sin.  Other dims pass through.
+ *   outputs     q_out[t, h, :] and idx_q_out[t, h, :] in bf16 (round to nearest
+ *               even), written for every token, padded ones included.
+ *   caches      cache[page*stride_page + h*stride_head + off*stride_token + d]:
+ *               FP8 E4M3 caches store e4m3(x * (1/scale)), round to nearest even,
+ *               saturating to +-448; BF16 caches store bf16(x) (no scale).
+ *               K and index-K take the normed, rotated values, V the raw ones.
+ *
+ * Arithmetic is fp32 inside the kernel.
+ *
+ * Ownership and threading: the caller owns every buffer.  The library
+ * allocates no memory, never synchronises, never reads device memory on the
+ * host, and enqueues at most one kernel on `stream`; a call is therefore
+ * stream-ordered and can be captured into a CUDA graph.  Calls on different
+ * streams that write the same cache cells race, as any two kernels would.
+ *
+ * Errors: every argument check runs on the host before any launch; a call that
+ * returns an error has enqueued nothing and written nothing.
+ */
+#ifndef MSA_PRODUCER_H
+#define MSA_PRODUCER_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MSA_OK = 0,
+    MSA_ERR_INVALID_ARGUMENT = 1,  /* null pointer, negative size, inconsistent count,
+                                      overlapping cache rows, unknown flag */
+    MSA_ERR_UNSUPPORTED = 2,       /* valid but not built: head_dim other than 64 or 128,
+                                      rotary_dim not a multiple of 16 (NeoX) or 8 (GPT-J),
+                                      unknown dtype, rope style or scale mode */
+    MSA_ERR_MISALIGNED = 3,        /* a base pointer or stride breaks the alignment below */
+    MSA_ERR_OFFSET_OVERFLOW = 4,   /* the furthest reachable cache byte does not fit in
+                                      a signed 64-bit offset or wraps the address space */
+    MSA_ERR_CUDA = 5               /* the CUDA runtime refused a query or the launch */
+} msa_status;
+
+typedef enum { MSA_DTYPE_BF16 = 0, MSA_DTYPE_FP8_E4M3 = 1 } msa_dtype;
+typedef enum { MSA_ROPE_NEOX = 0, MSA_ROPE_GPTJ = 1 } msa_rope_style;
+typedef enum { MSA_SCALE_PER_TENSOR = 0, MSA_SCALE_PER_HEAD = 1 } msa_scale_mode;
+
+/* Launch flags (bit set). */
+#define MSA_LAUNCH_PERSISTENT 1   /* grid of at most (SMs x resident CTAs) CTAs that
+                                     stride over the tokens; otherwise one CTA per token */
+#define MSA_LAUNCH_PDL 2          /* programmatic dependent launch: the kernel may be
+                                     scheduled while the previous kernel in the stream
+                                     finishes, and waits for it before reading inputs */
+
+/* One paged cache.  Element (page, head, off, d) lives at
+ *   data + (page*stride_page + head*stride_head + off*stride_token + d) * elem_size
+ * with elem_size 1 for FP8 E4M3 and 2 for BF16.  HND pages [num_heads, P, D] are
+ * stride_head = P*D, stride_token = D; any other non-overlapping strides work
+ * (padded pages, K and V interleaved in one pool, NHD).  Requirements: data
+ * 16-byte aligned; the three strides non-negative multiples of 8 elements; the
+ * rows (head, off) of different pages and heads must not overlap. */
+typedef struct {
+    void *data;              /* device memory; caller-owned */
+    int32_t dtype;           /* msa_dtype */
+    int32_t reserved;        /* must be 0 */
+    int64_t num_pages;       /* pages in this cache; pages >= num_pages are dropped */
+    int64_t num_heads;       /* must equal the number of heads written to it */
+    int64_t stride_page;     /* elements */
+    int64_t stride_head;     /* elements */
+    int64_t stride_token;    /* elements; the dim stride is 1 */
+} msa_cache_desc;
+
+typedef struct {
+    int32_t num_q_heads;      /* Hq  >= 0 */
+    int32_t num_kv_heads;     /* Hkv >= 0 (K and V each) */
+    int32_t num_idx_q_heads;  /* Hiq >= 0 */
+    int32_t num_idx_k_heads;  /* Hik >= 0 */
+    int32_t head_dim;         /* D: 64 or 128 */
+    int32_t rotary_dim;       /* 0 <= rotary_dim <= D */
+    int32_t rope_style;       /* msa_rope_style */
+    int32_t page_size;        /* P > 0 tokens per page */
+    float rope_theta;         /* > 0 */
+    float rms_eps;            /* >= 0 */
+    int32_t scale_mode;       /* msa_scale_mode */
+    int32_t reserved;         /* must be 0 */
+} msa_producer_cfg;
+
+/*
+ * Runs the fused producer over num_tokens tokens on `stream`.
+ *
+ * qkv            device bf16 [num_tokens, qkv_row_stride]; row t holds
+ *                [Q (Hq*D) | K (Hkv*D) | V (Hkv*D) | idx-Q (Hiq*D) | idx-K (Hik*D)],
+ *                each section head-major; qkv_row_stride >= that width, in
+ *                elements, a multiple of 8; qkv 16-byte aligned.
+ * positions      device int32 [num_tokens]: RoPE position of each token.
+ * slot_mapping   device int64 [num_tokens]: slot of each token (-1 = padding).
+ * page_table     device int32 [page_table_len] or NULL: logical block -> page
+ *                (a [seqs, max_blocks] table flattened row-major).  NULL: slots
+ *                are physical (page = slot / P).
+ * *_norm_w       device bf16 [D] RMSNorm weights for Q, K, idx-Q, idx-K; a weight
+ *                may be NULL only when its tensor has no heads or is not written.
+ * q_out          device bf16 [num_tokens, Hq, D], 16-byte aligned (NULL iff Hq = 0).
+ * idx_q_out      device bf16 [num_tokens, Hiq, D], 16-byte aligned (NULL iff Hiq = 0).
+ * k_cache, v_cache  required when Hkv > 0.  idx_k_cache: NULL skips index-K.
+ * scales         device fp32: per tensor [3] = {k, v, idx_k}; per head
+ *                [2*Hkv + Hik] = K heads, then V heads, then index-K heads.
+ *                Read only by FP8 caches; may be NULL when no cache is FP8.
+ * launch_flags   MSA_LAUNCH_* bits.
+ * stream         CUDA stream (0 = legacy default stream).
+ *
+ * num_tokens == 0 returns MSA_OK and launches nothing.  Device-side values
+ * (slots, table entries, positions) need no checking by the caller: any slot or
+ * table entry outside a cache is dropped, so no write leaves the cache extent
+ * the descriptor implies.  Two tokens of one call with the same valid slot
+ * leave that cell's contents unspecified (each 8-element piece comes from one
+ * of them); callers give every token its own slot.
+ */
+msa_status msa_producer_forward(const msa_producer_cfg *cfg, int64_t num_tokens,
+                                const void *qkv, int64_t qkv_row_stride,
+                                const int32_t *positions, const int64_t *slot_mapping,
+                                const int32_t *page_table, int64_t page_table_len,
+                                const void *q_norm_w, const void *k_norm_w,
+                                const void *idx_q_norm_w, const void *idx_k_norm_w,
+                                void *q_out, void *idx_q_out,
+                                const msa_cache_desc *k_cache, const msa_cache_desc *v_cache,
+                                const msa_cache_desc *idx_k_cache,
+                                const float *scales, int32_t launch_flags, cudaStream_t stream);
+
+/*
+ * The host-side checks of msa_producer_forward alone, with the same arguments
+ * minus the stream; touches no GPU state.  Lets a caller check a layer once
+ * before capturing it into a graph.
+ */
+msa_status msa_producer_validate(const msa_producer_cfg *cfg, int64_t num_tokens,
+                                 const void *qkv, int64_t qkv_row_stride,
+                                 const int32_t *positions, const int64_t *slot_mapping,
+                                 const int32_t *page_table, int64_t page_table_len,
+                                 const void *q_norm_w, const void *k_norm_w,
+                                 const void *idx_q_norm_w, const void *idx_k_norm_w,
+                                 void *q_out, void *idx_q_out,
+                                 const msa_cache_desc *k_cache, const msa_cache_desc *v_cache,
+                                 const msa_cache_desc *idx_k_cache,
+                                 const float *scales, int32_t launch_flags);
+
+/*
+ * Launch shape the forward call would use on the current device: CTAs, threads
+ * per CTA and dynamic shared memory bytes.  Returns MSA_ERR_CUDA when the device
+ * cannot be queried.  Host-side; enqueues nothing.
+ */
+msa_status msa_producer_launch_shape(const msa_producer_cfg *cfg, int64_t num_tokens,
+                                     int32_t launch_flags, int32_t *grid, int32_t *block,
+                                     int32_t *smem_bytes);
+
+/* Static, human-readable name of a status; never NULL. */
+const char *msa_status_string(msa_status status);
+
+/* Last detailed message of a failed check on this thread (static storage). */
+const char *msa_last_error_detail(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_PRODUCER_H */

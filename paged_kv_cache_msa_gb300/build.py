@@ -1,0 +1,70 @@
+"""Builds the producer's C-ABI shared library for sm_103a with nvcc, in-tree.
+
+Output: ``paged_kv_cache_msa_gb300/lib/libmsa_producer.so`` (git-ignored).  Run as
+``python -m paged_kv_cache_msa_gb300.build`` or call ``build()``.
+"""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+SOURCES = [os.path.join(PKG, "csrc", "msa_producer.cu")]
+INCLUDE = os.path.join(ROOT, "include")
+OUT_DIR = os.path.join(PKG, "lib")
+LIB_NAME = "libmsa_producer.so"
+LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
+
+ARCH = "-gencode=arch=compute_103a,code=sm_103a"
+
+
+def cuda_home() -> str:
+    for cand in (os.environ.get("CUDA_HOME"), os.environ.get("CUDA_PATH"), "/usr/local/cuda"):
+        if cand and os.path.exists(os.path.join(cand, "bin", "nvcc")):
+            return cand
+    nvcc = shutil.which("nvcc")
+    if nvcc:
+        return os.path.dirname(os.path.dirname(os.path.realpath(nvcc)))
+    raise RuntimeError("nvcc not found: set CUDA_HOME")
+
+
+def nvcc_command(out: str, verbose_ptxas: bool = False, extra=()) -> list:
+    home = cuda_home()
+    libdir = os.path.join(home, "lib64")
+    cmd = [os.path.join(home, "bin", "nvcc"), "-O3", "-std=c++17", ARCH, "-lineinfo",
+           "-Xcompiler", "-fPIC,-O2", "-shared", "-cudart", "shared", "-I", INCLUDE,
+           "-Xlinker", f"-rpath,{libdir}", "-o", out, *SOURCES, *extra]
+    if verbose_ptxas:
+        cmd.insert(1, "-Xptxas=-v")
+    return cmd
+
+
+def up_to_date() -> bool:
+    if not os.path.exists(LIB_PATH):
+        return False
+    t = os.path.getmtime(LIB_PATH)
+    deps = SOURCES + [os.path.join(INCLUDE, "msa_producer.h"), os.path.abspath(__file__)]
+    return all(os.path.getmtime(d) <= t for d in deps)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compiles the library unless it is newer than its sources; returns its path."""
+    if not force and up_to_date():
+        return LIB_PATH
+    os.makedirs(OUT_DIR, exist_ok=True)
+    tmp = LIB_PATH + f".{os.getpid()}.tmp"
+    cmd = nvcc_command(tmp, verbose_ptxas=verbose)
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
+    if verbose:
+        sys.stdout.write(r.stdout + r.stderr)
+    os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

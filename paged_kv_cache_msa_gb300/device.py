@@ -1,0 +1,81 @@
+"""Device-resident buffers for a workload, and the C-ABI call on them.
+
+``DeviceWorkload`` copies a ``workloads.Workload`` (rows, positions, slots, page
+table, weights, scales and sentinel-filled cache pools) into CUDA memory with
+torch, builds the cache descriptors, and calls ``msa_producer_forward`` through
+the binding.  torch is used for memory and streams only.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import binding as B
+from . import workloads as wl
+
+
+def _t(a: np.ndarray, device):
+    import torch
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+class DeviceWorkload:
+    def __init__(self, w: wl.Workload, device="cuda", host_pools: dict | None = None,
+                 pools_on_device: dict | None = None):
+        import torch
+        self.w = w
+        self.device = torch.device(device)
+        s = w.shape
+        self.cfg = B.make_cfg(s["num_q_heads"], s["num_kv_heads"], s["num_idx_q_heads"],
+                              s["num_idx_k_heads"], s["head_dim"], s["rotary_dim"], s["rope_style"],
+                              s["page_size"], s["rope_theta"], s["rms_eps"], s.get("scale_mode", 0))
+        self.qkv = _t(w.qkv, self.device)
+        self.positions = _t(w.positions, self.device)
+        self.slots = _t(w.slot_mapping, self.device)
+        self.page_table = None if w.page_table is None else _t(w.page_table.reshape(-1), self.device)
+        self.weights = {k: (None if v is None else _t(v, self.device)) for k, v in w.weights.items()}
+        self.scales = _t(w.scales, self.device)
+        T, D = w.num_tokens, s["head_dim"]
+        self.q_out = torch.zeros((T, s["num_q_heads"], D), dtype=torch.int16, device=self.device)
+        self.idx_q_out = torch.zeros((T, s["num_idx_q_heads"], D), dtype=torch.int16,
+                                     device=self.device)
+        if pools_on_device is not None:
+            self.pools = pools_on_device
+        else:
+            if host_pools is None:
+                host_pools = wl.host_pools(w)
+            self.pools = {k: _t(v, self.device) for k, v in host_pools.items()}
+        self.caches = {}
+        for key in ("k", "v", "idx_k"):
+            c = w.caches.get(key)
+            self.caches[key] = None if c is None else B.make_cache(
+                self.pools[c.pool].data_ptr() + c.offset, c.dtype, c.num_pages, c.num_heads,
+                c.stride_page, c.stride_head, c.stride_token)
+
+    def args(self, launch_flags=0, num_tokens=None, qkv_ptr=None):
+        """Positional arguments of msa_producer_forward minus the stream."""
+        w = self.w
+        p = lambda t: None if t is None else int(t.data_ptr())
+        T = w.num_tokens if num_tokens is None else int(num_tokens)
+        return (self.cfg, T, p(self.qkv) if qkv_ptr is None else qkv_ptr, w.row_stride,
+                p(self.positions), p(self.slots), p(self.page_table),
+                0 if self.page_table is None else self.page_table.numel(),
+                p(self.weights.get("q")), p(self.weights.get("k")), p(self.weights.get("idx_q")),
+                p(self.weights.get("idx_k")), p(self.q_out), p(self.idx_q_out),
+                self.caches["k"], self.caches["v"], self.caches["idx_k"], p(self.scales),
+                launch_flags)
+
+    def run(self, launch_flags=0, stream=None, num_tokens=None):
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        return B.msa_producer_forward(*self.args(launch_flags, num_tokens), stream=stream.cuda_stream)
+
+    def outputs_to_host(self):
+        q = self.q_out.cpu().numpy().view(np.uint16)
+        iq = self.idx_q_out.cpu().numpy().view(np.uint16)
+        return q, iq
+
+    def pools_to_host(self):
+        return {k: v.cpu().numpy() for k, v in self.pools.items()}
