@@ -211,10 +211,10 @@ class OracleRunner:
         return done, time.perf_counter() - t0
 
 
-def make_workload(name: str):
+def make_workload(name: str, prefill_seqs: int = 8):
     from paged_kv_cache_msa_gb300 import workloads as wl
     if name == "prefill":
-        return wl.config4_prefill()
+        return wl.config4_prefill(num_seqs=prefill_seqs)
     if name == "decode64":
         return wl.config2_decode64()
     if name == "mixed":
@@ -241,7 +241,7 @@ def run_reference(args):
     rank, world, _ = dist_setup(args.gpus)
     if rank != 0:
         return 0
-    w = make_workload(args.workload)
+    w = make_workload(args.workload, args.prefill_seqs)
     runner = OracleRunner(w)
     cores = 1
     sample = 64
@@ -323,7 +323,7 @@ def run_ours(args):
     B.load()
 
     t_gen = time.perf_counter()
-    w = make_workload(args.workload)
+    w = make_workload(args.workload, args.prefill_seqs)
     log(f"[bench] workload {w.name}: {w.num_tokens} tokens, generated in "
         f"{time.perf_counter() - t_gen:.1f}s")
     dw = DeviceWorkload(w, device=dev)
@@ -392,7 +392,8 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC[args.workload], "tokens_per_step": w.num_tokens,
+        "config": {"workload": WORKLOAD_DESC[args.workload] if args.prefill_seqs == 8 or args.workload != "prefill"
+                   else f"prefill {args.prefill_seqs}x8192 (reduced)", "tokens_per_step": w.num_tokens,
                    "global_batch": w.num_tokens * world, "launch": f"persistent grid {grid}x{block}",
                    "l2": "inputs larger than L2 (1.49 GB of rows per step), no flush",
                    "parallelism": f"replicas x{world}"},
@@ -467,6 +468,8 @@ def main():
     ap.add_argument("--no-decode-step", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--prefill-seqs", type=int, default=8,
+                    help="sequences of 8,192 tokens in the prefill workload (8 = the full batch)")
     args = ap.parse_args()
     if args.warmup < 3:
         log("[bench] warmup raised to 3 (timing rule)")

@@ -77,9 +77,13 @@ typedef enum { MSA_SCALE_PER_TENSOR = 0, MSA_SCALE_PER_HEAD = 1 } msa_scale_mode
 /* Launch flags (bit set). */
 #define MSA_LAUNCH_PERSISTENT 1   /* grid of at most (SMs x resident CTAs) CTAs that
                                      stride over the tokens; otherwise one CTA per token */
-#define MSA_LAUNCH_PDL 2          /* programmatic dependent launch: the kernel may be
-                                     scheduled while the previous kernel in the stream
-                                     finishes, and waits for it before reading inputs */
+#define MSA_LAUNCH_PDL 2          /* programmatic dependent launch: the kernel may start
+                                     while the previous kernel in the stream finishes.  It
+                                     waits for that kernel before reading qkv and before
+                                     any write; it reads the norm weights, positions, slot
+                                     mapping and page table before waiting, so the kernel
+                                     launched just before it must not write those (stage
+                                     them earlier in the step). */
 
 /* One paged cache.  Element (page, head, off, d) lives at
  *   data + (page*stride_page + head*stride_head + off*stride_token + d) * elem_size

@@ -42,29 +42,39 @@ def nvcc_command(out: str, verbose_ptxas: bool = False, extra=()) -> list:
     return cmd
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+STAMP_PATH = LIB_PATH + ".defines"
+
+
+def up_to_date(defines=()) -> bool:
+    if not os.path.exists(LIB_PATH) or not os.path.exists(STAMP_PATH):
         return False
+    with open(STAMP_PATH) as f:
+        if f.read() != " ".join(defines):
+            return False
     t = os.path.getmtime(LIB_PATH)
     deps = SOURCES + [os.path.join(INCLUDE, "msa_producer.h"), os.path.abspath(__file__)]
     return all(os.path.getmtime(d) <= t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compiles the library unless it is newer than its sources; returns its path."""
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, defines=()) -> str:
+    """Compiles the library unless it is newer than its sources; returns its path.
+    ``defines``: extra -D tuning macros (e.g. MSA_MIN_CTAS_PER_SM=4)."""
+    if not force and up_to_date(defines):
         return LIB_PATH
     os.makedirs(OUT_DIR, exist_ok=True)
     tmp = LIB_PATH + f".{os.getpid()}.tmp"
-    cmd = nvcc_command(tmp, verbose_ptxas=verbose)
+    cmd = nvcc_command(tmp, verbose_ptxas=verbose, extra=[f"-D{d}" for d in defines])
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
     if verbose:
         sys.stdout.write(r.stdout + r.stderr)
     os.replace(tmp, LIB_PATH)
+    with open(STAMP_PATH, "w") as f:
+        f.write(" ".join(defines))
     return LIB_PATH
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    defs = [a[2:] for a in sys.argv[1:] if a.startswith("-D")]
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, defines=defs))

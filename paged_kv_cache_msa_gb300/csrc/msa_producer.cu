@@ -5,29 +5,35 @@
 // "[None][perf] Fuse MiniMax-M3 MSA per-layer KV-cache writes into one kernel"
 // (PR 18614, "The problem" / "The fix").
 //
-// Design (GB300): the path is HBM-bound streaming work (~2-3 flop per byte, no
-// dense contraction), so it runs on the CUDA cores with wide coalesced memory
-// operations; there is nothing here for the tensor cores.
-//   * One CTA owns one token at a time.  Its threads cover the token's projection
-//     row in 16-byte chunks (8 bf16): a head row of D elements is D/8 adjacent
-//     lanes of one warp, so every load is a fully coalesced 128/256-byte segment
-//     and every cache row store is one 64/128-byte segment.
-//   * All of a thread's row loads are issued before any arithmetic, so a CTA has
-//     the whole 22.8 KB row in flight at once.
-//   * The per-token work that is the same for every head -- the slot -> (page,
-//     offset) derivation and the rotary cos/sin table -- is done once per token
-//     by a few threads into shared memory (double-buffered, one barrier per
-//     token), instead of once per head row.
-//   * RMSNorm's sum of squares is reduced with xor shuffles inside the head row's
-//     lane group; the NeoX rotate-half partner of a lane's 8 elements sits in one
-//     other lane of the same group (rotary_dim a multiple of 16), fetched with one
-//     shuffle per element; GPT-J pairs lie inside a lane.
-//   * FP8 E4M3 packing uses the cvt.rn.satfinite.e4m3x2.f32 instruction; bf16
-//     packing uses cvt.rn.bf16x2.f32.
-//   * One-shot grid (a CTA per token) or a persistent grid of at most
-//     SMs x resident CTAs that strides over the tokens.  No kernel waits on
-//     another CTA, a flag or a barrier other than __syncthreads, so nothing can
-//     spin.  Optional programmatic dependent launch.
+// Design (GB300).  The path is streaming work bound by HBM bandwidth (about two
+// flops per byte, no dense contraction), so it runs on the CUDA cores; there is
+// nothing here for the tensor cores.  What keeps such a kernel off the bandwidth
+// roofline is instruction issue, latency stalls and memory-level parallelism, and
+// the design spends all three carefully:
+//   * A CTA owns one token at a time and strides over the tokens (a persistent
+//     grid of SMs x resident CTAs, or one CTA per token).
+//   * Rows are staged into shared memory with cp.async, the next token's while
+//     the current one is computed, so every CTA always has a row in flight
+//     without holding it in registers.  Each thread copies exactly the pieces it
+//     later reads, so no barrier guards the ring; cp.async.wait_group waits on the
+//     thread's own copies only and cannot spin.
+//   * A head row of D elements is L = D/16 lanes; every lane holds two 8-element
+//     pieces chosen so that the NeoX rotate-half partners (dims k and k + rd/2)
+//     sit in the same lane: RoPE needs no shuffle, and the RMS reduction is
+//     log2(L) xor shuffles.  Pieces are 16 bytes, so loads and stores stay fully
+//     coalesced (L lanes x 16 bytes = one contiguous segment per piece set).
+//   * Arithmetic is fp32 with Blackwell's paired f32x2 FMA/MUL, halving the FP
+//     instruction count; conversion uses cvt.rn.bf16x2.f32 and
+//     cvt.rn.satfinite.e4m3x2.f32.
+//   * Per-token work shared by every head -- the slot -> (page, offset)
+//     derivation with its dependent page-table load, and the rotary cos/sin table
+//     -- is computed for a group of kGroup tokens at a time by all threads into a
+//     double-buffered shared table, with its loads issued one or two groups
+//     ahead.  One barrier per group publishes it; between barriers the warps run
+//     decoupled, so their memory and shuffle latencies overlap.
+//   * No wait on another CTA, flag or mbarrier exists, so nothing can spin.
+//     With programmatic dependent launch the kernel reads its constants and the
+//     first group's metadata before waiting for the previous kernel.
 
 #include "msa_producer.h"
 
@@ -40,10 +46,22 @@
 #include <cstring>
 #include <mutex>
 
+// Resident 256-thread CTAs per SM the register budget is sized for (3: 80 registers).
+#ifndef MSA_MIN_CTAS_PER_SM
+#define MSA_MIN_CTAS_PER_SM 3
+#endif
+// Rows in flight per CTA: the current token's and kStages - 1 ahead.
+#ifndef MSA_STAGES
+#define MSA_STAGES 2
+#endif
+
 namespace {
 
-constexpr int kMaxRotaryHalf = 64;   // rotary_dim / 2 <= head_dim / 2 <= 64
-constexpr int kMaxHeadScales = 256;  // per-head scale mode: 2*Hkv + Hik <= 256
+constexpr int kMaxRotaryHalf = 64;       // rotary_dim / 2 <= head_dim / 2 <= 64
+constexpr int kMaxHeadScales = 256;      // per-head scale mode: 2*Hkv + Hik <= 256
+constexpr int kStages = MSA_STAGES;
+constexpr int kGroup = 8;                // tokens per metadata group (one barrier each)
+constexpr int kMaxRowBytes = 96 * 1024;  // widest token row the shared-memory ring takes
 
 struct CacheArgs {
     uint8_t *data;          // nullptr: this cache is not written
@@ -69,12 +87,14 @@ struct Params {
     const float *scales;
     int64_t num_tokens;
     int32_t hq, hkv, hiq, hik;
+    int32_t htot;                   // head rows per token
+    int32_t row_bytes;              // htot * D * 2: bytes staged per token
     int32_t rotary_dim;
     int32_t rope_style;
     int32_t page_size;
     int32_t page_shift;             // log2(page_size) when a power of two, else -1
     int32_t scale_mode;
-    int32_t num_chunks;             // 8-element chunks in one token's row section
+    int32_t pdl;                    // launched with programmatic dependent launch
     float rms_eps;
     float inv_freq[kMaxRotaryHalf];
 };
@@ -83,19 +103,41 @@ struct Params {
 // device helpers
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ uint4 ld_row_chunk(const uint16_t *p)
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global.L2::128B [%0], [%1], 16;" ::"r"(dst), "l"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a)
 {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
+                 : "r"(a));
     return v;
 }
 
-__device__ __forceinline__ void st_v4(void *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+__device__ __forceinline__ void st_v4(void *p, uint4 v)
 {
-    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
                  : "memory");
 }
 
@@ -104,27 +146,26 @@ __device__ __forceinline__ void st_v2(void *p, uint32_t a, uint32_t b)
     asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
 }
 
-// bf16 pair -> two floats (element 0 is the low half)
-__device__ __forceinline__ void unpack_bf16x2(uint32_t v, float &lo, float &hi)
+// a bf16 pair -> (element 0, element 1) in fp32
+__device__ __forceinline__ float2 unpack2(uint32_t v)
 {
-    lo = __uint_as_float(v << 16);
-    hi = __uint_as_float(v & 0xFFFF0000u);
+    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
 }
 
-// two floats -> bf16 pair, round to nearest even; `lo` lands at the lower address
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+// (element 0, element 1) -> a bf16 pair, round to nearest even
+__device__ __forceinline__ uint32_t pack_bf16x2(float2 v)
 {
     uint32_t d;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(v.y), "f"(v.x));
     return d;
 }
 
-// four floats -> four E4M3 bytes, round to nearest even, saturating to +-448
-__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d)
+// two pairs -> four E4M3 bytes in element order; RNE, saturating to +-448
+__device__ __forceinline__ uint32_t pack_e4m3x4(float2 a, float2 b)
 {
     unsigned short lo, hi;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(a.y), "f"(a.x));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(b.y), "f"(b.x));
     return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
@@ -133,143 +174,266 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t h)
     return __uint_as_float(((uint32_t)h) << 16);
 }
 
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float2 *y)
+{
+    return make_uint4(pack_bf16x2(y[0]), pack_bf16x2(y[1]), pack_bf16x2(y[2]), pack_bf16x2(y[3]));
+}
+
+// ---------------------------------------------------------------------------
+// per-token placement
+// ---------------------------------------------------------------------------
+
+struct TokenMeta {
+    long long page;  // -1: no cache takes the token
+    int off;
+    int valid;       // bit c: cache c (k, v, idx_k) takes the token
+};
+
+// The page a slot points at before the page-count check: the table entry of its
+// logical block (-1 past the table), or the block itself without a table; -1 for
+// a padded slot.
+__device__ __forceinline__ long long table_entry(const Params &p, long long ls)
+{
+    if (ls < 0)
+        return -1;
+    const long long blk = p.page_shift >= 0 ? (ls >> p.page_shift) : ls / p.page_size;
+    if (!p.page_table)
+        return blk;
+    return blk < p.page_table_len ? (long long)__ldg(p.page_table + blk) : -1;
+}
+
+__device__ __forceinline__ TokenMeta place(const Params &p, long long ls, long long page)
+{
+    TokenMeta m;
+    m.page = page;
+    m.off = 0;
+    m.valid = 0;
+    if (ls < 0 || page < 0)
+        return m;
+    m.off = p.page_shift >= 0 ? (int)(ls & (long long)(p.page_size - 1))
+                              : (int)(ls - (ls / p.page_size) * p.page_size);
+#pragma unroll
+    for (int ci = 0; ci < 3; ++ci)
+        if (p.cache[ci].data && page < p.cache[ci].num_pages)
+            m.valid |= 1 << ci;
+    return m;
+}
+
 // ---------------------------------------------------------------------------
 // the producer kernel
 // ---------------------------------------------------------------------------
 //
-// D      head_dim (64 or 128); a head row is G = D/8 lanes of 8 elements
-// NT     threads per CTA (a multiple of 32, hence of G)
-// MAXCH  chunks a thread holds in registers at once; a row of more than
-//        NT*MAXCH chunks is processed in several batches
-template <int D, int NT, int MAXCH>
-__global__ void __launch_bounds__(NT) msa_producer_kernel(const __grid_constant__ Params p)
+// D   head_dim (64 or 128): a head row is L = D/16 lanes of 2 x 8 elements
+// NT  threads per CTA (a multiple of 32)
+//
+// A CTA takes the tokens blockIdx.x + i * gridDim.x, i = 0, 1, ...  in groups of
+// kGroup.  The metadata of group g + 1 is computed at the end of group g into the
+// other half of a double-buffered shared table and published by group g + 1's
+// single barrier.
+template <int D, int NT>
+__global__ void __launch_bounds__(NT, MSA_MIN_CTAS_PER_SM * 256 / NT)
+msa_producer_kernel(const __grid_constant__ Params p)
 {
-    constexpr int G = D / 8;
-    static_assert(NT % 32 == 0 && 32 % G == 0, "a head row must sit inside one warp");
+    constexpr int L = D / 16;
+    constexpr int RPP = NT / L;                       // head rows per pass
+    constexpr int ME = kGroup * kMaxRotaryHalf / NT;  // table entries per thread
+    static_assert(NT % 32 == 0 && 32 % L == 0, "a head row must sit inside one warp");
+    static_assert(kGroup <= NT && ME * NT == kGroup * kMaxRotaryHalf, "group geometry");
 
+    extern __shared__ __align__(128) uint8_t s_rows[];  // kStages x row_bytes
     __shared__ __align__(16) float s_w[4][D];
-    __shared__ float s_cos[2][kMaxRotaryHalf];
-    __shared__ float s_sin[2][kMaxRotaryHalf];
-    __shared__ float s_inv_scale[kMaxHeadScales];
-    __shared__ long long s_page[2];
-    __shared__ int s_off[2];
-    __shared__ int s_valid[2];
+    __shared__ __align__(16) float s_cs[2][kGroup][2][kMaxRotaryHalf];  // [buf][token][cos|sin][k]
+    __shared__ __align__(16) TokenMeta s_meta[2][kGroup];
+
+    // The next kernel in the stream may be scheduled right away: it still waits for
+    // this grid to complete before touching what this grid writes.
+    asm volatile("griddepcontrol.launch_dependents;" :::);
 
     const int tid = threadIdx.x;
-    const int g = tid % G;  // this thread's 8-element slot inside every head row it touches
+    const int warp = tid >> 5;
+    const int q = tid % L;          // lane position inside its head rows
+    const int row0 = tid / L;       // first head row of this thread
+    const int htot = p.htot;
+    // passes this warp makes (uniform across the warp, so shuffles stay converged)
+    const int warp_row0 = (warp * 32) / L;
+    const int npass = htot > warp_row0 ? (htot - warp_row0 + RPP - 1) / RPP : 0;
 
-    // Inputs may be produced by the previous kernel in the stream (programmatic
-    // dependent launch): wait for it before reading them.  A no-op otherwise.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-
+    // constants: may be read before waiting on the previous kernel
     for (int i = tid; i < 4 * D; i += NT) {
         const uint16_t *w = p.norm_w[i / D];
         s_w[i / D][i % D] = w ? bf16_to_f32(w[i % D]) : 1.0f;
     }
-    {
-        const int nscales = p.scale_mode == MSA_SCALE_PER_HEAD ? 2 * p.hkv + p.hik : 3;
-        if (p.scales)
-            for (int i = tid; i < nscales; i += NT)
-                s_inv_scale[i] = 1.0f / p.scales[i];
-    }
-    // Let the next kernel in the stream start its own prologue.
-    asm volatile("griddepcontrol.launch_dependents;" :::);
 
-    // RoPE geometry of this lane (fixed for every head row and token)
+    const int64_t T = p.num_tokens;
+    const int64_t G = gridDim.x;
+    const int64_t t0 = blockIdx.x;
+    if (t0 >= T)
+        return;
+    const int64_t ntok = (T - t0 + G - 1) / G;  // tokens of this CTA
+    auto token = [&](int64_t i) { return t0 + i * G; };
+
+    // ---- lane geometry: which 2 x 8 elements of a head row this lane holds ----
     const int rd = p.rotary_dim;
+    const int half = rd / 2;
     const bool neox = p.rope_style == MSA_ROPE_NEOX;
-    const bool rot = 8 * g < rd;
-    const bool first_half = 8 * g < rd / 2;
-    const int partner = neox ? (first_half ? g + rd / 16 : g - rd / 16) : g;
-    const int fbase = neox ? (first_half ? 8 * g : 8 * g - rd / 2) : 4 * g;
+    int aoff, boff;
+    bool pair = false, rot_a = false, rot_b = false;
+    if (neox) {
+        if (16 * q < rd) {            // rotated: dims k and k + rd/2 (k = 8q .. 8q+7)
+            aoff = 8 * q;
+            boff = 8 * q + half;
+            pair = true;
+        } else {                      // pass-through dims [rd, D)
+            aoff = rd + 16 * (q - rd / 16);
+            boff = aoff + 8;
+        }
+    } else {                          // GPT-J: pairs (2k, 2k+1) inside each piece
+        aoff = 16 * q;
+        boff = aoff + 8;
+        rot_a = aoff < rd;
+        rot_b = boff < rd;
+    }
 
-    const int hq = p.hq, hkv = p.hkv, hiq = p.hiq;
-    const int e_k = hq, e_v = hq + hkv, e_iq = hq + 2 * hkv, e_ik = hq + 2 * hkv + hiq;
+    const int e_k = p.hq, e_v = p.hq + p.hkv, e_iq = p.hq + 2 * p.hkv;
+    const int e_ik = e_iq + p.hiq;
 
-    int buf = 0;
-    for (int64_t t = blockIdx.x; t < p.num_tokens; t += gridDim.x, buf ^= 1) {
-        const uint16_t *row = p.qkv + t * p.row_stride;
-        float cs[8], sn[8];
+    const uint32_t rows_base = smem_addr(s_rows);
+    auto stage_row = [&](int64_t tok, int stage) {
+        const uint16_t *src = p.qkv + tok * p.row_stride;
+        const uint32_t dst = rows_base + (uint32_t)stage * (uint32_t)p.row_bytes;
+        for (int hr = row0; hr < htot; hr += RPP) {
+            const int e = hr * D;
+            cp_async16(dst + 2u * (uint32_t)(e + aoff), src + e + aoff);
+            cp_async16(dst + 2u * (uint32_t)(e + boff), src + e + boff);
+        }
+    };
 
-        for (int c0 = 0; c0 < p.num_chunks; c0 += NT * MAXCH) {
-            // 1. issue every row load of this batch
-            uint4 raw[MAXCH];
+    // ---- metadata pipeline ----
+    // Thread j < kGroup owns token j of every group: the slot and page-table entry
+    // of the group whose metadata is computed next (loaded a group earlier), and
+    // the slot of the group after that.  Table entry e = tid + m*NT is
+    // (token e / half, frequency e % half); its position is loaded a group early.
+    long long ls_n = -1, pte_n = -1, ls_nn = -1;
+    int pos_n[ME];
+    auto load_slot = [&](int64_t i) -> long long { return i < ntok ? __ldg(p.slots + token(i)) : -1; };
+    auto load_positions = [&](int64_t gbase) {
 #pragma unroll
-            for (int k = 0; k < MAXCH; ++k) {
-                const int c = c0 + k * NT + tid;
-                raw[k] = c < p.num_chunks ? ld_row_chunk(row + 8 * c) : make_uint4(0, 0, 0, 0);
+        for (int m = 0; m < ME; ++m) {
+            const int e = tid + m * NT;
+            const int64_t i = gbase + (half > 0 ? e / half : 0);
+            pos_n[m] = (half > 0 && e < kGroup * half && i < ntok) ? __ldg(p.positions + token(i)) : 0;
+        }
+    };
+    auto compute_meta = [&](int64_t gbase, int b) {
+        if (tid < kGroup)
+            s_meta[b][tid] = place(p, ls_n, pte_n);
+#pragma unroll
+        for (int m = 0; m < ME; ++m) {
+            const int e = tid + m * NT;
+            if (half > 0 && e < kGroup * half && gbase + e / half < ntok) {
+                const int j = e / half, k = e % half;
+                float s, c;
+                sincosf((float)pos_n[m] * p.inv_freq[k], &s, &c);
+                s_cs[b][j][0][k] = c;
+                s_cs[b][j][1][k] = s;
             }
+        }
+    };
+    auto prefetch_meta = [&](int64_t gbase) {  // for the group starting at gbase
+        if (tid < kGroup) {
+            ls_n = ls_nn;
+            pte_n = table_entry(p, ls_n);
+            ls_nn = load_slot(gbase + kGroup + tid);
+        }
+        load_positions(gbase);
+    };
+    auto stage_first_rows = [&]() {
+#pragma unroll
+        for (int s = 0; s < kStages - 1; ++s) {
+            if (s < ntok)
+                stage_row(token(s), s);
+            cp_async_commit();
+        }
+    };
 
-            if (c0 == 0) {
-                // 2. per-token work shared by every head row
-                if (tid < rd / 2) {
-                    const float a = (float)__ldg(p.positions + t) * p.inv_freq[tid];
-                    float s, c;
-                    sincosf(a, &s, &c);
-                    s_cos[buf][tid] = c;
-                    s_sin[buf][tid] = s;
-                }
-                if (tid == NT - 1) {
-                    const long long ls = __ldg(p.slots + t);
-                    long long page = -1;
-                    int off = 0;
-                    if (ls >= 0) {
-                        long long blk;
-                        if (p.page_shift >= 0) {
-                            blk = ls >> p.page_shift;
-                            off = (int)(ls & (long long)(p.page_size - 1));
-                        } else {
-                            blk = ls / p.page_size;
-                            off = (int)(ls - blk * p.page_size);
-                        }
-                        if (p.page_table)
-                            page = blk < p.page_table_len ? (long long)__ldg(p.page_table + blk) : -1;
-                        else
-                            page = blk;
-                    }
-                    int valid = 0;
-#pragma unroll
-                    for (int ci = 0; ci < 3; ++ci)
-                        if (p.cache[ci].data && page >= 0 && page < p.cache[ci].num_pages)
-                            valid |= 1 << ci;
-                    s_page[buf] = page;
-                    s_off[buf] = off;
-                    s_valid[buf] = valid;
-                }
-                __syncthreads();
-                if (rot) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int f = neox ? fbase + j : fbase + (j >> 1);
-                        cs[j] = s_cos[buf][f];
-                        sn[j] = s_sin[buf][f];
-                    }
-                }
+    // ---- prologue ----
+    // Under programmatic dependent launch the first group's metadata is computed
+    // before waiting on the previous kernel (positions, slots and the page table
+    // must not be written by the kernel launched just before this one) and the rows
+    // are read after it.  Otherwise the rows are requested first, so that their
+    // latency overlaps the metadata's dependent loads.
+    if (!p.pdl)
+        stage_first_rows();
+    if (tid < kGroup) {
+        ls_n = load_slot(tid);
+        pte_n = table_entry(p, ls_n);
+        ls_nn = load_slot(kGroup + tid);
+    }
+    load_positions(0);
+    compute_meta(0, 0);
+    prefetch_meta(kGroup);
+
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (p.pdl)
+        stage_first_rows();
+
+    for (int64_t g0 = 0; g0 < ntok; g0 += kGroup) {
+        const int buf = (int)((g0 / kGroup) & 1);
+        const int64_t gn = g0 + kGroup;
+        __syncthreads();  // publishes this group's metadata (and, the first time, the weights)
+
+        const int64_t gend = gn < ntok ? gn : ntok;
+        for (int64_t i = g0; i < gend; ++i) {
+            const int64_t t = token(i);
+            const int jt = (int)(i - g0);
+
+            // rows of the token kStages-1 ahead
+            {
+                const int64_t ip = i + kStages - 1;
+                if (ip < ntok)
+                    stage_row(token(ip), (int)(ip % kStages));
+                cp_async_commit();
             }
-            const long long page = s_page[buf];
-            const int off = s_off[buf];
-            const int valid = s_valid[buf];
+            const TokenMeta meta = s_meta[buf][jt];
+            const float *cos_row = &s_cs[buf][jt][0][8 * q];
+            const float *sin_row = &s_cs[buf][jt][1][8 * q];
 
-            // 3. normalise, rotate, convert and store each chunk
-#pragma unroll
-            for (int k = 0; k < MAXCH; ++k) {
-                const int c = c0 + k * NT + tid;
-                const bool active = c < p.num_chunks;
-                const int hr = c / G;  // head row inside the token's row
+            cp_async_wait<kStages - 1>();  // this thread's pieces of token t have landed
+            const uint32_t srow = rows_base + (uint32_t)(i % kStages) * (uint32_t)p.row_bytes;
+            uint16_t *q_tok = p.q_out + (int64_t)t * p.hq * D;
+            uint16_t *iq_tok = p.idx_q_out + (int64_t)t * p.hiq * D;
 
-                float x[8];
-                unpack_bf16x2(raw[k].x, x[0], x[1]);
-                unpack_bf16x2(raw[k].y, x[2], x[3]);
-                unpack_bf16x2(raw[k].z, x[4], x[5]);
-                unpack_bf16x2(raw[k].w, x[6], x[7]);
+            for (int pass = 0; pass < npass; ++pass) {
+                const int hr = row0 + pass * RPP;
+                const bool active = hr < htot;
 
-                float ss = 0.0f;
+                // y holds piece A in y[0..3] and piece B in y[4..7], as element pairs
+                float2 y[8];
+                if (active) {
+                    const uint4 ra = lds128(srow + 2u * (uint32_t)(hr * D + aoff));
+                    const uint4 rb = lds128(srow + 2u * (uint32_t)(hr * D + boff));
+                    y[0] = unpack2(ra.x); y[1] = unpack2(ra.y);
+                    y[2] = unpack2(ra.z); y[3] = unpack2(ra.w);
+                    y[4] = unpack2(rb.x); y[5] = unpack2(rb.y);
+                    y[6] = unpack2(rb.z); y[7] = unpack2(rb.w);
+                } else {
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    ss += x[j] * x[j];
+                    for (int j = 0; j < 8; ++j)
+                        y[j] = f2(0.0f);
+                }
+
+                float2 ss2 = __fmul2_rn(y[0], y[0]);
 #pragma unroll
-                for (int o = 1; o < G; o <<= 1)
-                    ss += __shfl_xor_sync(0xffffffffu, ss, o, G);
+                for (int j = 1; j < 8; ++j)
+                    ss2 = __ffma2_rn(y[j], y[j], ss2);
+                float ss = ss2.x + ss2.y;
+#pragma unroll
+                for (int o = 1; o < L; o <<= 1)
+                    ss += __shfl_xor_sync(0xffffffffu, ss, o, L);
+                if (!active)
+                    continue;
 
                 // section of this head row: 0 Q, 1 K, 2 V, 3 idx-Q, 4 idx-K
                 int sec, h;
@@ -278,80 +442,92 @@ __global__ void __launch_bounds__(NT) msa_producer_kernel(const __grid_constant_
                 else if (hr < e_iq) { sec = 2; h = hr - e_v; }
                 else if (hr < e_ik) { sec = 3; h = hr - e_iq; }
                 else { sec = 4; h = hr - e_ik; }
-                const bool normed = sec != 2;
-                const int widx = sec == 0 ? 0 : sec == 1 ? 1 : sec == 3 ? 2 : 3;
 
-                float y[8];
-                if (normed) {
-                    const float r = 1.0f / sqrtf(ss / (float)D + p.rms_eps);
-                    const float4 w0 = *reinterpret_cast<const float4 *>(&s_w[widx][8 * g]);
-                    const float4 w1 = *reinterpret_cast<const float4 *>(&s_w[widx][8 * g + 4]);
-                    y[0] = (x[0] * r) * w0.x; y[1] = (x[1] * r) * w0.y;
-                    y[2] = (x[2] * r) * w0.z; y[3] = (x[3] * r) * w0.w;
-                    y[4] = (x[4] * r) * w1.x; y[5] = (x[5] * r) * w1.y;
-                    y[6] = (x[6] * r) * w1.z; y[7] = (x[7] * r) * w1.w;
-                } else {
+                if (sec != 2) {
+                    const int widx = sec == 0 ? 0 : sec == 1 ? 1 : sec == 3 ? 2 : 3;
+                    const float2 r2 = f2(rsqrtf(fmaf(ss, 1.0f / (float)D, p.rms_eps)));
+                    {
+                        const float4 w0 = *reinterpret_cast<const float4 *>(&s_w[widx][aoff]);
+                        const float4 w1 = *reinterpret_cast<const float4 *>(&s_w[widx][aoff + 4]);
+                        y[0] = __fmul2_rn(__fmul2_rn(y[0], r2), make_float2(w0.x, w0.y));
+                        y[1] = __fmul2_rn(__fmul2_rn(y[1], r2), make_float2(w0.z, w0.w));
+                        y[2] = __fmul2_rn(__fmul2_rn(y[2], r2), make_float2(w1.x, w1.y));
+                        y[3] = __fmul2_rn(__fmul2_rn(y[3], r2), make_float2(w1.z, w1.w));
+                    }
+                    {
+                        const float4 w0 = *reinterpret_cast<const float4 *>(&s_w[widx][boff]);
+                        const float4 w1 = *reinterpret_cast<const float4 *>(&s_w[widx][boff + 4]);
+                        y[4] = __fmul2_rn(__fmul2_rn(y[4], r2), make_float2(w0.x, w0.y));
+                        y[5] = __fmul2_rn(__fmul2_rn(y[5], r2), make_float2(w0.z, w0.w));
+                        y[6] = __fmul2_rn(__fmul2_rn(y[6], r2), make_float2(w1.x, w1.y));
+                        y[7] = __fmul2_rn(__fmul2_rn(y[7], r2), make_float2(w1.z, w1.w));
+                    }
+                    if (pair) {
+                        // u' = u c - v s, v' = v c + u s, with u in piece A and v in piece B;
+                        // pair j of each piece is at frequencies 8q + 2j, 8q + 2j + 1
+                        const float4 c0 = *reinterpret_cast<const float4 *>(cos_row);
+                        const float4 c1 = *reinterpret_cast<const float4 *>(cos_row + 4);
+                        const float4 s0 = *reinterpret_cast<const float4 *>(sin_row);
+                        const float4 s1 = *reinterpret_cast<const float4 *>(sin_row + 4);
+                        const float2 cs[4] = {make_float2(c0.x, c0.y), make_float2(c0.z, c0.w),
+                                              make_float2(c1.x, c1.y), make_float2(c1.z, c1.w)};
+                        const float2 sn[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w),
+                                              make_float2(s1.x, s1.y), make_float2(s1.z, s1.w)};
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        y[j] = x[j];
-                }
-
-                if (neox) {
-                    // every lane takes part in the shuffles; only rotated lanes of
-                    // normed sections use the result
-                    float pv[8];
+                        for (int j = 0; j < 4; ++j) {
+                            const float2 u = y[j], v = y[4 + j];
+                            y[j] = __ffma2_rn(v, make_float2(-sn[j].x, -sn[j].y), __fmul2_rn(u, cs[j]));
+                            y[4 + j] = __ffma2_rn(u, sn[j], __fmul2_rn(v, cs[j]));
+                        }
+                    } else if (rot_a || rot_b) {
+                        // GPT-J: (y[2m], y[2m+1]) at frequency 8q + m (piece A), 8q + 4 + m (B)
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        pv[j] = __shfl_sync(0xffffffffu, y[j], partner, G);
-                    if (normed && rot) {
-                        if (first_half) {
-#pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                y[j] = y[j] * cs[j] - pv[j] * sn[j];
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                y[j] = y[j] * cs[j] + pv[j] * sn[j];
+                        for (int m = 0; m < 8; ++m) {
+                            if (m < 4 ? rot_a : rot_b) {
+                                const float c = cos_row[m], sn = sin_row[m];
+                                const float u = y[m].x, v = y[m].y;
+                                y[m] = make_float2(u * c - v * sn, v * c + u * sn);
+                            }
                         }
                     }
-                } else if (normed && rot) {
-#pragma unroll
-                    for (int j = 0; j < 8; j += 2) {
-                        const float u = y[j], v = y[j + 1];
-                        y[j] = u * cs[j] - v * sn[j];
-                        y[j + 1] = v * cs[j] + u * sn[j];
-                    }
                 }
 
-                if (!active)
-                    continue;
                 if (sec == 0 || sec == 3) {
-                    uint16_t *dst = sec == 0 ? p.q_out + ((int64_t)t * hq + h) * D + 8 * g
-                                             : p.idx_q_out + ((int64_t)t * hiq + h) * D + 8 * g;
-                    st_v4(dst, pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                          pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+                    uint16_t *dst = sec == 0 ? q_tok + h * D : iq_tok + h * D;
+                    st_v4(dst + aoff, pack_bf16x8(y));
+                    st_v4(dst + boff, pack_bf16x8(y + 4));
                 } else {
                     const int ci = sec == 1 ? 0 : sec == 2 ? 1 : 2;
-                    if (!((valid >> ci) & 1))
+                    if (!((meta.valid >> ci) & 1))
                         continue;
                     const CacheArgs &cc = p.cache[ci];
-                    const int64_t e = page * cc.stride_page + (int64_t)h * cc.stride_head +
-                                      (int64_t)off * cc.stride_token + 8 * g;
+                    const int64_t e = meta.page * cc.stride_page + (int64_t)h * cc.stride_head +
+                                      (int64_t)meta.off * cc.stride_token;
                     if (cc.fp8) {
                         const int si = p.scale_mode == MSA_SCALE_PER_HEAD
-                                           ? (ci == 0 ? h : ci == 1 ? hkv + h : 2 * hkv + h)
+                                           ? (ci == 0 ? h : ci == 1 ? p.hkv + h : 2 * p.hkv + h)
                                            : ci;
-                        const float inv = s_inv_scale[si];
-                        st_v2(cc.data + e, pack_e4m3x4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv),
-                              pack_e4m3x4(y[4] * inv, y[5] * inv, y[6] * inv, y[7] * inv));
+                        const float2 inv = f2(__frcp_rn(__ldg(p.scales + si)));
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            y[j] = __fmul2_rn(y[j], inv);
+                        uint8_t *dst = cc.data + e;
+                        st_v2(dst + aoff, pack_e4m3x4(y[0], y[1]), pack_e4m3x4(y[2], y[3]));
+                        st_v2(dst + boff, pack_e4m3x4(y[4], y[5]), pack_e4m3x4(y[6], y[7]));
                     } else {
-                        st_v4(cc.data + 2 * e, pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                              pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+                        uint16_t *dst = reinterpret_cast<uint16_t *>(cc.data) + e;
+                        st_v4(dst + aoff, pack_bf16x8(y));
+                        st_v4(dst + boff, pack_bf16x8(y + 4));
                     }
                 }
             }
         }
+        if (gn < ntok) {  // the next group's metadata, into the other buffer
+            compute_meta(gn, buf ^ 1);
+            prefetch_meta(gn + kGroup);
+        }
     }
+    cp_async_wait<0>();
 }
 
 // ---------------------------------------------------------------------------
@@ -457,8 +633,9 @@ msa_status validate(const msa_producer_cfg *cfg, int64_t T, const void *qkv, int
         return fail(MSA_ERR_INVALID_ARGUMENT, "head_dim %d", D);
     if (D != 64 && D != 128)
         return fail(MSA_ERR_UNSUPPORTED, "head_dim %d (built: 64, 128)", D);
-    if (Htot * (D / 8) > (int64_t)1 << 30)
-        return fail(MSA_ERR_UNSUPPORTED, "too many heads");
+    if (Htot * D * 2 > kMaxRowBytes)
+        return fail(MSA_ERR_UNSUPPORTED, "a token row of %lld bytes is wider than %d",
+                    (long long)(Htot * D * 2), kMaxRowBytes);
     if (cfg->rope_style != MSA_ROPE_NEOX && cfg->rope_style != MSA_ROPE_GPTJ)
         return fail(MSA_ERR_UNSUPPORTED, "rope_style %d", cfg->rope_style);
     if (rd < 0 || rd > D || (rd & 1))
@@ -548,54 +725,90 @@ msa_status validate(const msa_producer_cfg *cfg, int64_t T, const void *qkv, int
 struct Variant {
     const void *fn;
     int threads;
+    int id;
 };
 
-template <int D, int NT, int MAXCH>
-Variant variant_of()
+template <int D, int NT>
+Variant variant_of(int id)
 {
-    return Variant{reinterpret_cast<const void *>(&msa_producer_kernel<D, NT, MAXCH>), NT};
+    return Variant{reinterpret_cast<const void *>(&msa_producer_kernel<D, NT>), NT, id};
 }
 
-Variant pick_variant(int32_t D)
+constexpr int kNumVariants = 6;
+
+int64_t htot_of(const msa_producer_cfg *cfg)
 {
-    if (D == 128)
-        return variant_of<128, 256, 6>();
-    return variant_of<64, 128, 6>();
+    return (int64_t)cfg->num_q_heads + 2 * (int64_t)cfg->num_kv_heads + cfg->num_idx_q_heads +
+           cfg->num_idx_k_heads;
+}
+
+// Threads per CTA: enough lanes for one pass over a token's head rows, at most 256.
+Variant pick_variant(const msa_producer_cfg *cfg)
+{
+    const int64_t lanes = htot_of(cfg) * (cfg->head_dim / 16);
+    if (cfg->head_dim == 128) {
+        if (lanes <= 64) return variant_of<128, 64>(0);
+        if (lanes <= 128) return variant_of<128, 128>(1);
+        return variant_of<128, 256>(2);
+    }
+    if (lanes <= 64) return variant_of<64, 64>(3);
+    if (lanes <= 128) return variant_of<64, 128>(4);
+    return variant_of<64, 256>(5);
 }
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-int g_sms[kMaxDevices];
-int g_blocks_per_sm[kMaxDevices][2];
+struct DeviceInfo {
+    int sms = 0;
+    int max_dyn_smem[kNumVariants] = {};  // 0: not configured yet on this device
+};
+DeviceInfo g_dev[kMaxDevices];
 
-msa_status grid_for(const msa_producer_cfg *cfg, int64_t T, int32_t flags, int *grid, int *block)
+// Configures the variant on the current device once (its dynamic shared-memory
+// limit) and returns the launch shape.  Host-side queries only; nothing is
+// enqueued, so this is safe while a stream is being captured.
+msa_status launch_shape(const msa_producer_cfg *cfg, int64_t T, int32_t flags, Variant *v,
+                        int *grid, int *smem)
 {
-    const Variant v = pick_variant(cfg->head_dim);
-    *block = v.threads;
+    *v = pick_variant(cfg);
+    *smem = (int)(kStages * htot_of(cfg) * cfg->head_dim * 2);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return fail(MSA_ERR_CUDA, "cudaGetDevice failed");
+    DeviceInfo &di = g_dev[dev];
+    int max_dyn, sms;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        max_dyn = di.max_dyn_smem[v->id];
+        sms = di.sms;
+    }
+    if (max_dyn == 0 || sms == 0) {
+        int optin = 0;
+        cudaFuncAttributes fa;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaFuncGetAttributes(&fa, v->fn) != cudaSuccess)
+            return fail(MSA_ERR_CUDA, "device query failed");
+        max_dyn = optin - (int)fa.sharedSizeBytes;
+        if (cudaFuncSetAttribute(v->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn) !=
+            cudaSuccess)
+            return fail(MSA_ERR_CUDA, "cudaFuncSetAttribute failed");
+        std::lock_guard<std::mutex> lk(g_mu);
+        di.max_dyn_smem[v->id] = max_dyn;
+        di.sms = sms;
+    }
+    if (*smem > max_dyn)
+        return fail(MSA_ERR_UNSUPPORTED, "a row of %d bytes does not fit the shared-memory ring",
+                    *smem / kStages);
     if (!(flags & MSA_LAUNCH_PERSISTENT)) {
         *grid = (int)(T < 0x7fffffff ? T : 0x7fffffff);
         return MSA_OK;
     }
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-        return fail(MSA_ERR_CUDA, "cudaGetDevice failed");
-    const int vi = cfg->head_dim == 128 ? 0 : 1;
-    int sms, per_sm;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        sms = g_sms[dev];
-        per_sm = g_blocks_per_sm[dev][vi];
-    }
-    if (sms == 0 || per_sm == 0) {
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return fail(MSA_ERR_CUDA, "cudaDeviceGetAttribute failed");
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, v.fn, v.threads, 0) != cudaSuccess ||
-            per_sm <= 0)
-            return fail(MSA_ERR_CUDA, "occupancy query failed");
-        std::lock_guard<std::mutex> lk(g_mu);
-        g_sms[dev] = sms;
-        g_blocks_per_sm[dev][vi] = per_sm;
-    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, v->fn, v->threads, *smem) !=
+            cudaSuccess ||
+        per_sm <= 0)
+        return fail(MSA_ERR_CUDA, "occupancy query failed");
     const int64_t cap = (int64_t)sms * per_sm;
     *grid = (int)(T < cap ? T : cap);
     return MSA_OK;
@@ -673,6 +886,8 @@ msa_status msa_producer_forward(const msa_producer_cfg *cfg, int64_t num_tokens,
     p.hkv = cfg->num_kv_heads;
     p.hiq = cfg->num_idx_q_heads;
     p.hik = cfg->num_idx_k_heads;
+    p.htot = (int32_t)htot_of(cfg);
+    p.row_bytes = p.htot * cfg->head_dim * 2;
     p.rotary_dim = cfg->rotary_dim;
     p.rope_style = cfg->rope_style;
     p.page_size = cfg->page_size;
@@ -681,25 +896,24 @@ msa_status msa_producer_forward(const msa_producer_cfg *cfg, int64_t num_tokens,
         if ((1 << sh) == cfg->page_size)
             p.page_shift = sh;
     p.scale_mode = cfg->scale_mode;
-    const int64_t Htot = (int64_t)p.hq + 2 * p.hkv + p.hiq + p.hik;
-    p.num_chunks = (int32_t)(Htot * (cfg->head_dim / 8));
+    p.pdl = (launch_flags & MSA_LAUNCH_PDL) ? 1 : 0;
     p.rms_eps = cfg->rms_eps;
     // RoPE frequencies theta^(-2k/rd), evaluated in double and rounded once
     for (int k = 0; k < cfg->rotary_dim / 2; ++k)
         p.inv_freq[k] = (float)(1.0 / std::pow((double)cfg->rope_theta,
                                                2.0 * (double)k / (double)cfg->rotary_dim));
 
-    int grid = 0, block = 0;
-    s = grid_for(cfg, num_tokens, launch_flags, &grid, &block);
+    Variant v;
+    int grid = 0, smem = 0;
+    s = launch_shape(cfg, num_tokens, launch_flags, &v, &grid, &smem);
     if (s != MSA_OK)
         return s;
 
-    const Variant v = pick_variant(cfg->head_dim);
     cudaLaunchConfig_t lc;
     memset(&lc, 0, sizeof lc);
     lc.gridDim = dim3((unsigned)grid);
-    lc.blockDim = dim3((unsigned)block);
-    lc.dynamicSmemBytes = 0;
+    lc.blockDim = dim3((unsigned)v.threads);
+    lc.dynamicSmemBytes = (size_t)smem;
     lc.stream = stream;
     cudaLaunchAttribute attr[1];
     if (launch_flags & MSA_LAUNCH_PDL) {
@@ -723,13 +937,16 @@ msa_status msa_producer_launch_shape(const msa_producer_cfg *cfg, int64_t num_to
         return fail(MSA_ERR_INVALID_ARGUMENT, "launch_shape: bad arguments");
     if (cfg->head_dim != 64 && cfg->head_dim != 128)
         return fail(MSA_ERR_UNSUPPORTED, "head_dim %d", cfg->head_dim);
-    int g = 0, b = 0;
-    msa_status s = grid_for(cfg, num_tokens, launch_flags, &g, &b);
+    if (htot_of(cfg) <= 0 || htot_of(cfg) * cfg->head_dim * 2 > kMaxRowBytes)
+        return fail(MSA_ERR_UNSUPPORTED, "head counts");
+    Variant v;
+    int g = 0, sm = 0;
+    msa_status s = launch_shape(cfg, num_tokens, launch_flags, &v, &g, &sm);
     if (s != MSA_OK)
         return s;
     *grid = g;
-    *block = b;
-    *smem_bytes = 0;
+    *block = v.threads;
+    *smem_bytes = sm;
     return MSA_OK;
 }
 

@@ -201,7 +201,9 @@ def test_graph_replay_sees_new_inputs():
     """One capture, two replays with different row contents and slots."""
     w1 = _small(20, heads=wl.BIG, T_seqs=32)
     w2 = _small(21, heads=wl.BIG, T_seqs=32)
-    w2.page_table = w1.page_table
+    # the captured call keeps its pointers: only the contents of the rows,
+    # positions and slots change between replays
+    w2.page_table, w2.weights, w2.scales = w1.page_table, w1.weights, w1.scales
     dw = DeviceWorkload(w1)
     s = torch.cuda.Stream()
     torch.cuda.synchronize()
