@@ -260,10 +260,15 @@ msa_producer_kernel(const __grid_constant__ Params p)
     const int warp_row0 = (warp * 32) / L;
     const int npass = htot > warp_row0 ? (htot - warp_row0 + RPP - 1) / RPP : 0;
 
-    // constants: may be read before waiting on the previous kernel
-    for (int i = tid; i < 4 * D; i += NT) {
-        const uint16_t *w = p.norm_w[i / D];
-        s_w[i / D][i % D] = w ? bf16_to_f32(w[i % D]) : 1.0f;
+    // constants (may be read before waiting on the previous kernel): loaded into
+    // registers now, stored to shared memory once the other loads are in flight
+    constexpr int NW = (4 * D + NT - 1) / NT;
+    float wreg[NW];
+#pragma unroll
+    for (int m = 0; m < NW; ++m) {
+        const int i = tid + m * NT;
+        const uint16_t *w = i < 4 * D ? p.norm_w[i / D] : nullptr;
+        wreg[m] = w ? bf16_to_f32(__ldg(w + i % D)) : 1.0f;
     }
 
     const int64_t T = p.num_tokens;
@@ -374,6 +379,12 @@ msa_producer_kernel(const __grid_constant__ Params p)
     load_positions(0);
     compute_meta(0, 0);
     prefetch_meta(kGroup);
+#pragma unroll
+    for (int m = 0; m < NW; ++m) {
+        const int i = tid + m * NT;
+        if (i < 4 * D)
+            s_w[i / D][i % D] = wreg[m];
+    }
 
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (p.pdl)
