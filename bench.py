@@ -306,6 +306,30 @@ def decode_step_timing(replays: int, big: bool, pdl: bool):
             "shapes": "big" if big else "tiny", "pdl": pdl, "replays": replays}
 
 
+def graph_launch_us(dw, flags, launches: int, replays: int) -> float:
+    """Mean time of one producer launch inside a CUDA graph of `launches`
+    back-to-back launches (host submission cost excluded)."""
+    import torch
+    s = torch.cuda.Stream(device=dw.qkv.device)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(launches):
+            dw.run(flags, stream=s)
+    with torch.cuda.stream(s):
+        g.replay()
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(replays):
+            g.replay()
+        e1.record(s)
+        e1.synchronize()
+    us = 1e3 * e0.elapsed_time(e1) / (launches * replays)
+    del g
+    return us
+
+
 def run_ours(args):
     import torch
     from paged_kv_cache_msa_gb300 import binding as B
@@ -367,6 +391,9 @@ def run_ours(args):
     achieved = alg_bytes / (kernel_avg_ms / 1e3) / 1e9
     traffic = ncu_traffic(args.workload)
 
+    big = alg_bytes > 256e6
+    us_graph = graph_launch_us(dw, flags, launches=20 if big else 100, replays=5 if big else 20)
+
     # end to end: pinned host buffers, copies inside the timed region
     e2e = None
     if not args.no_e2e:
@@ -404,6 +431,7 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "kernel_avg_us": kernel_avg_ms * 1e3},
         "us_per_launch": kernel_avg_ms * 1e3,
+        "us_per_launch_in_graph": us_graph,
         "gpu_launches": args.steps,
         "clocks": clk,
         "e2e": e2e,
