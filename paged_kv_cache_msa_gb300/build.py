@@ -56,9 +56,16 @@ def up_to_date(defines=()) -> bool:
     return all(os.path.getmtime(d) <= t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, defines=()) -> str:
-    """Compiles the library unless it is newer than its sources; returns its path.
-    ``defines``: extra -D tuning macros (e.g. MSA_MIN_CTAS_PER_SM=4)."""
+def build(force: bool = False, verbose: bool = False, defines=None) -> str:
+    """Compiles the library unless it is newer than its sources and was built with
+    the same defines; returns its path.  ``defines``: extra -D tuning macros (e.g.
+    MSA_MIN_CTAS_PER_SM=4); by default the space-separated list in the
+    MSA_BUILD_DEFINES environment variable (empty: the tuned defaults).  With
+    MSA_NO_BUILD=1 an existing library is used as it is."""
+    if defines is None:
+        defines = tuple(os.environ.get("MSA_BUILD_DEFINES", "").split())
+    if os.environ.get("MSA_NO_BUILD") == "1" and os.path.exists(LIB_PATH):
+        return LIB_PATH
     if not force and up_to_date(defines):
         return LIB_PATH
     os.makedirs(OUT_DIR, exist_ok=True)
@@ -77,4 +84,4 @@ def build(force: bool = False, verbose: bool = False, defines=()) -> str:
 
 if __name__ == "__main__":
     defs = [a[2:] for a in sys.argv[1:] if a.startswith("-D")]
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, defines=defs))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, defines=defs or None))

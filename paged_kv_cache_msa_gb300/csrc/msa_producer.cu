@@ -55,12 +55,17 @@
 #define MSA_STAGES 2
 #endif
 
+// Tokens whose placement and rotary table are prepared together (one barrier each).
+#ifndef MSA_GROUP
+#define MSA_GROUP 8
+#endif
+
 namespace {
 
 constexpr int kMaxRotaryHalf = 64;       // rotary_dim / 2 <= head_dim / 2 <= 64
 constexpr int kMaxHeadScales = 256;      // per-head scale mode: 2*Hkv + Hik <= 256
 constexpr int kStages = MSA_STAGES;
-constexpr int kGroup = 8;                // tokens per metadata group (one barrier each)
+constexpr int kGroup = MSA_GROUP;        // tokens per metadata group (one barrier each)
 constexpr int kMaxRowBytes = 96 * 1024;  // widest token row the shared-memory ring takes
 
 struct CacheArgs {
