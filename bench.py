@@ -442,47 +442,48 @@ def run_ours(args):
     return 0
 
 
-def run_e2e(dw, w, flags, steps, warmup, world):
-    """Per step: pinned host -> device copies of rows, positions, slots and page
-    table; the producer; device -> pinned host copies of compact Q and index-Q."""
+def run_e2e(dw, w, flags, steps, warmup, world, chunk_tokens=8192):
+    """End to end from pinned host memory through the package's HostPipeline: per step
+    the rows, positions and slots go from host to device and the compact Q / index-Q
+    come back, either inside the kernel over the CPU-GPU link (zero copy, the
+    headline) or by chunked copies overlapped with the kernel.  Timed with the host
+    clock around whole steps."""
     import torch
-    dev = dw.qkv.device
+    from paged_kv_cache_msa_gb300.pipeline import HostPipeline
     h_qkv = torch.from_numpy(w.qkv.view(np.int16)).pin_memory()
     h_pos = torch.from_numpy(w.positions).pin_memory()
     h_slot = torch.from_numpy(w.slot_mapping).pin_memory()
-    h_pt = None if w.page_table is None else torch.from_numpy(w.page_table.reshape(-1)).pin_memory()
     h_q = torch.empty(dw.q_out.shape, dtype=torch.int16).pin_memory()
     h_iq = torch.empty(dw.idx_q_out.shape, dtype=torch.int16).pin_memory()
-    stream = torch.cuda.Stream(device=dev)
-    h2d = (h_qkv.numel() * 2 + h_pos.numel() * 4 + h_slot.numel() * 8
-           + (0 if h_pt is None else h_pt.numel() * 4))
+    pipe = HostPipeline(dw.cfg, w.row_stride, min(chunk_tokens, w.num_tokens), dw.qkv.device,
+                        (dw.weights.get("q"), dw.weights.get("k"), dw.weights.get("idx_q"),
+                         dw.weights.get("idx_k")),
+                        (dw.caches["k"], dw.caches["v"], dw.caches["idx_k"]), dw.scales,
+                        dw.page_table, flags)
+    h2d = h_qkv.numel() * 2 + h_pos.numel() * 4 + h_slot.numel() * 8
     d2h = h_q.numel() * 2 + h_iq.numel() * 2
-
-    def step():
-        dw.qkv.copy_(h_qkv, non_blocking=True)
-        dw.positions.copy_(h_pos, non_blocking=True)
-        dw.slots.copy_(h_slot, non_blocking=True)
-        if h_pt is not None:
-            dw.page_table.copy_(h_pt, non_blocking=True)
-        dw.run(flags, stream=stream)
-        h_q.copy_(dw.q_out, non_blocking=True)
-        h_iq.copy_(dw.idx_q_out, non_blocking=True)
-
-    with torch.cuda.stream(stream):
+    def timed(fn):
         for _ in range(warmup):
-            step()
-        stream.synchronize()
+            fn(h_qkv, h_pos, h_slot, h_q, h_iq)
+        torch.cuda.synchronize()
         barrier(world)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        t0 = time.perf_counter()
         for _ in range(steps):
-            step()
-        e1.record(stream)
-        e1.synchronize()
-    ms = max_over_ranks(e0.elapsed_time(e1), world)
-    return {"value": w.num_tokens * steps * world / (ms / 1e3), "unit": "tokens/s",
+            fn(h_qkv, h_pos, h_slot, h_q, h_iq)
+        torch.cuda.synchronize()
+        return max_over_ranks(1e3 * (time.perf_counter() - t0), world)
+
+    ms_zero = timed(pipe.run_zero_copy)
+    ms_copy = timed(pipe.run)
+    return {"value": w.num_tokens * steps * world / (ms_zero / 1e3), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "ms_per_step": ms / steps}
+            "ms_per_step": ms_zero / steps,
+            "api": "paged_kv_cache_msa_gb300.pipeline.HostPipeline.run_zero_copy: the kernel reads "
+                   "rows from and writes compact outputs to pinned host memory over NVLink-C2C",
+            "copy_pipeline": {"value": w.num_tokens * steps * world / (ms_copy / 1e3),
+                              "ms_per_step": ms_copy / steps,
+                              "chunk_tokens": min(chunk_tokens, w.num_tokens),
+                              "api": "HostPipeline.run: chunked cudaMemcpyAsync in, kernel, out"}}
 
 
 def main():

@@ -184,6 +184,17 @@ msa_status msa_producer_launch_shape(const msa_producer_cfg *cfg, int64_t num_to
                                      int32_t launch_flags, int32_t *grid, int32_t *block,
                                      int32_t *smem_bytes);
 
+/*
+ * Device address at which the GPU of the current device reaches host memory
+ * `host_ptr` (pinned, mapped host memory; on Grace-Blackwell the GPU reads and
+ * writes it over NVLink-C2C).  Sets *device_ptr and returns MSA_OK when the
+ * buffer is device-accessible; MSA_ERR_INVALID_ARGUMENT when it is not (pageable
+ * or unregistered memory) or an argument is NULL.  Lets a caller pass host
+ * buffers straight to msa_producer_forward (rows, positions, slots, compact
+ * outputs) with the copies done by the kernel itself.  Host-side; enqueues nothing.
+ */
+msa_status msa_host_buffer_device_address(const void *host_ptr, void **device_ptr);
+
 /* Static, human-readable name of a status; never NULL. */
 const char *msa_status_string(msa_status status);
 

@@ -32,7 +32,7 @@ MSA_LAUNCH_PDL = 2
 
 # every function the header declares
 EXPORTED = ("msa_producer_forward", "msa_producer_validate", "msa_producer_launch_shape",
-            "msa_status_string", "msa_last_error_detail")
+            "msa_host_buffer_device_address", "msa_status_string", "msa_last_error_detail")
 
 
 class MsaError(RuntimeError):
@@ -102,6 +102,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.msa_producer_launch_shape.argtypes = [cfgp, i64, i32, ctypes.POINTER(i32),
                                                 ctypes.POINTER(i32), ctypes.POINTER(i32)]
         L.msa_producer_launch_shape.restype = ctypes.c_int
+        L.msa_host_buffer_device_address.argtypes = [vp, ctypes.POINTER(ctypes.c_void_p)]
+        L.msa_host_buffer_device_address.restype = ctypes.c_int
         L.msa_status_string.argtypes = [ctypes.c_int]
         L.msa_status_string.restype = ctypes.c_char_p
         L.msa_last_error_detail.argtypes = []
@@ -183,6 +185,14 @@ def msa_producer_validate(cfg, num_tokens, qkv, qkv_row_stride, positions, slot_
                                                k_norm_w, idx_q_norm_w, idx_k_norm_w, q_out,
                                                idx_q_out, k_cache, v_cache, idx_k_cache, scales,
                                                launch_flags))
+
+
+def msa_host_buffer_device_address(host_ptr: int):
+    """Device address of pinned, mapped host memory, or None when the buffer is not
+    device-accessible."""
+    out = ctypes.c_void_p()
+    st = load().msa_host_buffer_device_address(host_ptr, ctypes.byref(out))
+    return out.value if st == MSA_OK else None
 
 
 def msa_producer_launch_shape(cfg, num_tokens, launch_flags=0):

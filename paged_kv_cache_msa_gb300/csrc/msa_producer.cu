@@ -966,6 +966,24 @@ msa_status msa_producer_launch_shape(const msa_producer_cfg *cfg, int64_t num_to
     return MSA_OK;
 }
 
+msa_status msa_host_buffer_device_address(const void *host_ptr, void **device_ptr)
+{
+    g_detail[0] = '\0';
+    if (!host_ptr || !device_ptr)
+        return fail(MSA_ERR_INVALID_ARGUMENT, "host_buffer_device_address: NULL argument");
+    cudaPointerAttributes a;
+    memset(&a, 0, sizeof a);
+    if (cudaPointerGetAttributes(&a, host_ptr) != cudaSuccess) {
+        (void)cudaGetLastError();  // an unregistered pointer is not a sticky error
+        return fail(MSA_ERR_INVALID_ARGUMENT, "pointer unknown to the CUDA runtime");
+    }
+    if (a.type != cudaMemoryTypeHost || !a.devicePointer)
+        return fail(MSA_ERR_INVALID_ARGUMENT, "not pinned, device-mapped host memory (type %d)",
+                    (int)a.type);
+    *device_ptr = a.devicePointer;
+    return MSA_OK;
+}
+
 const char *msa_status_string(msa_status status)
 {
     switch (status) {

@@ -223,3 +223,9 @@ def test_per_head_scale_limit(lib):
     a = good_call(cfg=c, k_cache=_cache(num_heads=200, stride_page=200 * 64 * 128),
                   v_cache=_cache(num_heads=200, stride_page=200 * 64 * 128))
     assert validate(a) == B.MSA_ERR_UNSUPPORTED
+
+
+def test_host_buffer_helper_rejects_null(lib):
+    out = ctypes.c_void_p()
+    assert lib.msa_host_buffer_device_address(None, ctypes.byref(out)) == B.MSA_ERR_INVALID_ARGUMENT
+    assert lib.msa_host_buffer_device_address(ctypes.c_void_p(BASE), None) == B.MSA_ERR_INVALID_ARGUMENT

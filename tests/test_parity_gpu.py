@@ -118,6 +118,21 @@ def test_rope_variants(style, rd, D):
     check_against_oracle(w, PERSISTENT)
 
 
+@pytest.mark.parametrize("draft_len", [1, 3, 7])
+def test_multi_token_decode_rows(draft_len):
+    """Speculative verify: every sequence brings 1 + draft_len new tokens at consecutive
+    positions (some crossing a page boundary), each with its own slot."""
+    rng = np.random.default_rng(50 + draft_len)
+    S = 48
+    starts = rng.integers(0, 1024 - draft_len - 1, size=S)
+    starts[:4] = [63 - draft_len // 2, 127 - draft_len, 0, 64]   # page-boundary crossings
+    seq_positions = [list(range(int(s0), int(s0) + 1 + draft_len)) for s0 in starts]
+    w = wl.make_batch(f"verify{draft_len}", 60 + draft_len, wl.BIG, seq_positions, max_blocks=16,
+                      num_pages=S * 16, pad_frac=0.05)
+    for flags in (PERSISTENT, PERSISTENT | B.MSA_LAUNCH_PDL):
+        check_against_oracle(w, flags)
+
+
 def test_physical_slots_without_page_table():
     w = _small(4, T_seqs=40, use_page_table=False, pad_frac=0.2)
     assert w.page_table is None
