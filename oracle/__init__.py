@@ -117,6 +117,11 @@ def load(path: str) -> ctypes.CDLL:
         ctypes.POINTER(OracleCache), vp,
     ]
     L.oracle_forward.restype = ctypes.c_int
+    L.oracle_indexer.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                 ctypes.c_int32, ctypes.c_int64, vp, vp, vp, vp, ctypes.c_int64,
+                                 ctypes.POINTER(OracleCache), ctypes.c_float, ctypes.c_int32,
+                                 vp, vp]
+    L.oracle_indexer.restype = ctypes.c_int
     return L
 
 
@@ -263,3 +268,26 @@ def forward(shape: dict, qkv: np.ndarray, row_stride: int, positions: np.ndarray
         ctypes.byref(ic) if ic else None, scales.ctypes.data)
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (rc={rc})")
+
+
+def indexer(idx_q: np.ndarray, kv_len: np.ndarray, table_offset: np.ndarray, page_table,
+            idx_k_cache: dict, k_scale: float, page_size: int, block_tokens: int, topk: int,
+            max_blocks: int):
+    """Block scores [T, max_blocks] (float32) and top-k block ids [T, topk] (int32).
+    idx_q: uint16 (bf16 bits) [T, H, D]; kv_len int32 [T]; table_offset int64 [T];
+    page_table int32 (flattened); idx_k_cache: see ``_cache_struct`` (one head)."""
+    T, H, D = idx_q.shape
+    assert idx_q.dtype == np.uint16 and idx_q.flags.c_contiguous
+    kv_len = np.ascontiguousarray(kv_len, dtype=np.int32)
+    table_offset = np.ascontiguousarray(table_offset, dtype=np.int64)
+    pt = np.ascontiguousarray(page_table, dtype=np.int32).reshape(-1)
+    scores = np.empty((T, max_blocks), dtype=np.float32)
+    top = np.empty((T, topk), dtype=np.int32)
+    c = _cache_struct(idx_k_cache)
+    rc = lib().oracle_indexer(H, D, int(page_size), int(block_tokens), int(topk), T,
+                              idx_q.ctypes.data, kv_len.ctypes.data, table_offset.ctypes.data,
+                              pt.ctypes.data, pt.size, ctypes.byref(c), float(k_scale),
+                              int(max_blocks), scores.ctypes.data, top.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle rejected the indexer arguments")
+    return scores, top

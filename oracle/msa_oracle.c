@@ -369,3 +369,96 @@ int oracle_forward(const oracle_shape *sh, int64_t num_tokens,
     free(y);
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* Indexer: block scores over the index-K cache and top-k block ids    */
+/* ------------------------------------------------------------------ */
+/*
+ * The downstream consumer of the index-K cache ("[None][perf] Fuse MiniMax-M3
+ * MSA per-layer KV-cache writes into one kernel", the layer walk-through: the
+ * indexer runs a proxy attention over index-K, max-reduces, and selects the top
+ * 16 of 128-token blocks; "[None][perf] Fuse MiniMax-M3 QKV and index
+ * projection", AFTER diagram: score visible index-K, max-pool scores by block,
+ * select top-k block ids).
+ *
+ * Readings: the score of visible token j for query t is max over index heads h
+ * of q[t,h,:] . k[j,:] (k dequantised as code * k_scale for an FP8 cache); a
+ * block's score is the max over its visible tokens; a positive softmax scale
+ * would change neither max nor order and is left out.  Token j of query t is
+ * visible when j < kv_len[t]; its page is page_table[table_offset[t] + j / P];
+ * a token whose table entry is outside the table or the cache is skipped.
+ * Blocks are block_tokens tokens; scores of blocks at or beyond the visible
+ * count (or with no scored token) are -inf.  Top-k: the k highest finite block
+ * scores in descending order, ties to the lower block id, padded with -1.
+ */
+int oracle_indexer(int32_t num_heads, int32_t head_dim, int32_t page_size, int32_t block_tokens,
+                   int32_t topk, int64_t num_tokens, const uint16_t *idx_q,
+                   const int32_t *kv_len, const int64_t *table_offset,
+                   const int32_t *page_table, int64_t page_table_len,
+                   const oracle_cache *idx_k_cache, float k_scale, int32_t max_blocks,
+                   float *block_scores, int32_t *topk_out)
+{
+    const int32_t D = head_dim, P = page_size;
+    if (D <= 0 || P <= 0 || block_tokens <= 0 || topk < 0 || max_blocks < 0 || num_heads <= 0)
+        return -1;
+    float *q = (float *)malloc(sizeof(float) * (size_t)num_heads * (size_t)D);
+    float *k = (float *)malloc(sizeof(float) * (size_t)D);
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        float *bs = block_scores + t * max_blocks;
+        for (int32_t b = 0; b < max_blocks; ++b)
+            bs[b] = -INFINITY;
+        for (int32_t h = 0; h < num_heads; ++h)
+            for (int32_t d = 0; d < D; ++d)
+                q[h * D + d] = oracle_bf16_decode(idx_q[(t * num_heads + h) * D + d]);
+        const int64_t L = kv_len[t];
+        for (int64_t j = 0; j < L; ++j) {
+            const int64_t b = j / block_tokens;
+            if (b >= max_blocks)
+                break;
+            const int64_t ti = table_offset[t] + j / P;
+            if (ti < 0 || ti >= page_table_len)
+                continue;
+            const int64_t page = page_table[ti];
+            if (page < 0 || page >= idx_k_cache->num_pages)
+                continue;
+            const int64_t e = page * idx_k_cache->stride_page + (j % P) * idx_k_cache->stride_token;
+            for (int32_t d = 0; d < D; ++d) {
+                if (idx_k_cache->dtype == ORACLE_DTYPE_E4M3)
+                    k[d] = oracle_e4m3_decode(idx_k_cache->data[e + d]) * k_scale;
+                else {
+                    uint16_t hbits;
+                    memcpy(&hbits, idx_k_cache->data + 2 * (e + d), 2);
+                    k[d] = oracle_bf16_decode(hbits);
+                }
+            }
+            for (int32_t h = 0; h < num_heads; ++h) {
+                float s = 0.0f;
+                for (int32_t d = 0; d < D; ++d)
+                    s += q[h * D + d] * k[d];
+                if (s > bs[b])
+                    bs[b] = s;
+            }
+        }
+        /* top-k by repeated selection: highest score, lowest id among equals */
+        int32_t *out = topk_out + t * topk;
+        for (int32_t r = 0; r < topk; ++r) {
+            int32_t best = -1;
+            for (int32_t b = 0; b < max_blocks; ++b) {
+                if (!(bs[b] > -INFINITY))
+                    continue;
+                int taken = 0;
+                for (int32_t u = 0; u < r; ++u)
+                    if (out[u] == b)
+                        taken = 1;
+                if (taken)
+                    continue;
+                if (best < 0 || bs[b] > bs[best])
+                    best = b;
+            }
+            out[r] = best;
+        }
+    }
+    free(q);
+    free(k);
+    return 0;
+}

@@ -412,3 +412,87 @@ def subset(w: Workload, idx) -> Workload:
     return Workload(w.name + f"[{len(idx)}]", w.shape, np.ascontiguousarray(w.qkv[idx]),
                     w.row_stride, w.positions[idx].copy(), w.slot_mapping[idx].copy(),
                     w.page_table, w.weights, w.scales, w.caches, w.pools, w.seed, meta)
+
+
+# ----------------------------------------------------------------------------
+# indexer inputs: queries over an index-K cache holding each sequence's history
+# ----------------------------------------------------------------------------
+
+@dataclass
+class IndexerWorkload:
+    name: str
+    idx_q: np.ndarray          # uint16 (bf16 bits) [T, H, D]
+    kv_len: np.ndarray         # int32 [T]: visible tokens of each query
+    table_offset: np.ndarray   # int64 [T]: start of the query's row in the flattened table
+    page_table: np.ndarray     # int32 [S, max_pages]
+    cache: CacheSpec           # one head
+    pool_bytes: int
+    pool_fill: np.ndarray      # uint8 pool contents (the history)
+    k_scale: float
+    page_size: int
+    block_tokens: int
+    topk: int
+    max_blocks: int
+    seed: int = 0
+
+    def algorithmic_bytes(self) -> int:
+        """Bytes an indexer must move: each query's heads and visible index-K rows read,
+        one page-table entry per page, the block scores and top-k ids written."""
+        T, H, D = self.idx_q.shape
+        es = self.cache.elem_size()
+        read = T * H * D * 2 + int(self.kv_len.sum()) * D * es
+        read += int(np.ceil(self.kv_len / self.page_size).sum()) * 4 + T * (4 + 8)
+        write = T * (self.max_blocks * 4 + self.topk * 4)
+        return read + write
+
+
+def _random_cache_codes(rng, n, dtype):
+    if dtype == DTYPE_E4M3:
+        # every finite E4M3 code, the two NaN codes (0x7F, 0xFF) excluded
+        codes = rng.integers(0, 254, size=n, dtype=np.uint16).astype(np.uint8)
+        return np.where(codes >= 0x7F, codes + 1, codes).astype(np.uint8)
+    vals = _to_bf16_bits(rng.standard_normal(n // 2, dtype=np.float32))
+    return vals.view(np.uint8)
+
+
+def make_indexer_batch(name: str, seed: int, kv_lens, heads: int = 8, head_dim: int = 128,
+                       page_size: int = 64, block_tokens: int = 128, topk: int = 16,
+                       dtype: int = DTYPE_E4M3, k_scale: float = 0.05, page_pad_bytes: int = 0,
+                       extra_pages: int = 16, max_blocks=None) -> IndexerWorkload:
+    """One decode query per sequence; sequence s sees kv_lens[s] tokens of history
+    in pages given by a seeded permutation; the pool holds random finite codes."""
+    rng = np.random.default_rng(seed)
+    kv_lens = np.asarray(kv_lens, dtype=np.int64)
+    S = len(kv_lens)
+    pages_per_seq = np.maximum(1, -(-kv_lens // page_size))
+    max_pages = int(pages_per_seq.max())
+    num_pages = int(pages_per_seq.sum()) + extra_pages
+    perm = rng.permutation(num_pages).astype(np.int32)
+    pt = np.full((S, max_pages), -1, dtype=np.int32)
+    k = 0
+    for s in range(S):
+        n = int(pages_per_seq[s])
+        pt[s, :n] = perm[k:k + n]
+        k += n
+    cache = _hnd_cache("idx_k", dtype, num_pages, 1, page_size, head_dim, page_pad_bytes)
+    pool_bytes = _pool_sizes({"idx_k": cache}, page_size, head_dim)["idx_k"]
+    pool = _random_cache_codes(rng, pool_bytes, dtype)
+    idx_q = _normal_bf16(rng, (S, heads, head_dim))
+    if max_blocks is None:
+        max_blocks = int(max(1, -(-int(kv_lens.max()) // block_tokens)))
+    return IndexerWorkload(name, idx_q, kv_lens.astype(np.int32),
+                           (np.arange(S, dtype=np.int64) * max_pages), pt, cache, pool_bytes,
+                           pool, float(k_scale), page_size, block_tokens, topk, max_blocks, seed)
+
+
+def indexer_decode64(seed: int = 6000) -> IndexerWorkload:
+    """The decode-batch-64 layer's indexer: 64 queries, contexts U{1..9216}, 8 index
+    heads of dim 128, fp8 index-K cache, top-16 of 128-token blocks."""
+    rng = np.random.default_rng(seed)
+    return make_indexer_batch("indexer_decode_64", seed + 1, rng.integers(1, 9216 + 1, size=64))
+
+
+def indexer_cache_arg(w: IndexerWorkload, pool: np.ndarray) -> dict:
+    c = w.cache
+    return dict(data=pool, offset=c.offset, dtype=c.dtype, num_pages=c.num_pages, num_heads=1,
+                stride_page=c.stride_page, stride_head=c.stride_head, stride_token=c.stride_token)

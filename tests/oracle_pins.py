@@ -398,4 +398,138 @@ def pin_producer_config1():
     _check_producer(wl.config1_tiny_decode())
 
 
+
+
+# ---------------------------------------------------------------------------
+# indexer
+# ---------------------------------------------------------------------------
+
+def _indexer_reference(w, pool):
+    """Float64 composition from library pieces: dequantise the pool with torch's
+    float8/bfloat16 views, gather each query's visible rows through the table,
+    matrix-multiply with numpy, max over heads, np.maximum.at per block, and a
+    stable lexsort for the ranking."""
+    T, H, D = w.idx_q.shape
+    c, P, BT = w.cache, w.page_size, w.block_tokens
+    q = bf16_bits_to_f32(w.idx_q).astype(np.float64)
+    base = torch.from_numpy(pool[c.offset:])
+    if c.dtype == wl.DTYPE_E4M3:
+        flat = base.view(torch.float8_e4m3fn).to(torch.float64).numpy() * np.float64(np.float32(w.k_scale))
+    else:
+        n = (base.numel() // 2) * 2
+        flat = base[:n].view(torch.bfloat16).to(torch.float64).numpy()
+    pt = w.page_table.reshape(-1)
+    scores = np.full((T, w.max_blocks), -np.inf)
+    for t in range(T):
+        L = int(w.kv_len[t])
+        j = np.arange(L)
+        j = j[j // BT < w.max_blocks]
+        ti = int(w.table_offset[t]) + j // P
+        ok = (ti >= 0) & (ti < pt.size)
+        j, ti = j[ok], ti[ok]
+        page = pt[ti].astype(np.int64)
+        ok = (page >= 0) & (page < c.num_pages)
+        j, page = j[ok], page[ok]
+        if j.size == 0:
+            continue
+        e = page * c.stride_page + (j % P) * c.stride_token
+        kj = flat[e[:, None] + np.arange(D)[None, :]]
+        tok = (q[t] @ kj.T).max(axis=0)
+        np.maximum.at(scores[t], j // BT, tok)
+    top = np.full((T, w.topk), -1, dtype=np.int64)
+    for t in range(T):
+        finite = np.nonzero(np.isfinite(scores[t]))[0]
+        order = finite[np.lexsort((finite, -scores[t][finite]))]
+        top[t, :min(w.topk, order.size)] = order[:w.topk]
+    return scores, top
+
+
+def _run_indexer_oracle(w, pool=None):
+    pool = w.pool_fill if pool is None else pool
+    return oracle.indexer(w.idx_q, w.kv_len, w.table_offset, w.page_table,
+                          wl.indexer_cache_arg(w, pool), w.k_scale, w.page_size, w.block_tokens,
+                          w.topk, w.max_blocks)
+
+
+def check_indexer_against_reference(w, s, top, ref_s, ref_top):
+    """Scores within fp32 accumulation error of the float64 reference; the ranking
+    equal wherever the reference separates neighbours by more than that error."""
+    fin = np.isfinite(ref_s)
+    assert np.array_equal(np.isfinite(s), fin)
+    tol = 1e-5 * (np.abs(ref_s[fin]).max(initial=1.0) + 1.0)
+    assert np.abs(s[fin] - ref_s[fin]).max(initial=0.0) <= tol
+    for t in range(s.shape[0]):
+        for r in range(w.topk):
+            a, b = int(top[t, r]), int(ref_top[t, r])
+            if a == b:
+                continue
+            assert a >= 0 and b >= 0, (t, r, a, b)
+            assert abs(ref_s[t, a] - ref_s[t, b]) <= 2 * tol, (t, r, a, b)
+
+
+def pin_indexer_hand_worked():
+    """H = 2 heads, D = 2, q = identity rows; bf16 cache of 2-token pages with the
+    table [1, 0]; rows j0 = (3, -1), j1 = (-2, 5), j2 = (0.5, 0.5).  Token scores
+    (max over heads) 3, 5, 0.5; 2-token blocks: block 0 = 5, block 1 = 0.5; top-3
+    = [0, 1, -1]."""
+    P, D = 2, 2
+    rows = np.array([[0.5, 0.5], [0.0, 0.0], [3.0, -1.0], [-2.0, 5.0]], dtype=np.float32)
+    pool = _torch_bf16(rows.reshape(-1)).view(np.uint8).copy()
+    w = wl.IndexerWorkload("hand", _torch_bf16(np.array([[[1, 0], [0, 1]]], dtype=np.float32)),
+                           np.array([3], dtype=np.int32), np.array([0], dtype=np.int64),
+                           np.array([[1, 0]], dtype=np.int32),
+                           wl.CacheSpec("idx_k", 0, wl.DTYPE_BF16, 2, 1, P * D, P * D, D),
+                           pool.size, pool, 1.0, P, 2, 3, 3)
+    s, top = _run_indexer_oracle(w)
+    assert np.array_equal(s[0, :2], np.array([5.0, 0.5], dtype=np.float32)) and s[0, 2] == -np.inf
+    assert top[0].tolist() == [0, 1, -1]
+
+
+def pin_indexer_vs_reference():
+    for dtype, D in ((wl.DTYPE_E4M3, 128), (wl.DTYPE_BF16, 64)):
+        w = wl.make_indexer_batch("pin", 31 + D, [1, 63, 64, 65, 127, 128, 129, 700, 2048], heads=4,
+                                  head_dim=D, dtype=dtype, topk=6)
+        pt = np.array(w.page_table, copy=True)
+        pt[7, 3] = -1                     # a hole: those tokens are skipped
+        w.page_table = pt
+        s, top = _run_indexer_oracle(w)
+        ref_s, ref_top = _indexer_reference(w, w.pool_fill)
+        check_indexer_against_reference(w, s, top, ref_s, ref_top)
+
+
+def pin_indexer_ties_and_empty():
+    w = wl.make_indexer_batch("ties", 41, [0, 256, 384], heads=2, head_dim=64,
+                              dtype=wl.DTYPE_BF16, topk=4)
+    pool = np.array(w.pool_fill, copy=True)
+    # make block 2 of query 2 an exact copy of its block 0 (same rows, other pages)
+    c = w.cache
+    pt = w.page_table
+    for j in range(128):
+        src = c.offset + 2 * (int(pt[2, j // 64]) * c.stride_page + (j % 64) * c.stride_token)
+        dst = c.offset + 2 * (int(pt[2, 4 + j // 64]) * c.stride_page + (j % 64) * c.stride_token)
+        pool[dst:dst + 128] = pool[src:src + 128]
+    s, top = _run_indexer_oracle(w, pool)
+    assert np.all(s[0] == -np.inf) and top[0].tolist() == [-1] * 4
+    assert s[2, 0] == s[2, 2]
+    r0, r2 = top[2].tolist().index(0), top[2].tolist().index(2)
+    assert r0 < r2 and (r2 == r0 + 1 or s[2, 1] == s[2, 0])
+    assert top[1, 2:].tolist() == [-1, -1]
+
+
+def pin_indexer_page_relabelling():
+    w = wl.make_indexer_batch("relabel", 43, [300, 1000], heads=8, head_dim=128, topk=8)
+    s0, t0 = _run_indexer_oracle(w)
+    rng = np.random.default_rng(5)
+    c = w.cache
+    perm = rng.permutation(c.num_pages)
+    pool = np.array(w.pool_fill, copy=True)
+    for old, new in enumerate(perm):
+        a = c.offset + old * c.stride_page
+        b = c.offset + int(new) * c.stride_page
+        pool[b:b + c.stride_page] = w.pool_fill[a:a + c.stride_page]
+    w.page_table = np.where(w.page_table >= 0, perm[np.maximum(w.page_table, 0)], -1).astype(np.int32)
+    s1, t1 = _run_indexer_oracle(w, pool)
+    assert np.array_equal(s0, s1) and np.array_equal(t0, t1)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -40,6 +40,12 @@ MUTANTS = {
                          "oracle_rmsnorm(x, w[0], D, sh->rms_eps, y);"),
     "stride_head_token_swapped": ("head * c->stride_head + off * c->stride_token",
                                   "head * c->stride_token + off * c->stride_head"),
+    "indexer_block_size": ("const int64_t b = j / block_tokens;", "const int64_t b = j / (block_tokens + 1);"),
+    "indexer_visibility": ("for (int64_t j = 0; j < L; ++j) {", "for (int64_t j = 0; j <= L; ++j) {"),
+    "indexer_ties_high": ("if (best < 0 || bs[b] > bs[best])", "if (best < 0 || bs[b] >= bs[best])"),
+    "indexer_scale_dropped": ("oracle_e4m3_decode(idx_k_cache->data[e + d]) * k_scale", "oracle_e4m3_decode(idx_k_cache->data[e + d])"),
+    "indexer_table_offset": ("const int64_t ti = table_offset[t] + j / P;", "const int64_t ti = j / P;"),
+    "indexer_sum_heads": ("                if (s > bs[b])\n                    bs[b] = s;", "                bs[b] = (bs[b] == -INFINITY ? 0.0f : bs[b]) + s;"),
 }
 
 
