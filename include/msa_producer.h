@@ -184,6 +184,60 @@ msa_status msa_producer_launch_shape(const msa_producer_cfg *cfg, int64_t num_to
                                      int32_t launch_flags, int32_t *grid, int32_t *block,
                                      int32_t *smem_bytes);
 
+/* ------------------------------------------------------------------------ */
+/* Indexer: the consumer of the index-K cache (decode)                      */
+/* ------------------------------------------------------------------------ */
+/*
+ * For each query token, scores the visible index-K history and selects the
+ * top-k blocks ("[None][perf] Fuse MiniMax-M3 MSA per-layer KV-cache writes into
+ * one kernel", the layer walk-through: proxy attention over index-K, max-reduce,
+ * select the top 16 of 128-token blocks; "[None][perf] Fuse MiniMax-M3 QKV and
+ * index projection", AFTER diagram: score visible index-K, max-pool scores by
+ * block, select top-k block ids).
+ *
+ *   token score   s_j = max over index heads h of idx_q[t,h,:] . k_j, where k_j is
+ *                 the index-K row of token j (FP8 codes times *k_scale, or bf16),
+ *                 for the visible tokens j < kv_len[t]; the page of token j is
+ *                 page_table[table_offset[t] + j / page_size]; a token whose table
+ *                 index or page falls outside the table or the cache is skipped.
+ *   block score   block_scores[t, b] = max of s_j over the tokens of block b
+ *                 (block_tokens tokens each), -inf when it has none; blocks at or
+ *                 beyond max_blocks are not scored.
+ *   top-k         topk_ids[t, :] = the ids of the topk highest finite block scores,
+ *                 highest first, ties to the lower id, padded with -1.
+ *
+ * A positive softmax scale would change neither a max nor the order, so none is
+ * applied.  Accumulation is fp32.  Two kernels are enqueued on `stream`; the
+ * library allocates nothing (block_scores is an output).
+ */
+typedef struct {
+    int32_t num_heads;     /* index-Q heads: 1..16 */
+    int32_t head_dim;      /* 64 or 128 */
+    int32_t page_size;     /* tokens per page of the index-K cache, > 0 */
+    int32_t block_tokens;  /* tokens per scored block: a multiple of 32, 32..1024 */
+    int32_t topk;          /* ids selected per query: 1..64 */
+    int32_t max_blocks;    /* columns of block_scores: 1..65536 */
+    int32_t reserved[2];   /* must be 0 */
+} msa_indexer_cfg;
+
+/*
+ * idx_q          device bf16 [num_queries, num_heads, head_dim], 16-byte aligned
+ *                (the compact index-Q the producer writes).
+ * kv_len         device int32 [num_queries]: visible tokens per query (< 0 as 0).
+ * table_offset   device int64 [num_queries]: start of the query's row in page_table.
+ * page_table     device int32 [page_table_len].
+ * idx_k_cache    one-head cache descriptor (the producer's index-K cache).
+ * k_scale        device fp32 [1]: dequantisation scale of an FP8 cache (NULL for bf16).
+ * block_scores   device fp32 [num_queries, max_blocks], written in full.
+ * topk_ids       device int32 [num_queries, topk].
+ * Errors as for msa_producer_forward; num_queries == 0 launches nothing.
+ */
+msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t num_queries, const void *idx_q,
+                               const int32_t *kv_len, const int64_t *table_offset,
+                               const int32_t *page_table, int64_t page_table_len,
+                               const msa_cache_desc *idx_k_cache, const float *k_scale,
+                               float *block_scores, int32_t *topk_ids, cudaStream_t stream);
+
 /*
  * Device address at which the GPU of the current device reaches host memory
  * `host_ptr` (pinned, mapped host memory; on Grace-Blackwell the GPU reads and

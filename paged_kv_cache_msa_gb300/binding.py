@@ -32,7 +32,8 @@ MSA_LAUNCH_PDL = 2
 
 # every function the header declares
 EXPORTED = ("msa_producer_forward", "msa_producer_validate", "msa_producer_launch_shape",
-            "msa_host_buffer_device_address", "msa_status_string", "msa_last_error_detail")
+            "msa_indexer_forward", "msa_host_buffer_device_address", "msa_status_string",
+            "msa_last_error_detail")
 
 
 class MsaError(RuntimeError):
@@ -71,6 +72,18 @@ class MsaProducerCfg(ctypes.Structure):
     ]
 
 
+class MsaIndexerCfg(ctypes.Structure):
+    _fields_ = [
+        ("num_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("block_tokens", ctypes.c_int32),
+        ("topk", ctypes.c_int32),
+        ("max_blocks", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 2),
+    ]
+
+
 _lib = None
 _lock = threading.Lock()
 
@@ -102,6 +115,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.msa_producer_launch_shape.argtypes = [cfgp, i64, i32, ctypes.POINTER(i32),
                                                 ctypes.POINTER(i32), ctypes.POINTER(i32)]
         L.msa_producer_launch_shape.restype = ctypes.c_int
+        L.msa_indexer_forward.argtypes = [ctypes.POINTER(MsaIndexerCfg), i64, vp, vp, vp, vp, i64,
+                                          cachep, vp, vp, vp, vp]
+        L.msa_indexer_forward.restype = ctypes.c_int
         L.msa_host_buffer_device_address.argtypes = [vp, ctypes.POINTER(ctypes.c_void_p)]
         L.msa_host_buffer_device_address.restype = ctypes.c_int
         L.msa_status_string.argtypes = [ctypes.c_int]
@@ -185,6 +201,29 @@ def msa_producer_validate(cfg, num_tokens, qkv, qkv_row_stride, positions, slot_
                                                k_norm_w, idx_q_norm_w, idx_k_norm_w, q_out,
                                                idx_q_out, k_cache, v_cache, idx_k_cache, scales,
                                                launch_flags))
+
+
+def make_indexer_cfg(num_heads, head_dim, page_size=64, block_tokens=128, topk=16,
+                     max_blocks=72) -> MsaIndexerCfg:
+    c = MsaIndexerCfg()
+    c.num_heads, c.head_dim, c.page_size = int(num_heads), int(head_dim), int(page_size)
+    c.block_tokens, c.topk, c.max_blocks = int(block_tokens), int(topk), int(max_blocks)
+    c.reserved[0] = c.reserved[1] = 0
+    return c
+
+
+def msa_indexer_forward(cfg, num_queries, idx_q, kv_len, table_offset, page_table,
+                        page_table_len, idx_k_cache, k_scale, block_scores, topk_ids, stream=0,
+                        check=True) -> int:
+    """The C entry point; pointers are integers or None.  Raises MsaError unless the
+    call returns MSA_OK (``check=False`` returns the status)."""
+    s = load().msa_indexer_forward(ctypes.byref(cfg) if cfg is not None else None,
+                                   int(num_queries), idx_q, kv_len, table_offset, page_table,
+                                   int(page_table_len), _ref(idx_k_cache), k_scale,
+                                   block_scores, topk_ids, stream)
+    if check and s != MSA_OK:
+        raise MsaError(s, "msa_indexer_forward", last_error_detail())
+    return s
 
 
 def msa_host_buffer_device_address(host_ptr: int):

@@ -12,7 +12,8 @@ import sys
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SOURCES = [os.path.join(PKG, "csrc", "msa_producer.cu")]
+SOURCES = [os.path.join(PKG, "csrc", "msa_producer.cu"), os.path.join(PKG, "csrc", "msa_indexer.cu")]
+HEADERS = [os.path.join(PKG, "csrc", "msa_internal.h")]
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "lib")
 LIB_NAME = "libmsa_producer.so"
@@ -36,6 +37,7 @@ def nvcc_command(out: str, verbose_ptxas: bool = False, extra=()) -> list:
     libdir = os.path.join(home, "lib64")
     cmd = [os.path.join(home, "bin", "nvcc"), "-O3", "-std=c++17", ARCH, "-lineinfo",
            "-Xcompiler", "-fPIC,-O2", "-shared", "-cudart", "shared", "-I", INCLUDE,
+           "-I", os.path.join(PKG, "csrc"),
            "-Xlinker", f"-rpath,{libdir}", "-o", out, *SOURCES, *extra]
     if verbose_ptxas:
         cmd.insert(1, "-Xptxas=-v")
@@ -52,7 +54,7 @@ def up_to_date(defines=()) -> bool:
         if f.read() != " ".join(defines):
             return False
     t = os.path.getmtime(LIB_PATH)
-    deps = SOURCES + [os.path.join(INCLUDE, "msa_producer.h"), os.path.abspath(__file__)]
+    deps = SOURCES + HEADERS + [os.path.join(INCLUDE, "msa_producer.h"), os.path.abspath(__file__)]
     return all(os.path.getmtime(d) <= t for d in deps)
 
 

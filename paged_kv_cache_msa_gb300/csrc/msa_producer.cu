@@ -36,6 +36,7 @@
 //     first group's metadata before waiting for the previous kernel.
 
 #include "msa_producer.h"
+#include "msa_internal.h"
 
 #include <cuda_runtime.h>
 
@@ -1000,3 +1001,15 @@ const char *msa_status_string(msa_status status)
 const char *msa_last_error_detail(void) { return g_detail; }
 
 }  // extern "C"
+
+// Shared with the indexer's translation unit (declared in msa_internal.h).
+void msa_internal_set_detail(const char *msg)
+{
+    snprintf(g_detail, sizeof g_detail, "%s", msg);
+}
+
+msa_status msa_internal_check_cache(const char *name, const msa_cache_desc *c, int64_t heads,
+                                    int32_t head_dim, int32_t page_size)
+{
+    return check_cache(name, c, heads, head_dim, page_size);
+}

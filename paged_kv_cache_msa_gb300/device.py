@@ -79,3 +79,36 @@ class DeviceWorkload:
 
     def pools_to_host(self):
         return {k: v.cpu().numpy() for k, v in self.pools.items()}
+
+
+class DeviceIndexer:
+    """Device copies of an indexer workload (queries, lengths, table, the index-K
+    history pool) and the C-ABI call on them."""
+
+    def __init__(self, w: wl.IndexerWorkload, device="cuda", pool=None):
+        import torch
+        self.w = w
+        self.device = torch.device(device)
+        T, H, D = w.idx_q.shape
+        self.cfg = B.make_indexer_cfg(H, D, w.page_size, w.block_tokens, w.topk, w.max_blocks)
+        self.idx_q = _t(w.idx_q, self.device)
+        self.kv_len = _t(w.kv_len, self.device)
+        self.table_offset = _t(w.table_offset, self.device)
+        self.page_table = _t(w.page_table.reshape(-1), self.device)
+        self.pool = _t(w.pool_fill if pool is None else pool, self.device)
+        self.k_scale = torch.tensor([w.k_scale], dtype=torch.float32, device=self.device)
+        self.block_scores = torch.empty((T, w.max_blocks), dtype=torch.float32, device=self.device)
+        self.topk_ids = torch.empty((T, w.topk), dtype=torch.int32, device=self.device)
+        c = w.cache
+        self.cache = B.make_cache(self.pool.data_ptr() + c.offset, c.dtype, c.num_pages, 1,
+                                  c.stride_page, c.stride_head, c.stride_token)
+
+    def run(self, stream=None):
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        p = lambda t: int(t.data_ptr())
+        return B.msa_indexer_forward(self.cfg, self.w.idx_q.shape[0], p(self.idx_q), p(self.kv_len),
+                                     p(self.table_offset), p(self.page_table),
+                                     self.page_table.numel(), self.cache, p(self.k_scale),
+                                     p(self.block_scores), p(self.topk_ids), stream.cuda_stream)

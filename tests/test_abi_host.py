@@ -229,3 +229,52 @@ def test_host_buffer_helper_rejects_null(lib):
     out = ctypes.c_void_p()
     assert lib.msa_host_buffer_device_address(None, ctypes.byref(out)) == B.MSA_ERR_INVALID_ARGUMENT
     assert lib.msa_host_buffer_device_address(ctypes.c_void_p(BASE), None) == B.MSA_ERR_INVALID_ARGUMENT
+
+
+# ---------------------------------------------------------------------------
+# the indexer's host checks
+# ---------------------------------------------------------------------------
+
+def good_indexer_call(**over):
+    cfg = B.make_indexer_cfg(8, 128, 64, 128, 16, 72)
+    cache = B.make_cache(BASE + 20 * 2**34, B.MSA_DTYPE_FP8_E4M3, 9216, 1, 64 * 128, 64 * 128, 128)
+    a = dict(cfg=cfg, num_queries=64, idx_q=BASE, kv_len=BASE + 2**32, table_offset=BASE + 2**33,
+             page_table=BASE + 3 * 2**32, page_table_len=9216, idx_k_cache=cache,
+             k_scale=BASE + 5 * 2**32, block_scores=BASE + 6 * 2**32, topk_ids=BASE + 7 * 2**32)
+    a.update(over)
+    return a
+
+
+def _icfg(**kw):
+    base = dict(num_heads=8, head_dim=128, page_size=64, block_tokens=128, topk=16, max_blocks=72)
+    base.update(kw)
+    return B.make_indexer_cfg(**base)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(num_queries=0, idx_q=None), B.MSA_OK),
+    (dict(cfg=None), B.MSA_ERR_INVALID_ARGUMENT),
+    (dict(num_queries=-1), B.MSA_ERR_INVALID_ARGUMENT),
+    (dict(idx_q=None), B.MSA_ERR_INVALID_ARGUMENT),
+    (dict(block_scores=None), B.MSA_ERR_INVALID_ARGUMENT),
+    (dict(k_scale=None), B.MSA_ERR_INVALID_ARGUMENT),
+    (dict(page_table_len=0), B.MSA_ERR_INVALID_ARGUMENT),
+    (dict(idx_q=BASE + 8), B.MSA_ERR_MISALIGNED),
+    (dict(table_offset=BASE + 2**33 + 4), B.MSA_ERR_MISALIGNED),
+    (dict(cfg=_icfg(num_heads=17)), B.MSA_ERR_UNSUPPORTED),
+    (dict(cfg=_icfg(head_dim=96)), B.MSA_ERR_UNSUPPORTED),
+    (dict(cfg=_icfg(block_tokens=100)), B.MSA_ERR_UNSUPPORTED),
+    (dict(cfg=_icfg(topk=0)), B.MSA_ERR_UNSUPPORTED),
+    (dict(cfg=_icfg(max_blocks=0)), B.MSA_ERR_UNSUPPORTED),
+    (dict(cfg=_icfg(page_size=0)), B.MSA_ERR_INVALID_ARGUMENT),
+    (dict(num_queries=2**30), B.MSA_ERR_UNSUPPORTED),
+    (dict(idx_k_cache=B.make_cache(BASE + 20 * 2**34, B.MSA_DTYPE_FP8_E4M3, 9216, 1, 64 * 128 + 8,
+                                   64 * 128, 128)), B.MSA_ERR_MISALIGNED),
+    (dict(idx_k_cache=B.make_cache(BASE + 20 * 2**34, B.MSA_DTYPE_FP8_E4M3, 9216, 2, 64 * 128,
+                                   64 * 128, 128)), B.MSA_ERR_INVALID_ARGUMENT),
+])
+def test_indexer_host_checks(lib, over, status):
+    a = good_indexer_call(**over)
+    # rejected calls (and an empty one) return before touching the GPU
+    got = B.msa_indexer_forward(**a, stream=0, check=False)
+    assert got == status, (B.status_string(got), B.last_error_detail())

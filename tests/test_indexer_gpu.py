@@ -1,0 +1,82 @@
+"""Parity of the CUDA indexer with the oracle, through the C ABI (GPU).
+
+Block scores: within fp32 accumulation error of the oracle (both fp32, different
+summation order), exact -inf pattern.  Top-k ids: equal to the oracle's wherever
+the oracle's ranking separates neighbours by more than that error; otherwise the
+two ids must be within it of each other (either order is a correct answer)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_msa_gb300 import build as build_mod
+from paged_kv_cache_msa_gb300 import workloads as wl
+from paged_kv_cache_msa_gb300.device import DeviceIndexer
+
+from oracle_pins import check_indexer_against_reference
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(w, pool=None):
+    build_mod.build()
+    pool = w.pool_fill if pool is None else pool
+    ref_s, ref_top = oracle.indexer(w.idx_q, w.kv_len, w.table_offset, w.page_table,
+                                    wl.indexer_cache_arg(w, pool), w.k_scale, w.page_size,
+                                    w.block_tokens, w.topk, w.max_blocks)
+    dv = DeviceIndexer(w, pool=pool)
+    dv.run()
+    torch.cuda.synchronize()
+    s = dv.block_scores.cpu().numpy()
+    top = dv.topk_ids.cpu().numpy()
+    check_indexer_against_reference(w, s, top, ref_s.astype(np.float64), ref_top)
+    # the ids are a valid ranking of the kernel's own scores
+    for t in range(s.shape[0]):
+        ids = [i for i in top[t] if i >= 0]
+        assert len(set(ids)) == len(ids)
+        vals = [s[t, i] for i in ids]
+        assert all(vals[i] >= vals[i + 1] for i in range(len(vals) - 1))
+        nfin = int(np.isfinite(s[t]).sum())
+        assert len(ids) == min(w.topk, nfin)
+    return dv
+
+
+def test_indexer_decode64():
+    _check(wl.indexer_decode64())
+
+
+@pytest.mark.parametrize("dtype,D,heads", [(wl.DTYPE_E4M3, 64, 4), (wl.DTYPE_BF16, 128, 8),
+                                           (wl.DTYPE_BF16, 64, 16), (wl.DTYPE_E4M3, 128, 1)])
+def test_indexer_shapes_and_dtypes(dtype, D, heads):
+    lens = [0, 1, 31, 32, 127, 128, 129, 1000, 4096, 9216]
+    _check(wl.make_indexer_batch("shapes", 70 + D + heads, lens, heads=heads, head_dim=D,
+                                 dtype=dtype, topk=16))
+
+
+@pytest.mark.parametrize("bt,topk,P", [(32, 1, 16), (256, 64, 64), (1024, 5, 48)])
+def test_indexer_block_sizes_topk_and_pages(bt, topk, P):
+    _check(wl.make_indexer_batch("blocks", 90 + bt, [5, 300, 2000, 5000], block_tokens=bt,
+                                 topk=topk, page_size=P))
+
+
+def test_indexer_table_holes_and_padded_pages():
+    w = wl.make_indexer_batch("holes", 97, [700, 1500, 64], page_pad_bytes=256)
+    pt = np.array(w.page_table, copy=True)
+    pt[0, 2] = -1
+    pt[1, 5] = 10**6
+    w.page_table = pt
+    _check(w)
+
+
+def test_indexer_exact_ties_rank_lower_id_first():
+    w = wl.make_indexer_batch("ties", 98, [512], heads=2, head_dim=64, dtype=wl.DTYPE_BF16, topk=4)
+    pool = np.array(w.pool_fill, copy=True)
+    c, pt = w.cache, w.page_table
+    for j in range(128):       # block 3 := block 1, so their scores are identical
+        src = c.offset + 2 * (int(pt[0, (128 + j) // 64]) * c.stride_page + (j % 64) * c.stride_token)
+        dst = c.offset + 2 * (int(pt[0, (384 + j) // 64]) * c.stride_page + (j % 64) * c.stride_token)
+        pool[dst:dst + 128] = pool[src:src + 128]
+    dv = _check(w, pool)
+    s = dv.block_scores.cpu().numpy()[0]
+    top = dv.topk_ids.cpu().numpy()[0].tolist()
+    assert s[1] == s[3] and top.index(1) < top.index(3)
