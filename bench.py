@@ -537,6 +537,8 @@ def main():
     ap.add_argument("--no-decode-step", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--indexer-only", action="store_true",
+                    help="time only the decode-batch-64 indexer and print its JSON")
     ap.add_argument("--prefill-seqs", type=int, default=8,
                     help="sequences of 8,192 tokens in the prefill workload (8 = the full batch)")
     args = ap.parse_args()
@@ -545,6 +547,11 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.indexer_only:
+        from paged_kv_cache_msa_gb300 import build as build_mod
+        build_mod.build()
+        print(json.dumps(indexer_timing(replays=max(1, args.steps), calls=20)), flush=True)
+        return 0
     return run_ours(args)
 
 
