@@ -6,18 +6,21 @@
 // top-16 of 128-token blocks) and "[None][perf] Fuse MiniMax-M3 QKV and index
 // projection" (AFTER diagram: score visible index-K, max-pool by block, top-k).
 //
-// Design (decode): each query has only a handful of index heads, too few rows for
-// a tensor-core tile, and its visible history is read exactly once, so the work
-// is a bandwidth-bound scan on the CUDA cores.
-//   * Score kernel: one CTA of 128 threads per (query, block); a thread owns one
-//     token at a time, reads its index-K row with 16-byte loads (the 32 rows of a
-//     warp are one contiguous run of the page), converts FP8 pairs with
-//     cvt.rn.f16x2.e4m3x2, and dots them against every head with paired f32x2
-//     FMAs, the query's heads being broadcast from shared memory.  The token's
-//     score is the max over heads; the block's score the CTA-wide max.
-//   * Top-k kernel: one warp per query; round r picks, among the entries ranked
-//     strictly after round r-1's pick (score descending, id ascending), the best
-//     one by a warp-wide arg-max, so nothing is marked or sorted in place.
+// Design (decode): the score is a small dense contraction per query -- its
+// index heads against every visible index-K row -- and the history is read
+// exactly once, so the kernel aims at the HBM roofline with the contraction on
+// the tensor cores.
+//   * Score kernel: a CTA of 4 warps takes 4 consecutive blocks of one query, a
+//     warp one block; 8 tokens at a time it issues D/16 mma.sync m16n8k16 (heads
+//     as rows, tokens as columns, fp32 accumulation).  Each lane loads one
+//     contiguous quarter of its token's row with 16-byte loads; FP8 code pairs
+//     become f16x2 operands with one cvt.rn.f16x2.e4m3x2.  Token score = max over
+//     real heads; block score = max over visible tokens, times the FP8 scale.
+//   * Top-k kernel: a CTA per query, launched programmatically dependent on the
+//     score kernel.  Rows up to 1024 blocks are staged in shared memory and every
+//     finite entry counts the entries ranked before it (score descending, id
+//     ascending), all in parallel.  Longer rows take topk rounds of warp-wide
+//     arg-max over the entries ranked after the last pick.
 //   * No scratch memory: block_scores is an output of the call.
 
 #include "msa_internal.h"
@@ -31,11 +34,14 @@
 #include <cstdio>
 #include <cstring>
 
+// Groups of 8 tokens whose index-K rows a warp has in flight at once.
+#ifndef MSA_INDEX_GROUPS
+#define MSA_INDEX_GROUPS 4
+#endif
+
 namespace {
 
 constexpr int kMaxHeads = 16;
-constexpr int kScoreThreads = 128;
-constexpr int kTopkWarps = 4;
 
 struct IndexerParams {
     const uint16_t *idx_q;          // [T, H, D] bf16
@@ -70,133 +76,229 @@ __device__ __forceinline__ uint4 ldg16(const void *p)
     return v;
 }
 
-// two E4M3 codes (element 0 in the low byte) -> (element 0, element 1) in fp32
-__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t two_codes)
+// ---------------------------------------------------------------------------
+// block scores on the tensor cores
+// ---------------------------------------------------------------------------
+//
+// One warp scores one block: it walks the block's tokens 8 at a time and, per
+// group, computes the [16 heads x 8 tokens] dot products with D/16 mma.sync
+// m16n8k16 steps (fp32 accumulation).  Heads are the A rows (padded to 16 and
+// masked), tokens the B columns.  Because a dot product may visit the head
+// dimension in any order, step s of lane (g, i) takes dims 4s..4s+3 of the
+// lane's own contiguous quarter of the row (dims [i*D/4, (i+1)*D/4)): lane i
+// reads one contiguous D/4-element piece of token g's index-K row, and the same
+// permutation is applied to the query when its A fragments are built.
+//   FP8 cache:  two codes convert to one f16x2 operand (cvt.rn.f16x2.e4m3x2); the
+//               query is rounded to f16 (exact for |q| < 65504), f16 MMA.
+//   bf16 cache: the row's bf16 pairs are the operands as they are; bf16 MMA.
+// The token score is the max over the real heads of its column, the block score
+// the max over its visible tokens, times the FP8 scale.
+
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+                 "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+                 "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t f2_to_f16x2(float lo, float hi)
+{
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t f2_to_bf16x2(float lo, float hi)
+{
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
 {
     uint32_t h2;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)two_codes));
-    float lo, hi;
-    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
-        : "=f"(lo), "=f"(hi)
-        : "r"(h2));
-    return make_float2(lo, hi);
+    return h2;
 }
 
-__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t v)
-{
-    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
-}
+constexpr int kScoreWarps = 4;   // blocks per CTA (one per warp)
 
-// ---------------------------------------------------------------------------
-// block scores
-// ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(kScoreThreads) msa_index_score_kernel(const __grid_constant__ IndexerParams p)
+__global__ void __launch_bounds__(kScoreWarps * 32) msa_index_score_kernel(const __grid_constant__ IndexerParams p)
 {
-    __shared__ __align__(16) float s_q[kMaxHeads][D];
-    __shared__ float s_red[kScoreThreads / 32];
+    constexpr int KS = D / 16;          // mma k-steps
+    __shared__ __align__(16) float s_q[16][D];
 
-    const int64_t cta = blockIdx.x;
-    const int64_t t = cta / p.max_blocks;
-    const int b = (int)(cta % p.max_blocks);
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, i = lane & 3;
+    const int cpq = (p.max_blocks + kScoreWarps - 1) / kScoreWarps;   // CTAs per query
+    const int64_t t = (int64_t)blockIdx.x / cpq;
+    const int b = (int)((int64_t)blockIdx.x % cpq) * kScoreWarps + warp;
     const int H = p.heads;
-
     const int64_t L = p.kv_len[t] > 0 ? (int64_t)p.kv_len[t] : 0;
-    const int64_t j0 = (int64_t)b * p.block_tokens;
-    float *out = p.block_scores + t * p.max_blocks + b;
-    if (j0 >= L) {
-        if (tid == 0)
-            *out = -INFINITY;
+    const int64_t cta_j0 = (int64_t)((int64_t)blockIdx.x % cpq) * kScoreWarps * p.block_tokens;
+    if (cta_j0 >= L) {   // every block of this CTA is past the visible tokens
+        if (lane == 0 && b < p.max_blocks)
+            p.block_scores[t * p.max_blocks + b] = -INFINITY;
         return;
     }
-    for (int i = tid; i < H * D; i += kScoreThreads)
-        s_q[i / D][i % D] = __uint_as_float(((uint32_t)p.idx_q[t * (int64_t)H * D + i]) << 16);
-    __syncthreads();
-
-    const float scale = p.fp8 ? __ldg(p.k_scale) : 1.0f;
+    // This warp's block, and its page-table entries, one per lane, requested before
+    // the query (when the block spans at most 32 pages; otherwise each token looks
+    // its page up itself).
+    const int64_t j0 = (int64_t)b * p.block_tokens;
     const int64_t jend = L < j0 + p.block_tokens ? L : j0 + p.block_tokens;
     const int64_t tbase = p.table_offset[t];
-    float best = -INFINITY;
-    for (int64_t j = j0 + tid; j < jend; j += kScoreThreads) {
-        const int64_t ti = tbase + (p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size);
-        if (ti < 0 || ti >= p.page_table_len)
-            continue;
-        const int64_t page = __ldg(p.page_table + ti);
-        if (page < 0 || page >= p.num_pages)
-            continue;
-        const int64_t off = p.page_shift >= 0 ? (j & (p.page_size - 1)) : j % p.page_size;
-        const int64_t e = page * p.stride_page + off * p.stride_token;
+    const int64_t blk0 = p.page_shift >= 0 ? (j0 >> p.page_shift) : j0 / p.page_size;
+    const int64_t jlast = jend > j0 ? jend - 1 : j0;
+    const int64_t blk1 = p.page_shift >= 0 ? (jlast >> p.page_shift) : jlast / p.page_size;
+    const bool pages_in_lanes = blk1 - blk0 < 32;
+    int64_t lane_page = -1;
+    if (b < p.max_blocks && pages_in_lanes && blk0 + lane <= blk1) {
+        const int64_t ti = tbase + blk0 + lane;
+        if (ti >= 0 && ti < p.page_table_len)
+            lane_page = __ldg(p.page_table + ti);
+    }
 
-        float2 acc[kMaxHeads];
+    // the query's heads (rows >= H zero): one 16-byte load of 8 bf16 per chunk
+    constexpr int NCH = 16 * D / 8, CPT = (NCH + kScoreWarps * 32 - 1) / (kScoreWarps * 32);
+    uint4 qraw[CPT];
 #pragma unroll
-        for (int h = 0; h < kMaxHeads; ++h)
-            acc[h] = make_float2(0.0f, 0.0f);
-        if (p.fp8) {
-            const uint8_t *row = p.kdata + e;
-#pragma unroll 2
-            for (int c = 0; c < D / 16; ++c) {
-                const uint4 r = ldg16(row + 16 * c);
-                float2 k[8];
-                k[0] = e4m3x2_to_f2(r.x & 0xFFFF); k[1] = e4m3x2_to_f2(r.x >> 16);
-                k[2] = e4m3x2_to_f2(r.y & 0xFFFF); k[3] = e4m3x2_to_f2(r.y >> 16);
-                k[4] = e4m3x2_to_f2(r.z & 0xFFFF); k[5] = e4m3x2_to_f2(r.z >> 16);
-                k[6] = e4m3x2_to_f2(r.w & 0xFFFF); k[7] = e4m3x2_to_f2(r.w >> 16);
+    for (int u = 0; u < CPT; ++u) {
+        const int ch = tid + u * kScoreWarps * 32;
+        const int h = ch * 8 / D;
+        qraw[u] = (ch < NCH && h < H) ? ldg16(p.idx_q + (t * H + h) * D + (ch * 8) % D)
+                                      : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
-                for (int h = 0; h < kMaxHeads; ++h) {
-                    if (h < H) {
-                        const float4 *qv = reinterpret_cast<const float4 *>(&s_q[h][16 * c]);
+    for (int u = 0; u < CPT; ++u) {
+        const int ch = tid + u * kScoreWarps * 32;
+        if (ch < NCH) {
+            float *dst = &s_q[ch * 8 / D][(ch * 8) % D];
+            const uint32_t wv[4] = {qraw[u].x, qraw[u].y, qraw[u].z, qraw[u].w};
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const float4 qq = qv[u];
-                            acc[h] = __ffma2_rn(make_float2(qq.x, qq.y), k[2 * u], acc[h]);
-                            acc[h] = __ffma2_rn(make_float2(qq.z, qq.w), k[2 * u + 1], acc[h]);
-                        }
-                    }
-                }
-            }
-        } else {
-            const uint16_t *row = reinterpret_cast<const uint16_t *>(p.kdata) + e;
-#pragma unroll 2
-            for (int c = 0; c < D / 8; ++c) {
-                const uint4 r = ldg16(row + 8 * c);
-                const float2 k[4] = {bf16x2_to_f2(r.x), bf16x2_to_f2(r.y), bf16x2_to_f2(r.z),
-                                     bf16x2_to_f2(r.w)};
-#pragma unroll
-                for (int h = 0; h < kMaxHeads; ++h) {
-                    if (h < H) {
-                        const float4 *qv = reinterpret_cast<const float4 *>(&s_q[h][8 * c]);
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const float4 qq = qv[u];
-                            acc[h] = __ffma2_rn(make_float2(qq.x, qq.y), k[2 * u], acc[h]);
-                            acc[h] = __ffma2_rn(make_float2(qq.z, qq.w), k[2 * u + 1], acc[h]);
-                        }
-                    }
-                }
+            for (int k = 0; k < 4; ++k) {
+                dst[2 * k] = __uint_as_float(wv[k] << 16);
+                dst[2 * k + 1] = __uint_as_float(wv[k] & 0xFFFF0000u);
             }
         }
-        float s = -INFINITY;
-#pragma unroll
-        for (int h = 0; h < kMaxHeads; ++h)
-            if (h < H)
-                s = fmaxf(s, acc[h].x + acc[h].y);
-        best = fmaxf(best, s * scale);
     }
-
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, o));
-    if ((tid & 31) == 0)
-        s_red[tid >> 5] = best;
+    asm volatile("griddepcontrol.launch_dependents;" :::);
     __syncthreads();
-    if (tid == 0) {
-        float m = s_red[0];
+    if (b >= p.max_blocks)
+        return;
+
+    // A fragments: rows g and g+8, step s, dims i*D/4 + 4s + {0,1} and {2,3}
+    uint32_t afrag[KS][4];
 #pragma unroll
-        for (int w = 1; w < kScoreThreads / 32; ++w)
-            m = fmaxf(m, s_red[w]);
-        *out = m;
+    for (int st = 0; st < KS; ++st) {
+        const int d = i * (D / 4) + 4 * st;
+        const float *r0 = &s_q[g][d], *r1 = &s_q[g + 8][d];
+        if (p.fp8) {
+            afrag[st][0] = f2_to_f16x2(r0[0], r0[1]);
+            afrag[st][1] = f2_to_f16x2(r1[0], r1[1]);
+            afrag[st][2] = f2_to_f16x2(r0[2], r0[3]);
+            afrag[st][3] = f2_to_f16x2(r1[2], r1[3]);
+        } else {
+            afrag[st][0] = f2_to_bf16x2(r0[0], r0[1]);
+            afrag[st][1] = f2_to_bf16x2(r1[0], r1[1]);
+            afrag[st][2] = f2_to_bf16x2(r0[2], r0[3]);
+            afrag[st][3] = f2_to_bf16x2(r1[2], r1[3]);
+        }
     }
+    const bool row0_real = g < H, row1_real = g + 8 < H;
+    if (lane_page >= p.num_pages)
+        lane_page = -1;
+
+
+    constexpr int NG = MSA_INDEX_GROUPS;        // token groups whose rows are in flight together
+    constexpr int NW8 = (D / 4) / 16 > 0 ? (D / 4) / 16 : 1;   // 16-byte loads per lane, FP8
+    constexpr int NW16 = (D / 4) / 8;                           // 16-byte loads per lane, bf16
+    constexpr int NWL = NW8 > NW16 ? NW8 : NW16;
+    float best = -INFINITY;
+    for (int64_t jb = j0; jb < jend; jb += 8 * NG) {
+        uint4 w[NG][NWL];
+        bool okg[NG];
+#pragma unroll
+        for (int u = 0; u < NG; ++u) {
+            // this lane loads token g of group u; its columns are tokens 2i, 2i+1
+            const int64_t j = jb + 8 * u + g;
+            bool ok = j < jend;
+            int64_t page = -1;
+            if (ok) {
+                const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
+                if (!pages_in_lanes) {
+                    const int64_t ti = tbase + blk;
+                    if (ti >= 0 && ti < p.page_table_len) {
+                        const int64_t pg = __ldg(p.page_table + ti);
+                        page = (pg >= 0 && pg < p.num_pages) ? pg : -1;
+                    }
+                }
+                (void)blk;
+            }
+            if (pages_in_lanes) {
+                const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
+                const int src = (int)(blk - blk0) & 31;
+                const long long pg = __shfl_sync(0xffffffffu, (long long)lane_page, src);
+                page = ok ? pg : -1;
+            }
+            ok = ok && page >= 0;
+            okg[u] = ok;
+            const int64_t off = p.page_shift >= 0 ? (j & (p.page_size - 1)) : j % p.page_size;
+            const int64_t e = ok ? page * p.stride_page + off * p.stride_token : 0;
+            if (p.fp8) {
+#pragma unroll
+                for (int v = 0; v < NW8; ++v)
+                    w[u][v] = ok ? ldg16(p.kdata + e + i * (D / 4) + 16 * v) : make_uint4(0, 0, 0, 0);
+            } else {
+                const uint16_t *row = reinterpret_cast<const uint16_t *>(p.kdata) + e;
+#pragma unroll
+                for (int v = 0; v < NW16; ++v)
+                    w[u][v] = ok ? ldg16(row + i * (D / 4) + 8 * v) : make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < NG; ++u) {
+            float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const uint32_t *words = reinterpret_cast<const uint32_t *>(w[u]);
+            if (p.fp8) {
+#pragma unroll
+                for (int st = 0; st < KS; ++st)
+                    mma_f16(c, afrag[st], e4m3x2_to_f16x2(words[st] & 0xFFFF),
+                            e4m3x2_to_f16x2(words[st] >> 16));
+            } else {
+#pragma unroll
+                for (int st = 0; st < KS; ++st)
+                    mma_bf16(c, afrag[st], words[2 * st], words[2 * st + 1]);
+            }
+            // columns 2i, 2i+1: max over the real heads (rows g, g+8 across lane groups)
+            float m0 = fmaxf(row0_real ? c[0] : -INFINITY, row1_real ? c[2] : -INFINITY);
+            float m1 = fmaxf(row0_real ? c[1] : -INFINITY, row1_real ? c[3] : -INFINITY);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+                m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+            }
+            // a column counts only if its token was loaded (lane 8i loaded token 2i)
+            const bool ok0 = __shfl_sync(0xffffffffu, okg[u], 8 * i);
+            const bool ok1 = __shfl_sync(0xffffffffu, okg[u], 8 * i + 4);
+            float m = fmaxf(ok0 ? m0 : -INFINITY, ok1 ? m1 : -INFINITY);
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            best = fmaxf(best, m);
+        }
+    }
+    if (lane == 0)
+        p.block_scores[t * p.max_blocks + b] = best * (p.fp8 ? __ldg(p.k_scale) : 1.0f);
 }
 
 // ---------------------------------------------------------------------------
@@ -208,26 +310,79 @@ __device__ __forceinline__ bool ranks_before(float a, int ia, float b, int ib)
     return a > b || (a == b && ia < ib);
 }
 
-__global__ void __launch_bounds__(kTopkWarps * 32) msa_index_topk_kernel(const __grid_constant__ IndexerParams p)
+constexpr int kTopkThreads = 128;
+constexpr int kRankMaxBlocks = 1024;   // rows up to this many blocks are ranked in shared memory
+
+// One CTA per query.  Short rows: the row is staged in shared memory and every
+// finite entry counts the entries ranked before it (all threads in parallel);
+// entries with rank < topk write their id at that rank.  Long rows: warp 0 takes
+// topk rounds, each an arg-max over the entries ranked after the previous pick.
+// Under programmatic dependent launch the kernel waits for the score kernel
+// before reading its output.
+__global__ void __launch_bounds__(kTopkThreads) msa_index_topk_kernel(const __grid_constant__ IndexerParams p)
 {
-    const int lane = threadIdx.x & 31;
-    const int64_t t = (int64_t)blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
-    if (t >= p.num_queries)
-        return;  // uniform across the warp
-    const float *row = p.block_scores + t * p.max_blocks;
+    __shared__ __align__(16) float s_row[kRankMaxBlocks];
+    __shared__ int s_nfin;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int64_t t = blockIdx.x;
+    const int n = p.max_blocks;
     int32_t *out = p.topk_ids + t * p.topk;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const float *row = p.block_scores + t * n;
+
+    if (n <= kRankMaxBlocks) {
+        if (tid == 0)
+            s_nfin = 0;
+        __syncthreads();
+        int nfin = 0;
+        const int npad = (n + 3) & ~3;
+        for (int b = tid; b < npad; b += kTopkThreads) {
+            const float v = b < n ? row[b] : -INFINITY;
+            s_row[b] = v;
+            nfin += (v > -INFINITY) ? 1 : 0;   // NaN and -inf are not candidates
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            nfin += __shfl_xor_sync(0xffffffffu, nfin, o);
+        if (lane == 0)
+            atomicAdd(&s_nfin, nfin);
+        __syncthreads();
+        const float4 *r4 = reinterpret_cast<const float4 *>(s_row);
+        for (int b = tid; b < n; b += kTopkThreads) {
+            const float v = s_row[b];
+            if (!(v > -INFINITY))
+                continue;
+            int rank = 0;
+            for (int u4 = 0; u4 < npad / 4; ++u4) {
+                const float4 w = r4[u4];
+                const int u = 4 * u4;
+                rank += (w.x > v || (w.x == v && u < b)) ? 1 : 0;
+                rank += (w.y > v || (w.y == v && u + 1 < b)) ? 1 : 0;
+                rank += (w.z > v || (w.z == v && u + 2 < b)) ? 1 : 0;
+                rank += (w.w > v || (w.w == v && u + 3 < b)) ? 1 : 0;
+            }
+            if (rank < p.topk)
+                out[rank] = b;
+        }
+        for (int r = s_nfin + tid; r < p.topk; r += kTopkThreads)
+            out[r] = -1;
+        return;
+    }
+
+    if (tid >= 32)
+        return;
     float prev_s = INFINITY;
     int prev_i = -1;
     int r = 0;
     for (; r < p.topk; ++r) {
         float bs = -INFINITY;
         int bi = -1;
-        for (int b = lane; b < p.max_blocks; b += 32) {
+        for (int b = lane; b < n; b += 32) {
             const float v = row[b];
-            if (!(v > -INFINITY))      // -inf: no scored token; NaN: ignored
+            if (!(v > -INFINITY))
                 continue;
             if (!ranks_before(prev_s, prev_i, v, b))
-                continue;              // picked in an earlier round
+                continue;
             if (bi < 0 || ranks_before(v, b, bs, bi)) {
                 bs = v;
                 bi = b;
@@ -245,7 +400,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32) msa_index_topk_kernel(const _
         if (lane == 0)
             out[r] = bi;
         if (bi < 0)
-            break;                     // same on every lane after the butterfly
+            break;
         prev_s = bs;
         prev_i = bi;
     }
@@ -357,17 +512,28 @@ extern "C" msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t nu
     p.topk = cfg->topk;
     p.max_blocks = cfg->max_blocks;
 
-    const unsigned grid_a = (unsigned)(num_queries * cfg->max_blocks);
+    const int64_t cpq = (cfg->max_blocks + kScoreWarps - 1) / kScoreWarps;
+    const unsigned grid_a = (unsigned)(num_queries * cpq);
     if (cfg->head_dim == 128)
-        msa_index_score_kernel<128><<<grid_a, kScoreThreads, 0, stream>>>(p);
+        msa_index_score_kernel<128><<<grid_a, kScoreWarps * 32, 0, stream>>>(p);
     else
-        msa_index_score_kernel<64><<<grid_a, kScoreThreads, 0, stream>>>(p);
+        msa_index_score_kernel<64><<<grid_a, kScoreWarps * 32, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(MSA_ERR_CUDA, "score kernel launch failed: %s", cudaGetErrorString(e));
-    const unsigned grid_b = (unsigned)((num_queries + kTopkWarps - 1) / kTopkWarps);
-    msa_index_topk_kernel<<<grid_b, kTopkWarps * 32, 0, stream>>>(p);
-    e = cudaGetLastError();
+    // top-k: one CTA per query, launched programmatically dependent on the scores
+    cudaLaunchConfig_t lc;
+    memset(&lc, 0, sizeof lc);
+    lc.gridDim = dim3((unsigned)num_queries);
+    lc.blockDim = dim3(kTopkThreads);
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    void *args[] = {&p};
+    e = cudaLaunchKernelExC(&lc, reinterpret_cast<const void *>(&msa_index_topk_kernel), args);
     if (e != cudaSuccess)
         return fail(MSA_ERR_CUDA, "top-k kernel launch failed: %s", cudaGetErrorString(e));
     return MSA_OK;
