@@ -38,6 +38,10 @@
 #ifndef MSA_INDEX_GROUPS
 #define MSA_INDEX_GROUPS 4
 #endif
+// Resident 128-thread score CTAs per SM the register budget is sized for.
+#ifndef MSA_INDEX_MIN_CTAS
+#define MSA_INDEX_MIN_CTAS 4
+#endif
 
 namespace {
 
@@ -133,11 +137,12 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
 
 constexpr int kScoreWarps = 4;   // blocks per CTA (one per warp)
 
-template <int D>
-__global__ void __launch_bounds__(kScoreWarps * 32) msa_index_score_kernel(const __grid_constant__ IndexerParams p)
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kScoreWarps * 32, MSA_INDEX_MIN_CTAS) msa_index_score_kernel(const __grid_constant__ IndexerParams p)
 {
     constexpr int KS = D / 16;          // mma k-steps
     __shared__ __align__(16) float s_q[16][D];
+    __shared__ __align__(16) uint4 s_af[KS][32];   // A fragments of each k-step, per lane
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, i = lane & 3;
@@ -194,36 +199,36 @@ __global__ void __launch_bounds__(kScoreWarps * 32) msa_index_score_kernel(const
     }
     asm volatile("griddepcontrol.launch_dependents;" :::);
     __syncthreads();
-    if (b >= p.max_blocks)
-        return;
 
-    // A fragments: rows g and g+8, step s, dims i*D/4 + 4s + {0,1} and {2,3}
-    uint32_t afrag[KS][4];
-#pragma unroll
-    for (int st = 0; st < KS; ++st) {
+    // A fragments, built once per CTA: k-step st of lane (g, i) holds rows g and g+8
+    // at dims i*D/4 + 4st + {0,1} and {2,3}; warp w builds the steps st = w mod 4
+    for (int st = warp; st < KS; st += kScoreWarps) {
         const int d = i * (D / 4) + 4 * st;
         const float *r0 = &s_q[g][d], *r1 = &s_q[g + 8][d];
-        if (p.fp8) {
-            afrag[st][0] = f2_to_f16x2(r0[0], r0[1]);
-            afrag[st][1] = f2_to_f16x2(r1[0], r1[1]);
-            afrag[st][2] = f2_to_f16x2(r0[2], r0[3]);
-            afrag[st][3] = f2_to_f16x2(r1[2], r1[3]);
+        uint4 f;
+        if (FP8) {
+            f.x = f2_to_f16x2(r0[0], r0[1]);
+            f.y = f2_to_f16x2(r1[0], r1[1]);
+            f.z = f2_to_f16x2(r0[2], r0[3]);
+            f.w = f2_to_f16x2(r1[2], r1[3]);
         } else {
-            afrag[st][0] = f2_to_bf16x2(r0[0], r0[1]);
-            afrag[st][1] = f2_to_bf16x2(r1[0], r1[1]);
-            afrag[st][2] = f2_to_bf16x2(r0[2], r0[3]);
-            afrag[st][3] = f2_to_bf16x2(r1[2], r1[3]);
+            f.x = f2_to_bf16x2(r0[0], r0[1]);
+            f.y = f2_to_bf16x2(r1[0], r1[1]);
+            f.z = f2_to_bf16x2(r0[2], r0[3]);
+            f.w = f2_to_bf16x2(r1[2], r1[3]);
         }
+        s_af[st][lane] = f;
     }
+    __syncthreads();
+    if (b >= p.max_blocks)
+        return;
     const bool row0_real = g < H, row1_real = g + 8 < H;
     if (lane_page >= p.num_pages)
         lane_page = -1;
 
 
     constexpr int NG = MSA_INDEX_GROUPS;        // token groups whose rows are in flight together
-    constexpr int NW8 = (D / 4) / 16 > 0 ? (D / 4) / 16 : 1;   // 16-byte loads per lane, FP8
-    constexpr int NW16 = (D / 4) / 8;                           // 16-byte loads per lane, bf16
-    constexpr int NWL = NW8 > NW16 ? NW8 : NW16;
+    constexpr int NWL = FP8 ? (D / 4) / 16 : (D / 4) / 8;   // 16-byte loads per lane and token
     float best = -INFINITY;
     for (int64_t jb = j0; jb < jend; jb += 8 * NG) {
         uint4 w[NG][NWL];
@@ -255,14 +260,14 @@ __global__ void __launch_bounds__(kScoreWarps * 32) msa_index_score_kernel(const
             okg[u] = ok;
             const int64_t off = p.page_shift >= 0 ? (j & (p.page_size - 1)) : j % p.page_size;
             const int64_t e = ok ? page * p.stride_page + off * p.stride_token : 0;
-            if (p.fp8) {
+            if (FP8) {
 #pragma unroll
-                for (int v = 0; v < NW8; ++v)
+                for (int v = 0; v < NWL; ++v)
                     w[u][v] = ok ? ldg16(p.kdata + e + i * (D / 4) + 16 * v) : make_uint4(0, 0, 0, 0);
             } else {
                 const uint16_t *row = reinterpret_cast<const uint16_t *>(p.kdata) + e;
 #pragma unroll
-                for (int v = 0; v < NW16; ++v)
+                for (int v = 0; v < NWL; ++v)
                     w[u][v] = ok ? ldg16(row + i * (D / 4) + 8 * v) : make_uint4(0, 0, 0, 0);
             }
         }
@@ -270,15 +275,14 @@ __global__ void __launch_bounds__(kScoreWarps * 32) msa_index_score_kernel(const
         for (int u = 0; u < NG; ++u) {
             float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             const uint32_t *words = reinterpret_cast<const uint32_t *>(w[u]);
-            if (p.fp8) {
 #pragma unroll
-                for (int st = 0; st < KS; ++st)
-                    mma_f16(c, afrag[st], e4m3x2_to_f16x2(words[st] & 0xFFFF),
-                            e4m3x2_to_f16x2(words[st] >> 16));
-            } else {
-#pragma unroll
-                for (int st = 0; st < KS; ++st)
-                    mma_bf16(c, afrag[st], words[2 * st], words[2 * st + 1]);
+            for (int st = 0; st < KS; ++st) {
+                const uint4 f = s_af[st][lane];
+                const uint32_t a[4] = {f.x, f.y, f.z, f.w};
+                if (FP8)
+                    mma_f16(c, a, e4m3x2_to_f16x2(words[st] & 0xFFFF), e4m3x2_to_f16x2(words[st] >> 16));
+                else
+                    mma_bf16(c, a, words[2 * st], words[2 * st + 1]);
             }
             // columns 2i, 2i+1: max over the real heads (rows g, g+8 across lane groups)
             float m0 = fmaxf(row0_real ? c[0] : -INFINITY, row1_real ? c[2] : -INFINITY);
@@ -298,7 +302,7 @@ __global__ void __launch_bounds__(kScoreWarps * 32) msa_index_score_kernel(const
         }
     }
     if (lane == 0)
-        p.block_scores[t * p.max_blocks + b] = best * (p.fp8 ? __ldg(p.k_scale) : 1.0f);
+        p.block_scores[t * p.max_blocks + b] = best * (FP8 ? __ldg(p.k_scale) : 1.0f);
 }
 
 // ---------------------------------------------------------------------------
@@ -514,10 +518,14 @@ extern "C" msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t nu
 
     const int64_t cpq = (cfg->max_blocks + kScoreWarps - 1) / kScoreWarps;
     const unsigned grid_a = (unsigned)(num_queries * cpq);
-    if (cfg->head_dim == 128)
-        msa_index_score_kernel<128><<<grid_a, kScoreWarps * 32, 0, stream>>>(p);
+    if (cfg->head_dim == 128 && p.fp8)
+        msa_index_score_kernel<128, true><<<grid_a, kScoreWarps * 32, 0, stream>>>(p);
+    else if (cfg->head_dim == 128)
+        msa_index_score_kernel<128, false><<<grid_a, kScoreWarps * 32, 0, stream>>>(p);
+    else if (p.fp8)
+        msa_index_score_kernel<64, true><<<grid_a, kScoreWarps * 32, 0, stream>>>(p);
     else
-        msa_index_score_kernel<64><<<grid_a, kScoreWarps * 32, 0, stream>>>(p);
+        msa_index_score_kernel<64, false><<<grid_a, kScoreWarps * 32, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(MSA_ERR_CUDA, "score kernel launch failed: %s", cudaGetErrorString(e));
