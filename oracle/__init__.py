@@ -122,6 +122,9 @@ def load(path: str) -> ctypes.CDLL:
                                  ctypes.POINTER(OracleCache), ctypes.c_float, ctypes.c_int32,
                                  vp, vp]
     L.oracle_indexer.restype = ctypes.c_int
+    L.oracle_projection.argtypes = [ctypes.c_int64, ctypes.c_int64, vp, ctypes.c_int64,
+                                    ctypes.c_int64, vp, ctypes.c_int64, vp, ctypes.c_int64]
+    L.oracle_projection.restype = ctypes.c_int
     return L
 
 
@@ -291,3 +294,22 @@ def indexer(idx_q: np.ndarray, kv_len: np.ndarray, table_offset: np.ndarray, pag
     if rc != 0:
         raise ValueError("oracle rejected the indexer arguments")
     return scores, top
+
+
+def projection(hidden: np.ndarray, weight: np.ndarray) -> np.ndarray:
+    """The projection rows [T, W] (uint16, bf16 bits) of hidden [T, K] and the
+    output-major weight [W, K] (both uint16 bf16 bits; row strides may exceed K,
+    given as a wider array whose first K columns are used: pass a column slice)."""
+    assert hidden.dtype == np.uint16 and weight.dtype == np.uint16
+    assert hidden.ndim == 2 and weight.ndim == 2
+    T, K = hidden.shape
+    W, K2 = weight.shape
+    assert K == K2
+    assert hidden.strides[1] == 2 and weight.strides[1] == 2
+    rows = np.empty((T, W), dtype=np.uint16)
+    rc = lib().oracle_projection(T, K, hidden.ctypes.data, hidden.strides[0] // 2, W,
+                                 weight.ctypes.data, weight.strides[0] // 2,
+                                 rows.ctypes.data, W)
+    if rc != 0:
+        raise ValueError("oracle rejected the projection arguments")
+    return rows

@@ -462,3 +462,40 @@ int oracle_indexer(int32_t num_heads, int32_t head_dim, int32_t page_size, int32
     free(k);
     return 0;
 }
+
+/*
+ * The wide projection that feeds the producer ("[None][perf] Fuse MiniMax-M3 QKV
+ * and index projection", Description, AFTER diagram: hidden states -> one wider
+ * fused GEMM [Q | K | V | index-Q | index-K] -> one fused producer).
+ *
+ * rows[t, j] = bf16(fp32(sum_k hidden[t, k] * weight[j, k])) for j < width: the
+ * weight is stored output-major ([width, hidden_size], row j is the weights of
+ * output j), so that output j of token t is the dot product of two rows.  The sum
+ * is accumulated in double in index order (a product of two bf16 values is exact
+ * in double), rounded once to fp32 and then to bf16 with round-to-nearest-even:
+ * the bf16 row that a GEMM with an fp32 accumulator stores, up to the rounding
+ * of its own accumulation.
+ *
+ * Reading: the pages do not say whether the fused epilogue consumes the fp32
+ * accumulator or the bf16 row; the bf16 row is taken, so that projection and
+ * producer together equal the unfused GEMM followed by the producer.
+ */
+int oracle_projection(int64_t num_tokens, int64_t hidden_size, const uint16_t *hidden,
+                      int64_t hidden_stride, int64_t width, const uint16_t *weight,
+                      int64_t weight_stride, uint16_t *rows, int64_t row_stride)
+{
+    if (num_tokens < 0 || hidden_size < 0 || width < 0 || hidden_stride < hidden_size ||
+        weight_stride < hidden_size || row_stride < width)
+        return -1;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        const uint16_t *x = hidden + t * hidden_stride;
+        for (int64_t j = 0; j < width; ++j) {
+            const uint16_t *wrow = weight + j * weight_stride;
+            double acc = 0.0;
+            for (int64_t k = 0; k < hidden_size; ++k)
+                acc += (double)oracle_bf16_decode(x[k]) * (double)oracle_bf16_decode(wrow[k]);
+            rows[t * row_stride + j] = oracle_bf16_encode((float)acc);
+        }
+    }
+    return 0;
+}

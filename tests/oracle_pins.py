@@ -532,4 +532,94 @@ def pin_indexer_page_relabelling():
     assert np.array_equal(s0, s1) and np.array_equal(t0, t1)
 
 
+# ---------------------------------------------------------------------------
+# the projection that feeds the producer
+# ---------------------------------------------------------------------------
+
+_BF16_NAN = 0x7FC0
+
+
+def _round_significant(a: int, bits: int) -> int:
+    """The non-negative integer a rounded to ``bits`` significant bits, ties to even."""
+    shift = max(0, a.bit_length() - bits)
+    q, r = divmod(a, 1 << shift)
+    half = (1 << shift) >> 1
+    if shift and (r > half or (r == half and (q & 1))):
+        q += 1
+    return q << shift
+
+
+def _bf16_rne_of_int(n: int) -> int:
+    """bf16 bits of the integer n after rounding to fp32 (24 significant bits) and
+    then to bf16 (8 significant bits), each with ties to even, by integer
+    arithmetic alone."""
+    if n == 0:
+        return 0
+    sign = 0x8000 if n < 0 else 0
+    v = _round_significant(_round_significant(abs(n), 24), 8)
+    e = v.bit_length() - 1
+    mant = (v >> (e - 7)) if e >= 7 else (v << (7 - e))
+    return sign | ((e + 127) << 7) | (mant & 0x7F)
+
+
+def _int_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Exact bf16 bits of small integers (|a| <= 256)."""
+    out = np.array([_bf16_rne_of_int(int(v)) for v in a.reshape(-1)], dtype=np.uint16)
+    assert all(bf16_bits_to_f32(np.array([b], dtype=np.uint16))[0] == float(v)
+               for b, v in zip(out, a.reshape(-1)))
+    return out.reshape(a.shape)
+
+
+def _padded(bits: np.ndarray, pad: int) -> np.ndarray:
+    """The same matrix inside a wider one whose extra columns hold NaN."""
+    out = np.full((bits.shape[0], bits.shape[1] + pad), _BF16_NAN, dtype=np.uint16)
+    out[:, :bits.shape[1]] = bits
+    return out[:, :bits.shape[1]]
+
+
+def pin_projection_exact_integers():
+    """Small-integer operands: every dot product is an integer computed exactly in
+    int64, then rounded to bf16 by integer arithmetic.  Row strides wider than the
+    hidden size with NaN in the gap, magnitudes that force rounding, and a row whose
+    exact sum needs cancellation beyond fp32 (2^25 + 1 - 2^25 = 1)."""
+    rng = np.random.default_rng(71)
+    T, K, W = 7, 40, 24
+    h = rng.integers(-8, 9, size=(T, K))
+    w = rng.integers(-8, 9, size=(W, K))
+    w[5] = rng.integers(-128, 129, size=K)        # sums up to ~40k: rounded to 8 bits
+    h[3] = rng.integers(-128, 129, size=K)
+    w[0] = 1
+    h[6] = 0
+    hb = _int_to_bf16_bits(h)
+    wb = _int_to_bf16_bits(w)
+    # cancellation row: hidden [2^25, 1, -2^25, 0, ...]
+    hb[6, 0], hb[6, 1], hb[6, 2] = 0x4C00, 0x3F80, 0xCC00
+    h6 = np.zeros(K, dtype=object)
+    h6[0], h6[1], h6[2] = 2**25, 1, -(2**25)
+    exact = [[int(v) for v in row] for row in h.astype(np.int64) @ w.astype(np.int64).T]
+    exact[6] = [int(sum(int(a) * int(b) for a, b in zip(h6, w[j]))) for j in range(W)]
+    expect = np.array([[_bf16_rne_of_int(v) for v in row] for row in exact], dtype=np.uint16)
+    got = oracle.projection(_padded(hb, 8), _padded(wb, 16))
+    assert got[6, 0] == 0x3F80, "cancellation: the sum must be exact before rounding"
+    assert np.array_equal(got, expect), np.argwhere(got != expect)[:5]
+
+
+def pin_projection_signed_permutation():
+    """Weight rows that are signed unit vectors pick (and negate) single hidden
+    columns, so every output equals one input bit for bit: output j of token t is
+    sign_j * hidden[t, perm_j], which fixes which operand is indexed by what."""
+    rng = np.random.default_rng(72)
+    T, K, W = 5, 48, 64
+    x = rng.standard_normal((T, K)).astype(np.float32)
+    x[np.abs(x) < 1e-3] = 0.5
+    hb = np.asarray(torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy()).view(np.uint16)
+    perm = rng.integers(0, K, size=W)
+    sign = rng.choice([1, -1], size=W)
+    wb = np.zeros((W, K), dtype=np.uint16)
+    wb[np.arange(W), perm] = np.where(sign > 0, 0x3F80, 0xBF80)
+    got = oracle.projection(_padded(hb, 24), wb)
+    expect = hb[:, perm] ^ np.where(sign > 0, 0, 0x8000).astype(np.uint16)[None, :]
+    assert np.array_equal(got, expect)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]
