@@ -12,7 +12,7 @@ import sys
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SOURCES = [os.path.join(PKG, "csrc", "msa_producer.cu"), os.path.join(PKG, "csrc", "msa_indexer.cu")]
+SOURCES = [os.path.join(PKG, "csrc", n) for n in ("msa_producer.cu", "msa_indexer.cu", "msa_projection.cu")]
 HEADERS = [os.path.join(PKG, "csrc", "msa_internal.h")]
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "lib")
@@ -54,7 +54,8 @@ def up_to_date(defines=()) -> bool:
         if f.read() != " ".join(defines):
             return False
     t = os.path.getmtime(LIB_PATH)
-    deps = SOURCES + HEADERS + [os.path.join(INCLUDE, "msa_producer.h"), os.path.abspath(__file__)]
+    deps = SOURCES + HEADERS + [os.path.join(INCLUDE, h) for h in ("msa_producer.h", "msa_projection.h")]
+    deps.append(os.path.abspath(__file__))
     return all(os.path.getmtime(d) <= t for d in deps)
 
 

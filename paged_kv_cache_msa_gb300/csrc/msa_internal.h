@@ -10,3 +10,16 @@ void msa_internal_set_detail(const char *msg);
 // alignment, int64 extent, non-overlapping rows).
 msa_status msa_internal_check_cache(const char *name, const msa_cache_desc *c, int64_t heads,
                                     int32_t head_dim, int32_t page_size);
+
+// Every check of msa_producer_forward except those of the token rows (qkv, its
+// stride and the row-size limit of the producer's shared-memory ring), for entry
+// points that compute the rows themselves.  Sets the detail message.
+msa_status msa_internal_validate_producer(const msa_producer_cfg *cfg, int64_t num_tokens,
+                                          const int32_t *positions, const int64_t *slot_mapping,
+                                          const int32_t *page_table, int64_t page_table_len,
+                                          const void *q_norm_w, const void *k_norm_w,
+                                          const void *idx_q_norm_w, const void *idx_k_norm_w,
+                                          void *q_out, void *idx_q_out,
+                                          const msa_cache_desc *k_cache,
+                                          const msa_cache_desc *v_cache,
+                                          const msa_cache_desc *idx_k_cache, const float *scales);

@@ -628,12 +628,14 @@ msa_status check_cache(const char *name, const msa_cache_desc *c, int64_t heads,
     return MSA_OK;
 }
 
+// rows == false: everything except the token rows (qkv, its stride and the
+// shared-memory row limit), for callers that make the rows themselves.
 msa_status validate(const msa_producer_cfg *cfg, int64_t T, const void *qkv, int64_t row_stride,
                     const int32_t *positions, const int64_t *slots, const int32_t *page_table,
                     int64_t page_table_len, const void *wq, const void *wk, const void *wiq,
                     const void *wik, void *q_out, void *iq_out, const msa_cache_desc *kc,
                     const msa_cache_desc *vc, const msa_cache_desc *ikc, const float *scales,
-                    int32_t flags)
+                    int32_t flags, bool rows = true)
 {
     g_detail[0] = '\0';
     if (!cfg)
@@ -650,7 +652,7 @@ msa_status validate(const msa_producer_cfg *cfg, int64_t T, const void *qkv, int
         return fail(MSA_ERR_INVALID_ARGUMENT, "head_dim %d", D);
     if (D != 64 && D != 128)
         return fail(MSA_ERR_UNSUPPORTED, "head_dim %d (built: 64, 128)", D);
-    if (Htot * D * 2 > kMaxRowBytes)
+    if (rows && Htot * D * 2 > kMaxRowBytes)
         return fail(MSA_ERR_UNSUPPORTED, "a token row of %lld bytes is wider than %d",
                     (long long)(Htot * D * 2), kMaxRowBytes);
     if (cfg->rope_style != MSA_ROPE_NEOX && cfg->rope_style != MSA_ROPE_GPTJ)
@@ -681,17 +683,23 @@ msa_status validate(const msa_producer_cfg *cfg, int64_t T, const void *qkv, int
         return MSA_OK;
 
     const int64_t W = Htot * D;
-    if (!qkv || !positions || !slots)
-        return fail(MSA_ERR_INVALID_ARGUMENT, "qkv, positions and slot_mapping are required");
-    if (row_stride < W)
-        return fail(MSA_ERR_INVALID_ARGUMENT, "qkv_row_stride %lld < row width %lld",
-                    (long long)row_stride, (long long)W);
-    if (!aligned(qkv, 16) || row_stride % 8)
-        return fail(MSA_ERR_MISALIGNED, "qkv must be 16-byte aligned with a row stride of 8k elements");
+    if (!positions || !slots)
+        return fail(MSA_ERR_INVALID_ARGUMENT, "positions and slot_mapping are required");
+    int64_t tmp;
+    if (rows) {
+        if (!qkv)
+            return fail(MSA_ERR_INVALID_ARGUMENT, "qkv is required");
+        if (row_stride < W)
+            return fail(MSA_ERR_INVALID_ARGUMENT, "qkv_row_stride %lld < row width %lld",
+                        (long long)row_stride, (long long)W);
+        if (!aligned(qkv, 16) || row_stride % 8)
+            return fail(MSA_ERR_MISALIGNED, "qkv must be 16-byte aligned with a row stride of 8k elements");
+        if (!mul_add_ok(T - 1, row_stride, W, &tmp))
+            return fail(MSA_ERR_OFFSET_OVERFLOW, "token count times row size overflows int64");
+    }
     if (!aligned(positions, 4) || !aligned(slots, 8))
         return fail(MSA_ERR_MISALIGNED, "positions / slot_mapping misaligned");
-    int64_t tmp;
-    if (!mul_add_ok(T - 1, row_stride, W, &tmp) || !mul_add_ok(T, (int64_t)(Hq > Hiq ? Hq : Hiq) * D, 0, &tmp))
+    if (!mul_add_ok(T, (int64_t)(Hq > Hiq ? Hq : Hiq) * D, 0, &tmp))
         return fail(MSA_ERR_OFFSET_OVERFLOW, "token count times row size overflows int64");
     if (page_table) {
         if (page_table_len <= 0)
@@ -1006,6 +1014,21 @@ const char *msa_last_error_detail(void) { return g_detail; }
 void msa_internal_set_detail(const char *msg)
 {
     snprintf(g_detail, sizeof g_detail, "%s", msg);
+}
+
+msa_status msa_internal_validate_producer(const msa_producer_cfg *cfg, int64_t num_tokens,
+                                          const int32_t *positions, const int64_t *slot_mapping,
+                                          const int32_t *page_table, int64_t page_table_len,
+                                          const void *q_norm_w, const void *k_norm_w,
+                                          const void *idx_q_norm_w, const void *idx_k_norm_w,
+                                          void *q_out, void *idx_q_out,
+                                          const msa_cache_desc *k_cache,
+                                          const msa_cache_desc *v_cache,
+                                          const msa_cache_desc *idx_k_cache, const float *scales)
+{
+    return validate(cfg, num_tokens, nullptr, 0, positions, slot_mapping, page_table,
+                    page_table_len, q_norm_w, k_norm_w, idx_q_norm_w, idx_k_norm_w, q_out,
+                    idx_q_out, k_cache, v_cache, idx_k_cache, scales, 0, false);
 }
 
 msa_status msa_internal_check_cache(const char *name, const msa_cache_desc *c, int64_t heads,

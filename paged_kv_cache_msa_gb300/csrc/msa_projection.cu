@@ -1,0 +1,953 @@
+// The wide [Q | K | V | index-Q | index-K] projection on the tcgen05 tensor cores,
+// with the MSA producer in its epilogue ("[None][perf] Fuse MiniMax-M3 QKV and
+// index projection", Description, AFTER diagram: one wider fused GEMM feeding one
+// fused producer).  The producer's arithmetic is the one msa_producer_forward
+// applies to a row; only where the row comes from differs: here it is the fp32
+// accumulator of a 128-token x 256-output tile in tensor memory, rounded to bf16.
+//
+// Kernel structure (one persistent CTA per SM, 192 threads):
+//   warp 0      TMA producer: hidden and weight tiles of 64 elements of K into a
+//               4-stage shared-memory ring (128-byte swizzle, K-major)
+//   warp 1      tensor memory owner and MMA issuer: tcgen05.mma kind::f16,
+//               M = 128, N = 256, K = 16, fp32 accumulators in tensor memory,
+//               two accumulators (512 columns) so that the epilogue of one tile
+//               overlaps the main loop of the next
+//   warps 2..5  epilogue: thread r of the four warps owns token row r of the tile
+//               (tensor-memory lane r) and runs the producer on the tile's heads
+//
+// Tiles are visited output-group-major: for each group of n_group 256-wide output
+// tiles, every 128-token tile in order, so that the group's weight panels stay in
+// L2 while the hidden rows stream through once per group.
+//
+// Every mbarrier wait is bounded by %globaltimer; a wait that runs out sets
+// MSA_STATUS_WAIT_TIMEOUT in the caller's status word and the CTA winds down
+// (waiting, again bounded, for its own copies and MMAs in flight) and releases
+// its tensor memory.
+
+#include <cuda.h>  // CUtensorMap and its enums; the encoder is fetched at run time
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "msa_internal.h"
+#include "msa_producer.h"
+#include "msa_projection.h"
+
+#ifndef MSA_PROJ_NGROUP
+#define MSA_PROJ_NGROUP 16
+#endif
+
+namespace {
+
+constexpr int kBM = 128;                  // tokens per tile: tensor-memory lanes
+constexpr int kBN = 256;                  // projection outputs per tile: accumulator columns
+constexpr int kBK = 64;                   // K elements per stage: one 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kTileABytes = kBM * kBK * 2;
+constexpr uint32_t kTileBBytes = kBN * kBK * 2;
+constexpr uint32_t kStageBytes = kTileABytes + kTileBBytes;
+constexpr int kDynSmem = kStages * kStageBytes + 1024;  // + alignment slack for the ring
+constexpr uint32_t kTmemCols = 2 * kBN;
+constexpr int kMaxRotaryHalf = 64;
+constexpr int kMaxHeadScales = 256;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// tcgen05 instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
+// and B (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bit 17,
+// M >> 4 at bit 24.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
+                            ((uint32_t)(kBM >> 4) << 24);
+
+struct CacheArgs {
+    uint8_t *data;  // nullptr: not written
+    int64_t num_pages;
+    int64_t stride_page;
+    int64_t stride_head;
+    int64_t stride_token;
+    int32_t fp8;
+    int32_t pad;
+};
+
+struct Params {
+    const int32_t *positions;
+    const int64_t *slots;
+    const int32_t *page_table;
+    int64_t page_table_len;
+    const uint16_t *norm_w[4];  // q, k, idx_q, idx_k
+    uint16_t *q_out;
+    uint16_t *idx_q_out;
+    CacheArgs cache[3];         // k, v, idx_k
+    const float *scales;
+    uint16_t *rows_out;
+    int64_t rows_out_stride;
+    uint32_t *status;
+    int64_t num_tokens;
+    int32_t num_k_blocks;
+    int32_t m_tiles, n_tiles, n_group;
+    int32_t hq, hkv, hiq, hik, htot;
+    int32_t rotary_dim;
+    int32_t rope_style;
+    int32_t page_size;
+    int32_t page_shift;
+    int32_t scale_mode;
+    float rms_eps;
+    float inv_freq[kMaxRotaryHalf];
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// true once the phase with the given parity has completed; false after the limit
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try(bar, parity))
+            return true;
+        if ((n & 63) == 0 && globaltimer() - t0 > kWaitLimitNs)
+            return false;
+    }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes, groups of 8 rows 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    uint64_t d = (uint64_t)((saddr & 0x3FFFF) >> 4);  // start address
+    d |= (uint64_t)1 << 16;                           // leading byte offset (unused here)
+    d |= (uint64_t)(1024 >> 4) << 32;                 // stride byte offset
+    d |= (uint64_t)1 << 46;                           // descriptor version
+    d |= (uint64_t)2 << 61;                           // 128-byte swizzle
+    return d;
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
+        : "memory");
+}
+
+// the mbarrier arrives once every tcgen05.mma issued so far by this thread is done
+__device__ __forceinline__ void tc_commit(uint32_t bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 lanes x 32 bit, N consecutive columns per thread
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// number formats and stores
+// ---------------------------------------------------------------------------
+
+// (element 0, element 1) -> a bf16 pair, round to nearest even
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// four values -> four E4M3 bytes in element order; RNE, saturating to +-448
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d)
+{
+    unsigned short lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+    return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ void st_v4(void *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_v2(void *p, uint32_t a, uint32_t b)
+{
+    asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+
+// 8 accumulator words -> the bf16 row values (as bf16 pairs) and their fp32 values
+__device__ __forceinline__ void round_row8(const uint32_t (&acc)[8], uint32_t (&bits)[4], float (&x)[8])
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        bits[j] = pack_bf16x2(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1]));
+        x[2 * j] = bf16_lo(bits[j]);
+        x[2 * j + 1] = bf16_hi(bits[j]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// per-token placement (the rule of msa_producer_forward)
+// ---------------------------------------------------------------------------
+
+struct Place {
+    long long page;
+    int off;
+    int valid;  // bit c: cache c (k, v, idx_k) takes the token
+};
+
+__device__ __forceinline__ Place place_token(const Params &p, long long ls)
+{
+    Place m;
+    m.page = -1;
+    m.off = 0;
+    m.valid = 0;
+    if (ls < 0)
+        return m;
+    const long long blk = p.page_shift >= 0 ? (ls >> p.page_shift) : ls / p.page_size;
+    long long page = blk;
+    if (p.page_table)
+        page = blk < p.page_table_len ? (long long)__ldg(p.page_table + blk) : -1;
+    if (page < 0)
+        return m;
+    m.page = page;
+    m.off = p.page_shift >= 0 ? (int)(ls & (long long)(p.page_size - 1))
+                              : (int)(ls - blk * p.page_size);
+#pragma unroll
+    for (int ci = 0; ci < 3; ++ci)
+        if (p.cache[ci].data && page < p.cache[ci].num_pages)
+            m.valid |= 1 << ci;
+    return m;
+}
+
+// ---------------------------------------------------------------------------
+// the epilogue: one token row of one 128 x 256 tile
+// ---------------------------------------------------------------------------
+
+struct Head {
+    int sec;  // 0 Q, 1 K, 2 V, 3 idx-Q, 4 idx-K; -1 past the last head
+    int h;    // head index inside its section
+};
+
+__device__ __forceinline__ Head head_of(const Params &p, int g)
+{
+    const int e_k = p.hq, e_v = e_k + p.hkv, e_iq = e_v + p.hkv, e_ik = e_iq + p.hiq;
+    Head r;
+    if (g >= p.htot) { r.sec = -1; r.h = 0; }
+    else if (g < e_k) { r.sec = 0; r.h = g; }
+    else if (g < e_v) { r.sec = 1; r.h = g - e_k; }
+    else if (g < e_iq) { r.sec = 2; r.h = g - e_v; }
+    else if (g < e_ik) { r.sec = 3; r.h = g - e_iq; }
+    else { r.sec = 4; r.h = g - e_ik; }
+    return r;
+}
+
+// Stores 8 finished values of dims [d0, d0 + 8) of head hd for token t.
+template <int D>
+__device__ __forceinline__ void emit8(const Params &p, const Head &hd, int64_t t, bool live,
+                                      const Place &pl, int d0, const float (&y)[8])
+{
+    if (!live)
+        return;
+    if (hd.sec == 0 || hd.sec == 3) {
+        uint16_t *dst = hd.sec == 0 ? p.q_out + ((int64_t)t * p.hq + hd.h) * D
+                                    : p.idx_q_out + ((int64_t)t * p.hiq + hd.h) * D;
+        st_v4(dst + d0, pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+              pack_bf16x2(y[6], y[7]));
+        return;
+    }
+    const int ci = hd.sec == 1 ? 0 : hd.sec == 2 ? 1 : 2;
+    if (!((pl.valid >> ci) & 1))
+        return;
+    const CacheArgs &cc = p.cache[ci];
+    const int64_t e = pl.page * cc.stride_page + (int64_t)hd.h * cc.stride_head +
+                      (int64_t)pl.off * cc.stride_token + d0;
+    if (cc.fp8) {
+        const int si = p.scale_mode == MSA_SCALE_PER_HEAD
+                           ? (ci == 0 ? hd.h : ci == 1 ? p.hkv + hd.h : 2 * p.hkv + hd.h)
+                           : ci;
+        const float inv = __frcp_rn(__ldg(p.scales + si));
+        st_v2(cc.data + e, pack_e4m3x4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv),
+              pack_e4m3x4(y[4] * inv, y[5] * inv, y[6] * inv, y[7] * inv));
+    } else {
+        st_v4(reinterpret_cast<uint16_t *>(cc.data) + e, pack_bf16x2(y[0], y[1]),
+              pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+    }
+}
+
+// taddr: tensor-memory address of this warp's lanes at the tile's first column
+template <int D>
+__device__ __forceinline__ void epilogue_tile(const Params &p, const float (*s_w)[D],
+                                              uint32_t taddr, int n_tile, int64_t t, bool live)
+{
+    constexpr int HPT = kBN / D;  // heads per tile
+    const int g0 = n_tile * HPT;
+
+    // token metadata
+    int pos = 0;
+    Place pl;
+    pl.page = -1;
+    pl.off = 0;
+    pl.valid = 0;
+    if (live) {
+        pos = __ldg(p.positions + t);
+        pl = place_token(p, __ldg(p.slots + t));
+    }
+
+    // pass 1: bf16 row values, optional row store, and each head's norm factor
+    float rn[HPT];
+#pragma unroll
+    for (int hh = 0; hh < HPT; ++hh) {
+        rn[hh] = 0.0f;
+        if (g0 + hh >= p.htot)
+            continue;
+        float ss = 0.0f;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(taddr + (uint32_t)(hh * D + c), r);
+            tmem_wait_ld();
+            uint32_t bits[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                bits[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                const float a = bf16_lo(bits[j]), b = bf16_hi(bits[j]);
+                ss = fmaf(a, a, ss);
+                ss = fmaf(b, b, ss);
+            }
+            if (p.rows_out && live) {
+                uint16_t *dst = p.rows_out + (int64_t)t * p.rows_out_stride +
+                                (int64_t)(g0 + hh) * D + c;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    st_v4(dst + 8 * j, bits[4 * j], bits[4 * j + 1], bits[4 * j + 2], bits[4 * j + 3]);
+            }
+        }
+        rn[hh] = rsqrtf(fmaf(ss, 1.0f / (float)D, p.rms_eps));
+    }
+
+    Head hd[HPT];
+    bool normed_any = false;
+#pragma unroll
+    for (int hh = 0; hh < HPT; ++hh) {
+        hd[hh] = head_of(p, g0 + hh);
+        normed_any |= hd[hh].sec >= 0 && hd[hh].sec != 2;
+    }
+    const int rd = p.rotary_dim;
+
+    // pass 2a: normed heads (Q, K, idx-Q, idx-K)
+    if (normed_any) {
+        if (p.rope_style == MSA_ROPE_NEOX) {
+            const int half = rd / 2;
+            // rotated pairs (k, k + rd/2), 8 frequencies at a time
+            for (int k0 = 0; k0 < half; k0 += 8) {
+                float cs[8], sn[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    sincosf((float)pos * p.inv_freq[k0 + j], &sn[j], &cs[j]);
+#pragma unroll
+                for (int hh = 0; hh < HPT; ++hh) {
+                    if (hd[hh].sec < 0 || hd[hh].sec == 2)
+                        continue;
+                    const float *w = s_w[hd[hh].sec == 0 ? 0 : hd[hh].sec == 1 ? 1 : hd[hh].sec == 3 ? 2 : 3];
+                    uint32_t ru[8], rv[8], bu[4], bv[4];
+                    float u[8], v[8];
+                    tmem_ld8(taddr + (uint32_t)(hh * D + k0), ru);
+                    tmem_ld8(taddr + (uint32_t)(hh * D + k0 + half), rv);
+                    tmem_wait_ld();
+                    round_row8(ru, bu, u);
+                    round_row8(rv, bv, v);
+                    float yu[8], yv[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float a = (u[j] * rn[hh]) * w[k0 + j];
+                        const float b = (v[j] * rn[hh]) * w[k0 + half + j];
+                        yu[j] = fmaf(-b, sn[j], a * cs[j]);
+                        yv[j] = fmaf(a, sn[j], b * cs[j]);
+                    }
+                    emit8<D>(p, hd[hh], t, live, pl, k0, yu);
+                    emit8<D>(p, hd[hh], t, live, pl, k0 + half, yv);
+                }
+            }
+            // pass-through dims [rd, D)
+            for (int c = rd; c < D; c += 8) {
+#pragma unroll
+                for (int hh = 0; hh < HPT; ++hh) {
+                    if (hd[hh].sec < 0 || hd[hh].sec == 2)
+                        continue;
+                    const float *w = s_w[hd[hh].sec == 0 ? 0 : hd[hh].sec == 1 ? 1 : hd[hh].sec == 3 ? 2 : 3];
+                    uint32_t ru[8], bu[4];
+                    float u[8], y[8];
+                    tmem_ld8(taddr + (uint32_t)(hh * D + c), ru);
+                    tmem_wait_ld();
+                    round_row8(ru, bu, u);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        y[j] = (u[j] * rn[hh]) * w[c + j];
+                    emit8<D>(p, hd[hh], t, live, pl, c, y);
+                }
+            }
+        } else {
+            // GPT-J: pairs (2k, 2k + 1); a chunk of 8 dims is rotated whole or not at all
+            for (int c = 0; c < D; c += 8) {
+                const bool rot = c < rd;
+                float cs[4], sn[4];
+                if (rot) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        sincosf((float)pos * p.inv_freq[c / 2 + j], &sn[j], &cs[j]);
+                }
+#pragma unroll
+                for (int hh = 0; hh < HPT; ++hh) {
+                    if (hd[hh].sec < 0 || hd[hh].sec == 2)
+                        continue;
+                    const float *w = s_w[hd[hh].sec == 0 ? 0 : hd[hh].sec == 1 ? 1 : hd[hh].sec == 3 ? 2 : 3];
+                    uint32_t ru[8], bu[4];
+                    float u[8], y[8];
+                    tmem_ld8(taddr + (uint32_t)(hh * D + c), ru);
+                    tmem_wait_ld();
+                    round_row8(ru, bu, u);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        y[j] = (u[j] * rn[hh]) * w[c + j];
+                    if (rot) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float a = y[2 * j], b = y[2 * j + 1];
+                            y[2 * j] = fmaf(-b, sn[j], a * cs[j]);
+                            y[2 * j + 1] = fmaf(a, sn[j], b * cs[j]);
+                        }
+                    }
+                    emit8<D>(p, hd[hh], t, live, pl, c, y);
+                }
+            }
+        }
+    }
+
+    // pass 2b: V heads (no norm, no RoPE)
+#pragma unroll
+    for (int hh = 0; hh < HPT; ++hh) {
+        if (hd[hh].sec != 2)
+            continue;
+        for (int c = 0; c < D; c += 8) {
+            uint32_t ru[8], bu[4];
+            float u[8];
+            tmem_ld8(taddr + (uint32_t)(hh * D + c), ru);
+            tmem_wait_ld();
+            round_row8(ru, bu, u);
+            emit8<D>(p, hd[hh], t, live, pl, c, u);
+        }
+    }
+}
+
+__device__ __forceinline__ void tile_coords(const Params &p, int64_t tile, int &m, int &n)
+{
+    const int64_t per_group = (int64_t)p.n_group * p.m_tiles;
+    const int64_t g = tile / per_group;
+    const int64_t r = tile - g * per_group;
+    const int n0 = (int)g * p.n_group;
+    const int gn = min(p.n_group, p.n_tiles - n0);
+    m = (int)(r / gn);
+    n = n0 + (int)(r % gn);
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                      const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_full[kStages];
+    __shared__ __align__(8) uint64_t bar_empty[kStages];
+    __shared__ __align__(8) uint64_t bar_tfull[2];
+    __shared__ __align__(8) uint64_t bar_tempty[2];
+    __shared__ __align__(8) uint64_t bar_drain;
+    __shared__ uint32_t s_tmem;
+    __shared__ __align__(16) float s_w[4][D];
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t ring = (raw + 1023u) & ~1023u;  // the swizzle pattern needs 1024-byte alignment
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&bar_full[s]), 1);
+            mbar_init(smem_u32(&bar_empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bar_tfull[b]), 1);
+            mbar_init(smem_u32(&bar_tempty[b]), 4 * 32);
+        }
+        mbar_init(smem_u32(&bar_drain), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_x) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_w) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&s_tmem)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    for (int i = threadIdx.x; i < 4 * D; i += kThreads) {
+        const uint16_t *w = p.norm_w[i / D];
+        s_w[i / D][i % D] = w ? __uint_as_float((uint32_t)__ldg(w + i % D) << 16) : 1.0f;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    const int64_t num_tiles = (int64_t)p.m_tiles * p.n_tiles;
+    bool ok = true;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            int filled = 0;  // fills issued (for the wind-down after a timeout)
+            for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                int m, n;
+                tile_coords(p, tile, m, n);
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full = smem_u32(&bar_full[stage]);
+                    const uint32_t a = ring + stage * kStageBytes;
+                    mbar_expect_tx(full, kStageBytes);
+                    tma_load_2d(a, &tmap_x, kb * kBK, m * kBM, full);
+                    tma_load_2d(a + kTileABytes, &tmap_w, kb * kBK, n * kBN, full);
+                    ++filled;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                // the copies in flight land before the CTA may exit: wait for the
+                // last fill of every stage (bounded)
+                for (int j = 1; j <= kStages && j <= filled; ++j) {
+                    const int f = filled - j;  // fill index
+                    const int s = f % kStages;
+                    const uint32_t par = (uint32_t)((f / kStages) & 1);
+                    (void)mbar_wait(smem_u32(&bar_full[s]), par);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, acc_i = 0;
+            for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++acc_i) {
+                const uint32_t b = acc_i & 1, use_par = (acc_i >> 1) & 1;
+                if (!mbar_wait(smem_u32(&bar_tempty[b]), use_par ^ 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + b * kBN;
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!mbar_wait(smem_u32(&bar_full[stage]), phase)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a = ring + stage * kStageBytes;
+                    const uint32_t bb = a + kTileABytes;
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k)
+                        tc_mma(d_tmem, sw128_desc(a + 32u * k), sw128_desc(bb + 32u * k),
+                               (kb | k) != 0);
+                    tc_commit(smem_u32(&bar_empty[stage]));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok)
+                    break;
+                tc_commit(smem_u32(&bar_tfull[b]));
+            }
+            // every MMA of this CTA is complete before its tensor memory is released
+            tc_commit(smem_u32(&bar_drain));
+            if (!mbar_wait(smem_u32(&bar_drain), 0))
+                ok = false;
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue ----------------
+        const int quarter = warp & 3;  // the tensor-memory lanes this warp may read
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        uint32_t acc_i = 0;
+        for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++acc_i) {
+            int m, n;
+            tile_coords(p, tile, m, n);
+            const uint32_t b = acc_i & 1, use_par = (acc_i >> 1) & 1;
+            const bool got = mbar_wait(smem_u32(&bar_tfull[b]), use_par);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int64_t t = (int64_t)m * kBM + row;
+            epilogue_tile<D>(p, s_w, tmem + lane_base + b * kBN, n, t, t < p.num_tokens);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_tempty[b]));
+        }
+    }
+
+    if (!ok && p.status)
+        atomicOr(p.status, MSA_STATUS_WAIT_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+msa_status fail(msa_status s, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+msa_status fail(msa_status s, const char *fmt, ...)
+{
+    char buf[256];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    msa_internal_set_detail(buf);
+    return s;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::mutex g_mu;
+EncodeTiledFn g_encode = nullptr;
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+    int sms = 0;
+    bool configured[2] = {false, false};
+};
+DeviceInfo g_dev[kMaxDevices];
+
+EncodeTiledFn encoder()
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    return g_encode;
+}
+
+// A [rows, cols] bf16 matrix with a row stride of `stride` elements, read in boxes
+// of box_rows x 64 with the 128-byte swizzle; out-of-range elements read as zero.
+bool encode_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t stride,
+                int box_rows)
+{
+    EncodeTiledFn enc = encoder();
+    if (!enc)
+        return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)stride * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+void fill_cache(CacheArgs &a, const msa_cache_desc *c)
+{
+    memset(&a, 0, sizeof a);
+    if (!c)
+        return;
+    a.data = static_cast<uint8_t *>(c->data);
+    a.num_pages = c->num_pages;
+    a.stride_page = c->stride_page;
+    a.stride_head = c->stride_head;
+    a.stride_token = c->stride_token;
+    a.fp8 = c->dtype == MSA_DTYPE_FP8_E4M3;
+}
+
+msa_status validate(const msa_producer_cfg *cfg, int64_t num_tokens, const void *hidden,
+                    int64_t hidden_size, int64_t hidden_row_stride, const void *weight,
+                    int64_t weight_row_stride, const int32_t *positions,
+                    const int64_t *slot_mapping, const int32_t *page_table,
+                    int64_t page_table_len, const void *q_norm_w, const void *k_norm_w,
+                    const void *idx_q_norm_w, const void *idx_k_norm_w, void *q_out,
+                    void *idx_q_out, const msa_cache_desc *k_cache, const msa_cache_desc *v_cache,
+                    const msa_cache_desc *idx_k_cache, const float *scales, void *rows_out,
+                    int64_t rows_out_stride, uint32_t *status)
+{
+    msa_status s = msa_internal_validate_producer(
+        cfg, num_tokens, positions, slot_mapping, page_table, page_table_len, q_norm_w, k_norm_w,
+        idx_q_norm_w, idx_k_norm_w, q_out, idx_q_out, k_cache, v_cache, idx_k_cache, scales);
+    if (s != MSA_OK || num_tokens == 0)
+        return s;
+    const int64_t htot = (int64_t)cfg->num_q_heads + 2 * (int64_t)cfg->num_kv_heads +
+                         cfg->num_idx_q_heads + cfg->num_idx_k_heads;
+    const int64_t W = htot * cfg->head_dim;
+    if (num_tokens >= (int64_t)0x7fffffff - kBM)
+        return fail(MSA_ERR_UNSUPPORTED, "num_tokens %lld (limit 2^31 - 129)", (long long)num_tokens);
+    if (!hidden || !weight)
+        return fail(MSA_ERR_INVALID_ARGUMENT, "hidden and weight are required");
+    if (hidden_size < 1)
+        return fail(MSA_ERR_INVALID_ARGUMENT, "hidden_size %lld", (long long)hidden_size);
+    if (hidden_row_stride < hidden_size || weight_row_stride < hidden_size)
+        return fail(MSA_ERR_INVALID_ARGUMENT, "row strides must be at least hidden_size");
+    if (!aligned(hidden, 16) || !aligned(weight, 16) || hidden_row_stride % 8 ||
+        weight_row_stride % 8)
+        return fail(MSA_ERR_MISALIGNED,
+                    "hidden / weight must be 16-byte aligned with row strides of 8k elements");
+    if (hidden_size > ((int64_t)1 << 31) || W > ((int64_t)1 << 31) ||
+        hidden_row_stride > ((int64_t)1 << 36) || weight_row_stride > ((int64_t)1 << 36))
+        return fail(MSA_ERR_UNSUPPORTED, "hidden_size, width or row stride out of range");
+    if (rows_out) {
+        if (rows_out_stride < W)
+            return fail(MSA_ERR_INVALID_ARGUMENT, "rows_out_stride %lld < width %lld",
+                        (long long)rows_out_stride, (long long)W);
+        if (!aligned(rows_out, 16) || rows_out_stride % 8)
+            return fail(MSA_ERR_MISALIGNED, "rows_out must be 16-byte aligned, stride 8k elements");
+        int64_t tmp;
+        if (__builtin_mul_overflow(num_tokens, rows_out_stride, &tmp))
+            return fail(MSA_ERR_OFFSET_OVERFLOW, "rows_out extent overflows int64");
+    }
+    if (status && !aligned(status, 4))
+        return fail(MSA_ERR_MISALIGNED, "status misaligned");
+    return MSA_OK;
+}
+
+}  // namespace
+
+extern "C" msa_status msa_projection_validate(
+    const msa_producer_cfg *cfg, int64_t num_tokens, const void *hidden, int64_t hidden_size,
+    int64_t hidden_row_stride, const void *weight, int64_t weight_row_stride,
+    const int32_t *positions, const int64_t *slot_mapping, const int32_t *page_table,
+    int64_t page_table_len, const void *q_norm_w, const void *k_norm_w, const void *idx_q_norm_w,
+    const void *idx_k_norm_w, void *q_out, void *idx_q_out, const msa_cache_desc *k_cache,
+    const msa_cache_desc *v_cache, const msa_cache_desc *idx_k_cache, const float *scales,
+    void *rows_out, int64_t rows_out_stride, uint32_t *status)
+{
+    return validate(cfg, num_tokens, hidden, hidden_size, hidden_row_stride, weight,
+                    weight_row_stride, positions, slot_mapping, page_table, page_table_len,
+                    q_norm_w, k_norm_w, idx_q_norm_w, idx_k_norm_w, q_out, idx_q_out, k_cache,
+                    v_cache, idx_k_cache, scales, rows_out, rows_out_stride, status);
+}
+
+extern "C" msa_status msa_projection_forward(
+    const msa_producer_cfg *cfg, int64_t num_tokens, const void *hidden, int64_t hidden_size,
+    int64_t hidden_row_stride, const void *weight, int64_t weight_row_stride,
+    const int32_t *positions, const int64_t *slot_mapping, const int32_t *page_table,
+    int64_t page_table_len, const void *q_norm_w, const void *k_norm_w, const void *idx_q_norm_w,
+    const void *idx_k_norm_w, void *q_out, void *idx_q_out, const msa_cache_desc *k_cache,
+    const msa_cache_desc *v_cache, const msa_cache_desc *idx_k_cache, const float *scales,
+    void *rows_out, int64_t rows_out_stride, uint32_t *status, cudaStream_t stream)
+{
+    msa_status s = validate(cfg, num_tokens, hidden, hidden_size, hidden_row_stride, weight,
+                            weight_row_stride, positions, slot_mapping, page_table, page_table_len,
+                            q_norm_w, k_norm_w, idx_q_norm_w, idx_k_norm_w, q_out, idx_q_out,
+                            k_cache, v_cache, idx_k_cache, scales, rows_out, rows_out_stride, status);
+    if (s != MSA_OK || num_tokens == 0)
+        return s;
+    const int32_t D = cfg->head_dim;
+    const int64_t htot = (int64_t)cfg->num_q_heads + 2 * (int64_t)cfg->num_kv_heads +
+                         cfg->num_idx_q_heads + cfg->num_idx_k_heads;
+    const int64_t W = htot * D;
+
+    Params p;
+    memset(&p, 0, sizeof p);
+    p.positions = positions;
+    p.slots = slot_mapping;
+    p.page_table = page_table;
+    p.page_table_len = page_table ? page_table_len : 0;
+    p.norm_w[0] = static_cast<const uint16_t *>(q_norm_w);
+    p.norm_w[1] = static_cast<const uint16_t *>(k_norm_w);
+    p.norm_w[2] = static_cast<const uint16_t *>(idx_q_norm_w);
+    p.norm_w[3] = static_cast<const uint16_t *>(idx_k_norm_w);
+    p.q_out = static_cast<uint16_t *>(q_out);
+    p.idx_q_out = static_cast<uint16_t *>(idx_q_out);
+    fill_cache(p.cache[0], cfg->num_kv_heads > 0 ? k_cache : nullptr);
+    fill_cache(p.cache[1], cfg->num_kv_heads > 0 ? v_cache : nullptr);
+    fill_cache(p.cache[2], cfg->num_idx_k_heads > 0 ? idx_k_cache : nullptr);
+    p.scales = scales;
+    p.rows_out = static_cast<uint16_t *>(rows_out);
+    p.rows_out_stride = rows_out_stride;
+    p.status = status;
+    p.num_tokens = num_tokens;
+    p.num_k_blocks = (int32_t)((hidden_size + kBK - 1) / kBK);
+    p.m_tiles = (int32_t)((num_tokens + kBM - 1) / kBM);
+    p.n_tiles = (int32_t)((W + kBN - 1) / kBN);
+    p.n_group = p.n_tiles < MSA_PROJ_NGROUP ? p.n_tiles : MSA_PROJ_NGROUP;
+    p.hq = cfg->num_q_heads;
+    p.hkv = cfg->num_kv_heads;
+    p.hiq = cfg->num_idx_q_heads;
+    p.hik = cfg->num_idx_k_heads;
+    p.htot = (int32_t)htot;
+    p.rotary_dim = cfg->rotary_dim;
+    p.rope_style = cfg->rope_style;
+    p.page_size = cfg->page_size;
+    p.page_shift = -1;
+    for (int sh = 0; sh < 31; ++sh)
+        if ((1 << sh) == cfg->page_size)
+            p.page_shift = sh;
+    p.scale_mode = cfg->scale_mode;
+    p.rms_eps = cfg->rms_eps;
+    // RoPE frequencies theta^(-2k/rd), evaluated in double and rounded once
+    for (int k = 0; k < cfg->rotary_dim / 2; ++k)
+        p.inv_freq[k] = (float)(1.0 / std::pow((double)cfg->rope_theta,
+                                               2.0 * (double)k / (double)cfg->rotary_dim));
+
+    CUtensorMap mx, mw;
+    if (!encode_map(&mx, hidden, num_tokens, hidden_size, hidden_row_stride, kBM) ||
+        !encode_map(&mw, weight, W, hidden_size, weight_row_stride, kBN))
+        return fail(MSA_ERR_CUDA, "tensor map encoding failed");
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return fail(MSA_ERR_CUDA, "cudaGetDevice failed");
+    const void *fn = D == 128 ? reinterpret_cast<const void *>(&msa_projection_kernel<128>)
+                              : reinterpret_cast<const void *>(&msa_projection_kernel<64>);
+    const int vi = D == 128 ? 1 : 0;
+    int sms;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        sms = g_dev[dev].sms;
+        if (!g_dev[dev].configured[vi] || sms == 0) {
+            int major = 0;
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+                return fail(MSA_ERR_CUDA, "device query failed");
+            if (major != 10)
+                return fail(MSA_ERR_UNSUPPORTED, "tcgen05 tensor cores need compute capability 10.x");
+            if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem) !=
+                cudaSuccess)
+                return fail(MSA_ERR_CUDA, "cudaFuncSetAttribute failed");
+            g_dev[dev].sms = sms;
+            g_dev[dev].configured[vi] = true;
+        }
+    }
+    const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
+    const int grid = (int)(tiles < sms ? tiles : sms);
+    if (D == 128)
+        msa_projection_kernel<128><<<grid, kThreads, kDynSmem, stream>>>(mx, mw, p);
+    else
+        msa_projection_kernel<64><<<grid, kThreads, kDynSmem, stream>>>(mx, mw, p);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(MSA_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    msa_internal_set_detail("");
+    return MSA_OK;
+}

@@ -112,3 +112,49 @@ class DeviceIndexer:
                                      p(self.table_offset), p(self.page_table),
                                      self.page_table.numel(), self.cache, p(self.k_scale),
                                      p(self.block_scores), p(self.topk_ids), stream.cuda_stream)
+
+
+class DeviceProjection:
+    """Device copies of a projection workload: hidden states, the packed weight and,
+    through a ``DeviceWorkload`` of the producer part, everything the epilogue
+    writes; ``run`` calls msa_projection_forward on them."""
+
+    def __init__(self, pw: wl.ProjectionWorkload, device="cuda", pools_on_device: dict | None = None,
+                 rows_out: bool = False):
+        import torch
+        self.pw = pw
+        self.dw = DeviceWorkload(pw.producer, device, pools_on_device=pools_on_device)
+        self.device = self.dw.device
+        self.hidden = _t(pw.hidden, self.device)
+        self.weight = _t(pw.weight, self.device)
+        self.rows_out = (torch.zeros((pw.num_tokens, pw.width), dtype=torch.int16, device=self.device)
+                         if rows_out else None)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    @property
+    def pools(self):
+        return self.dw.pools
+
+    def args(self):
+        """Positional arguments of msa_projection_forward minus the stream."""
+        dw, pw = self.dw, self.pw
+        p = lambda t: None if t is None else int(t.data_ptr())
+        return (dw.cfg, pw.num_tokens, p(self.hidden), pw.hidden_size, pw.hidden.shape[1],
+                p(self.weight), pw.weight.shape[1], p(dw.positions), p(dw.slots), p(dw.page_table),
+                0 if dw.page_table is None else dw.page_table.numel(),
+                p(dw.weights.get("q")), p(dw.weights.get("k")), p(dw.weights.get("idx_q")),
+                p(dw.weights.get("idx_k")), p(dw.q_out), p(dw.idx_q_out), dw.caches["k"],
+                dw.caches["v"], dw.caches["idx_k"], p(dw.scales), p(self.rows_out),
+                0 if self.rows_out is None else pw.width, p(self.status))
+
+    def run(self, stream=None):
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        return B.msa_projection_forward(*self.args(), stream=stream.cuda_stream)
+
+    def outputs_to_host(self):
+        return self.dw.outputs_to_host()
+
+    def rows_to_host(self):
+        return self.rows_out.cpu().numpy().view(np.uint16)

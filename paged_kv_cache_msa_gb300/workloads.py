@@ -191,7 +191,7 @@ def make_batch(name: str, seed: int, heads: dict, seq_positions: list, max_block
                num_pages: int, *, rotary_dim=None, rope_style=ROPE_NEOX, page_size=64,
                row_pad=0, kv_dtype=DTYPE_E4M3, idx_k_dtype=DTYPE_E4M3, with_idx_k=True,
                page_pad_bytes=0, pad_frac=0.0, outlier_frac=0.0, use_page_table=True,
-               scale=0.05, scale_mode=0, shuffle_pages=True) -> Workload:
+               scale=0.05, scale_mode=0, shuffle_pages=True, make_rows=True) -> Workload:
     """A batch of sequences; ``seq_positions[s]`` lists the new tokens' positions of
     sequence s.  Logical slot = s * max_blocks * P + pos through a page table that
     is a seeded permutation of the pages, or, with ``use_page_table=False``, the
@@ -225,7 +225,10 @@ def make_batch(name: str, seed: int, heads: dict, seq_positions: list, max_block
     W = (heads["num_q_heads"] + 2 * heads["num_kv_heads"] + heads["num_idx_q_heads"]
          + heads["num_idx_k_heads"]) * D
     row_stride = W + row_pad
-    qkv = _normal_bf16(rng, (T, row_stride), outlier_frac=outlier_frac)
+    if make_rows:
+        qkv = _normal_bf16(rng, (T, row_stride), outlier_frac=outlier_frac)
+    else:   # the rows are made by a projection from hidden states instead
+        qkv = np.zeros((T, 0), dtype=np.uint16)
     weights = _weights(rng, D)
     nscales = 3 if scale_mode == 0 else 2 * heads["num_kv_heads"] + heads["num_idx_k_heads"]
     scales = np.full(nscales, scale, dtype=np.float32)
@@ -496,3 +499,88 @@ def indexer_cache_arg(w: IndexerWorkload, pool: np.ndarray) -> dict:
     c = w.cache
     return dict(data=pool, offset=c.offset, dtype=c.dtype, num_pages=c.num_pages, num_heads=1,
                 stride_page=c.stride_page, stride_head=c.stride_head, stride_token=c.stride_token)
+
+
+# ----------------------------------------------------------------------------
+# projection inputs: hidden states and the packed [Q | K | V | idx-Q | idx-K]
+# weight, for the projection with the producer in its epilogue
+# ----------------------------------------------------------------------------
+
+@dataclass
+class ProjectionWorkload:
+    """Hidden states and an output-major weight whose product is the producer's
+    rows; ``producer`` holds everything else (heads, positions, slots, page table,
+    norm weights, scales, caches) and has no rows of its own (qkv is [T, 0])."""
+    name: str
+    producer: Workload
+    hidden: np.ndarray         # uint16 (bf16 bits) [T, hidden_stride]
+    hidden_size: int
+    weight: np.ndarray         # uint16 (bf16 bits) [W, weight_stride]
+
+    @property
+    def num_tokens(self) -> int:
+        return self.producer.num_tokens
+
+    @property
+    def width(self) -> int:
+        return self.producer.width
+
+    def flops(self) -> int:
+        """Multiply-adds x 2 of the projection."""
+        return 2 * self.num_tokens * self.width * self.hidden_size
+
+    def with_rows(self, rows: np.ndarray) -> Workload:
+        """The producer workload with the given projection rows [T, W]."""
+        w = self.producer
+        return Workload(w.name, w.shape, np.ascontiguousarray(rows), rows.shape[1], w.positions,
+                        w.slot_mapping, w.page_table, w.weights, w.scales, w.caches, w.pools,
+                        w.seed, w.meta)
+
+
+def make_projection_batch(name: str, seed: int, heads: dict, seq_positions: list,
+                          hidden_size: int, *, hidden_pad: int = 0, weight_pad: int = 0,
+                          **batch_kw) -> ProjectionWorkload:
+    """Hidden states N(0, 1) and weights N(0, 1/hidden_size), both rounded to bf16, so
+    that the projection rows are about N(0, 1) like the producer's own inputs; the
+    rest from ``make_batch`` (same keyword arguments) without rows.  Row strides are
+    widened by ``hidden_pad`` / ``weight_pad`` elements (filled with NaN, which no
+    correct kernel reads)."""
+    w = make_batch(name, seed, heads, seq_positions, make_rows=False, **batch_kw)
+    rng = np.random.default_rng(seed + 7919)
+    T, W, K = w.num_tokens, w.width, int(hidden_size)
+    hidden = np.full((T, K + hidden_pad), 0x7FC0, dtype=np.uint16)
+    hidden[:, :K] = _normal_bf16(rng, (T, K))
+    weight = np.full((W, K + weight_pad), 0x7FC0, dtype=np.uint16)
+    for r0 in range(0, W, 2048):
+        r1 = min(W, r0 + 2048)
+        x = rng.standard_normal((r1 - r0, K), dtype=np.float32) * np.float32(1.0 / np.sqrt(K))
+        weight[r0:r1, :K] = _to_bf16_bits(x)
+    return ProjectionWorkload(name, w, hidden, K, weight)
+
+
+PROJECTION_HIDDEN = 6144
+
+
+def projection_prefill(seed: int = 7000, num_seqs: int = 8, seq_len: int = 8192,
+                       hidden_size: int = PROJECTION_HIDDEN) -> ProjectionWorkload:
+    """The prefill batch of the producer (8 sequences x 8192 tokens, big shapes,
+    1,024 shuffled pages, contiguous HND fp8 caches) made from hidden states of
+    size 6,144 through the packed 11,392-output projection."""
+    P = 64
+    max_blocks = seq_len // P
+    pos = [list(range(seq_len)) for _ in range(num_seqs)]
+    return make_projection_batch(f"projection_prefill_{num_seqs}x{seq_len}_h{hidden_size}", seed,
+                                 BIG, pos, hidden_size, max_blocks=max_blocks,
+                                 num_pages=num_seqs * max_blocks)
+
+
+def projection_decode(seed: int = 7100, batch: int = 64,
+                      hidden_size: int = PROJECTION_HIDDEN) -> ProjectionWorkload:
+    """Decode: ``batch`` sequences x 1 token with contexts U{1..9216}, big shapes,
+    9,216 shuffled pages padded by 256 bytes, 10% padded slots."""
+    rng = np.random.default_rng(seed)
+    L = rng.integers(1, 9216 + 1, size=batch)
+    pos = [[int(l) - 1] for l in L]
+    return make_projection_batch(f"projection_decode_{batch}_h{hidden_size}", seed + 1, BIG, pos,
+                                 hidden_size, max_blocks=144, num_pages=9216, page_pad_bytes=256,
+                                 pad_frac=0.10)

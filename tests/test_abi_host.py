@@ -24,10 +24,16 @@ def lib():
 
 
 def declared_functions():
-    with open(os.path.join(ROOT, "include", "msa_producer.h")) as f:
-        text = f.read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(msa_[a-z_]+)\s*\(", text)))
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for h in sorted(os.listdir(inc)):
+        if not h.endswith(".h"):
+            continue
+        with open(os.path.join(inc, h)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(msa_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_binding_surface():
@@ -278,3 +284,59 @@ def test_indexer_host_checks(lib, over, status):
     # rejected calls (and an empty one) return before touching the GPU
     got = B.msa_indexer_forward(**a, stream=0, check=False)
     assert got == status, (B.status_string(got), B.last_error_detail())
+
+
+# ---------------------------------------------------------------------------
+# the projection entry point: host-side checks
+# ---------------------------------------------------------------------------
+
+def good_projection(**over):
+    a = good_call()
+    for k in ("qkv", "qkv_row_stride", "launch_flags"):
+        a.pop(k)
+    a.update(hidden=BASE + 9 * 2**32, hidden_size=6144, hidden_row_stride=6144,
+             weight=BASE + 10 * 2**32, weight_row_stride=6144, rows_out=None, rows_out_stride=0,
+             status=BASE + 11 * 2**32)
+    a.update(over)
+    return a
+
+
+def test_projection_well_formed_calls_pass(lib):
+    assert B.msa_projection_validate(**good_projection()) == B.MSA_OK
+    assert B.msa_projection_validate(**good_projection(status=None)) == B.MSA_OK
+    assert B.msa_projection_validate(**good_projection(hidden_size=200, hidden_row_stride=208,
+                                                       weight_row_stride=200)) == B.MSA_OK
+    assert B.msa_projection_validate(**good_projection(rows_out=BASE + 12 * 2**32,
+                                                       rows_out_stride=89 * 128)) == B.MSA_OK
+
+
+def test_projection_zero_tokens_is_ok_without_launch(lib):
+    a = good_projection(num_tokens=0, hidden=None, weight=None, positions=None, slot_mapping=None)
+    assert B.msa_projection_validate(**a) == B.MSA_OK
+    assert B.msa_projection_forward(**a, stream=0, check=False) == B.MSA_OK
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(hidden=None), B.MSA_ERR_INVALID_ARGUMENT),
+    (dict(weight=None), B.MSA_ERR_INVALID_ARGUMENT),
+    (dict(hidden_size=0), B.MSA_ERR_INVALID_ARGUMENT),
+    (dict(hidden_row_stride=6136), B.MSA_ERR_INVALID_ARGUMENT),
+    (dict(weight_row_stride=6136), B.MSA_ERR_INVALID_ARGUMENT),
+    (dict(hidden=BASE + 9 * 2**32 + 8), B.MSA_ERR_MISALIGNED),
+    (dict(weight=BASE + 10 * 2**32 + 2), B.MSA_ERR_MISALIGNED),
+    (dict(hidden_row_stride=6148), B.MSA_ERR_MISALIGNED),
+    (dict(weight_row_stride=6150), B.MSA_ERR_MISALIGNED),
+    (dict(rows_out=BASE + 12 * 2**32, rows_out_stride=89 * 128 - 8), B.MSA_ERR_INVALID_ARGUMENT),
+    (dict(rows_out=BASE + 12 * 2**32 + 4, rows_out_stride=89 * 128), B.MSA_ERR_MISALIGNED),
+    (dict(status=BASE + 11 * 2**32 + 2), B.MSA_ERR_MISALIGNED),
+    (dict(num_tokens=2**31), B.MSA_ERR_UNSUPPORTED),
+    (dict(positions=None), B.MSA_ERR_INVALID_ARGUMENT),
+    (dict(q_out=None), B.MSA_ERR_INVALID_ARGUMENT),
+    (dict(k_cache=None), B.MSA_ERR_INVALID_ARGUMENT),
+    (dict(scales=None), B.MSA_ERR_INVALID_ARGUMENT),
+    (dict(cfg=_cfg(head_dim=96, rotary_dim=96)), B.MSA_ERR_UNSUPPORTED),
+])
+def test_projection_malformed_call_is_rejected(lib, over, status):
+    a = good_projection(**over)
+    assert B.msa_projection_validate(**a) == status, B.last_error_detail()
+    assert B.msa_projection_forward(**a, stream=0, check=False) == status
