@@ -10,6 +10,9 @@ is needed between steps.
 
 Also reported: the 60-layer decode step at batch 256 (tiny shapes, one launch per
 layer, all 60 captured in one CUDA graph; microseconds per layer and per step),
+the decode indexer, the projection GEMM with the producer in its epilogue
+(hidden 6,144 -> 11,392 outputs on the tcgen05 tensor cores, against the measured
+cuBLAS bf16 peak and against cuBLAS GEMM + producer),
 an end-to-end figure through the same C-ABI call with pinned host buffers and the
 host<->device copies inside the timed region, the roofline of the producer kernel
 against the measured HBM copy bandwidth, and the CPU oracle timed on a bounded
@@ -365,6 +368,71 @@ def indexer_timing(replays: int = 200, calls: int = 20):
             "index_k_tokens_scanned": int(w.kv_len.sum())}
 
 
+def tensor_peaks():
+    """(burst, sustained) dense bf16 TFLOP/s measured on this machine (cuBLAS), with
+    the kind; the fallback figures when the measurement file is absent."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, "fallback"
+
+
+def projection_timing(launches: int = 10, warmup: int = 3, num_seqs: int = 8):
+    """The projection GEMM with the producer in its epilogue on the prefill batch
+    (8 x 8192 tokens, hidden 6,144 -> 11,392 outputs, big shapes, fp8 caches),
+    against the unfused pair it replaces: cuBLAS bf16 GEMM (torch.matmul) writing
+    the rows, then msa_producer_forward on them."""
+    import torch
+    from paged_kv_cache_msa_gb300 import binding as B
+    from paged_kv_cache_msa_gb300 import workloads as wl
+    from paged_kv_cache_msa_gb300.device import DeviceProjection, DeviceWorkload
+    pw = wl.projection_prefill(num_seqs=num_seqs)
+    dp = DeviceProjection(pw)
+    s = torch.cuda.Stream()
+
+    def timed(fn):
+        with torch.cuda.stream(s):
+            for _ in range(warmup):
+                fn()
+            s.synchronize()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(launches)]
+            for a, b in ev:
+                a.record(s)
+                fn()
+                b.record(s)
+            s.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / launches
+
+    ms = timed(lambda: dp.run(stream=s))
+    status = int(dp.status.item())
+    X = dp.hidden.view(torch.bfloat16)[:, :pw.hidden_size]
+    Wt = dp.weight.view(torch.bfloat16)[:, :pw.hidden_size]
+    rows = torch.empty((pw.num_tokens, pw.width), dtype=torch.bfloat16, device=dp.device)
+    ms_gemm = timed(lambda: torch.matmul(X, Wt.t(), out=rows))
+    dw = DeviceWorkload(pw.producer, pools_on_device=dp.pools)
+    args = list(dw.args(B.MSA_LAUNCH_PERSISTENT))
+    args[2], args[3] = int(rows.data_ptr()), pw.width
+    ms_prod = timed(lambda: B.msa_producer_forward(*args, stream=s.cuda_stream))
+    fl = pw.flops()
+    tf = fl / (ms * 1e-3) / 1e12
+    burst, sustained, kind = tensor_peaks()
+    return {"workload": f"prefill {num_seqs}x8192 tokens, hidden {pw.hidden_size} -> {pw.width} "
+                        "outputs (64/8/8/1 heads x 128), fp8 caches; bf16 operands, fp32 accumulate",
+            "ms_per_launch": ms, "tokens_per_s": pw.num_tokens / (ms * 1e-3),
+            "launches_per_step": 1, "status": status,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": burst, "unit": "TFLOP/s",
+                         "frac": tf / burst, "frac_of_sustained": tf / sustained,
+                         "peak_kind": f"{kind} cuBLAS bf16 (burst; sustained {sustained})",
+                         "flops_per_launch": fl, "traffic": None},
+            "unfused": {"cublas_gemm_ms": ms_gemm, "producer_ms": ms_prod,
+                        "total_ms": ms_gemm + ms_prod,
+                        "cublas_tflops": fl / (ms_gemm * 1e-3) / 1e12},
+            "speedup_vs_unfused": (ms_gemm + ms_prod) / ms}
+
+
 def run_ours(args):
     import torch
     from paged_kv_cache_msa_gb300 import binding as B
@@ -444,6 +512,10 @@ def run_ours(args):
     if not args.no_decode_step:
         indexer = indexer_timing()
 
+    projection = None
+    if not args.no_projection:
+        projection = projection_timing(num_seqs=args.projection_seqs)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         n, dt = OracleRunner(w).timed(budget_s=args.cpu_budget)
@@ -476,6 +548,7 @@ def run_ours(args):
         "e2e": e2e,
         "decode_step": decode,
         "indexer": indexer,
+        "projection": projection,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
@@ -539,6 +612,12 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--indexer-only", action="store_true",
                     help="time only the decode-batch-64 indexer and print its JSON")
+    ap.add_argument("--no-projection", action="store_true",
+                    help="skip the projection GEMM + producer leg")
+    ap.add_argument("--projection-only", action="store_true",
+                    help="time only the projection GEMM + producer and print its JSON")
+    ap.add_argument("--projection-seqs", type=int, default=8,
+                    help="sequences of 8,192 tokens in the projection leg (8 = the full batch)")
     ap.add_argument("--prefill-seqs", type=int, default=8,
                     help="sequences of 8,192 tokens in the prefill workload (8 = the full batch)")
     args = ap.parse_args()
@@ -547,6 +626,12 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.projection_only:
+        from paged_kv_cache_msa_gb300 import build as build_mod
+        build_mod.build()
+        print(json.dumps(projection_timing(launches=max(1, args.steps), warmup=args.warmup,
+                                           num_seqs=args.projection_seqs)), flush=True)
+        return 0
     if args.indexer_only:
         from paged_kv_cache_msa_gb300 import build as build_mod
         build_mod.build()
