@@ -5,18 +5,27 @@
 // applies to a row; only where the row comes from differs: here it is the fp32
 // accumulator of a 128-token x 256-output tile in tensor memory, rounded to bf16.
 //
-// Kernel structure (one persistent CTA per SM, 192 threads):
-//   warp 0      TMA producer: hidden and weight tiles of 64 elements of K into a
-//               4-stage shared-memory ring (128-byte swizzle, K-major)
-//   warp 1      tensor memory owner and MMA issuer: tcgen05.mma kind::f16,
-//               M = 128, N = 256, K = 16, fp32 accumulators in tensor memory,
-//               two accumulators (512 columns) so that the epilogue of one tile
-//               overlaps the main loop of the next
-//   warps 2..5  epilogue: thread r of the four warps owns token row r of the tile
-//               (tensor-memory lane r) and runs the producer on the tile's heads
+// Kernel structure: persistent clusters of two CTAs (one per SM), 192 threads each.
+// A cluster computes 256-token x 256-output tiles with the 2-SM MMA: CTA r of the
+// pair holds tokens [128r, 128r + 128) of the tile and weight rows [128r, 128r +
+// 128) of its outputs, and its tensor memory receives the accumulator of its own
+// 128 tokens over all 256 outputs.  Per CTA:
+//   warp 0      TMA producer: 64-element K blocks of its hidden rows and weight
+//               rows into a 7-stage shared-memory ring (128-byte swizzle,
+//               K-major); the copies of both CTAs complete on the leader's barrier
+//   warp 1      tensor-memory owner; in the leader CTA (rank 0) one thread issues
+//               tcgen05.mma.cta_group::2 kind::f16 (M 256, N 256, K 16) into one of
+//               two accumulators (2 x 256 columns), so that the epilogue of a tile
+//               overlaps the main loop of the next, and commits to both CTAs
+//   warps 2..5  epilogue: thread r of the four warps owns token row r of its CTA's
+//               half of the tile (tensor-memory lane r) and runs the producer on
+//               the tile's heads
+// Per SM a K block moves 32 KB through shared memory for 128 x 256 x 64 MACs
+// (half of what a one-SM 128 x 256 tile needs), which is what lets 7 stages --
+// about 2 us of loads -- be in flight.
 //
 // Tiles are visited output-group-major: for each group of n_group 256-wide output
-// tiles, every 128-token tile in order, so that the group's weight panels stay in
+// tiles, every 256-token tile in order, so that the group's weight panels stay in
 // L2 while the hidden rows stream through once per group.
 //
 // Every mbarrier wait is bounded by %globaltimer; a wait that runs out sets
@@ -39,30 +48,34 @@
 #include "msa_projection.h"
 
 #ifndef MSA_PROJ_NGROUP
-#define MSA_PROJ_NGROUP 16
+#define MSA_PROJ_NGROUP 8
+#endif
+#ifndef MSA_PROJ_STAGES
+#define MSA_PROJ_STAGES 7
 #endif
 
 namespace {
 
-constexpr int kBM = 128;                  // tokens per tile: tensor-memory lanes
+constexpr int kBM = 128;                  // tokens per CTA and tile half: tensor-memory lanes
+constexpr int kPairM = 2 * kBM;           // tokens per cluster tile (the 2-SM MMA's M)
 constexpr int kBN = 256;                  // projection outputs per tile: accumulator columns
+constexpr int kHalfN = kBN / 2;           // weight rows each CTA stages
 constexpr int kBK = 64;                   // K elements per stage: one 128-byte swizzle row
-constexpr int kStages = 4;
+constexpr int kStages = MSA_PROJ_STAGES;
 constexpr int kThreads = 192;
 constexpr uint32_t kTileABytes = kBM * kBK * 2;
-constexpr uint32_t kTileBBytes = kBN * kBK * 2;
-constexpr uint32_t kStageBytes = kTileABytes + kTileBBytes;
-constexpr int kDynSmem = kStages * kStageBytes + 1024;  // + alignment slack for the ring
+constexpr uint32_t kTileBBytes = kHalfN * kBK * 2;
+constexpr uint32_t kStageBytes = kTileABytes + kTileBBytes;  // per CTA
+constexpr int kDynSmem = kStages * kStageBytes + 1024;        // + alignment slack for the ring
 constexpr uint32_t kTmemCols = 2 * kBN;
 constexpr int kMaxRotaryHalf = 64;
-constexpr int kMaxHeadScales = 256;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 // tcgen05 instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
 // and B (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bit 17,
-// M >> 4 at bit 24.
+// M >> 4 at bit 24 (M = 256: the pair's tile).
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
-                            ((uint32_t)(kBM >> 4) << 24);
+                            ((uint32_t)(kPairM >> 4) << 24);
 
 struct CacheArgs {
     uint8_t *data;  // nullptr: not written
@@ -146,24 +159,49 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
     }
 }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
 
+// arrive on an mbarrier of another CTA of the cluster (shared::cluster address)
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// the shared::cluster address of the same shared-memory location in CTA `rank`
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank)
+{
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+    return d;
+}
+
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+// A tile of the pair's operands into this CTA's shared memory; the transferred
+// bytes are counted on `bar`, which may be the leader CTA's barrier.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            uint32_t bar)
+                                            uint32_t cluster_bar)
 {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(map), "r"(x), "r"(y), "r"(bar)
+        "l"(map), "r"(x), "r"(y), "r"(cluster_bar)
         : "memory");
 }
 
@@ -179,20 +217,33 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
     return d;
 }
 
+// The 2-SM MMA: A and B descriptors address the leader's tiles; the peer's halves
+// sit at the same shared-memory offsets in the peer CTA.
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
         : "memory");
 }
 
-// the mbarrier arrives once every tcgen05.mma issued so far by this thread is done
+// The mbarrier at this offset in both CTAs of the pair arrives once every
+// tcgen05.mma issued so far by this thread is done.
+__device__ __forceinline__ void tc_commit_both(uint32_t bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"((unsigned short)3)
+        : "memory");
+}
+
+// the same, on this CTA's barrier only
 __device__ __forceinline__ void tc_commit(uint32_t bar)
 {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
         : "memory");
 }
 
@@ -360,9 +411,15 @@ __device__ __forceinline__ void emit8(const Params &p, const Head &hd, int64_t t
 }
 
 // taddr: tensor-memory address of this warp's lanes at the tile's first column
+// norm weight element i of a tensor (unit weight when absent)
+__device__ __forceinline__ float norm_weight(const uint16_t *w, int i)
+{
+    return w ? __uint_as_float((uint32_t)__ldg(w + i) << 16) : 1.0f;
+}
+
 template <int D>
-__device__ __forceinline__ void epilogue_tile(const Params &p, const float (*s_w)[D],
-                                              uint32_t taddr, int n_tile, int64_t t, bool live)
+__device__ __forceinline__ void epilogue_tile(const Params &p, uint32_t taddr, int n_tile, int64_t t,
+                                              bool live)
 {
     constexpr int HPT = kBN / D;  // heads per tile
     const int g0 = n_tile * HPT;
@@ -433,7 +490,7 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const float (*s_w
                 for (int hh = 0; hh < HPT; ++hh) {
                     if (hd[hh].sec < 0 || hd[hh].sec == 2)
                         continue;
-                    const float *w = s_w[hd[hh].sec == 0 ? 0 : hd[hh].sec == 1 ? 1 : hd[hh].sec == 3 ? 2 : 3];
+                    const uint16_t *w = p.norm_w[hd[hh].sec == 0 ? 0 : hd[hh].sec == 1 ? 1 : hd[hh].sec == 3 ? 2 : 3];
                     uint32_t ru[8], rv[8], bu[4], bv[4];
                     float u[8], v[8];
                     tmem_ld8(taddr + (uint32_t)(hh * D + k0), ru);
@@ -444,8 +501,8 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const float (*s_w
                     float yu[8], yv[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const float a = (u[j] * rn[hh]) * w[k0 + j];
-                        const float b = (v[j] * rn[hh]) * w[k0 + half + j];
+                        const float a = (u[j] * rn[hh]) * norm_weight(w, k0 + j);
+                        const float b = (v[j] * rn[hh]) * norm_weight(w, k0 + half + j);
                         yu[j] = fmaf(-b, sn[j], a * cs[j]);
                         yv[j] = fmaf(a, sn[j], b * cs[j]);
                     }
@@ -459,7 +516,7 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const float (*s_w
                 for (int hh = 0; hh < HPT; ++hh) {
                     if (hd[hh].sec < 0 || hd[hh].sec == 2)
                         continue;
-                    const float *w = s_w[hd[hh].sec == 0 ? 0 : hd[hh].sec == 1 ? 1 : hd[hh].sec == 3 ? 2 : 3];
+                    const uint16_t *w = p.norm_w[hd[hh].sec == 0 ? 0 : hd[hh].sec == 1 ? 1 : hd[hh].sec == 3 ? 2 : 3];
                     uint32_t ru[8], bu[4];
                     float u[8], y[8];
                     tmem_ld8(taddr + (uint32_t)(hh * D + c), ru);
@@ -467,7 +524,7 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const float (*s_w
                     round_row8(ru, bu, u);
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        y[j] = (u[j] * rn[hh]) * w[c + j];
+                        y[j] = (u[j] * rn[hh]) * norm_weight(w, c + j);
                     emit8<D>(p, hd[hh], t, live, pl, c, y);
                 }
             }
@@ -485,7 +542,7 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const float (*s_w
                 for (int hh = 0; hh < HPT; ++hh) {
                     if (hd[hh].sec < 0 || hd[hh].sec == 2)
                         continue;
-                    const float *w = s_w[hd[hh].sec == 0 ? 0 : hd[hh].sec == 1 ? 1 : hd[hh].sec == 3 ? 2 : 3];
+                    const uint16_t *w = p.norm_w[hd[hh].sec == 0 ? 0 : hd[hh].sec == 1 ? 1 : hd[hh].sec == 3 ? 2 : 3];
                     uint32_t ru[8], bu[4];
                     float u[8], y[8];
                     tmem_ld8(taddr + (uint32_t)(hh * D + c), ru);
@@ -493,7 +550,7 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const float (*s_w
                     round_row8(ru, bu, u);
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        y[j] = (u[j] * rn[hh]) * w[c + j];
+                        y[j] = (u[j] * rn[hh]) * norm_weight(w, c + j);
                     if (rot) {
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
@@ -545,16 +602,16 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
                       const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ Params p)
 {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_full[kStages];
-    __shared__ __align__(8) uint64_t bar_empty[kStages];
-    __shared__ __align__(8) uint64_t bar_tfull[2];
-    __shared__ __align__(8) uint64_t bar_tempty[2];
+    __shared__ __align__(8) uint64_t bar_full[kStages];   // leader: both CTAs' copies landed
+    __shared__ __align__(8) uint64_t bar_empty[kStages];  // both: the MMAs have read the stage
+    __shared__ __align__(8) uint64_t bar_tfull[2];        // both: accumulator b is complete
+    __shared__ __align__(8) uint64_t bar_tempty[2];       // leader: both epilogues drained b
     __shared__ __align__(8) uint64_t bar_drain;
     __shared__ uint32_t s_tmem;
-    __shared__ __align__(16) float s_w[4][D];
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t ring = (raw + 1023u) & ~1023u;  // the swizzle pattern needs 1024-byte alignment
 
@@ -565,7 +622,7 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bar_tfull[b]), 1);
-            mbar_init(smem_u32(&bar_tempty[b]), 4 * 32);
+            mbar_init(smem_u32(&bar_tempty[b]), 2 * 4);  // one arrival per epilogue warp of the pair
         }
         mbar_init(smem_u32(&bar_drain), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -575,43 +632,44 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_w) : "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+        // one warp of each CTA of the pair: the same columns in both tensor memories
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(&s_tmem)),
                      "r"(kTmemCols)
                      : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    for (int i = threadIdx.x; i < 4 * D; i += kThreads) {
-        const uint16_t *w = p.norm_w[i / D];
-        s_w[i / D][i % D] = w ? __uint_as_float((uint32_t)__ldg(w + i % D) << 16) : 1.0f;
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // barriers initialised and tensor memory allocated in both CTAs
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
     const int64_t num_tiles = (int64_t)p.m_tiles * p.n_tiles;
+    const int64_t cluster_id = blockIdx.x / 2;
+    const int64_t num_clusters = gridDim.x / 2;
     bool ok = true;
 
     if (warp == 0) {
-        // ---------------- TMA producer ----------------
+        // ---------------- TMA producer (both CTAs) ----------------
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
-            int filled = 0;  // fills issued (for the wind-down after a timeout)
-            for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            for (int64_t tile = cluster_id; tile < num_tiles && ok; tile += num_clusters) {
                 int m, n;
                 tile_coords(p, tile, m, n);
+                const int row_x = m * kPairM + (int)rank * kBM;
+                const int row_w = n * kBN + (int)rank * kHalfN;
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
                     if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1)) {
                         ok = false;
                         break;
                     }
                     const uint32_t full = smem_u32(&bar_full[stage]);
+                    if (rank == 0)  // the leader expects the bytes of both CTAs
+                        mbar_expect_tx(full, 2 * kStageBytes);
+                    const uint32_t full_leader = map_to_rank(full, 0);
                     const uint32_t a = ring + stage * kStageBytes;
-                    mbar_expect_tx(full, kStageBytes);
-                    tma_load_2d(a, &tmap_x, kb * kBK, m * kBM, full);
-                    tma_load_2d(a + kTileABytes, &tmap_w, kb * kBK, n * kBN, full);
-                    ++filled;
+                    tma_load_2d(a, &tmap_x, kb * kBK, row_x, full_leader);
+                    tma_load_2d(a + kTileABytes, &tmap_w, kb * kBK, row_w, full_leader);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1;
@@ -619,22 +677,18 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 }
             }
             if (!ok) {
-                // the copies in flight land before the CTA may exit: wait for the
-                // last fill of every stage (bounded)
-                for (int j = 1; j <= kStages && j <= filled; ++j) {
-                    const int f = filled - j;  // fill index
-                    const int s = f % kStages;
-                    const uint32_t par = (uint32_t)((f / kStages) & 1);
-                    (void)mbar_wait(smem_u32(&bar_full[s]), par);
+                // let the copies in flight land before the CTA may exit
+                const uint64_t t0 = globaltimer();
+                while (globaltimer() - t0 < 200000ull) {
                 }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
+        // ---------------- MMA issuer (leader CTA) ----------------
+        if (lane == 0 && rank == 0) {
             uint32_t stage = 0, phase = 0, acc_i = 0;
-            for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++acc_i) {
+            for (int64_t tile = cluster_id; tile < num_tiles && ok; tile += num_clusters, ++acc_i) {
                 const uint32_t b = acc_i & 1, use_par = (acc_i >> 1) & 1;
                 if (!mbar_wait(smem_u32(&bar_tempty[b]), use_par ^ 1)) {
                     ok = false;
@@ -654,7 +708,7 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
                     for (int k = 0; k < kBK / 16; ++k)
                         tc_mma(d_tmem, sw128_desc(a + 32u * k), sw128_desc(bb + 32u * k),
                                (kb | k) != 0);
-                    tc_commit(smem_u32(&bar_empty[stage]));
+                    tc_commit_both(smem_u32(&bar_empty[stage]));
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1;
@@ -662,21 +716,21 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 }
                 if (!ok)
                     break;
-                tc_commit(smem_u32(&bar_tfull[b]));
+                tc_commit_both(smem_u32(&bar_tfull[b]));
             }
-            // every MMA of this CTA is complete before its tensor memory is released
+            // every MMA of the pair is complete before tensor memory is released
             tc_commit(smem_u32(&bar_drain));
             if (!mbar_wait(smem_u32(&bar_drain), 0))
                 ok = false;
         }
         __syncwarp();
     } else {
-        // ---------------- epilogue ----------------
+        // ---------------- epilogue (both CTAs) ----------------
         const int quarter = warp & 3;  // the tensor-memory lanes this warp may read
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         uint32_t acc_i = 0;
-        for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++acc_i) {
+        for (int64_t tile = cluster_id; tile < num_tiles; tile += num_clusters, ++acc_i) {
             int m, n;
             tile_coords(p, tile, m, n);
             const uint32_t b = acc_i & 1, use_par = (acc_i >> 1) & 1;
@@ -686,20 +740,22 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 break;
             }
             tc_fence_after();
-            const int64_t t = (int64_t)m * kBM + row;
-            epilogue_tile<D>(p, s_w, tmem + lane_base + b * kBN, n, t, t < p.num_tokens);
+            const int64_t t = (int64_t)m * kPairM + (int64_t)rank * kBM + row;
+            epilogue_tile<D>(p, tmem + lane_base + b * kBN, n, t, t < p.num_tokens);
             tc_fence_before();
-            mbar_arrive(smem_u32(&bar_tempty[b]));
+            __syncwarp();
+            if (lane == 0)  // this warp is done reading accumulator b
+                mbar_arrive_remote(map_to_rank(smem_u32(&bar_tempty[b]), 0));
         }
     }
 
     if (!ok && p.status)
         atomicOr(p.status, MSA_STATUS_WAIT_TIMEOUT);
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // no MMA, copy or tensor-memory read of the pair is still running
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols)
                      : "memory");
     }
@@ -732,8 +788,7 @@ std::mutex g_mu;
 EncodeTiledFn g_encode = nullptr;
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
-    int sms = 0;
-    bool configured[2] = {false, false};
+    int clusters[2] = {0, 0};  // resident clusters of two CTAs, per head_dim variant
 };
 DeviceInfo g_dev[kMaxDevices];
 
@@ -800,8 +855,8 @@ msa_status validate(const msa_producer_cfg *cfg, int64_t num_tokens, const void 
     const int64_t htot = (int64_t)cfg->num_q_heads + 2 * (int64_t)cfg->num_kv_heads +
                          cfg->num_idx_q_heads + cfg->num_idx_k_heads;
     const int64_t W = htot * cfg->head_dim;
-    if (num_tokens >= (int64_t)0x7fffffff - kBM)
-        return fail(MSA_ERR_UNSUPPORTED, "num_tokens %lld (limit 2^31 - 129)", (long long)num_tokens);
+    if (num_tokens >= (int64_t)0x7fffffff - kPairM)
+        return fail(MSA_ERR_UNSUPPORTED, "num_tokens %lld (limit 2^31 - 257)", (long long)num_tokens);
     if (!hidden || !weight)
         return fail(MSA_ERR_INVALID_ARGUMENT, "hidden and weight are required");
     if (hidden_size < 1)
@@ -888,7 +943,7 @@ extern "C" msa_status msa_projection_forward(
     p.status = status;
     p.num_tokens = num_tokens;
     p.num_k_blocks = (int32_t)((hidden_size + kBK - 1) / kBK);
-    p.m_tiles = (int32_t)((num_tokens + kBM - 1) / kBM);
+    p.m_tiles = (int32_t)((num_tokens + kPairM - 1) / kPairM);
     p.n_tiles = (int32_t)((W + kBN - 1) / kBN);
     p.n_group = p.n_tiles < MSA_PROJ_NGROUP ? p.n_tiles : MSA_PROJ_NGROUP;
     p.hq = cfg->num_q_heads;
@@ -912,7 +967,7 @@ extern "C" msa_status msa_projection_forward(
 
     CUtensorMap mx, mw;
     if (!encode_map(&mx, hidden, num_tokens, hidden_size, hidden_row_stride, kBM) ||
-        !encode_map(&mw, weight, W, hidden_size, weight_row_stride, kBN))
+        !encode_map(&mw, weight, W, hidden_size, weight_row_stride, kHalfN))
         return fail(MSA_ERR_CUDA, "tensor map encoding failed");
 
     int dev = 0;
@@ -921,30 +976,44 @@ extern "C" msa_status msa_projection_forward(
     const void *fn = D == 128 ? reinterpret_cast<const void *>(&msa_projection_kernel<128>)
                               : reinterpret_cast<const void *>(&msa_projection_kernel<64>);
     const int vi = D == 128 ? 1 : 0;
-    int sms;
+    cudaLaunchConfig_t lc;
+    memset(&lc, 0, sizeof lc);
+    lc.blockDim = dim3(kThreads);
+    lc.dynamicSmemBytes = kDynSmem;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    int clusters;
     {
         std::lock_guard<std::mutex> lk(g_mu);
-        sms = g_dev[dev].sms;
-        if (!g_dev[dev].configured[vi] || sms == 0) {
+        clusters = g_dev[dev].clusters[vi];
+        if (clusters == 0) {
             int major = 0;
-            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-                cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+            if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
                 return fail(MSA_ERR_CUDA, "device query failed");
             if (major != 10)
                 return fail(MSA_ERR_UNSUPPORTED, "tcgen05 tensor cores need compute capability 10.x");
             if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem) !=
                 cudaSuccess)
                 return fail(MSA_ERR_CUDA, "cudaFuncSetAttribute failed");
-            g_dev[dev].sms = sms;
-            g_dev[dev].configured[vi] = true;
+            lc.gridDim = dim3(2);
+            if (cudaOccupancyMaxActiveClusters(&clusters, fn, &lc) != cudaSuccess || clusters <= 0)
+                return fail(MSA_ERR_CUDA, "no cluster of two CTAs fits on this device");
+            g_dev[dev].clusters[vi] = clusters;
         }
     }
     const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
-    const int grid = (int)(tiles < sms ? tiles : sms);
-    if (D == 128)
-        msa_projection_kernel<128><<<grid, kThreads, kDynSmem, stream>>>(mx, mw, p);
-    else
-        msa_projection_kernel<64><<<grid, kThreads, kDynSmem, stream>>>(mx, mw, p);
+    lc.gridDim = dim3((unsigned)(2 * (tiles < clusters ? tiles : clusters)));
+    void *args[] = {&mx, &mw, &p};
+    if (cudaLaunchKernelExC(&lc, fn, args) != cudaSuccess) {
+        const cudaError_t e = cudaGetLastError();
+        return fail(MSA_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(MSA_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
