@@ -122,8 +122,9 @@ def load(path: str) -> ctypes.CDLL:
                                  ctypes.POINTER(OracleCache), ctypes.c_float, ctypes.c_int32,
                                  vp, vp]
     L.oracle_indexer.restype = ctypes.c_int
-    L.oracle_projection.argtypes = [ctypes.c_int64, ctypes.c_int64, vp, ctypes.c_int64,
-                                    ctypes.c_int64, vp, ctypes.c_int64, vp, ctypes.c_int64]
+    L.oracle_projection.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, vp,
+                                    ctypes.c_int64, vp, ctypes.c_int64, vp, ctypes.c_int64, vp,
+                                    vp, ctypes.c_int64]
     L.oracle_projection.restype = ctypes.c_int
     return L
 
@@ -296,20 +297,29 @@ def indexer(idx_q: np.ndarray, kv_len: np.ndarray, table_offset: np.ndarray, pag
     return scores, top
 
 
-def projection(hidden: np.ndarray, weight: np.ndarray) -> np.ndarray:
+def projection(hidden: np.ndarray, weight: np.ndarray, hidden_scales=None,
+               weight_scales=None) -> np.ndarray:
     """The projection rows [T, W] (uint16, bf16 bits) of hidden [T, K] and the
-    output-major weight [W, K] (both uint16 bf16 bits; row strides may exceed K,
-    given as a wider array whose first K columns are used: pass a column slice)."""
-    assert hidden.dtype == np.uint16 and weight.dtype == np.uint16
+    output-major weight [W, K]: both uint16 (bf16 bits) or both uint8 (E4M3
+    codes).  Row strides may exceed K (pass a column slice of a wider array).
+    ``hidden_scales`` float32 [T] and ``weight_scales`` float32 [W] (or None: 1)."""
+    assert hidden.dtype == weight.dtype and hidden.dtype in (np.uint16, np.uint8)
     assert hidden.ndim == 2 and weight.ndim == 2
+    es = hidden.itemsize
+    dtype = DTYPE_BF16 if es == 2 else DTYPE_E4M3
     T, K = hidden.shape
     W, K2 = weight.shape
     assert K == K2
-    assert hidden.strides[1] == 2 and weight.strides[1] == 2
+    assert hidden.strides[1] == es and weight.strides[1] == es
+    sx = None if hidden_scales is None else np.ascontiguousarray(hidden_scales, dtype=np.float32)
+    sw = None if weight_scales is None else np.ascontiguousarray(weight_scales, dtype=np.float32)
+    assert sx is None or sx.shape == (T,)
+    assert sw is None or sw.shape == (W,)
     rows = np.empty((T, W), dtype=np.uint16)
-    rc = lib().oracle_projection(T, K, hidden.ctypes.data, hidden.strides[0] // 2, W,
-                                 weight.ctypes.data, weight.strides[0] // 2,
-                                 rows.ctypes.data, W)
+    rc = lib().oracle_projection(T, K, dtype, hidden.ctypes.data, hidden.strides[0] // es,
+                                 None if sx is None else sx.ctypes.data, W,
+                                 weight.ctypes.data, weight.strides[0] // es,
+                                 None if sw is None else sw.ctypes.data, rows.ctypes.data, W)
     if rc != 0:
         raise ValueError("oracle rejected the projection arguments")
     return rows

@@ -466,35 +466,56 @@ int oracle_indexer(int32_t num_heads, int32_t head_dim, int32_t page_size, int32
 /*
  * The wide projection that feeds the producer ("[None][perf] Fuse MiniMax-M3 QKV
  * and index projection", Description, AFTER diagram: hidden states -> one wider
- * fused GEMM [Q | K | V | index-Q | index-K] -> one fused producer).
+ * fused GEMM [Q | K | V | index-Q | index-K] -> one fused producer; the change
+ * "packs Q, K, V, index-Q, and index-K into one quantized ... projection").
  *
- * rows[t, j] = bf16(fp32(sum_k hidden[t, k] * weight[j, k])) for j < width: the
- * weight is stored output-major ([width, hidden_size], row j is the weights of
- * output j), so that output j of token t is the dot product of two rows.  The sum
- * is accumulated in double in index order (a product of two bf16 values is exact
- * in double), rounded once to fp32 and then to bf16 with round-to-nearest-even:
- * the bf16 row that a GEMM with an fp32 accumulator stores, up to the rounding
- * of its own accumulation.
+ *   rows[t, j] = bf16(fp32(hidden_scale[t] * weight_scale[j] *
+ *                          sum_k x[t, k] * w[j, k]))            for j < width
  *
- * Reading: the pages do not say whether the fused epilogue consumes the fp32
+ * x and w are the decoded operands: bf16, or FP8 E4M3 codes (dtype 0 / 1, as for
+ * the caches).  The weight is stored output-major ([width, hidden_size], row j is
+ * the weights of output j).  The scales are the dequantisation factors of a
+ * quantised projection: one per token, one per output (NULL: 1).  The sum is
+ * accumulated in double in index order (a product of two bf16 or E4M3 values is
+ * exact in double), multiplied by the scales in double, rounded once to fp32
+ * and then to bf16 with round-to-nearest-even: the row that a GEMM with an fp32
+ * accumulator stores, up to the rounding of its own accumulation and scaling.
+ *
+ * Readings: the pages do not say whether the fused epilogue consumes the fp32
  * accumulator or the bf16 row; the bf16 row is taken, so that projection and
- * producer together equal the unfused GEMM followed by the producer.
+ * producer together equal the unfused GEMM followed by the producer.  The pages
+ * name a quantised projection without its format; per-token and per-output
+ * scales over E4M3 operands are taken.
  */
-int oracle_projection(int64_t num_tokens, int64_t hidden_size, const uint16_t *hidden,
-                      int64_t hidden_stride, int64_t width, const uint16_t *weight,
-                      int64_t weight_stride, uint16_t *rows, int64_t row_stride)
+static double projection_operand(const uint8_t *base, int32_t dtype, int64_t idx)
+{
+    if (dtype == ORACLE_DTYPE_E4M3)
+        return (double)oracle_e4m3_decode(base[idx]);
+    uint16_t h;
+    memcpy(&h, base + 2 * idx, 2);
+    return (double)oracle_bf16_decode(h);
+}
+
+int oracle_projection(int64_t num_tokens, int64_t hidden_size, int32_t dtype, const void *hidden,
+                      int64_t hidden_stride, const float *hidden_scales, int64_t width,
+                      const void *weight, int64_t weight_stride, const float *weight_scales,
+                      uint16_t *rows, int64_t row_stride)
 {
     if (num_tokens < 0 || hidden_size < 0 || width < 0 || hidden_stride < hidden_size ||
-        weight_stride < hidden_size || row_stride < width)
+        weight_stride < hidden_size || row_stride < width ||
+        (dtype != ORACLE_DTYPE_BF16 && dtype != ORACLE_DTYPE_E4M3))
         return -1;
+    const uint8_t *hx = (const uint8_t *)hidden;
+    const uint8_t *hw = (const uint8_t *)weight;
     for (int64_t t = 0; t < num_tokens; ++t) {
-        const uint16_t *x = hidden + t * hidden_stride;
         for (int64_t j = 0; j < width; ++j) {
-            const uint16_t *wrow = weight + j * weight_stride;
             double acc = 0.0;
             for (int64_t k = 0; k < hidden_size; ++k)
-                acc += (double)oracle_bf16_decode(x[k]) * (double)oracle_bf16_decode(wrow[k]);
-            rows[t * row_stride + j] = oracle_bf16_encode((float)acc);
+                acc += projection_operand(hx, dtype, t * hidden_stride + k) *
+                       projection_operand(hw, dtype, j * weight_stride + k);
+            const double sx = hidden_scales ? (double)hidden_scales[t] : 1.0;
+            const double sw = weight_scales ? (double)weight_scales[j] : 1.0;
+            rows[t * row_stride + j] = oracle_bf16_encode((float)(acc * sx * sw));
         }
     }
     return 0;

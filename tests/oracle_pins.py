@@ -622,4 +622,92 @@ def pin_projection_signed_permutation():
     assert np.array_equal(got, expect)
 
 
+def _round_sig_frac(v, bits: int):
+    """The rational v rounded to ``bits`` significant bits, ties to even (exact)."""
+    from fractions import Fraction
+    v = Fraction(v)
+    if v == 0:
+        return Fraction(0)
+    sign = -1 if v < 0 else 1
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    unit = Fraction(2) ** (e - bits + 1)       # the spacing at this magnitude
+    q, r = divmod(a, unit)
+    q = int(q)
+    if r > unit / 2 or (r == unit / 2 and (q & 1)):
+        q += 1
+    return sign * q * unit
+
+
+def _bf16_bits_of_fraction(v) -> int:
+    """bf16 bits of the rational v after rounding to fp32 and then to bf16 (RNE),
+    by exact rational arithmetic (normal range only)."""
+    from fractions import Fraction
+    r = _round_sig_frac(_round_sig_frac(v, 24), 8)
+    if r == 0:
+        return 0
+    sign = 0x8000 if r < 0 else 0
+    a = abs(r)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    mant = int(a / Fraction(2) ** (e - 7)) & 0x7F
+    return sign | ((e + 127) << 7) | mant
+
+
+def _e4m3_codes(x: np.ndarray) -> np.ndarray:
+    """E4M3 codes of values that E4M3 holds exactly, through torch's cast."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.float8_e4m3fn)
+    codes = t.view(torch.uint8).numpy().copy()
+    back = t.to(torch.float32).numpy()
+    assert np.array_equal(back, x.astype(np.float32)), "value not exact in E4M3"
+    return codes
+
+
+def pin_projection_e4m3_exact_integers_and_scales():
+    """E4M3 operands holding small integers, dyadic per-token and per-output scales:
+    every output is an exact rational, rounded to fp32 then bf16 by exact rational
+    arithmetic.  Distinct scales per token and per output fix which scale goes
+    where."""
+    from fractions import Fraction
+    rng = np.random.default_rng(73)
+    T, K, W = 6, 48, 20
+    h = rng.integers(-8, 9, size=(T, K))
+    w = rng.integers(-8, 9, size=(W, K))
+    sx = np.array([0.5, 0.375, 1.25, 3.0, 0.0625, 1.0][:T], dtype=np.float32)
+    sw = (np.array([0.25, 1.5, 0.625, 2.0, 0.75], dtype=np.float32)[np.arange(W) % 5]
+          * np.float32(2.0) ** (np.arange(W) // 5)).astype(np.float32)
+    hb = _e4m3_codes(h.astype(np.float32))
+    wb = _e4m3_codes(w.astype(np.float32))
+    pad_h = np.full((T, K + 16), 0x7F, dtype=np.uint8)
+    pad_h[:, :K] = hb
+    dots = h.astype(np.int64) @ w.astype(np.int64).T
+    expect = np.array([[_bf16_bits_of_fraction(Fraction(int(dots[t, j])) * Fraction(float(sx[t]))
+                                               * Fraction(float(sw[j])))
+                        for j in range(W)] for t in range(T)], dtype=np.uint16)
+    got = oracle.projection(pad_h[:, :K], wb, sx, sw)
+    assert np.array_equal(got, expect), np.argwhere(got != expect)[:5]
+
+
+def pin_projection_e4m3_signed_permutation():
+    """E4M3 weights that are signed unit vectors: each output is one E4M3 hidden
+    value, negated or not, which bf16 holds exactly."""
+    rng = np.random.default_rng(74)
+    T, K, W = 4, 64, 40
+    codes = rng.integers(0, 256, size=(T, K)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x38          # no NaN codes
+    codes[(codes & 0x7F) == 0x00] = 0x38          # no zeros (signed zeros would blur the check)
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float32)
+    vbits = vals.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    perm = rng.integers(0, K, size=W)
+    sign = rng.choice([1, -1], size=W)
+    wb = np.zeros((W, K), dtype=np.uint8)
+    wb[np.arange(W), perm] = np.where(sign > 0, 0x38, 0xB8)   # +-1.0
+    got = oracle.projection(codes, wb)
+    expect = vbits[:, perm] ^ np.where(sign > 0, 0, 0x8000).astype(np.uint16)[None, :]
+    assert np.array_equal(got, expect)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

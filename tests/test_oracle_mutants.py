@@ -45,12 +45,17 @@ MUTANTS = {
     "indexer_ties_high": ("if (best < 0 || bs[b] > bs[best])", "if (best < 0 || bs[b] >= bs[best])"),
     "indexer_scale_dropped": ("oracle_e4m3_decode(idx_k_cache->data[e + d]) * k_scale", "oracle_e4m3_decode(idx_k_cache->data[e + d])"),
     "indexer_table_offset": ("const int64_t ti = table_offset[t] + j / P;", "const int64_t ti = j / P;"),
-    "projection_weight_transposed": ("(double)oracle_bf16_decode(wrow[k])",
-                                     "(double)oracle_bf16_decode(weight[k * weight_stride + j])"),
+    "projection_weight_transposed": ("projection_operand(hw, dtype, j * weight_stride + k)",
+                                     "projection_operand(hw, dtype, k * weight_stride + j)"),
     "projection_dropped_term": ("for (int64_t k = 0; k < hidden_size; ++k)",
                                 "for (int64_t k = 1; k < hidden_size; ++k)"),
     "projection_fp32_accumulator": ("double acc = 0.0;", "float acc = 0.0f;"),
-    "projection_hidden_stride": ("hidden + t * hidden_stride;", "hidden + t * hidden_size;"),
+    "projection_hidden_stride": ("projection_operand(hx, dtype, t * hidden_stride + k)",
+                                 "projection_operand(hx, dtype, t * hidden_size + k)"),
+    "projection_weight_scale_by_token": ("(double)weight_scales[j]", "(double)weight_scales[t % width]"),
+    "projection_scale_dropped": ("(float)(acc * sx * sw)", "(float)(acc * sx)"),
+    "projection_e4m3_as_bf16": ("if (dtype == ORACLE_DTYPE_E4M3)\n        return (double)oracle_e4m3_decode",
+                                "if (dtype != ORACLE_DTYPE_E4M3)\n        return (double)oracle_e4m3_decode"),
     "indexer_sum_heads": ("                if (s > bs[b])\n                    bs[b] = s;", "                bs[b] = (bs[b] == -INFINITY ? 0.0f : bs[b]) + s;"),
 }
 
