@@ -379,16 +379,20 @@ def tensor_peaks():
         return 1900.0, 1700.0, "fallback"
 
 
-def projection_timing(launches: int = 10, warmup: int = 3, num_seqs: int = 8):
+def projection_timing(launches: int = 10, warmup: int = 3, num_seqs: int = 8,
+                      operand_dtype: int = 0):
     """The projection GEMM with the producer in its epilogue on the prefill batch
-    (8 x 8192 tokens, hidden 6,144 -> 11,392 outputs, big shapes, fp8 caches),
-    against the unfused pair it replaces: cuBLAS bf16 GEMM (torch.matmul) writing
-    the rows, then msa_producer_forward on them."""
+    (8 x 8192 tokens, hidden 6,144 -> 11,392 outputs, big shapes, fp8 caches), with
+    bf16 operands (0) or E4M3 operands with per-token / per-output scales (1),
+    against the unfused pair it replaces: the cuBLAS GEMM of the same operand type
+    (torch.matmul, or torch._scaled_mm for E4M3) writing the bf16 rows, then
+    msa_producer_forward on them."""
     import torch
     from paged_kv_cache_msa_gb300 import binding as B
     from paged_kv_cache_msa_gb300 import workloads as wl
     from paged_kv_cache_msa_gb300.device import DeviceProjection, DeviceWorkload
-    pw = wl.projection_prefill(num_seqs=num_seqs)
+    fp8 = operand_dtype == wl.DTYPE_E4M3
+    pw = wl.projection_prefill(num_seqs=num_seqs, operand_dtype=operand_dtype)
     dp = DeviceProjection(pw)
     s = torch.cuda.Stream()
 
@@ -408,10 +412,25 @@ def projection_timing(launches: int = 10, warmup: int = 3, num_seqs: int = 8):
 
     ms = timed(lambda: dp.run(stream=s))
     status = int(dp.status.item())
-    X = dp.hidden.view(torch.bfloat16)[:, :pw.hidden_size]
-    Wt = dp.weight.view(torch.bfloat16)[:, :pw.hidden_size]
+    K = pw.hidden_size
     rows = torch.empty((pw.num_tokens, pw.width), dtype=torch.bfloat16, device=dp.device)
-    ms_gemm = timed(lambda: torch.matmul(X, Wt.t(), out=rows))
+    comparator = None
+    try:
+        if fp8:
+            X = dp.hidden.view(torch.float8_e4m3fn)[:, :K]
+            Wt = dp.weight.view(torch.float8_e4m3fn)[:, :K]
+            one = torch.ones((), dtype=torch.float32, device=dp.device)
+            gemm = lambda: torch._scaled_mm(X, Wt.t(), scale_a=one, scale_b=one,
+                                            out_dtype=torch.bfloat16, out=rows)
+            comparator = "cuBLAS E4M3 GEMM (torch._scaled_mm, per-tensor scales) + producer"
+        else:
+            X = dp.hidden.view(torch.bfloat16)[:, :K]
+            Wt = dp.weight.view(torch.bfloat16)[:, :K]
+            gemm = lambda: torch.matmul(X, Wt.t(), out=rows)
+            comparator = "cuBLAS bf16 GEMM (torch.matmul) + producer"
+        ms_gemm = timed(gemm)
+    except Exception as e:   # a torch build without the comparator GEMM
+        ms_gemm, comparator = None, f"unavailable: {type(e).__name__}: {e}"[:160]
     dw = DeviceWorkload(pw.producer, pools_on_device=dp.pools)
     args = list(dw.args(B.MSA_LAUNCH_PERSISTENT))
     args[2], args[3] = int(rows.data_ptr()), pw.width
@@ -419,18 +438,23 @@ def projection_timing(launches: int = 10, warmup: int = 3, num_seqs: int = 8):
     fl = pw.flops()
     tf = fl / (ms * 1e-3) / 1e12
     burst, sustained, kind = tensor_peaks()
-    return {"workload": f"prefill {num_seqs}x8192 tokens, hidden {pw.hidden_size} -> {pw.width} "
-                        "outputs (64/8/8/1 heads x 128), fp8 caches; bf16 operands, fp32 accumulate",
-            "ms_per_launch": ms, "tokens_per_s": pw.num_tokens / (ms * 1e-3),
-            "launches_per_step": 1, "status": status,
-            "roofline": {"bound": "tensor", "achieved": tf, "peak": burst, "unit": "TFLOP/s",
-                         "frac": tf / burst, "frac_of_sustained": tf / sustained,
-                         "peak_kind": f"{kind} cuBLAS bf16 (burst; sustained {sustained})",
-                         "flops_per_launch": fl, "traffic": None},
-            "unfused": {"cublas_gemm_ms": ms_gemm, "producer_ms": ms_prod,
-                        "total_ms": ms_gemm + ms_prod,
-                        "cublas_tflops": fl / (ms_gemm * 1e-3) / 1e12},
-            "speedup_vs_unfused": (ms_gemm + ms_prod) / ms}
+    ratio = 2.0 if fp8 else 1.0   # nominal dense E4M3 : bf16 tensor rate (4.5 : 2.25 PFLOP/s)
+    out = {"workload": f"prefill {num_seqs}x8192 tokens, hidden {K} -> {pw.width} outputs "
+                       f"(64/8/8/1 heads x 128), fp8 caches; {'E4M3' if fp8 else 'bf16'} operands"
+                       f"{' with per-token / per-output scales' if fp8 else ''}, fp32 accumulate",
+           "ms_per_launch": ms, "tokens_per_s": pw.num_tokens / (ms * 1e-3),
+           "launches_per_step": 1, "status": status,
+           "roofline": {"bound": "tensor", "achieved": tf, "peak": burst * ratio, "unit": "TFLOP/s",
+                        "frac": tf / (burst * ratio), "frac_of_sustained": tf / (sustained * ratio),
+                        "peak_kind": (f"{kind} cuBLAS bf16 (burst; sustained {sustained})"
+                                      + (" x 2, the nominal E4M3 : bf16 ratio" if fp8 else "")),
+                        "flops_per_launch": fl, "traffic": None},
+           "unfused": {"comparator": comparator, "gemm_ms": ms_gemm, "producer_ms": ms_prod}}
+    if ms_gemm is not None:
+        out["unfused"].update(total_ms=ms_gemm + ms_prod,
+                              gemm_tflops=fl / (ms_gemm * 1e-3) / 1e12)
+        out["speedup_vs_unfused"] = (ms_gemm + ms_prod) / ms
+    return out
 
 
 def run_ours(args):
@@ -514,7 +538,8 @@ def run_ours(args):
 
     projection = None
     if not args.no_projection:
-        projection = projection_timing(num_seqs=args.projection_seqs)
+        projection = {"bf16": projection_timing(num_seqs=args.projection_seqs, operand_dtype=0),
+                      "e4m3": projection_timing(num_seqs=args.projection_seqs, operand_dtype=1)}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -629,8 +654,9 @@ def main():
     if args.projection_only:
         from paged_kv_cache_msa_gb300 import build as build_mod
         build_mod.build()
-        print(json.dumps(projection_timing(launches=max(1, args.steps), warmup=args.warmup,
-                                           num_seqs=args.projection_seqs)), flush=True)
+        print(json.dumps({dt: projection_timing(launches=max(1, args.steps), warmup=args.warmup,
+                                                num_seqs=args.projection_seqs, operand_dtype=i)
+                          for i, dt in enumerate(("bf16", "e4m3"))}), flush=True)
         return 0
     if args.indexer_only:
         from paged_kv_cache_msa_gb300 import build as build_mod

@@ -13,9 +13,12 @@
  * What is computed, per token t and projection output j < W, W = (Hq + 2*Hkv +
  * Hiq + Hik) * head_dim:
  *
- *     row[t, j] = bf16_rne( sum_k hidden[t, k] * weight[j, k] )
+ *     row[t, j] = bf16_rne( (sum_k hidden[t, k] * weight[j, k]) * sx[t] * sw[j] )
  *
- * accumulated in fp32 on the tensor cores, then exactly what msa_producer_forward
+ * with the operands bf16, or FP8 E4M3 with dequantisation scales sx (per token)
+ * and sw (per output) -- the pages' "one quantized ... projection"; the sum is
+ * accumulated in fp32 on the tensor cores and scaled as (sum * sx[t]) * sw[j] in
+ * fp32 -- then exactly what msa_producer_forward
  * does to a row it reads (see msa_producer.h): the same configuration, placement,
  * norm, RoPE, compact outputs, cache encodings, scales, padded-slot containment
  * and error checks.  The result equals msa_producer_forward applied to the bf16
@@ -46,14 +49,18 @@ extern "C" {
  * norm weights, q_out, idx_q_out, k_cache, v_cache, idx_k_cache, scales: exactly
  * as for msa_producer_forward (same meaning, layout, nullability and checks).
  *
- * hidden             device bf16 [num_tokens, hidden_row_stride]; the first
- *                    hidden_size elements of each row are the token's hidden state.
- *                    16-byte aligned; hidden_row_stride a multiple of 8 elements.
+ * hidden             device [num_tokens, hidden_row_stride] of operand_dtype; the
+ *                    first hidden_size elements of each row are the token's hidden
+ *                    state.  16-byte aligned; the row stride a multiple of 16 bytes.
  * hidden_size        K >= 1 (any value; no multiple is required).
- * weight             device bf16 [W, weight_row_stride], output-major: row j holds
- *                    the K weights of projection output j, in the section order
- *                    [Q | K | V | index-Q | index-K], each section head-major.
- *                    16-byte aligned; weight_row_stride a multiple of 8, >= K.
+ * weight             device [W, weight_row_stride] of operand_dtype, output-major:
+ *                    row j holds the K weights of projection output j, in the
+ *                    section order [Q | K | V | index-Q | index-K], each section
+ *                    head-major.  16-byte aligned; the row stride a multiple of 16
+ *                    bytes, >= K.
+ * operand_dtype      MSA_DTYPE_BF16 or MSA_DTYPE_FP8_E4M3 (both operands).
+ * hidden_scales      optional device fp32 [num_tokens]: sx (NULL: 1).
+ * weight_scales      optional device fp32 [W]: sw (NULL: 1).
  * rows_out           optional (NULL: not written) device bf16 [num_tokens,
  *                    rows_out_stride]: the bf16 projection rows themselves.
  *                    16-byte aligned; rows_out_stride a multiple of 8, >= W.
@@ -73,7 +80,9 @@ extern "C" {
 msa_status msa_projection_forward(const msa_producer_cfg *cfg, int64_t num_tokens,
                                   const void *hidden, int64_t hidden_size,
                                   int64_t hidden_row_stride, const void *weight,
-                                  int64_t weight_row_stride, const int32_t *positions,
+                                  int64_t weight_row_stride, msa_dtype operand_dtype,
+                                  const float *hidden_scales, const float *weight_scales,
+                                  const int32_t *positions,
                                   const int64_t *slot_mapping, const int32_t *page_table,
                                   int64_t page_table_len, const void *q_norm_w,
                                   const void *k_norm_w, const void *idx_q_norm_w,
@@ -92,7 +101,9 @@ msa_status msa_projection_forward(const msa_producer_cfg *cfg, int64_t num_token
 msa_status msa_projection_validate(const msa_producer_cfg *cfg, int64_t num_tokens,
                                    const void *hidden, int64_t hidden_size,
                                    int64_t hidden_row_stride, const void *weight,
-                                   int64_t weight_row_stride, const int32_t *positions,
+                                   int64_t weight_row_stride, msa_dtype operand_dtype,
+                                   const float *hidden_scales, const float *weight_scales,
+                                   const int32_t *positions,
                                    const int64_t *slot_mapping, const int32_t *page_table,
                                    int64_t page_table_len, const void *q_norm_w,
                                    const void *k_norm_w, const void *idx_q_norm_w,

@@ -120,8 +120,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.msa_indexer_forward.argtypes = [ctypes.POINTER(MsaIndexerCfg), i64, vp, vp, vp, vp, i64,
                                           cachep, vp, vp, vp, vp]
         L.msa_indexer_forward.restype = ctypes.c_int
-        proj = [cfgp, i64, vp, i64, i64, vp, i64, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp,
-                cachep, cachep, cachep, vp, vp, i64, vp]
+        proj = [cfgp, i64, vp, i64, i64, vp, i64, ctypes.c_int, vp, vp, vp, vp, vp, i64, vp, vp,
+                vp, vp, vp, vp, cachep, cachep, cachep, vp, vp, i64, vp]
         L.msa_projection_forward.argtypes = proj + [vp]
         L.msa_projection_forward.restype = ctypes.c_int
         L.msa_projection_validate.argtypes = proj
@@ -212,46 +212,50 @@ def msa_producer_validate(cfg, num_tokens, qkv, qkv_row_stride, positions, slot_
 
 
 def _projection_args(cfg, num_tokens, hidden, hidden_size, hidden_row_stride, weight,
-                     weight_row_stride, positions, slot_mapping, page_table, page_table_len,
-                     q_norm_w, k_norm_w, idx_q_norm_w, idx_k_norm_w, q_out, idx_q_out, k_cache,
-                     v_cache, idx_k_cache, scales, rows_out, rows_out_stride, status):
+                     weight_row_stride, operand_dtype, hidden_scales, weight_scales, positions,
+                     slot_mapping, page_table, page_table_len, q_norm_w, k_norm_w, idx_q_norm_w,
+                     idx_k_norm_w, q_out, idx_q_out, k_cache, v_cache, idx_k_cache, scales,
+                     rows_out, rows_out_stride, status):
     return (ctypes.byref(cfg) if cfg is not None else None, int(num_tokens), hidden,
-            int(hidden_size), int(hidden_row_stride), weight, int(weight_row_stride), positions,
-            slot_mapping, page_table, int(page_table_len), q_norm_w, k_norm_w, idx_q_norm_w,
-            idx_k_norm_w, q_out, idx_q_out, _ref(k_cache), _ref(v_cache), _ref(idx_k_cache),
-            scales, rows_out, int(rows_out_stride), status)
+            int(hidden_size), int(hidden_row_stride), weight, int(weight_row_stride),
+            int(operand_dtype), hidden_scales, weight_scales, positions, slot_mapping, page_table,
+            int(page_table_len), q_norm_w, k_norm_w, idx_q_norm_w, idx_k_norm_w, q_out, idx_q_out,
+            _ref(k_cache), _ref(v_cache), _ref(idx_k_cache), scales, rows_out,
+            int(rows_out_stride), status)
 
 
 def msa_projection_forward(cfg, num_tokens, hidden, hidden_size, hidden_row_stride, weight,
-                           weight_row_stride, positions, slot_mapping, page_table, page_table_len,
-                           q_norm_w, k_norm_w, idx_q_norm_w, idx_k_norm_w, q_out, idx_q_out,
-                           k_cache, v_cache, idx_k_cache, scales, rows_out=None,
-                           rows_out_stride=0, status=None, stream=0, check=True) -> int:
+                           weight_row_stride, operand_dtype, hidden_scales, weight_scales,
+                           positions, slot_mapping, page_table, page_table_len, q_norm_w,
+                           k_norm_w, idx_q_norm_w, idx_k_norm_w, q_out, idx_q_out, k_cache,
+                           v_cache, idx_k_cache, scales, rows_out=None, rows_out_stride=0,
+                           status=None, stream=0, check=True) -> int:
     """The projection GEMM with the producer in its epilogue (one launch); pointers
     are integers (device addresses) or None.  Raises MsaError unless MSA_OK
     (``check=False`` returns the status)."""
     L = load()
     s = L.msa_projection_forward(*_projection_args(
         cfg, num_tokens, hidden, hidden_size, hidden_row_stride, weight, weight_row_stride,
-        positions, slot_mapping, page_table, page_table_len, q_norm_w, k_norm_w, idx_q_norm_w,
-        idx_k_norm_w, q_out, idx_q_out, k_cache, v_cache, idx_k_cache, scales, rows_out,
-        rows_out_stride, status), stream)
+        operand_dtype, hidden_scales, weight_scales, positions, slot_mapping, page_table,
+        page_table_len, q_norm_w, k_norm_w, idx_q_norm_w, idx_k_norm_w, q_out, idx_q_out, k_cache,
+        v_cache, idx_k_cache, scales, rows_out, rows_out_stride, status), stream)
     if check and s != MSA_OK:
         raise MsaError(s, "msa_projection_forward", last_error_detail())
     return s
 
 
 def msa_projection_validate(cfg, num_tokens, hidden, hidden_size, hidden_row_stride, weight,
-                            weight_row_stride, positions, slot_mapping, page_table,
-                            page_table_len, q_norm_w, k_norm_w, idx_q_norm_w, idx_k_norm_w,
-                            q_out, idx_q_out, k_cache, v_cache, idx_k_cache, scales,
-                            rows_out=None, rows_out_stride=0, status=None) -> int:
+                            weight_row_stride, operand_dtype, hidden_scales, weight_scales,
+                            positions, slot_mapping, page_table, page_table_len, q_norm_w,
+                            k_norm_w, idx_q_norm_w, idx_k_norm_w, q_out, idx_q_out, k_cache,
+                            v_cache, idx_k_cache, scales, rows_out=None, rows_out_stride=0,
+                            status=None) -> int:
     """The checks of msa_projection_forward alone; returns the status."""
     return load().msa_projection_validate(*_projection_args(
         cfg, num_tokens, hidden, hidden_size, hidden_row_stride, weight, weight_row_stride,
-        positions, slot_mapping, page_table, page_table_len, q_norm_w, k_norm_w, idx_q_norm_w,
-        idx_k_norm_w, q_out, idx_q_out, k_cache, v_cache, idx_k_cache, scales, rows_out,
-        rows_out_stride, status))
+        operand_dtype, hidden_scales, weight_scales, positions, slot_mapping, page_table,
+        page_table_len, q_norm_w, k_norm_w, idx_q_norm_w, idx_k_norm_w, q_out, idx_q_out, k_cache,
+        v_cache, idx_k_cache, scales, rows_out, rows_out_stride, status))
 
 
 def make_indexer_cfg(num_heads, head_dim, page_size=64, block_tokens=128, topk=16,

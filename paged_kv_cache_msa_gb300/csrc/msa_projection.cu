@@ -60,22 +60,24 @@ constexpr int kBM = 128;                  // tokens per CTA and tile half: tenso
 constexpr int kPairM = 2 * kBM;           // tokens per cluster tile (the 2-SM MMA's M)
 constexpr int kBN = 256;                  // projection outputs per tile: accumulator columns
 constexpr int kHalfN = kBN / 2;           // weight rows each CTA stages
-constexpr int kBK = 64;                   // K elements per stage: one 128-byte swizzle row
+constexpr int kBKBytes = 128;             // K bytes per stage: one 128-byte swizzle row
 constexpr int kStages = MSA_PROJ_STAGES;
-constexpr int kThreads = 192;
-constexpr uint32_t kTileABytes = kBM * kBK * 2;
-constexpr uint32_t kTileBBytes = kHalfN * kBK * 2;
+constexpr int kEpilogueWarps = 8;     // two per tensor-memory lane quarter
+constexpr int kThreads = 64 + 32 * kEpilogueWarps;
+constexpr uint32_t kTileABytes = kBM * kBKBytes;
+constexpr uint32_t kTileBBytes = kHalfN * kBKBytes;
 constexpr uint32_t kStageBytes = kTileABytes + kTileBBytes;  // per CTA
 constexpr int kDynSmem = kStages * kStageBytes + 1024;        // + alignment slack for the ring
 constexpr uint32_t kTmemCols = 2 * kBN;
 constexpr int kMaxRotaryHalf = 64;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
-// tcgen05 instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
-// and B (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bit 17,
-// M >> 4 at bit 24 (M = 256: the pair's tile).
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
-                            ((uint32_t)(kPairM >> 4) << 24);
+// tcgen05 instruction descriptors: fp32 accumulator (bits 4-5 = 1), A and B formats
+// at bits 7-9 and 10-12 (kind::f16: 1 = bf16; kind::f8f6f4: 0 = E4M3), both K-major
+// (bits 15, 16 = 0), N >> 3 at bit 17, M >> 4 at bit 24 (M = 256: the pair's tile).
+constexpr uint32_t kIdescShape = ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kPairM >> 4) << 24);
+constexpr uint32_t kIdescBf16 = (1u << 4) | (1u << 7) | (1u << 10) | kIdescShape;
+constexpr uint32_t kIdescE4m3 = (1u << 4) | kIdescShape;
 
 struct CacheArgs {
     uint8_t *data;  // nullptr: not written
@@ -99,6 +101,8 @@ struct Params {
     const float *scales;
     uint16_t *rows_out;
     int64_t rows_out_stride;
+    const float *hidden_scales;  // per token (nullptr: 1)
+    const float *weight_scales;  // per output (nullptr: 1)
     uint32_t *status;
     int64_t num_tokens;
     int32_t num_k_blocks;
@@ -165,10 +169,14 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
                  : "memory");
 }
 
-// arrive on an mbarrier of another CTA of the cluster (shared::cluster address)
+// Arrive on an mbarrier of any CTA of the cluster (shared::cluster address), with
+// no memory ordering: it only tells the MMA issuer that this warp's tensor-memory
+// reads are complete (tcgen05.wait::ld and tcgen05.fence::before_thread_sync
+// precede it).  A release here would make the warp wait for all of its global
+// stores -- the compact outputs and cache rows -- to be acknowledged first.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar)
 {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                  : "memory");
 }
 
@@ -217,15 +225,24 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
     return d;
 }
 
-// The 2-SM MMA: A and B descriptors address the leader's tiles; the peer's halves
-// sit at the same shared-memory offsets in the peer CTA.
+// The 2-SM MMA (32 bytes of K per row: 16 bf16 or 32 E4M3 elements): A and B
+// descriptors address the leader's tiles; the peer's halves sit at the same
+// shared-memory offsets in the peer CTA.
+template <bool FP8>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc)
 {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
-        : "memory");
+    if (FP8)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a), "l"(b), "r"(kIdescE4m3), "r"(acc)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a), "l"(b), "r"(kIdescBf16), "r"(acc)
+            : "memory");
 }
 
 // The mbarrier at this offset in both CTAs of the pair arrives once every
@@ -310,12 +327,32 @@ __device__ __forceinline__ void st_v2(void *p, uint32_t a, uint32_t b)
     asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
 }
 
-// 8 accumulator words -> the bf16 row values (as bf16 pairs) and their fp32 values
-__device__ __forceinline__ void round_row8(const uint32_t (&acc)[8], uint32_t (&bits)[4], float (&x)[8])
+// The dequantised accumulator of output `col`: (acc * hidden scale) * weight
+// scale; the accumulator itself when the projection has no scales.
+struct RowScale {
+    float sx;             // this token's scale
+    const float *sw;      // per-output scales, or nullptr
+    bool any;
+};
+
+__device__ __forceinline__ float dequant(const RowScale &rs, uint32_t acc, int col)
+{
+    const float a = __uint_as_float(acc);
+    if (!rs.any)
+        return a;
+    const float v = a * rs.sx;
+    return rs.sw ? v * __ldg(rs.sw + col) : v;
+}
+
+// 8 accumulator words of outputs [col, col + 8) -> the bf16 row values (as bf16
+// pairs) and their fp32 values
+__device__ __forceinline__ void round_row8(const RowScale &rs, const uint32_t (&acc)[8], int col,
+                                           uint32_t (&bits)[4], float (&x)[8])
 {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        bits[j] = pack_bf16x2(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1]));
+        bits[j] = pack_bf16x2(dequant(rs, acc[2 * j], col + 2 * j),
+                              dequant(rs, acc[2 * j + 1], col + 2 * j + 1));
         x[2 * j] = bf16_lo(bits[j]);
         x[2 * j + 1] = bf16_hi(bits[j]);
     }
@@ -377,49 +414,189 @@ __device__ __forceinline__ Head head_of(const Params &p, int g)
     return r;
 }
 
-// Stores 8 finished values of dims [d0, d0 + 8) of head hd for token t.
+// Where one head row of one token goes: its first byte, how it is encoded, and the
+// reciprocal of its cache scale; computed once per (token, head).
+struct Dest {
+    uint8_t *row;  // nullptr: nothing is written (padded token, or a cache not taken)
+    int fp8;       // 1: E4M3 codes of x * inv; 0: bf16
+    float inv;
+};
+
 template <int D>
-__device__ __forceinline__ void emit8(const Params &p, const Head &hd, int64_t t, bool live,
-                                      const Place &pl, int d0, const float (&y)[8])
+__device__ __forceinline__ Dest make_dest(const Params &p, const Head &hd, int64_t t, bool live,
+                                          const Place &pl)
 {
-    if (!live)
-        return;
+    Dest ds;
+    ds.row = nullptr;
+    ds.fp8 = 0;
+    ds.inv = 1.0f;
+    if (!live || hd.sec < 0)
+        return ds;
     if (hd.sec == 0 || hd.sec == 3) {
-        uint16_t *dst = hd.sec == 0 ? p.q_out + ((int64_t)t * p.hq + hd.h) * D
-                                    : p.idx_q_out + ((int64_t)t * p.hiq + hd.h) * D;
-        st_v4(dst + d0, pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-              pack_bf16x2(y[6], y[7]));
-        return;
+        uint16_t *r = hd.sec == 0 ? p.q_out + ((int64_t)t * p.hq + hd.h) * D
+                                  : p.idx_q_out + ((int64_t)t * p.hiq + hd.h) * D;
+        ds.row = reinterpret_cast<uint8_t *>(r);
+        return ds;
     }
     const int ci = hd.sec == 1 ? 0 : hd.sec == 2 ? 1 : 2;
     if (!((pl.valid >> ci) & 1))
-        return;
+        return ds;
     const CacheArgs &cc = p.cache[ci];
     const int64_t e = pl.page * cc.stride_page + (int64_t)hd.h * cc.stride_head +
-                      (int64_t)pl.off * cc.stride_token + d0;
+                      (int64_t)pl.off * cc.stride_token;
     if (cc.fp8) {
         const int si = p.scale_mode == MSA_SCALE_PER_HEAD
                            ? (ci == 0 ? hd.h : ci == 1 ? p.hkv + hd.h : 2 * p.hkv + hd.h)
                            : ci;
-        const float inv = __frcp_rn(__ldg(p.scales + si));
-        st_v2(cc.data + e, pack_e4m3x4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv),
+        ds.row = cc.data + e;
+        ds.fp8 = 1;
+        ds.inv = __frcp_rn(__ldg(p.scales + si));
+    } else {
+        ds.row = cc.data + 2 * e;
+    }
+    return ds;
+}
+
+// Stores 8 finished values of dims [d0, d0 + 8) of a head row.
+__device__ __forceinline__ void emit8(const Dest &ds, int d0, const float (&y)[8])
+{
+    if (!ds.row)
+        return;
+    if (ds.fp8) {
+        const float inv = ds.inv;
+        st_v2(ds.row + d0, pack_e4m3x4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv),
               pack_e4m3x4(y[4] * inv, y[5] * inv, y[6] * inv, y[7] * inv));
     } else {
-        st_v4(reinterpret_cast<uint16_t *>(cc.data) + e, pack_bf16x2(y[0], y[1]),
-              pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+        st_v4(ds.row + 2 * d0, pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+              pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
     }
 }
 
-// taddr: tensor-memory address of this warp's lanes at the tile's first column
 // norm weight element i of a tensor (unit weight when absent)
 __device__ __forceinline__ float norm_weight(const uint16_t *w, int i)
 {
     return w ? __uint_as_float((uint32_t)__ldg(w + i) << 16) : 1.0f;
 }
 
+// which of the four norm weights a section takes (Q, K, idx-Q, idx-K)
+__device__ __forceinline__ int norm_index(int sec)
+{
+    return sec == 0 ? 0 : sec == 1 ? 1 : sec == 3 ? 2 : 3;
+}
+
+// Sine and cosine of a RoPE angle.  Below 2^16 the angle is reduced to [-pi, pi]
+// by k = rint(a / 2pi), r = a - k * 2pi, with 2pi split into three floats whose
+// first, 6.28125, has 8 significant bits so that k * 6.28125 is exact (Cody and
+// Waite's additive range reduction), and the hardware approximations take r
+// (absolute error about 2^-21 on [-pi, pi]); larger angles use sincosf.
+__device__ __forceinline__ void rope_sincos(float a, float *s, float *c)
+{
+    if (fabsf(a) < 65536.0f) {
+        const float k = rintf(a * 0.15915494f);
+        float r = fmaf(-k, 6.28125f, a);
+        r = fmaf(-k, 1.9353071693331003e-3f, r);
+        r = fmaf(-k, 1.0253131677018246e-11f, r);
+        __sincosf(r, s, c);
+    } else {
+        sincosf(a, s, c);
+    }
+}
+
+// One head of one token row, for NeoX RoPE over the first ROT of D dims (ROT = D,
+// D/2 or 0).  The accumulator is read from tensor memory once and the bf16 row
+// is kept in registers; the head's norm weights and per-output scales are held by
+// the lanes of the warp (lane l: dims l, l + 32, ...) and shuffled to every lane.
+template <int D, int ROT>
+__device__ __forceinline__ void head_fast(const Params &p, const Head &hd, uint32_t taddr, int col,
+                                          int64_t t, bool live, const Place &pl, int pos,
+                                          const RowScale &rs, int lane)
+{
+    constexpr int NW = D / 32;
+    const bool normed = hd.sec != 2;
+    const Dest ds = make_dest<D>(p, hd, t, live, pl);
+    const uint16_t *w = normed ? p.norm_w[norm_index(hd.sec)] : nullptr;
+    float wr[NW], swr[NW];
+#pragma unroll
+    for (int m = 0; m < NW; ++m) {
+        wr[m] = norm_weight(w, 32 * m + lane);
+        swr[m] = rs.sw ? __ldg(rs.sw + col + 32 * m + lane) : 1.0f;
+    }
+
+    // pass 1: the bf16 row (dequantised accumulator, rounded) and its sum of squares
+    uint32_t row[D / 2];
+    float ss = 0.0f;
+#pragma unroll
+    for (int c = 0; c < D; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(taddr + (uint32_t)c, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            float a = __uint_as_float(r[2 * j]), b = __uint_as_float(r[2 * j + 1]);
+            if (rs.any) {
+                a = (a * rs.sx) * __shfl_sync(0xffffffffu, swr[c / 32], 2 * j);
+                b = (b * rs.sx) * __shfl_sync(0xffffffffu, swr[c / 32], 2 * j + 1);
+            }
+            row[c / 2 + j] = pack_bf16x2(a, b);
+            const float ra = bf16_lo(row[c / 2 + j]), rb = bf16_hi(row[c / 2 + j]);
+            ss = fmaf(ra, ra, ss);
+            ss = fmaf(rb, rb, ss);
+        }
+    }
+    if (p.rows_out && live) {
+        uint16_t *dst = p.rows_out + (int64_t)t * p.rows_out_stride + col;
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i)
+            st_v4(dst + 8 * i, row[4 * i], row[4 * i + 1], row[4 * i + 2], row[4 * i + 3]);
+    }
+    auto elt = [&](int i) { return (i & 1) ? bf16_hi(row[i >> 1]) : bf16_lo(row[i >> 1]); };
+    if (!normed) {  // V: the row itself, into its cache
+#pragma unroll
+        for (int c = 0; c < D; c += 8) {
+            float y[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                y[j] = elt(c + j);
+            emit8(ds, c, y);
+        }
+        return;
+    }
+
+    // pass 2: norm, RoPE, store
+    const float rn = rsqrtf(fmaf(ss, 1.0f / (float)D, p.rms_eps));
+    auto wgt = [&](int i) { return __shfl_sync(0xffffffffu, wr[i >> 5], i & 31); };
+    constexpr int H = ROT / 2;
+#pragma unroll
+    for (int k0 = 0; k0 < H; k0 += 8) {
+        float yu[8], yv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float sn, cs;
+            rope_sincos((float)pos * p.inv_freq[k0 + j], &sn, &cs);
+            const float a = (elt(k0 + j) * rn) * wgt(k0 + j);
+            const float b = (elt(k0 + H + j) * rn) * wgt(k0 + H + j);
+            yu[j] = fmaf(-b, sn, a * cs);
+            yv[j] = fmaf(a, sn, b * cs);
+        }
+        emit8(ds, k0, yu);
+        emit8(ds, k0 + H, yv);
+    }
+#pragma unroll
+    for (int c = ROT; c < D; c += 8) {
+        float y[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            y[j] = (elt(c + j) * rn) * wgt(c + j);
+        emit8(ds, c, y);
+    }
+}
+
+// taddr: tensor-memory address of this warp's lanes at the tile's first column.
+// The warp runs the producer on the tile's heads hh with hh % 2 == hgroup (the
+// other epilogue warp of the same tensor-memory lanes takes the rest).
 template <int D>
 __device__ __forceinline__ void epilogue_tile(const Params &p, uint32_t taddr, int n_tile, int64_t t,
-                                              bool live)
+                                              bool live, int hgroup, int lane)
 {
     constexpr int HPT = kBN / D;  // heads per tile
     const int g0 = n_tile * HPT;
@@ -434,13 +611,39 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, uint32_t taddr, i
         pos = __ldg(p.positions + t);
         pl = place_token(p, __ldg(p.slots + t));
     }
+    RowScale rs;
+    rs.sw = p.weight_scales;
+    rs.sx = (p.hidden_scales && live) ? __ldg(p.hidden_scales + t) : 1.0f;
+    rs.any = p.hidden_scales || p.weight_scales;
+    const int col0 = n_tile * kBN;  // projection output of the tile's first column
+
+    const int rd = p.rotary_dim;
+    if (p.rope_style == MSA_ROPE_NEOX && (rd == D || rd == D / 2 || rd == 0)) {
+#pragma unroll
+        for (int hh = hgroup; hh < HPT; hh += 2) {
+            const Head hd = head_of(p, g0 + hh);
+            if (hd.sec < 0)
+                continue;
+            const uint32_t ta = taddr + (uint32_t)(hh * D);
+            const int col = col0 + hh * D;
+            if (rd == D)
+                head_fast<D, D>(p, hd, ta, col, t, live, pl, pos, rs, lane);
+            else if (rd == D / 2)
+                head_fast<D, D / 2>(p, hd, ta, col, t, live, pl, pos, rs, lane);
+            else
+                head_fast<D, 0>(p, hd, ta, col, t, live, pl, pos, rs, lane);
+        }
+        return;
+    }
+
+    // any other RoPE: the accumulator is read twice (norm factor, then values)
 
     // pass 1: bf16 row values, optional row store, and each head's norm factor
     float rn[HPT];
 #pragma unroll
     for (int hh = 0; hh < HPT; ++hh) {
         rn[hh] = 0.0f;
-        if (g0 + hh >= p.htot)
+        if (g0 + hh >= p.htot || (hh & 1) != hgroup)
             continue;
         float ss = 0.0f;
 #pragma unroll
@@ -451,7 +654,8 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, uint32_t taddr, i
             uint32_t bits[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                bits[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                const int col = col0 + hh * D + c + 2 * j;
+                bits[j] = pack_bf16x2(dequant(rs, r[2 * j], col), dequant(rs, r[2 * j + 1], col + 1));
                 const float a = bf16_lo(bits[j]), b = bf16_hi(bits[j]);
                 ss = fmaf(a, a, ss);
                 ss = fmaf(b, b, ss);
@@ -468,13 +672,16 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, uint32_t taddr, i
     }
 
     Head hd[HPT];
+    Dest ds[HPT];
     bool normed_any = false;
 #pragma unroll
     for (int hh = 0; hh < HPT; ++hh) {
         hd[hh] = head_of(p, g0 + hh);
+        if ((hh & 1) != hgroup)
+            hd[hh].sec = -1;  // the other warp's head
+        ds[hh] = make_dest<D>(p, hd[hh], t, live, pl);
         normed_any |= hd[hh].sec >= 0 && hd[hh].sec != 2;
     }
-    const int rd = p.rotary_dim;
 
     // pass 2a: normed heads (Q, K, idx-Q, idx-K)
     if (normed_any) {
@@ -496,8 +703,8 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, uint32_t taddr, i
                     tmem_ld8(taddr + (uint32_t)(hh * D + k0), ru);
                     tmem_ld8(taddr + (uint32_t)(hh * D + k0 + half), rv);
                     tmem_wait_ld();
-                    round_row8(ru, bu, u);
-                    round_row8(rv, bv, v);
+                    round_row8(rs, ru, col0 + hh * D + k0, bu, u);
+                    round_row8(rs, rv, col0 + hh * D + k0 + half, bv, v);
                     float yu[8], yv[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -506,8 +713,8 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, uint32_t taddr, i
                         yu[j] = fmaf(-b, sn[j], a * cs[j]);
                         yv[j] = fmaf(a, sn[j], b * cs[j]);
                     }
-                    emit8<D>(p, hd[hh], t, live, pl, k0, yu);
-                    emit8<D>(p, hd[hh], t, live, pl, k0 + half, yv);
+                    emit8(ds[hh], k0, yu);
+                    emit8(ds[hh], k0 + half, yv);
                 }
             }
             // pass-through dims [rd, D)
@@ -521,11 +728,11 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, uint32_t taddr, i
                     float u[8], y[8];
                     tmem_ld8(taddr + (uint32_t)(hh * D + c), ru);
                     tmem_wait_ld();
-                    round_row8(ru, bu, u);
+                    round_row8(rs, ru, col0 + hh * D + c, bu, u);
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
                         y[j] = (u[j] * rn[hh]) * norm_weight(w, c + j);
-                    emit8<D>(p, hd[hh], t, live, pl, c, y);
+                    emit8(ds[hh], c, y);
                 }
             }
         } else {
@@ -547,7 +754,7 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, uint32_t taddr, i
                     float u[8], y[8];
                     tmem_ld8(taddr + (uint32_t)(hh * D + c), ru);
                     tmem_wait_ld();
-                    round_row8(ru, bu, u);
+                    round_row8(rs, ru, col0 + hh * D + c, bu, u);
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
                         y[j] = (u[j] * rn[hh]) * norm_weight(w, c + j);
@@ -559,7 +766,7 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, uint32_t taddr, i
                             y[2 * j + 1] = fmaf(a, sn[j], b * cs[j]);
                         }
                     }
-                    emit8<D>(p, hd[hh], t, live, pl, c, y);
+                    emit8(ds[hh], c, y);
                 }
             }
         }
@@ -575,8 +782,8 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, uint32_t taddr, i
             float u[8];
             tmem_ld8(taddr + (uint32_t)(hh * D + c), ru);
             tmem_wait_ld();
-            round_row8(ru, bu, u);
-            emit8<D>(p, hd[hh], t, live, pl, c, u);
+            round_row8(rs, ru, col0 + hh * D + c, bu, u);
+            emit8(ds[hh], c, u);
         }
     }
 }
@@ -596,7 +803,7 @@ __device__ __forceinline__ void tile_coords(const Params &p, int64_t tile, int &
 // the kernel
 // ---------------------------------------------------------------------------
 
-template <int D>
+template <int D, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
 msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
                       const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ Params p)
@@ -622,7 +829,7 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bar_tfull[b]), 1);
-            mbar_init(smem_u32(&bar_tempty[b]), 2 * 4);  // one arrival per epilogue warp of the pair
+            mbar_init(smem_u32(&bar_tempty[b]), 2 * kEpilogueWarps);  // each epilogue warp of the pair
         }
         mbar_init(smem_u32(&bar_drain), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -644,6 +851,7 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
+    constexpr int kBKElems = FP8 ? kBKBytes : kBKBytes / 2;  // K elements per stage
     const int64_t num_tiles = (int64_t)p.m_tiles * p.n_tiles;
     const int64_t cluster_id = blockIdx.x / 2;
     const int64_t num_clusters = gridDim.x / 2;
@@ -668,8 +876,8 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
                         mbar_expect_tx(full, 2 * kStageBytes);
                     const uint32_t full_leader = map_to_rank(full, 0);
                     const uint32_t a = ring + stage * kStageBytes;
-                    tma_load_2d(a, &tmap_x, kb * kBK, row_x, full_leader);
-                    tma_load_2d(a + kTileABytes, &tmap_w, kb * kBK, row_w, full_leader);
+                    tma_load_2d(a, &tmap_x, kb * kBKElems, row_x, full_leader);
+                    tma_load_2d(a + kTileABytes, &tmap_w, kb * kBKElems, row_w, full_leader);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1;
@@ -705,9 +913,9 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
                     const uint32_t a = ring + stage * kStageBytes;
                     const uint32_t bb = a + kTileABytes;
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k)
-                        tc_mma(d_tmem, sw128_desc(a + 32u * k), sw128_desc(bb + 32u * k),
-                               (kb | k) != 0);
+                    for (int k = 0; k < kBKBytes / 32; ++k)
+                        tc_mma<FP8>(d_tmem, sw128_desc(a + 32u * k), sw128_desc(bb + 32u * k),
+                                    (kb | k) != 0);
                     tc_commit_both(smem_u32(&bar_empty[stage]));
                     if (++stage == kStages) {
                         stage = 0;
@@ -727,6 +935,7 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
     } else {
         // ---------------- epilogue (both CTAs) ----------------
         const int quarter = warp & 3;  // the tensor-memory lanes this warp may read
+        const int hgroup = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         uint32_t acc_i = 0;
@@ -741,7 +950,7 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
             }
             tc_fence_after();
             const int64_t t = (int64_t)m * kPairM + (int64_t)rank * kBM + row;
-            epilogue_tile<D>(p, tmem + lane_base + b * kBN, n, t, t < p.num_tokens);
+            epilogue_tile<D>(p, tmem + lane_base + b * kBN, n, t, t < p.num_tokens, hgroup, lane);
             tc_fence_before();
             __syncwarp();
             if (lane == 0)  // this warp is done reading accumulator b
@@ -788,7 +997,7 @@ std::mutex g_mu;
 EncodeTiledFn g_encode = nullptr;
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
-    int clusters[2] = {0, 0};  // resident clusters of two CTAs, per head_dim variant
+    int clusters[4] = {0, 0, 0, 0};  // resident clusters of two CTAs, per kernel variant
 };
 DeviceInfo g_dev[kMaxDevices];
 
@@ -806,19 +1015,21 @@ EncodeTiledFn encoder()
     return g_encode;
 }
 
-// A [rows, cols] bf16 matrix with a row stride of `stride` elements, read in boxes
-// of box_rows x 64 with the 128-byte swizzle; out-of-range elements read as zero.
+// A [rows, cols] matrix of bf16 (elem_size 2) or 8-bit codes (1) with a row stride
+// of `stride` elements, read in boxes of box_rows x 128 bytes with the 128-byte
+// swizzle; out-of-range elements read as zero.
 bool encode_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t stride,
-                int box_rows)
+                int box_rows, int elem_size)
 {
     EncodeTiledFn enc = encoder();
     if (!enc)
         return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)stride * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    cuuint64_t strides[1] = {(cuuint64_t)stride * (cuuint64_t)elem_size};
+    cuuint32_t box[2] = {(cuuint32_t)(kBKBytes / elem_size), (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+    return enc(m, elem_size == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+               const_cast<void *>(base), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -839,7 +1050,8 @@ void fill_cache(CacheArgs &a, const msa_cache_desc *c)
 
 msa_status validate(const msa_producer_cfg *cfg, int64_t num_tokens, const void *hidden,
                     int64_t hidden_size, int64_t hidden_row_stride, const void *weight,
-                    int64_t weight_row_stride, const int32_t *positions,
+                    int64_t weight_row_stride, msa_dtype operand_dtype, const float *hidden_scales,
+                    const float *weight_scales, const int32_t *positions,
                     const int64_t *slot_mapping, const int32_t *page_table,
                     int64_t page_table_len, const void *q_norm_w, const void *k_norm_w,
                     const void *idx_q_norm_w, const void *idx_k_norm_w, void *q_out,
@@ -859,14 +1071,19 @@ msa_status validate(const msa_producer_cfg *cfg, int64_t num_tokens, const void 
         return fail(MSA_ERR_UNSUPPORTED, "num_tokens %lld (limit 2^31 - 257)", (long long)num_tokens);
     if (!hidden || !weight)
         return fail(MSA_ERR_INVALID_ARGUMENT, "hidden and weight are required");
+    if (operand_dtype != MSA_DTYPE_BF16 && operand_dtype != MSA_DTYPE_FP8_E4M3)
+        return fail(MSA_ERR_UNSUPPORTED, "operand_dtype %d", (int)operand_dtype);
+    const int64_t align_elems = operand_dtype == MSA_DTYPE_BF16 ? 8 : 16;  // 16 bytes
     if (hidden_size < 1)
         return fail(MSA_ERR_INVALID_ARGUMENT, "hidden_size %lld", (long long)hidden_size);
     if (hidden_row_stride < hidden_size || weight_row_stride < hidden_size)
         return fail(MSA_ERR_INVALID_ARGUMENT, "row strides must be at least hidden_size");
-    if (!aligned(hidden, 16) || !aligned(weight, 16) || hidden_row_stride % 8 ||
-        weight_row_stride % 8)
+    if (!aligned(hidden, 16) || !aligned(weight, 16) || hidden_row_stride % align_elems ||
+        weight_row_stride % align_elems)
         return fail(MSA_ERR_MISALIGNED,
-                    "hidden / weight must be 16-byte aligned with row strides of 8k elements");
+                    "hidden / weight must be 16-byte aligned with row strides of 16 bytes");
+    if ((hidden_scales && !aligned(hidden_scales, 4)) || (weight_scales && !aligned(weight_scales, 4)))
+        return fail(MSA_ERR_MISALIGNED, "scales misaligned");
     if (hidden_size > ((int64_t)1 << 31) || W > ((int64_t)1 << 31) ||
         hidden_row_stride > ((int64_t)1 << 36) || weight_row_stride > ((int64_t)1 << 36))
         return fail(MSA_ERR_UNSUPPORTED, "hidden_size, width or row stride out of range");
@@ -890,6 +1107,7 @@ msa_status validate(const msa_producer_cfg *cfg, int64_t num_tokens, const void 
 extern "C" msa_status msa_projection_validate(
     const msa_producer_cfg *cfg, int64_t num_tokens, const void *hidden, int64_t hidden_size,
     int64_t hidden_row_stride, const void *weight, int64_t weight_row_stride,
+    msa_dtype operand_dtype, const float *hidden_scales, const float *weight_scales,
     const int32_t *positions, const int64_t *slot_mapping, const int32_t *page_table,
     int64_t page_table_len, const void *q_norm_w, const void *k_norm_w, const void *idx_q_norm_w,
     const void *idx_k_norm_w, void *q_out, void *idx_q_out, const msa_cache_desc *k_cache,
@@ -897,7 +1115,8 @@ extern "C" msa_status msa_projection_validate(
     void *rows_out, int64_t rows_out_stride, uint32_t *status)
 {
     return validate(cfg, num_tokens, hidden, hidden_size, hidden_row_stride, weight,
-                    weight_row_stride, positions, slot_mapping, page_table, page_table_len,
+                    weight_row_stride, operand_dtype, hidden_scales, weight_scales, positions,
+                    slot_mapping, page_table, page_table_len,
                     q_norm_w, k_norm_w, idx_q_norm_w, idx_k_norm_w, q_out, idx_q_out, k_cache,
                     v_cache, idx_k_cache, scales, rows_out, rows_out_stride, status);
 }
@@ -905,6 +1124,7 @@ extern "C" msa_status msa_projection_validate(
 extern "C" msa_status msa_projection_forward(
     const msa_producer_cfg *cfg, int64_t num_tokens, const void *hidden, int64_t hidden_size,
     int64_t hidden_row_stride, const void *weight, int64_t weight_row_stride,
+    msa_dtype operand_dtype, const float *hidden_scales, const float *weight_scales,
     const int32_t *positions, const int64_t *slot_mapping, const int32_t *page_table,
     int64_t page_table_len, const void *q_norm_w, const void *k_norm_w, const void *idx_q_norm_w,
     const void *idx_k_norm_w, void *q_out, void *idx_q_out, const msa_cache_desc *k_cache,
@@ -912,7 +1132,8 @@ extern "C" msa_status msa_projection_forward(
     void *rows_out, int64_t rows_out_stride, uint32_t *status, cudaStream_t stream)
 {
     msa_status s = validate(cfg, num_tokens, hidden, hidden_size, hidden_row_stride, weight,
-                            weight_row_stride, positions, slot_mapping, page_table, page_table_len,
+                            weight_row_stride, operand_dtype, hidden_scales, weight_scales,
+                            positions, slot_mapping, page_table, page_table_len,
                             q_norm_w, k_norm_w, idx_q_norm_w, idx_k_norm_w, q_out, idx_q_out,
                             k_cache, v_cache, idx_k_cache, scales, rows_out, rows_out_stride, status);
     if (s != MSA_OK || num_tokens == 0)
@@ -940,9 +1161,14 @@ extern "C" msa_status msa_projection_forward(
     p.scales = scales;
     p.rows_out = static_cast<uint16_t *>(rows_out);
     p.rows_out_stride = rows_out_stride;
+    p.hidden_scales = hidden_scales;
+    p.weight_scales = weight_scales;
     p.status = status;
     p.num_tokens = num_tokens;
-    p.num_k_blocks = (int32_t)((hidden_size + kBK - 1) / kBK);
+    const bool fp8 = operand_dtype == MSA_DTYPE_FP8_E4M3;
+    const int es = fp8 ? 1 : 2;
+    const int64_t k_per_block = kBKBytes / es;
+    p.num_k_blocks = (int32_t)((hidden_size + k_per_block - 1) / k_per_block);
     p.m_tiles = (int32_t)((num_tokens + kPairM - 1) / kPairM);
     p.n_tiles = (int32_t)((W + kBN - 1) / kBN);
     p.n_group = p.n_tiles < MSA_PROJ_NGROUP ? p.n_tiles : MSA_PROJ_NGROUP;
@@ -966,16 +1192,19 @@ extern "C" msa_status msa_projection_forward(
                                                2.0 * (double)k / (double)cfg->rotary_dim));
 
     CUtensorMap mx, mw;
-    if (!encode_map(&mx, hidden, num_tokens, hidden_size, hidden_row_stride, kBM) ||
-        !encode_map(&mw, weight, W, hidden_size, weight_row_stride, kHalfN))
+    if (!encode_map(&mx, hidden, num_tokens, hidden_size, hidden_row_stride, kBM, es) ||
+        !encode_map(&mw, weight, W, hidden_size, weight_row_stride, kHalfN, es))
         return fail(MSA_ERR_CUDA, "tensor map encoding failed");
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return fail(MSA_ERR_CUDA, "cudaGetDevice failed");
-    const void *fn = D == 128 ? reinterpret_cast<const void *>(&msa_projection_kernel<128>)
-                              : reinterpret_cast<const void *>(&msa_projection_kernel<64>);
-    const int vi = D == 128 ? 1 : 0;
+    const void *fns[4] = {reinterpret_cast<const void *>(&msa_projection_kernel<64, false>),
+                          reinterpret_cast<const void *>(&msa_projection_kernel<128, false>),
+                          reinterpret_cast<const void *>(&msa_projection_kernel<64, true>),
+                          reinterpret_cast<const void *>(&msa_projection_kernel<128, true>)};
+    const int vi = (D == 128 ? 1 : 0) + (fp8 ? 2 : 0);
+    const void *fn = fns[vi];
     cudaLaunchConfig_t lc;
     memset(&lc, 0, sizeof lc);
     lc.blockDim = dim3(kThreads);

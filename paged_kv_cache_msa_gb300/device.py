@@ -127,6 +127,8 @@ class DeviceProjection:
         self.device = self.dw.device
         self.hidden = _t(pw.hidden, self.device)
         self.weight = _t(pw.weight, self.device)
+        self.hidden_scales = None if pw.hidden_scales is None else _t(pw.hidden_scales, self.device)
+        self.weight_scales = None if pw.weight_scales is None else _t(pw.weight_scales, self.device)
         self.rows_out = (torch.zeros((pw.num_tokens, pw.width), dtype=torch.int16, device=self.device)
                          if rows_out else None)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
@@ -140,7 +142,8 @@ class DeviceProjection:
         dw, pw = self.dw, self.pw
         p = lambda t: None if t is None else int(t.data_ptr())
         return (dw.cfg, pw.num_tokens, p(self.hidden), pw.hidden_size, pw.hidden.shape[1],
-                p(self.weight), pw.weight.shape[1], p(dw.positions), p(dw.slots), p(dw.page_table),
+                p(self.weight), pw.weight.shape[1], pw.operand_dtype, p(self.hidden_scales),
+                p(self.weight_scales), p(dw.positions), p(dw.slots), p(dw.page_table),
                 0 if dw.page_table is None else dw.page_table.numel(),
                 p(dw.weights.get("q")), p(dw.weights.get("k")), p(dw.weights.get("idx_q")),
                 p(dw.weights.get("idx_k")), p(dw.q_out), p(dw.idx_q_out), dw.caches["k"],

@@ -510,12 +510,20 @@ def indexer_cache_arg(w: IndexerWorkload, pool: np.ndarray) -> dict:
 class ProjectionWorkload:
     """Hidden states and an output-major weight whose product is the producer's
     rows; ``producer`` holds everything else (heads, positions, slots, page table,
-    norm weights, scales, caches) and has no rows of its own (qkv is [T, 0])."""
+    norm weights, scales, caches) and has no rows of its own (qkv is [T, 0]).
+    Operands are bf16 bits (uint16) or E4M3 codes (uint8) with per-token and
+    per-output dequantisation scales."""
     name: str
     producer: Workload
-    hidden: np.ndarray         # uint16 (bf16 bits) [T, hidden_stride]
+    hidden: np.ndarray         # [T, hidden_stride]: uint16 bf16 bits or uint8 E4M3 codes
     hidden_size: int
-    weight: np.ndarray         # uint16 (bf16 bits) [W, weight_stride]
+    weight: np.ndarray         # [W, weight_stride], same element type
+    hidden_scales: np.ndarray | None = None   # float32 [T]
+    weight_scales: np.ndarray | None = None   # float32 [W]
+
+    @property
+    def operand_dtype(self) -> int:
+        return DTYPE_BF16 if self.hidden.dtype == np.uint16 else DTYPE_E4M3
 
     @property
     def num_tokens(self) -> int:
@@ -537,50 +545,78 @@ class ProjectionWorkload:
                         w.seed, w.meta)
 
 
+def _e4m3_rows(x: np.ndarray):
+    """Per-row E4M3 quantisation of float32 rows (input preparation): the scale is
+    the row's largest magnitude / 448 (1 for an all-zero row) and the codes are
+    torch's rounding cast of x / scale."""
+    import torch
+    amax = np.abs(x).max(axis=1)
+    scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    t = torch.from_numpy(np.ascontiguousarray(x / scale[:, None], dtype=np.float32))
+    codes = t.to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+    return codes, scale
+
+
 def make_projection_batch(name: str, seed: int, heads: dict, seq_positions: list,
                           hidden_size: int, *, hidden_pad: int = 0, weight_pad: int = 0,
-                          **batch_kw) -> ProjectionWorkload:
-    """Hidden states N(0, 1) and weights N(0, 1/hidden_size), both rounded to bf16, so
-    that the projection rows are about N(0, 1) like the producer's own inputs; the
-    rest from ``make_batch`` (same keyword arguments) without rows.  Row strides are
-    widened by ``hidden_pad`` / ``weight_pad`` elements (filled with NaN, which no
-    correct kernel reads)."""
+                          operand_dtype: int = DTYPE_BF16, **batch_kw) -> ProjectionWorkload:
+    """Hidden states N(0, 1) and weights N(0, 1/hidden_size), so that the projection
+    rows are about N(0, 1) like the producer's own inputs, as bf16 or as E4M3 with
+    one scale per token and per output row; the rest from ``make_batch`` (same
+    keyword arguments) without rows.  Row strides are widened by ``hidden_pad`` /
+    ``weight_pad`` elements filled with NaN, which no correct kernel reads."""
     w = make_batch(name, seed, heads, seq_positions, make_rows=False, **batch_kw)
     rng = np.random.default_rng(seed + 7919)
     T, W, K = w.num_tokens, w.width, int(hidden_size)
-    hidden = np.full((T, K + hidden_pad), 0x7FC0, dtype=np.uint16)
-    hidden[:, :K] = _normal_bf16(rng, (T, K))
-    weight = np.full((W, K + weight_pad), 0x7FC0, dtype=np.uint16)
+    fp8 = operand_dtype == DTYPE_E4M3
+    etype, nan = (np.uint8, 0x7F) if fp8 else (np.uint16, 0x7FC0)
+    hidden = np.full((T, K + hidden_pad), nan, dtype=etype)
+    weight = np.full((W, K + weight_pad), nan, dtype=etype)
+    sx = np.empty(T, dtype=np.float32) if fp8 else None
+    sw = np.empty(W, dtype=np.float32) if fp8 else None
+    for r0 in range(0, T, 4096):
+        r1 = min(T, r0 + 4096)
+        x = rng.standard_normal((r1 - r0, K), dtype=np.float32)
+        if fp8:
+            hidden[r0:r1, :K], sx[r0:r1] = _e4m3_rows(x)
+        else:
+            hidden[r0:r1, :K] = _to_bf16_bits(x)
     for r0 in range(0, W, 2048):
         r1 = min(W, r0 + 2048)
         x = rng.standard_normal((r1 - r0, K), dtype=np.float32) * np.float32(1.0 / np.sqrt(K))
-        weight[r0:r1, :K] = _to_bf16_bits(x)
-    return ProjectionWorkload(name, w, hidden, K, weight)
+        if fp8:
+            weight[r0:r1, :K], sw[r0:r1] = _e4m3_rows(x)
+        else:
+            weight[r0:r1, :K] = _to_bf16_bits(x)
+    return ProjectionWorkload(name, w, hidden, K, weight, sx, sw)
 
 
 PROJECTION_HIDDEN = 6144
 
 
 def projection_prefill(seed: int = 7000, num_seqs: int = 8, seq_len: int = 8192,
-                       hidden_size: int = PROJECTION_HIDDEN) -> ProjectionWorkload:
+                       hidden_size: int = PROJECTION_HIDDEN,
+                       operand_dtype: int = DTYPE_BF16) -> ProjectionWorkload:
     """The prefill batch of the producer (8 sequences x 8192 tokens, big shapes,
     1,024 shuffled pages, contiguous HND fp8 caches) made from hidden states of
-    size 6,144 through the packed 11,392-output projection."""
+    size 6,144 through the packed 11,392-output projection (bf16 or E4M3 operands)."""
     P = 64
     max_blocks = seq_len // P
     pos = [list(range(seq_len)) for _ in range(num_seqs)]
-    return make_projection_batch(f"projection_prefill_{num_seqs}x{seq_len}_h{hidden_size}", seed,
-                                 BIG, pos, hidden_size, max_blocks=max_blocks,
-                                 num_pages=num_seqs * max_blocks)
+    tag = "e4m3" if operand_dtype == DTYPE_E4M3 else "bf16"
+    return make_projection_batch(f"projection_prefill_{num_seqs}x{seq_len}_h{hidden_size}_{tag}",
+                                 seed, BIG, pos, hidden_size, max_blocks=max_blocks,
+                                 num_pages=num_seqs * max_blocks, operand_dtype=operand_dtype)
 
 
-def projection_decode(seed: int = 7100, batch: int = 64,
-                      hidden_size: int = PROJECTION_HIDDEN) -> ProjectionWorkload:
+def projection_decode(seed: int = 7100, batch: int = 64, hidden_size: int = PROJECTION_HIDDEN,
+                      operand_dtype: int = DTYPE_BF16) -> ProjectionWorkload:
     """Decode: ``batch`` sequences x 1 token with contexts U{1..9216}, big shapes,
     9,216 shuffled pages padded by 256 bytes, 10% padded slots."""
     rng = np.random.default_rng(seed)
     L = rng.integers(1, 9216 + 1, size=batch)
     pos = [[int(l) - 1] for l in L]
-    return make_projection_batch(f"projection_decode_{batch}_h{hidden_size}", seed + 1, BIG, pos,
-                                 hidden_size, max_blocks=144, num_pages=9216, page_pad_bytes=256,
-                                 pad_frac=0.10)
+    tag = "e4m3" if operand_dtype == DTYPE_E4M3 else "bf16"
+    return make_projection_batch(f"projection_decode_{batch}_h{hidden_size}_{tag}", seed + 1, BIG,
+                                 pos, hidden_size, max_blocks=144, num_pages=9216,
+                                 page_pad_bytes=256, pad_frac=0.10, operand_dtype=operand_dtype)

@@ -295,7 +295,8 @@ def good_projection(**over):
     for k in ("qkv", "qkv_row_stride", "launch_flags"):
         a.pop(k)
     a.update(hidden=BASE + 9 * 2**32, hidden_size=6144, hidden_row_stride=6144,
-             weight=BASE + 10 * 2**32, weight_row_stride=6144, rows_out=None, rows_out_stride=0,
+             weight=BASE + 10 * 2**32, weight_row_stride=6144, operand_dtype=B.MSA_DTYPE_BF16,
+             hidden_scales=None, weight_scales=None, rows_out=None, rows_out_stride=0,
              status=BASE + 11 * 2**32)
     a.update(over)
     return a
@@ -308,6 +309,10 @@ def test_projection_well_formed_calls_pass(lib):
                                                        weight_row_stride=200)) == B.MSA_OK
     assert B.msa_projection_validate(**good_projection(rows_out=BASE + 12 * 2**32,
                                                        rows_out_stride=89 * 128)) == B.MSA_OK
+    fp8 = dict(operand_dtype=B.MSA_DTYPE_FP8_E4M3, hidden_scales=BASE + 13 * 2**32,
+               weight_scales=BASE + 14 * 2**32)
+    assert B.msa_projection_validate(**good_projection(**fp8)) == B.MSA_OK
+    assert B.msa_projection_validate(**good_projection(**fp8, hidden_row_stride=6160)) == B.MSA_OK
 
 
 def test_projection_zero_tokens_is_ok_without_launch(lib):
@@ -335,6 +340,11 @@ def test_projection_zero_tokens_is_ok_without_launch(lib):
     (dict(k_cache=None), B.MSA_ERR_INVALID_ARGUMENT),
     (dict(scales=None), B.MSA_ERR_INVALID_ARGUMENT),
     (dict(cfg=_cfg(head_dim=96, rotary_dim=96)), B.MSA_ERR_UNSUPPORTED),
+    (dict(operand_dtype=7), B.MSA_ERR_UNSUPPORTED),
+    (dict(operand_dtype=B.MSA_DTYPE_FP8_E4M3, hidden_row_stride=6152), B.MSA_ERR_MISALIGNED),
+    (dict(operand_dtype=B.MSA_DTYPE_FP8_E4M3, weight_row_stride=6152), B.MSA_ERR_MISALIGNED),
+    (dict(hidden_scales=BASE + 13 * 2**32 + 2), B.MSA_ERR_MISALIGNED),
+    (dict(weight_scales=BASE + 14 * 2**32 + 1), B.MSA_ERR_MISALIGNED),
 ])
 def test_projection_malformed_call_is_rejected(lib, over, status):
     a = good_projection(**over)

@@ -33,18 +33,37 @@ def _bf16_f64(bits: np.ndarray) -> np.ndarray:
     return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
+def _operands_f64(a: np.ndarray) -> np.ndarray:
+    """bf16 bits or E4M3 codes -> float64 (E4M3 through torch's float8 type)."""
+    if a.dtype == np.uint16:
+        return _bf16_f64(a)
+    t = torch.from_numpy(np.ascontiguousarray(a)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+def _exact_and_acc(pw: wl.ProjectionWorkload, idx):
+    """Exact scaled dot products and the fp32-accumulation error bound of the
+    kernel's value, K * 2^-24 * sum_k |x_k w_k| * |sx sw| plus the rounding of its
+    two scale multiplications (2^-23 of the value)."""
+    K = pw.hidden_size
+    x = _operands_f64(pw.hidden[idx, :K])
+    w = _operands_f64(pw.weight[:, :K])
+    sx = np.ones(x.shape[0]) if pw.hidden_scales is None else pw.hidden_scales[idx].astype(np.float64)
+    sw = np.ones(w.shape[0]) if pw.weight_scales is None else pw.weight_scales.astype(np.float64)
+    s = sx[:, None] * sw[None, :]
+    exact = (x @ w.T) * s
+    acc = K * 2.0**-24 * (np.abs(x) @ np.abs(w).T) * np.abs(s) + 2.0**-23 * np.abs(exact)
+    return exact, acc
+
+
 def check_rows(got: np.ndarray, pw: wl.ProjectionWorkload, rows: np.ndarray):
     """The kernel's bf16 rows against the oracle's: at least 99% identical, and
     every one within the error of an fp32 accumulation of K products,
     K * 2^-24 * sum_k |x_k w_k|, plus one bf16 step of the exact value."""
-    K = pw.hidden_size
-    x = _bf16_f64(pw.hidden[:, :K])
-    w = _bf16_f64(pw.weight[:, :K])
-    exact = x @ w.T
-    mag = np.abs(x) @ np.abs(w).T
+    exact, acc = _exact_and_acc(pw, np.arange(pw.num_tokens))
     a = np.abs(exact)
     step = np.where(a > 0, np.exp2(np.floor(np.log2(np.maximum(a, 1e-300))) - 7), 0.0)
-    bound = step + K * 2.0**-24 * mag
+    bound = step + acc
     err = np.abs(_bf16_f64(got) - exact)
     bad = err > bound
     assert not bad.any(), (f"projection rows: {int(bad.sum())} beyond the fp32 accumulation bound; "
@@ -54,9 +73,11 @@ def check_rows(got: np.ndarray, pw: wl.ProjectionWorkload, rows: np.ndarray):
 
 def oracle_rows(pw: wl.ProjectionWorkload, idx=None) -> np.ndarray:
     h = pw.hidden[:, :pw.hidden_size]
+    sx = pw.hidden_scales
     if idx is not None:
         h = np.ascontiguousarray(h[idx])
-    return oracle.projection(h, pw.weight[:, :pw.hidden_size])
+        sx = None if sx is None else sx[idx]
+    return oracle.projection(h, pw.weight[:, :pw.hidden_size], sx, pw.weight_scales)
 
 
 def row_error_bound(pw: wl.ProjectionWorkload, idx) -> np.ndarray:
@@ -65,11 +86,8 @@ def row_error_bound(pw: wl.ProjectionWorkload, idx) -> np.ndarray:
     acc = K * 2^-24 * sum_k |x_k w_k| of the exact one, the oracle the exact sum
     itself (through fp32), so the two bf16 values are at most one bf16 step (at the
     larger magnitude) plus acc apart."""
-    K = pw.hidden_size
-    x = _bf16_f64(pw.hidden[idx, :K])
-    w = _bf16_f64(pw.weight[:, :K])
-    acc = K * 2.0**-24 * (np.abs(x) @ np.abs(w).T)
-    a = np.abs(x @ w.T) + acc
+    exact, acc = _exact_and_acc(pw, idx)
+    a = np.abs(exact) + acc
     step = np.where(a > 0, np.exp2(np.floor(np.log2(np.maximum(a, 1e-300))) - 7), 2.0**-133)
     return step + acc
 
@@ -208,6 +226,9 @@ def check_projection(pw: wl.ProjectionWorkload):
 
 
 def _batch(seed, heads, T, hidden, **kw):
+    mult = 16 if kw.get("operand_dtype") == wl.DTYPE_E4M3 else 8   # 16-byte row strides
+    kw["hidden_pad"] = kw.get("hidden_pad", 0) + (-(hidden + kw.get("hidden_pad", 0))) % mult
+    kw["weight_pad"] = kw.get("weight_pad", 0) + (-(hidden + kw.get("weight_pad", 0))) % mult
     rng = np.random.default_rng(seed)
     P = kw.get("page_size", 64)
     max_blocks = -(-(T + 64) // P)
@@ -218,19 +239,25 @@ def _batch(seed, heads, T, hidden, **kw):
                                     max_blocks=max_blocks, **kw)
 
 
-@pytest.mark.parametrize("T,hidden", [(1, 64), (127, 128), (300, 200), (513, 72)])
-def test_tiny_shapes_ragged_tiles(T, hidden):
+OPERANDS = [wl.DTYPE_BF16, wl.DTYPE_E4M3]
+OPERAND_IDS = ["bf16", "e4m3"]
+
+
+@pytest.mark.parametrize("dt", OPERANDS, ids=OPERAND_IDS)
+@pytest.mark.parametrize("T,hidden", [(1, 64), (127, 128), (300, 200), (513, 72), (40, 330)])
+def test_tiny_shapes_ragged_tiles(T, hidden, dt):
     """Tiny shapes (15 heads of 64: 4 output tiles, the last one partly past the
-    row), token counts and hidden sizes that leave ragged tiles, NaN-padded
-    row strides."""
-    pw = _batch(10 + T, wl.TINY, T, hidden, hidden_pad=8, weight_pad=16, pad_frac=0.1,
-                idx_k_dtype=wl.DTYPE_BF16)
+    row), token counts and hidden sizes that leave ragged tiles (in tokens, outputs
+    and K), NaN-padded row strides."""
+    pw = _batch(10 + T, wl.TINY, T, hidden, hidden_pad=16, weight_pad=16, pad_frac=0.1,
+                idx_k_dtype=wl.DTYPE_BF16, operand_dtype=dt)
     check_projection(pw)
 
 
-@pytest.mark.parametrize("T,hidden", [(64, 512), (200, 256)])
-def test_big_shapes(T, hidden):
-    pw = _batch(20 + T, wl.BIG, T, hidden, pad_frac=0.1, page_pad_bytes=256)
+@pytest.mark.parametrize("dt", OPERANDS, ids=OPERAND_IDS)
+@pytest.mark.parametrize("T,hidden", [(64, 512), (200, 256), (257, 384)])
+def test_big_shapes(T, hidden, dt):
+    pw = _batch(20 + T, wl.BIG, T, hidden, pad_frac=0.1, page_pad_bytes=256, operand_dtype=dt)
     check_projection(pw)
 
 
@@ -257,9 +284,10 @@ def test_no_index_k_cache_and_odd_sections():
     check_projection(pw)
 
 
-def test_decode_batch_64_hidden_6144():
+@pytest.mark.parametrize("dt", OPERANDS, ids=OPERAND_IDS)
+def test_decode_batch_64_hidden_6144(dt):
     """The decode batch (64 tokens, big shapes, hidden 6,144): every output."""
-    check_projection(wl.projection_decode())
+    check_projection(wl.projection_decode(operand_dtype=dt))
 
 
 def test_zero_tokens_launches_nothing():
@@ -294,12 +322,13 @@ def test_graph_replay_matches_direct_launch():
     assert int(dp.status.item()) == 0
 
 
-def test_prefill_65536_tokens_hidden_6144_sampled():
+@pytest.mark.parametrize("dt", OPERANDS, ids=OPERAND_IDS)
+def test_prefill_65536_tokens_hidden_6144_sampled(dt):
     """The full-size prefill (65,536 tokens, hidden 6,144, 11,392 outputs): the
     written cache bytes exactly against the oracle's placement of every token
     (two sentinel runs), and sampled tokens (tile edges, first and last tokens,
     random ones) element by element against the oracle."""
-    pw = wl.projection_prefill()
+    pw = wl.projection_prefill(operand_dtype=dt)
     T = pw.num_tokens
     rng = np.random.default_rng(77)
     idx = np.unique(np.concatenate([[0, 1, 127, 128, 129, 255, 256, T - 129, T - 128, T - 1],
