@@ -74,3 +74,39 @@ def test_random_indexer_configuration(seed):
                               dtype=int(rng.choice([wl.DTYPE_E4M3, wl.DTYPE_BF16])),
                               page_pad_bytes=16 * int(rng.integers(0, 3)))
     _check(w)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_projection_configuration(seed):
+    """The projection with the producer in its epilogue over random head counts,
+    head_dim, RoPE style and rotary dim, token counts, hidden sizes, row padding,
+    operand type (with per-token / per-output scales for E4M3), cache dtypes,
+    scale mode and padded slots."""
+    from test_projection_gpu import check_projection
+    rng = np.random.default_rng(50_000 + seed)
+    D = int(rng.choice([64, 128]))
+    heads = dict(num_q_heads=int(rng.integers(0, 12)), num_kv_heads=int(rng.integers(1, 5)),
+                 num_idx_q_heads=int(rng.integers(0, 5)), num_idx_k_heads=int(rng.integers(0, 2)),
+                 head_dim=D)
+    style = int(rng.integers(0, 2))
+    step = 16 if style == wl.ROPE_NEOX else 8
+    rd = int(rng.choice([D, D // 2, 0, int(rng.integers(0, D // step + 1)) * step]))
+    T = int(rng.choice([1, 17, 128, 129, 255, 256, 300]))
+    K = int(rng.integers(1, 40)) * 8
+    dt = int(rng.choice([wl.DTYPE_BF16, wl.DTYPE_E4M3]))
+    mult = 16 if dt == wl.DTYPE_E4M3 else 8
+    P = int(rng.choice([16, 64]))
+    start = int(rng.integers(0, 64))
+    max_blocks = -(-(start + T) // P)
+    pw = wl.make_projection_batch(
+        f"pfuzz{seed}", 60_000 + seed, heads, [list(range(start, start + T))], K,
+        hidden_pad=(-K) % mult + mult * int(rng.integers(0, 3)),
+        weight_pad=(-K) % mult + mult * int(rng.integers(0, 3)), operand_dtype=dt,
+        max_blocks=max_blocks, num_pages=max_blocks + int(rng.integers(0, 4)), page_size=P,
+        rotary_dim=rd, rope_style=style,
+        kv_dtype=int(rng.choice([wl.DTYPE_E4M3, wl.DTYPE_BF16])),
+        idx_k_dtype=int(rng.choice([wl.DTYPE_E4M3, wl.DTYPE_BF16])),
+        with_idx_k=bool(rng.integers(0, 4)), pad_frac=float(rng.choice([0.0, 0.2])),
+        use_page_table=bool(rng.integers(0, 3)), scale_mode=int(rng.integers(0, 2)),
+        scale=float(rng.uniform(0.02, 0.3)))
+    check_projection(pw)
