@@ -336,34 +336,42 @@ def graph_launch_us(dw, flags, launches: int, replays: int) -> float:
 def indexer_timing(replays: int = 200, calls: int = 20):
     """The indexer of the decode-batch-64 layer (64 queries, contexts U{1..9216},
     8 index heads of dim 128, fp8 index-K): one call = score kernel + top-k kernel;
-    `calls` back-to-back calls captured in a graph."""
+    `calls` back-to-back calls captured in a graph, with programmatic dependent
+    launch of the score kernel (and, for comparison, without)."""
     import torch
+    from paged_kv_cache_msa_gb300 import binding as B
     from paged_kv_cache_msa_gb300 import workloads as wl
     from paged_kv_cache_msa_gb300.device import DeviceIndexer
     w = wl.indexer_decode64()
     dv = DeviceIndexer(w)
     s = torch.cuda.Stream()
     torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        for _ in range(calls):
-            dv.run(stream=s)
-    with torch.cuda.stream(s):
-        for _ in range(3):
-            g.replay()
-        s.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(s)
-        for _ in range(replays):
-            g.replay()
-        e1.record(s)
-        e1.synchronize()
-    us = 1e3 * e0.elapsed_time(e1) / (replays * calls)
+
+    def graph_us(flags):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(calls):
+                dv.run(stream=s, launch_flags=flags)
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                g.replay()
+            s.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(replays):
+                g.replay()
+            e1.record(s)
+            e1.synchronize()
+        return 1e3 * e0.elapsed_time(e1) / (replays * calls)
+
+    us_plain = graph_us(0)
+    us = graph_us(B.MSA_LAUNCH_PDL)
     alg = w.algorithmic_bytes()
     peak, _ = peaks()
     return {"workload": "decode batch 64, contexts U{1..9216}, 8 index heads x 128, fp8 index-K, "
                         "top-16 of 128-token blocks",
-            "us_per_call": us, "launches_per_call": 2, "algorithmic_bytes": alg,
+            "us_per_call": us, "us_per_call_without_pdl": us_plain, "launches_per_call": 2,
+            "algorithmic_bytes": alg,
             "gbs": alg / (us * 1e-6) / 1e9, "frac_of_peak": alg / (us * 1e-6) / 1e9 / peak,
             "index_k_tokens_scanned": int(w.kv_len.sum())}
 

@@ -230,13 +230,20 @@ typedef struct {
  * k_scale        device fp32 [1]: dequantisation scale of an FP8 cache (NULL for bf16).
  * block_scores   device fp32 [num_queries, max_blocks], written in full.
  * topk_ids       device int32 [num_queries, topk].
+ * launch_flags   0 or MSA_LAUNCH_PDL: the score kernel is launched with
+ *                programmatic dependent launch and reads kv_len, table_offset and
+ *                page_table before waiting for the kernel launched just before it on
+ *                the stream (which must therefore not write them); idx_q, the cache,
+ *                k_scale and the outputs are touched only after the wait.  The top-k
+ *                kernel lets the next kernel on the stream start likewise.
  * Errors as for msa_producer_forward; num_queries == 0 launches nothing.
  */
 msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t num_queries, const void *idx_q,
                                const int32_t *kv_len, const int64_t *table_offset,
                                const int32_t *page_table, int64_t page_table_len,
                                const msa_cache_desc *idx_k_cache, const float *k_scale,
-                               float *block_scores, int32_t *topk_ids, cudaStream_t stream);
+                               float *block_scores, int32_t *topk_ids, int32_t launch_flags,
+                               cudaStream_t stream);
 
 /*
  * Device address at which the GPU of the current device reaches host memory

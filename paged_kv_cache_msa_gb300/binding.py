@@ -118,7 +118,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                                 ctypes.POINTER(i32), ctypes.POINTER(i32)]
         L.msa_producer_launch_shape.restype = ctypes.c_int
         L.msa_indexer_forward.argtypes = [ctypes.POINTER(MsaIndexerCfg), i64, vp, vp, vp, vp, i64,
-                                          cachep, vp, vp, vp, vp]
+                                          cachep, vp, vp, vp, i32, vp]
         L.msa_indexer_forward.restype = ctypes.c_int
         proj = [cfgp, i64, vp, i64, i64, vp, i64, ctypes.c_int, vp, vp, vp, vp, vp, i64, vp, vp,
                 vp, vp, vp, vp, cachep, cachep, cachep, vp, vp, i64, vp]
@@ -268,14 +268,14 @@ def make_indexer_cfg(num_heads, head_dim, page_size=64, block_tokens=128, topk=1
 
 
 def msa_indexer_forward(cfg, num_queries, idx_q, kv_len, table_offset, page_table,
-                        page_table_len, idx_k_cache, k_scale, block_scores, topk_ids, stream=0,
-                        check=True) -> int:
+                        page_table_len, idx_k_cache, k_scale, block_scores, topk_ids,
+                        launch_flags=0, stream=0, check=True) -> int:
     """The C entry point; pointers are integers or None.  Raises MsaError unless the
     call returns MSA_OK (``check=False`` returns the status)."""
     s = load().msa_indexer_forward(ctypes.byref(cfg) if cfg is not None else None,
                                    int(num_queries), idx_q, kv_len, table_offset, page_table,
                                    int(page_table_len), _ref(idx_k_cache), k_scale,
-                                   block_scores, topk_ids, stream)
+                                   block_scores, topk_ids, int(launch_flags), stream)
     if check and s != MSA_OK:
         raise MsaError(s, "msa_indexer_forward", last_error_detail())
     return s

@@ -68,7 +68,7 @@ struct IndexerParams {
     int32_t block_tokens;
     int32_t topk;
     int32_t max_blocks;
-    int32_t pad;
+    int32_t pdl;                    // launched with programmatic dependent launch
 };
 
 __device__ __forceinline__ uint4 ldg16(const void *p)
@@ -150,9 +150,16 @@ __global__ void __launch_bounds__(kScoreWarps * 32, MSA_INDEX_MIN_CTAS) msa_inde
     const int64_t t = (int64_t)blockIdx.x / cpq;
     const int b = (int)((int64_t)blockIdx.x % cpq) * kScoreWarps + warp;
     const int H = p.heads;
-    const int64_t L = p.kv_len[t] > 0 ? (int64_t)p.kv_len[t] : 0;
+    // Metadata first, in one round of independent loads: under programmatic
+    // dependent launch it is read before waiting on the previous kernel (kv_len,
+    // table_offset and page_table must not be written by it); the query, the
+    // index-K rows and every output are touched only after the wait.
+    const int32_t len_raw = __ldg(p.kv_len + t);
+    const int64_t tbase = __ldg(p.table_offset + t);
+    const int64_t L = len_raw > 0 ? (int64_t)len_raw : 0;
     const int64_t cta_j0 = (int64_t)((int64_t)blockIdx.x % cpq) * kScoreWarps * p.block_tokens;
     if (cta_j0 >= L) {   // every block of this CTA is past the visible tokens
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         if (lane == 0 && b < p.max_blocks)
             p.block_scores[t * p.max_blocks + b] = -INFINITY;
         return;
@@ -162,7 +169,6 @@ __global__ void __launch_bounds__(kScoreWarps * 32, MSA_INDEX_MIN_CTAS) msa_inde
     // its page up itself).
     const int64_t j0 = (int64_t)b * p.block_tokens;
     const int64_t jend = L < j0 + p.block_tokens ? L : j0 + p.block_tokens;
-    const int64_t tbase = p.table_offset[t];
     const int64_t blk0 = p.page_shift >= 0 ? (j0 >> p.page_shift) : j0 / p.page_size;
     const int64_t jlast = jend > j0 ? jend - 1 : j0;
     const int64_t blk1 = p.page_shift >= 0 ? (jlast >> p.page_shift) : jlast / p.page_size;
@@ -173,6 +179,8 @@ __global__ void __launch_bounds__(kScoreWarps * 32, MSA_INDEX_MIN_CTAS) msa_inde
         if (ti >= 0 && ti < p.page_table_len)
             lane_page = __ldg(p.page_table + ti);
     }
+
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // the query's heads (rows >= H zero): one 16-byte load of 8 bf16 per chunk
     constexpr int NCH = 16 * D / 8, CPT = (NCH + kScoreWarps * 32 - 1) / (kScoreWarps * 32);
@@ -331,6 +339,9 @@ __global__ void __launch_bounds__(kTopkThreads) msa_index_topk_kernel(const __gr
     const int64_t t = blockIdx.x;
     const int n = p.max_blocks;
     int32_t *out = p.topk_ids + t * p.topk;
+    // the next kernel may start its own prologue now; it still waits for this grid
+    // to complete before it reads what this grid writes
+    asm volatile("griddepcontrol.launch_dependents;" :::);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const float *row = p.block_scores + t * n;
 
@@ -433,11 +444,13 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 msa_status validate(const msa_indexer_cfg *cfg, int64_t T, const void *idx_q, const int32_t *kv_len,
                     const int64_t *table_offset, const int32_t *page_table, int64_t page_table_len,
                     const msa_cache_desc *kc, const float *k_scale, float *block_scores,
-                    int32_t *topk_ids)
+                    int32_t *topk_ids, int32_t flags)
 {
     msa_internal_set_detail("");
     if (!cfg)
         return fail(MSA_ERR_INVALID_ARGUMENT, "cfg is NULL");
+    if (flags & ~MSA_LAUNCH_PDL)
+        return fail(MSA_ERR_INVALID_ARGUMENT, "launch flags 0x%x (only MSA_LAUNCH_PDL)", flags);
     if (cfg->num_heads < 1 || cfg->num_heads > kMaxHeads)
         return fail(MSA_ERR_UNSUPPORTED, "num_heads %d (1..%d)", cfg->num_heads, kMaxHeads);
     if (cfg->head_dim != 64 && cfg->head_dim != 128)
@@ -484,10 +497,12 @@ extern "C" msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t nu
                                           const int64_t *table_offset, const int32_t *page_table,
                                           int64_t page_table_len, const msa_cache_desc *idx_k_cache,
                                           const float *k_scale, float *block_scores,
-                                          int32_t *topk_ids, cudaStream_t stream)
+                                          int32_t *topk_ids, int32_t launch_flags,
+                                          cudaStream_t stream)
 {
     msa_status s = validate(cfg, num_queries, idx_q, kv_len, table_offset, page_table,
-                            page_table_len, idx_k_cache, k_scale, block_scores, topk_ids);
+                            page_table_len, idx_k_cache, k_scale, block_scores, topk_ids,
+                            launch_flags);
     if (s != MSA_OK || num_queries == 0)
         return s;
     IndexerParams p;
@@ -515,18 +530,29 @@ extern "C" msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t nu
     p.block_tokens = cfg->block_tokens;
     p.topk = cfg->topk;
     p.max_blocks = cfg->max_blocks;
+    p.pdl = (launch_flags & MSA_LAUNCH_PDL) ? 1 : 0;
 
     const int64_t cpq = (cfg->max_blocks + kScoreWarps - 1) / kScoreWarps;
-    const unsigned grid_a = (unsigned)(num_queries * cpq);
-    if (cfg->head_dim == 128 && p.fp8)
-        msa_index_score_kernel<128, true><<<grid_a, kScoreWarps * 32, 0, stream>>>(p);
-    else if (cfg->head_dim == 128)
-        msa_index_score_kernel<128, false><<<grid_a, kScoreWarps * 32, 0, stream>>>(p);
-    else if (p.fp8)
-        msa_index_score_kernel<64, true><<<grid_a, kScoreWarps * 32, 0, stream>>>(p);
-    else
-        msa_index_score_kernel<64, false><<<grid_a, kScoreWarps * 32, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    const void *score_fn =
+        cfg->head_dim == 128
+            ? (p.fp8 ? reinterpret_cast<const void *>(&msa_index_score_kernel<128, true>)
+                     : reinterpret_cast<const void *>(&msa_index_score_kernel<128, false>))
+            : (p.fp8 ? reinterpret_cast<const void *>(&msa_index_score_kernel<64, true>)
+                     : reinterpret_cast<const void *>(&msa_index_score_kernel<64, false>));
+    cudaLaunchConfig_t sc;
+    memset(&sc, 0, sizeof sc);
+    sc.gridDim = dim3((unsigned)(num_queries * cpq));
+    sc.blockDim = dim3(kScoreWarps * 32);
+    sc.stream = stream;
+    cudaLaunchAttribute sattr[1];
+    if (p.pdl) {
+        sattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        sattr[0].val.programmaticStreamSerializationAllowed = 1;
+        sc.attrs = sattr;
+        sc.numAttrs = 1;
+    }
+    void *sargs[] = {&p};
+    cudaError_t e = cudaLaunchKernelExC(&sc, score_fn, sargs);
     if (e != cudaSuccess)
         return fail(MSA_ERR_CUDA, "score kernel launch failed: %s", cudaGetErrorString(e));
     // top-k: one CTA per query, launched programmatically dependent on the scores

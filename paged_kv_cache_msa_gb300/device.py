@@ -103,7 +103,7 @@ class DeviceIndexer:
         self.cache = B.make_cache(self.pool.data_ptr() + c.offset, c.dtype, c.num_pages, 1,
                                   c.stride_page, c.stride_head, c.stride_token)
 
-    def run(self, stream=None):
+    def run(self, stream=None, launch_flags=0):
         import torch
         if stream is None:
             stream = torch.cuda.current_stream(self.device)
@@ -111,7 +111,8 @@ class DeviceIndexer:
         return B.msa_indexer_forward(self.cfg, self.w.idx_q.shape[0], p(self.idx_q), p(self.kv_len),
                                      p(self.table_offset), p(self.page_table),
                                      self.page_table.numel(), self.cache, p(self.k_scale),
-                                     p(self.block_scores), p(self.topk_ids), stream.cuda_stream)
+                                     p(self.block_scores), p(self.topk_ids), launch_flags,
+                                     stream=stream.cuda_stream)
 
 
 class DeviceProjection:

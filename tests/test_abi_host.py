@@ -278,6 +278,8 @@ def _icfg(**kw):
                                    64 * 128, 128)), B.MSA_ERR_MISALIGNED),
     (dict(idx_k_cache=B.make_cache(BASE + 20 * 2**34, B.MSA_DTYPE_FP8_E4M3, 9216, 2, 64 * 128,
                                    64 * 128, 128)), B.MSA_ERR_INVALID_ARGUMENT),
+    (dict(launch_flags=B.MSA_LAUNCH_PERSISTENT), B.MSA_ERR_INVALID_ARGUMENT),
+    (dict(launch_flags=8), B.MSA_ERR_INVALID_ARGUMENT),
 ])
 def test_indexer_host_checks(lib, over, status):
     a = good_indexer_call(**over)

@@ -80,3 +80,30 @@ def test_indexer_exact_ties_rank_lower_id_first():
     s = dv.block_scores.cpu().numpy()[0]
     top = dv.topk_ids.cpu().numpy()[0].tolist()
     assert s[1] == s[3] and top.index(1) < top.index(3)
+
+
+def test_indexer_pdl_back_to_back_in_a_graph():
+    """Programmatic dependent launch: back-to-back calls in one CUDA graph reuse the
+    same output buffers (the score kernel of call i+1 may start while the top-k of
+    call i runs), after a kernel that rewrites the queries; results equal a plain
+    call's."""
+    from paged_kv_cache_msa_gb300 import binding as B
+    w = wl.indexer_decode64()
+    ref = _check(w)
+    dv = DeviceIndexer(w)
+    real_q = dv.idx_q.clone()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        dv.idx_q.zero_()
+        dv.run(stream=s, launch_flags=B.MSA_LAUNCH_PDL)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            dv.idx_q.copy_(real_q)            # the previous kernel writes the queries
+            for _ in range(4):
+                dv.run(stream=s, launch_flags=B.MSA_LAUNCH_PDL)
+        for _ in range(3):
+            g.replay()
+        s.synchronize()
+    assert torch.equal(ref.block_scores, dv.block_scores)
+    assert torch.equal(ref.topk_ids, dv.topk_ids)
