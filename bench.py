@@ -376,6 +376,49 @@ def indexer_timing(replays: int = 200, calls: int = 20):
             "index_k_tokens_scanned": int(w.kv_len.sum())}
 
 
+def indexer_prefill_timing(reps: int = 5):
+    """The indexer of the prefill batch (8 x 8192 causal queries, 8 index heads of
+    dim 128, fp8 index-K, top-16 of 128-token blocks): the query-run kernel (tiles
+    of 16 queries on the tcgen05 tensor cores) and, for comparison, the per-query
+    kernel; each call = score kernel + top-k kernel, CUDA events on the stream."""
+    import torch
+    from paged_kv_cache_msa_gb300 import binding as B
+    from paged_kv_cache_msa_gb300 import workloads as wl
+    from paged_kv_cache_msa_gb300.device import DeviceIndexer
+    w = wl.indexer_prefill()
+    dv = DeviceIndexer(w)
+    s = torch.cuda.Stream()
+
+    def timed(flags):
+        with torch.cuda.stream(s):
+            for _ in range(2):
+                dv.run(stream=s, launch_flags=flags)
+            s.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(reps):
+                dv.run(stream=s, launch_flags=flags)
+            e1.record(s)
+            e1.synchronize()
+        return 1e3 * e0.elapsed_time(e1) / reps
+
+    us_runs = timed(B.MSA_LAUNCH_QUERY_RUNS)
+    us_plain = timed(0)
+    T, H, D = w.idx_q.shape
+    flops = 2.0 * float(w.kv_len.astype(np.int64).sum()) * H * D   # visible (query, key, head) dots
+    burst, _, kind = tensor_peaks()
+    tf = flops / (us_runs * 1e-6) / 1e12
+    return {"workload": "prefill 8 x 8192 causal queries, 8 index heads x 128, fp8 index-K, "
+                        "top-16 of 128-token blocks",
+            "us_per_call": us_runs, "us_per_call_per_query_kernel": us_plain,
+            "queries_per_s": T / (us_runs * 1e-6), "launches_per_call": 2,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": burst, "unit": "TFLOP/s",
+                         "frac": tf / burst, "flops_per_call": flops,
+                         "note": "visible query-key-head dot products only; the tiles also "
+                                 "multiply padded and invisible entries",
+                         "peak_kind": f"{kind} cuBLAS bf16 burst (the MMA runs f16 operands)"}}
+
+
 def tensor_peaks():
     """(burst, sustained) dense bf16 TFLOP/s measured on this machine (cuBLAS), with
     the kind; the fallback figures when the measurement file is absent."""
@@ -543,6 +586,7 @@ def run_ours(args):
     indexer = None
     if not args.no_decode_step:
         indexer = indexer_timing()
+        indexer["prefill"] = indexer_prefill_timing()
 
     projection = None
     if not args.no_projection:
@@ -669,7 +713,9 @@ def main():
     if args.indexer_only:
         from paged_kv_cache_msa_gb300 import build as build_mod
         build_mod.build()
-        print(json.dumps(indexer_timing(replays=max(1, args.steps), calls=20)), flush=True)
+        out = indexer_timing(replays=max(1, args.steps), calls=20)
+        out["prefill"] = indexer_prefill_timing()
+        print(json.dumps(out), flush=True)
         return 0
     return run_ours(args)
 

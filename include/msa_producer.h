@@ -84,6 +84,15 @@ typedef enum { MSA_SCALE_PER_TENSOR = 0, MSA_SCALE_PER_HEAD = 1 } msa_scale_mode
                                      mapping and page table before waiting, so the kernel
                                      launched just before it must not write those (stage
                                      them earlier in the step). */
+#define MSA_LAUNCH_QUERY_RUNS 4   /* msa_indexer_forward only: the queries come in runs of
+                                     one sequence (consecutive queries with the same
+                                     table_offset, as in a prefill chunk), so tiles of 8
+                                     or 16 consecutive queries are scored together on the
+                                     tcgen05 tensor cores against each 128-token block they
+                                     share (block_tokens 128; other block sizes take the
+                                     per-query kernel).  The results are those of the
+                                     per-query kernel; a tile spanning several sequences
+                                     is scored one sequence at a time. */
 
 /* One paged cache.  Element (page, head, off, d) lives at
  *   data + (page*stride_page + head*stride_head + off*stride_token + d) * elem_size
@@ -230,12 +239,14 @@ typedef struct {
  * k_scale        device fp32 [1]: dequantisation scale of an FP8 cache (NULL for bf16).
  * block_scores   device fp32 [num_queries, max_blocks], written in full.
  * topk_ids       device int32 [num_queries, topk].
- * launch_flags   0 or MSA_LAUNCH_PDL: the score kernel is launched with
- *                programmatic dependent launch and reads kv_len, table_offset and
- *                page_table before waiting for the kernel launched just before it on
- *                the stream (which must therefore not write them); idx_q, the cache,
- *                k_scale and the outputs are touched only after the wait.  The top-k
- *                kernel lets the next kernel on the stream start likewise.
+ * launch_flags   MSA_LAUNCH_PDL: the score kernel is launched with programmatic
+ *                dependent launch; the per-query kernel reads kv_len, table_offset
+ *                and page_table before waiting for the kernel launched just before it
+ *                on the stream (which must therefore not write them); idx_q, the
+ *                cache, k_scale and the outputs are touched only after the wait (the
+ *                query-run kernel waits before reading anything).  The top-k kernel
+ *                lets the next kernel on the stream start likewise.
+ *                MSA_LAUNCH_QUERY_RUNS: see its definition.
  * Errors as for msa_producer_forward; num_queries == 0 launches nothing.
  */
 msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t num_queries, const void *idx_q,

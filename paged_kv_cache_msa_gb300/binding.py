@@ -29,6 +29,7 @@ MSA_SCALE_PER_TENSOR = 0
 MSA_SCALE_PER_HEAD = 1
 MSA_LAUNCH_PERSISTENT = 1
 MSA_LAUNCH_PDL = 2
+MSA_LAUNCH_QUERY_RUNS = 4
 
 # every function the header declares
 EXPORTED = ("msa_producer_forward", "msa_producer_validate", "msa_producer_launch_shape",

@@ -314,6 +314,321 @@ __global__ void __launch_bounds__(kScoreWarps * 32, MSA_INDEX_MIN_CTAS) msa_inde
 }
 
 // ---------------------------------------------------------------------------
+// block scores of query runs on the tcgen05 tensor cores (prefill)
+// ---------------------------------------------------------------------------
+//
+// When queries come in runs of one sequence (a prefill chunk), the queries of a run
+// share every index-K block they see, so a CTA takes a tile of QT consecutive
+// queries and scores them together: the tile's query heads are the 128 rows of the
+// MMA (row = query * HP + head, HP = 8 or 16 rows per query, QT = 128 / HP) and a
+// block of 128 keys is its 128 columns, with K = head_dim; fp32 accumulators in
+// tensor memory.  Per block the CTA gathers the keys' rows through the page table
+// into shared memory (E4M3 codes become f16 exactly, with the query rounded to f16
+// as in the per-query kernel; bf16 rows stay bf16), one thread issues the D/16
+// tcgen05.mma (M 128, N 128), and while the tensor cores work on that block the
+// threads read the previous block's accumulator (two accumulators, 2 x 128
+// columns): thread r owns row r, takes the max over the keys visible to its query
+// (key < kv_len, page inside the table and the cache), then the max over its
+// query's heads by shuffles.  Keys with no valid page, and heads past num_heads,
+// take no part.  A tile whose queries belong to several sequences (different
+// table rows) is scored one sequence at a time.  Every mbarrier wait is bounded;
+// a block whose wait ran out is scored NaN (never selected).
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// true once the phase with the given parity has completed; false after 2 s
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try(bar, parity))
+            return true;
+        if ((n & 63) == 0 && globaltimer() - t0 > 2000000000ull)
+            return false;
+    }
+}
+
+// K-major operand tile in the 128-byte swizzle layout: 16-byte chunk c of row r (of
+// 128 rows) at atom c / 8, row r, slot (c % 8) ^ (r % 8)
+__device__ __forceinline__ uint32_t swz(uint32_t base, int r, int c)
+{
+    return base + (uint32_t)(c >> 3) * (128u * 128u) + (uint32_t)r * 128u +
+           (uint32_t)(((c & 7) ^ (r & 7)) << 4);
+}
+
+__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    uint64_t d = (uint64_t)((saddr & 0x3FFFF) >> 4);
+    d |= (uint64_t)1 << 16;            // leading byte offset (unused with the swizzle)
+    d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: 8 rows x 128 bytes
+    d |= (uint64_t)1 << 46;            // descriptor version
+    d |= (uint64_t)2 << 61;            // 128-byte swizzle
+    return d;
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+constexpr int kTileThreads = 128;
+constexpr int kTileKeys = 128;   // keys per MMA tile: the 128-token blocks of the pages
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kTileThreads, 2)
+msa_index_tiled_kernel(const __grid_constant__ IndexerParams p)
+{
+    constexpr uint32_t kOperandBytes = 128u * D * 2u;   // one 128-row f16/bf16 tile
+    constexpr int CH = D / 8;                           // 16-byte chunks of a 2-byte row
+    // idesc: fp32 accumulator; A and B f16 (FP8 cache) or bf16; K-major; N 128, M 128
+    constexpr uint32_t kIdesc = (1u << 4) | ((FP8 ? 0u : 1u) << 7) | ((FP8 ? 0u : 1u) << 10) |
+                                ((uint32_t)(kTileKeys >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_mma[2];
+    __shared__ uint32_t s_tmem;
+    __shared__ int64_t s_toff[16];
+    __shared__ int32_t s_len[16];
+    // keys of a block with a valid page (bit j of word w: key 32w + j), for the last
+    // four blocks: block i's mask is written before the barrier of iteration i and
+    // read in its epilogue, which some warps may still run while others write
+    // block i + 2's
+    __shared__ uint32_t s_kmask[4][4];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int HP = p.heads <= 8 ? 8 : 16;
+    const int QT = 128 / HP;
+    const int64_t t0 = (int64_t)blockIdx.x * QT;
+    const uint32_t opA = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t opB0 = opA + kOperandBytes;
+
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (tid < QT) {
+        const int64_t t = t0 + tid;
+        const int32_t len = t < p.num_queries ? __ldg(p.kv_len + t) : 0;
+        s_len[tid] = len > 0 ? len : 0;
+        s_toff[tid] = t < p.num_queries ? __ldg(p.table_offset + t) : INT64_MIN;
+    }
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_mma[0])));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_mma[1])));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&s_tmem)),
+                     "r"(2 * kTileKeys)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // the query tile: row tid = (query tid / HP, head tid % HP); absent rows zero
+    {
+        const int q = tid / HP, h = tid % HP;
+        const int64_t t = t0 + q;
+        const bool real = h < p.heads && t < p.num_queries;
+        const uint16_t *src = p.idx_q + (t * p.heads + h) * D;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            uint4 v = real ? ldg16(src + 8 * c) : make_uint4(0, 0, 0, 0);
+            if (FP8) {   // bf16 -> f16 (exact for the normal f16 range)
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    o[k] = f2_to_f16x2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
+                v = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            sts128(swz(opA, tid, c), v.x, v.y, v.z, v.w);
+        }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = s_tmem;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float kscale = FP8 ? __ldg(p.k_scale) : 1.0f;
+
+    // this thread's row in the epilogue
+    const int eq = tid / HP, eh = tid % HP;
+    const int64_t et = t0 + eq;
+
+    uint32_t done = 0;             // queries of the tile already scored (bit q)
+    const uint32_t all = (1u << QT) - 1u;
+    uint32_t iter = 0;             // blocks issued so far (phases of the two barriers)
+    while (done != all) {
+        // the next sequence: the table row of the first query not yet scored
+        const int q0 = __ffs(~done & all) - 1;
+        const int64_t toff = s_toff[q0];
+        uint32_t seg = 0;
+        int32_t seg_len = 0;
+        for (int q = 0; q < QT; ++q)
+            if (!((done >> q) & 1) && s_toff[q] == toff) {
+                seg |= 1u << q;
+                seg_len = s_len[q] > seg_len ? s_len[q] : seg_len;
+            }
+        const bool absent = toff == INT64_MIN;     // queries past num_queries
+        int nb = absent ? 0 : (seg_len + kTileKeys - 1) / kTileKeys;
+        if (nb > p.max_blocks)
+            nb = p.max_blocks;
+        const bool mine = (seg >> eq) & 1;
+
+        auto epilogue = [&](int b, uint32_t it) {
+            const uint32_t st = it & 1;
+            const bool got = mbar_wait(smem_u32(&bar_mma[st]), (it >> 1) & 1);
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const int32_t len = s_len[eq];
+            float m = -INFINITY;
+#pragma unroll
+            for (int c0 = 0; c0 < kTileKeys; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + st * kTileKeys + c0, r);
+                const uint32_t valid = s_kmask[it & 3][c0 >> 5];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int key = b * kTileKeys + c0 + j;
+                    if (((valid >> j) & 1) && key < len)
+                        m = fmaxf(m, __uint_as_float(r[j]));
+                }
+            }
+            if (eh >= p.heads)
+                m = -INFINITY;
+            for (int o = 1; o < HP; o <<= 1)
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (eh == 0 && mine && et < p.num_queries)
+                p.block_scores[et * p.max_blocks + b] =
+                    got ? (m > -INFINITY ? m * kscale : -INFINITY) : __int_as_float(0x7fc00000);
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        };
+
+        for (int b = 0; b < nb; ++b, ++iter) {
+            const uint32_t st = iter & 1;
+            const uint32_t opB = opB0 + st * kOperandBytes;
+            // key row tid of block b, through the sequence's page-table row
+            const int64_t j = (int64_t)b * kTileKeys + tid;
+            bool ok = j < seg_len;
+            const uint8_t *row = nullptr;
+            if (ok) {
+                const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
+                const int64_t off = p.page_shift >= 0 ? (j & (p.page_size - 1)) : j % p.page_size;
+                const int64_t ti = toff + blk;
+                int64_t page = -1;
+                if (ti >= 0 && ti < p.page_table_len)
+                    page = __ldg(p.page_table + ti);
+                ok = page >= 0 && page < p.num_pages;
+                if (ok)
+                    row = p.kdata + (page * p.stride_page + off * p.stride_token) * (FP8 ? 1 : 2);
+            }
+            const uint32_t vmask = __ballot_sync(0xffffffffu, ok);
+            if (lane == 0)
+                s_kmask[iter & 3][warp] = vmask;
+            if (FP8) {
+#pragma unroll
+                for (int c = 0; c < D / 16; ++c) {   // 16 codes -> two f16 chunks
+                    const uint4 v = ok ? ldg16(row + 16 * c) : make_uint4(0, 0, 0, 0);
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                    uint32_t h[8];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        h[2 * k] = e4m3x2_to_f16x2(w[k] & 0xFFFF);
+                        h[2 * k + 1] = e4m3x2_to_f16x2(w[k] >> 16);
+                    }
+                    sts128(swz(opB, tid, 2 * c), h[0], h[1], h[2], h[3]);
+                    sts128(swz(opB, tid, 2 * c + 1), h[4], h[5], h[6], h[7]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < CH; ++c) {
+                    const uint4 v = ok ? ldg16(row + 16 * c) : make_uint4(0, 0, 0, 0);
+                    sts128(swz(opB, tid, c), v.x, v.y, v.z, v.w);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncthreads();
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            if (tid == 0) {
+                const uint32_t d = tmem + st * kTileKeys;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t koff = (uint32_t)(ks >> 2) * (128u * 128u) + (uint32_t)(ks & 3) * 32u;
+                    const uint64_t ad = sw128_desc(opA + koff), bd = sw128_desc(opB + koff);
+                    asm volatile(
+                        "{\n\t.reg .pred pp;\n\tsetp.ne.b32 pp, %4, 0;\n\t"
+                        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pp;\n\t}" ::"r"(d),
+                        "l"(ad), "l"(bd), "r"(kIdesc), "r"((uint32_t)ks)
+                        : "memory");
+                }
+                asm volatile(
+                    "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                        smem_u32(&bar_mma[st]))
+                    : "memory");
+            }
+            __syncwarp();
+            if (b > 0)
+                epilogue(b - 1, iter - 1);   // overlaps the MMAs just issued
+        }
+        if (nb > 0)
+            epilogue(nb - 1, iter - 1);
+        // blocks the sequence's queries do not reach
+        for (int idx = tid; idx < QT * (p.max_blocks - nb); idx += kTileThreads) {
+            const int q = idx / (p.max_blocks - nb), b = nb + idx % (p.max_blocks - nb);
+            if ((seg >> q) & 1 && t0 + q < p.num_queries)
+                p.block_scores[(t0 + q) * p.max_blocks + b] = -INFINITY;
+        }
+        done |= seg;
+        __syncthreads();   // s_kmask and the operand tiles are reused by the next sequence
+    }
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(2 * kTileKeys)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
 // top-k block ids
 // ---------------------------------------------------------------------------
 // (a, ia) ranks before (b, ib): higher score first, lower id among equals.
@@ -449,8 +764,9 @@ msa_status validate(const msa_indexer_cfg *cfg, int64_t T, const void *idx_q, co
     msa_internal_set_detail("");
     if (!cfg)
         return fail(MSA_ERR_INVALID_ARGUMENT, "cfg is NULL");
-    if (flags & ~MSA_LAUNCH_PDL)
-        return fail(MSA_ERR_INVALID_ARGUMENT, "launch flags 0x%x (only MSA_LAUNCH_PDL)", flags);
+    if (flags & ~(MSA_LAUNCH_PDL | MSA_LAUNCH_QUERY_RUNS))
+        return fail(MSA_ERR_INVALID_ARGUMENT,
+                    "launch flags 0x%x (MSA_LAUNCH_PDL, MSA_LAUNCH_QUERY_RUNS)", flags);
     if (cfg->num_heads < 1 || cfg->num_heads > kMaxHeads)
         return fail(MSA_ERR_UNSUPPORTED, "num_heads %d (1..%d)", cfg->num_heads, kMaxHeads);
     if (cfg->head_dim != 64 && cfg->head_dim != 128)
@@ -532,6 +848,7 @@ extern "C" msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t nu
     p.max_blocks = cfg->max_blocks;
     p.pdl = (launch_flags & MSA_LAUNCH_PDL) ? 1 : 0;
 
+    const bool tiled = (launch_flags & MSA_LAUNCH_QUERY_RUNS) && cfg->block_tokens == kTileKeys;
     const int64_t cpq = (cfg->max_blocks + kScoreWarps - 1) / kScoreWarps;
     const void *score_fn =
         cfg->head_dim == 128
@@ -544,6 +861,27 @@ extern "C" msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t nu
     sc.gridDim = dim3((unsigned)(num_queries * cpq));
     sc.blockDim = dim3(kScoreWarps * 32);
     sc.stream = stream;
+    if (tiled) {
+        const int D = cfg->head_dim;
+        const int qt = cfg->num_heads <= 8 ? 16 : 8;
+        const int smem = 3 * 128 * D * 2 + 1024;
+        score_fn = D == 128 ? (p.fp8 ? reinterpret_cast<const void *>(&msa_index_tiled_kernel<128, true>)
+                                     : reinterpret_cast<const void *>(&msa_index_tiled_kernel<128, false>))
+                            : (p.fp8 ? reinterpret_cast<const void *>(&msa_index_tiled_kernel<64, true>)
+                                     : reinterpret_cast<const void *>(&msa_index_tiled_kernel<64, false>));
+        if (cudaFuncSetAttribute(score_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
+            return fail(MSA_ERR_CUDA, "cudaFuncSetAttribute failed");
+        int major = 0, dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+            return fail(MSA_ERR_CUDA, "device query failed");
+        if (major != 10)
+            return fail(MSA_ERR_UNSUPPORTED, "query runs need tcgen05 tensor cores (compute capability 10.x)");
+        sc.gridDim = dim3((unsigned)((num_queries + qt - 1) / qt));
+        sc.blockDim = dim3(kTileThreads);
+        sc.dynamicSmemBytes = (size_t)smem;
+    }
     cudaLaunchAttribute sattr[1];
     if (p.pdl) {
         sattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

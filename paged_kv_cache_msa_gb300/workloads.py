@@ -495,6 +495,38 @@ def indexer_decode64(seed: int = 6000) -> IndexerWorkload:
     return make_indexer_batch("indexer_decode_64", seed + 1, rng.integers(1, 9216 + 1, size=64))
 
 
+def make_indexer_prefill(name: str, seed: int, seq_lens, heads: int = 8, head_dim: int = 128,
+                         page_size: int = 64, block_tokens: int = 128, topk: int = 16,
+                         dtype: int = DTYPE_E4M3, k_scale: float = 0.05, page_pad_bytes: int = 0,
+                         interleave: bool = False, max_blocks=None) -> IndexerWorkload:
+    """Prefill queries: sequence s contributes seq_lens[s] queries, the one at
+    position p seeing the p + 1 tokens up to and including itself (causal), all
+    through the sequence's row of the page table.  Queries come sequence by
+    sequence in position order, or (``interleave``) in a seeded shuffled order so
+    that runs of one sequence are broken up."""
+    base = make_indexer_batch(name, seed, seq_lens, heads, head_dim, page_size, block_tokens, topk,
+                              dtype, k_scale, page_pad_bytes, max_blocks=max_blocks)
+    rng = np.random.default_rng(seed + 17)
+    seq_lens = np.asarray(seq_lens, dtype=np.int64)
+    kv = np.concatenate([np.arange(1, int(L) + 1, dtype=np.int64) for L in seq_lens])
+    seq = np.concatenate([np.full(int(L), s, dtype=np.int64) for s, L in enumerate(seq_lens)])
+    if interleave:
+        order = rng.permutation(kv.shape[0])
+        kv, seq = kv[order], seq[order]
+    max_pages = base.page_table.shape[1]
+    idx_q = _normal_bf16(rng, (kv.shape[0], heads, head_dim))
+    return IndexerWorkload(name, idx_q, kv.astype(np.int32), seq * max_pages, base.page_table,
+                           base.cache, base.pool_bytes, base.pool_fill, base.k_scale, page_size,
+                           block_tokens, topk, base.max_blocks, seed)
+
+
+def indexer_prefill(seed: int = 6100, num_seqs: int = 8, seq_len: int = 8192) -> IndexerWorkload:
+    """The prefill batch's indexer: 8 sequences x 8192 queries, causal, 8 index heads
+    of dim 128, fp8 index-K cache, top-16 of 128-token blocks (64 per query row)."""
+    return make_indexer_prefill(f"indexer_prefill_{num_seqs}x{seq_len}", seed,
+                                [seq_len] * num_seqs)
+
+
 def indexer_cache_arg(w: IndexerWorkload, pool: np.ndarray) -> dict:
     c = w.cache
     return dict(data=pool, offset=c.offset, dtype=c.dtype, num_pages=c.num_pages, num_heads=1,

@@ -18,14 +18,14 @@ from oracle_pins import check_indexer_against_reference
 pytestmark = pytest.mark.gpu
 
 
-def _check(w, pool=None):
+def _check(w, pool=None, flags=0):
     build_mod.build()
     pool = w.pool_fill if pool is None else pool
     ref_s, ref_top = oracle.indexer(w.idx_q, w.kv_len, w.table_offset, w.page_table,
                                     wl.indexer_cache_arg(w, pool), w.k_scale, w.page_size,
                                     w.block_tokens, w.topk, w.max_blocks)
     dv = DeviceIndexer(w, pool=pool)
-    dv.run()
+    dv.run(launch_flags=flags)
     torch.cuda.synchronize()
     s = dv.block_scores.cpu().numpy()
     top = dv.topk_ids.cpu().numpy()
@@ -107,3 +107,87 @@ def test_indexer_pdl_back_to_back_in_a_graph():
         s.synchronize()
     assert torch.equal(ref.block_scores, dv.block_scores)
     assert torch.equal(ref.topk_ids, dv.topk_ids)
+
+
+
+# ---------------------------------------------------------------------------
+# query runs (prefill): tiles of consecutive queries on the tcgen05 tensor cores
+# ---------------------------------------------------------------------------
+
+def _runs():
+    from paged_kv_cache_msa_gb300 import binding as B
+    return B.MSA_LAUNCH_QUERY_RUNS
+
+
+@pytest.mark.parametrize("dtype", [wl.DTYPE_E4M3, wl.DTYPE_BF16], ids=["fp8", "bf16"])
+@pytest.mark.parametrize("D,heads", [(128, 8), (64, 8), (128, 12), (64, 3)])
+def test_query_runs_prefill_shapes(dtype, D, heads):
+    """Causal prefill queries of ragged sequences (tiles with partial and empty
+    rows, blocks with partial visibility), 8 and 16 rows per query."""
+    w = wl.make_indexer_prefill(f"runs{D}_{heads}", 300 + D + heads, [300, 129, 16, 1, 257],
+                                heads=heads, head_dim=D, dtype=dtype)
+    _check(w, flags=_runs())
+
+
+@pytest.mark.parametrize("P", [16, 64, 96])
+def test_query_runs_interleaved_sequences_and_pages(P):
+    """Queries of three sequences in shuffled order: most tiles hold several
+    sequences and are scored one sequence at a time; page sizes that split blocks."""
+    w = wl.make_indexer_prefill(f"inter{P}", 400 + P, [200, 333, 90], page_size=P,
+                                interleave=True, page_pad_bytes=32)
+    _check(w, flags=_runs())
+
+
+def test_query_runs_table_holes_and_topk_sizes():
+    w = wl.make_indexer_prefill("holes_runs", 501, [700, 260], topk=3)
+    pt = np.array(w.page_table, copy=True)
+    pt[0, 2] = -1
+    pt[1, 1] = 10**6
+    w.page_table = pt
+    _check(w, flags=_runs())
+
+
+def test_query_runs_match_the_per_query_kernel():
+    """The same prefill batch through both score kernels: the block scores agree to
+    fp32 accumulation error and the -inf pattern is identical."""
+    w = wl.make_indexer_prefill("both", 502, [400, 130])
+    a = DeviceIndexer(w)
+    a.run()
+    b = DeviceIndexer(w)
+    b.run(launch_flags=_runs())
+    torch.cuda.synchronize()
+    sa, sb = a.block_scores.cpu().numpy(), b.block_scores.cpu().numpy()
+    assert np.array_equal(np.isfinite(sa), np.isfinite(sb))
+    fin = np.isfinite(sa)
+    assert np.allclose(sa[fin], sb[fin], rtol=1e-5, atol=1e-3)
+
+
+def test_query_runs_prefill_65536_sampled():
+    """The prefill batch (8 x 8192 causal queries, 8 heads x 128, fp8 index-K):
+    block scores and top-k of sampled queries (sequence starts and ends, tile edges,
+    random) against the oracle; every row's ids a valid ranking of its scores."""
+    from dataclasses import replace
+    w = wl.indexer_prefill()
+    dv = DeviceIndexer(w)
+    dv.run(launch_flags=_runs())
+    torch.cuda.synchronize()
+    s_all = dv.block_scores.cpu().numpy()
+    top_all = dv.topk_ids.cpu().numpy()
+    T = w.kv_len.shape[0]
+    rng = np.random.default_rng(5)
+    idx = np.unique(np.concatenate([[0, 1, 15, 16, 17, 8191, 8192, 8193, T - 17, T - 16, T - 1],
+                                    rng.integers(0, T, size=37)]))
+    sub = replace(w, idx_q=np.ascontiguousarray(w.idx_q[idx]), kv_len=w.kv_len[idx].copy(),
+                  table_offset=w.table_offset[idx].copy())
+    ref_s, ref_top = oracle.indexer(sub.idx_q, sub.kv_len, sub.table_offset, sub.page_table,
+                                    wl.indexer_cache_arg(sub, sub.pool_fill), sub.k_scale,
+                                    sub.page_size, sub.block_tokens, sub.topk, sub.max_blocks)
+    check_indexer_against_reference(sub, s_all[idx], top_all[idx], ref_s.astype(np.float64), ref_top)
+    fin = np.isfinite(s_all)
+    nfin = fin.sum(axis=1)
+    assert np.array_equal(nfin, np.minimum(-(-w.kv_len // 128), w.max_blocks))
+    for t in rng.integers(0, T, size=200):
+        ids = [i for i in top_all[t] if i >= 0]
+        vals = [s_all[t, i] for i in ids]
+        assert len(ids) == min(w.topk, int(nfin[t]))
+        assert all(vals[i] >= vals[i + 1] for i in range(len(vals) - 1))
