@@ -516,18 +516,35 @@ msa_index_tiled_kernel(const __grid_constant__ IndexerParams p)
             const bool got = mbar_wait(smem_u32(&bar_mma[st]), (it >> 1) & 1);
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const int32_t len = s_len[eq];
+            const uint32_t *km = s_kmask[it & 3];
+            // every key of the block valid and visible to this query: no masking
+            const bool whole = (km[0] & km[1] & km[2] & km[3]) == 0xffffffffu &&
+                               (b + 1) * kTileKeys <= len;
             float m = -INFINITY;
 #pragma unroll
             for (int c0 = 0; c0 < kTileKeys; c0 += 32) {
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_base + st * kTileKeys + c0, r);
-                const uint32_t valid = s_kmask[it & 3][c0 >> 5];
+                float v[32];
+                if (whole) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int key = b * kTileKeys + c0 + j;
-                    if (((valid >> j) & 1) && key < len)
-                        m = fmaxf(m, __uint_as_float(r[j]));
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = __uint_as_float(r[j]);
+                } else {
+                    const uint32_t valid = km[c0 >> 5];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int key = b * kTileKeys + c0 + j;
+                        v[j] = (((valid >> j) & 1) && key < len) ? __uint_as_float(r[j]) : -INFINITY;
+                    }
                 }
+                // a tree, not a chain: five dependent steps instead of 32
+#pragma unroll
+                for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+                    for (int j = 0; j < w; ++j)
+                        v[j] = fmaxf(v[j], v[j + w]);
+                m = fmaxf(m, v[0]);
             }
             if (eh >= p.heads)
                 m = -INFINITY;
@@ -539,32 +556,45 @@ msa_index_tiled_kernel(const __grid_constant__ IndexerParams p)
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         };
 
+        // Key row tid of each block is fetched ahead: its page-table entry two blocks
+        // ahead, its row one block ahead, so that both latencies overlap the MMAs and
+        // the previous block's epilogue.
+        constexpr int NV = FP8 ? D / 16 : CH;   // 16-byte pieces of a key row
+        auto table_entry = [&](int bb) -> int64_t {
+            const int64_t j = (int64_t)bb * kTileKeys + tid;
+            if (bb >= nb || j >= seg_len)
+                return -1;
+            const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
+            const int64_t ti = toff + blk;
+            return (ti >= 0 && ti < p.page_table_len) ? (int64_t)__ldg(p.page_table + ti) : -1;
+        };
+        uint4 raw[NV];
+        bool raw_ok = false;
+        auto fetch_row = [&](int bb, int64_t page) {
+            const int64_t j = (int64_t)bb * kTileKeys + tid;
+            raw_ok = bb < nb && j < seg_len && page >= 0 && page < p.num_pages;
+            const int64_t off = p.page_shift >= 0 ? (j & (p.page_size - 1)) : j % p.page_size;
+            const uint8_t *row =
+                raw_ok ? p.kdata + (page * p.stride_page + off * p.stride_token) * (FP8 ? 1 : 2)
+                       : nullptr;
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+                raw[v] = raw_ok ? ldg16(row + 16 * v) : make_uint4(0, 0, 0, 0);
+        };
+        int64_t page_next = table_entry(1);
+        fetch_row(0, table_entry(0));
+
         for (int b = 0; b < nb; ++b, ++iter) {
             const uint32_t st = iter & 1;
             const uint32_t opB = opB0 + st * kOperandBytes;
-            // key row tid of block b, through the sequence's page-table row
-            const int64_t j = (int64_t)b * kTileKeys + tid;
-            bool ok = j < seg_len;
-            const uint8_t *row = nullptr;
-            if (ok) {
-                const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
-                const int64_t off = p.page_shift >= 0 ? (j & (p.page_size - 1)) : j % p.page_size;
-                const int64_t ti = toff + blk;
-                int64_t page = -1;
-                if (ti >= 0 && ti < p.page_table_len)
-                    page = __ldg(p.page_table + ti);
-                ok = page >= 0 && page < p.num_pages;
-                if (ok)
-                    row = p.kdata + (page * p.stride_page + off * p.stride_token) * (FP8 ? 1 : 2);
-            }
-            const uint32_t vmask = __ballot_sync(0xffffffffu, ok);
+            const int64_t page_after = table_entry(b + 2);
+            const uint32_t vmask = __ballot_sync(0xffffffffu, raw_ok);
             if (lane == 0)
                 s_kmask[iter & 3][warp] = vmask;
             if (FP8) {
 #pragma unroll
                 for (int c = 0; c < D / 16; ++c) {   // 16 codes -> two f16 chunks
-                    const uint4 v = ok ? ldg16(row + 16 * c) : make_uint4(0, 0, 0, 0);
-                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                    const uint32_t w[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
                     uint32_t h[8];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
@@ -576,11 +606,12 @@ msa_index_tiled_kernel(const __grid_constant__ IndexerParams p)
                 }
             } else {
 #pragma unroll
-                for (int c = 0; c < CH; ++c) {
-                    const uint4 v = ok ? ldg16(row + 16 * c) : make_uint4(0, 0, 0, 0);
-                    sts128(swz(opB, tid, c), v.x, v.y, v.z, v.w);
-                }
+                for (int c = 0; c < CH; ++c)
+                    sts128(swz(opB, tid, c), raw[c].x, raw[c].y, raw[c].z, raw[c].w);
             }
+            if (b + 1 < nb)
+                fetch_row(b + 1, page_next);
+            page_next = page_after;
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncthreads();
