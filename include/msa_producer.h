@@ -268,6 +268,18 @@ msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t num_queries, 
 msa_status msa_host_buffer_device_address(const void *host_ptr, void **device_ptr);
 
 /* Static, human-readable name of a status; never NULL. */
+/*
+ * msa_checked_violations -- diagnostics of a checked build (compiled with
+ * -DMSA_CHECKED, the stand-in for a memory sanitizer): every global store of the
+ * producer and projection kernels is checked against the byte range its
+ * destination's descriptor implies (compact outputs: num_tokens rows; caches: up
+ * to the furthest element their page count and strides reach), and a store
+ * outside it is skipped and counted.  Synchronises the device, writes the count
+ * of skipped stores since the last reset to *count and, if reset != 0, zeroes it.
+ * A normal build returns MSA_ERR_UNSUPPORTED with *count = 0.
+ */
+msa_status msa_checked_violations(uint64_t *count, int32_t reset);
+
 const char *msa_status_string(msa_status status);
 
 /* Last detailed message of a failed check on this thread (static storage). */

@@ -34,7 +34,8 @@ MSA_LAUNCH_QUERY_RUNS = 4
 # every function the header declares
 EXPORTED = ("msa_producer_forward", "msa_producer_validate", "msa_producer_launch_shape",
             "msa_indexer_forward", "msa_host_buffer_device_address", "msa_status_string",
-            "msa_last_error_detail", "msa_projection_forward", "msa_projection_validate")
+            "msa_last_error_detail", "msa_projection_forward", "msa_projection_validate",
+            "msa_checked_violations")
 
 MSA_STATUS_WAIT_TIMEOUT = 1
 
@@ -129,6 +130,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.msa_projection_validate.restype = ctypes.c_int
         L.msa_host_buffer_device_address.argtypes = [vp, ctypes.POINTER(ctypes.c_void_p)]
         L.msa_host_buffer_device_address.restype = ctypes.c_int
+        L.msa_checked_violations.argtypes = [ctypes.POINTER(ctypes.c_uint64), i32]
+        L.msa_checked_violations.restype = ctypes.c_int
         L.msa_status_string.argtypes = [ctypes.c_int]
         L.msa_status_string.restype = ctypes.c_char_p
         L.msa_last_error_detail.argtypes = []
@@ -280,6 +283,18 @@ def msa_indexer_forward(cfg, num_queries, idx_q, kv_len, table_offset, page_tabl
     if check and s != MSA_OK:
         raise MsaError(s, "msa_indexer_forward", last_error_detail())
     return s
+
+
+def msa_checked_violations(reset: bool = True):
+    """Stores skipped by a checked build since the last reset (synchronises the
+    device); None for a normal build."""
+    n = ctypes.c_uint64(0)
+    s = load().msa_checked_violations(ctypes.byref(n), 1 if reset else 0)
+    if s == MSA_ERR_UNSUPPORTED:
+        return None
+    if s != MSA_OK:
+        raise MsaError(s, "msa_checked_violations", last_error_detail())
+    return int(n.value)
 
 
 def msa_host_buffer_device_address(host_ptr: int):

@@ -85,6 +85,32 @@ def build(force: bool = False, verbose: bool = False, defines=None) -> str:
     return LIB_PATH
 
 
+CHECKED_LIB_PATH = os.path.join(OUT_DIR, "libmsa_producer_checked.so")
+
+
+def build_checked(force: bool = False) -> str:
+    """Compiles the checked library (-DMSA_CHECKED: every global store of the
+    producer and projection kernels is checked against the extent of its
+    destination, and a store outside it is skipped and counted) next to the normal
+    one, and returns its path.  A diagnostic build; the product uses build()."""
+    stamp = CHECKED_LIB_PATH + ".stamp"
+    deps = SOURCES + HEADERS + [os.path.join(INCLUDE, h) for h in ("msa_producer.h", "msa_projection.h")]
+    deps.append(os.path.abspath(__file__))
+    if (not force and os.path.exists(CHECKED_LIB_PATH) and os.path.exists(stamp)
+            and all(os.path.getmtime(d) <= os.path.getmtime(CHECKED_LIB_PATH) for d in deps)):
+        return CHECKED_LIB_PATH
+    os.makedirs(OUT_DIR, exist_ok=True)
+    tmp = CHECKED_LIB_PATH + f".{os.getpid()}.tmp"
+    cmd = nvcc_command(tmp, extra=["-DMSA_CHECKED"])
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
+    os.replace(tmp, CHECKED_LIB_PATH)
+    with open(stamp, "w") as f:
+        f.write("MSA_CHECKED")
+    return CHECKED_LIB_PATH
+
+
 if __name__ == "__main__":
     defs = [a[2:] for a in sys.argv[1:] if a.startswith("-D")]
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, defines=defs or None))

@@ -23,3 +23,13 @@ msa_status msa_internal_validate_producer(const msa_producer_cfg *cfg, int64_t n
                                           const msa_cache_desc *k_cache,
                                           const msa_cache_desc *v_cache,
                                           const msa_cache_desc *idx_k_cache, const float *scales);
+
+// First byte past the reachable extent of a cache (the checked build's bound).
+const uint8_t *msa_internal_cache_end(uint8_t *const *data, int64_t heads, int64_t num_pages,
+                                      int64_t stride_page, int64_t stride_head,
+                                      int64_t stride_token, int64_t elem_size, int32_t head_dim,
+                                      int32_t page_size);
+
+// Checked build: the projection kernel's violation counter (read, and optionally
+// reset); synchronises the device.
+msa_status msa_internal_projection_violations(uint64_t *count, int32_t reset);

@@ -103,7 +103,29 @@ struct Params {
     int32_t pdl;                    // launched with programmatic dependent launch
     float rms_eps;
     float inv_freq[kMaxRotaryHalf];
+#ifdef MSA_CHECKED
+    const uint8_t *out_hi[2];       // first byte past q_out, idx_q_out
+    const uint8_t *cache_hi[3];     // first byte past each cache's reachable extent
+#endif
 };
+
+#ifdef MSA_CHECKED
+// Checked build: a global store whose bytes leave its destination's extent is
+// skipped and counted here (read by msa_checked_violations).
+__device__ unsigned long long g_msa_violations;
+
+__device__ __forceinline__ bool msa_in_range(const void *ptr, int n, const void *lo, const void *hi)
+{
+    const uint8_t *b = static_cast<const uint8_t *>(ptr);
+    if (b >= static_cast<const uint8_t *>(lo) && b + n <= static_cast<const uint8_t *>(hi))
+        return true;
+    atomicAdd(&g_msa_violations, 1ull);
+    return false;
+}
+#define MSA_GUARD(ptr, n, lo, hi) if (!msa_in_range((ptr), (n), (lo), (hi))) {} else
+#else
+#define MSA_GUARD(ptr, n, lo, hi)
+#endif
 
 // ---------------------------------------------------------------------------
 // device helpers
@@ -511,8 +533,12 @@ msa_producer_kernel(const __grid_constant__ Params p)
 
                 if (sec == 0 || sec == 3) {
                     uint16_t *dst = sec == 0 ? q_tok + h * D : iq_tok + h * D;
-                    st_v4(dst + aoff, pack_bf16x8(y));
-                    st_v4(dst + boff, pack_bf16x8(y + 4));
+#ifdef MSA_CHECKED
+                    const void *lo = sec == 0 ? (const void *)p.q_out : (const void *)p.idx_q_out;
+                    const void *hi = p.out_hi[sec == 0 ? 0 : 1];
+#endif
+                    MSA_GUARD(dst + aoff, 16, lo, hi) st_v4(dst + aoff, pack_bf16x8(y));
+                    MSA_GUARD(dst + boff, 16, lo, hi) st_v4(dst + boff, pack_bf16x8(y + 4));
                 } else {
                     const int ci = sec == 1 ? 0 : sec == 2 ? 1 : 2;
                     if (!((meta.valid >> ci) & 1))
@@ -529,11 +555,15 @@ msa_producer_kernel(const __grid_constant__ Params p)
                         for (int j = 0; j < 8; ++j)
                             y[j] = __fmul2_rn(y[j], inv);
                         uint8_t *dst = cc.data + e;
+                        MSA_GUARD(dst + aoff, 8, cc.data, p.cache_hi[ci])
                         st_v2(dst + aoff, pack_e4m3x4(y[0], y[1]), pack_e4m3x4(y[2], y[3]));
+                        MSA_GUARD(dst + boff, 8, cc.data, p.cache_hi[ci])
                         st_v2(dst + boff, pack_e4m3x4(y[4], y[5]), pack_e4m3x4(y[6], y[7]));
                     } else {
                         uint16_t *dst = reinterpret_cast<uint16_t *>(cc.data) + e;
+                        MSA_GUARD(dst + aoff, 16, cc.data, p.cache_hi[ci])
                         st_v4(dst + aoff, pack_bf16x8(y));
+                        MSA_GUARD(dst + boff, 16, cc.data, p.cache_hi[ci])
                         st_v4(dst + boff, pack_bf16x8(y + 4));
                     }
                 }
@@ -922,6 +952,21 @@ msa_status msa_producer_forward(const msa_producer_cfg *cfg, int64_t num_tokens,
             p.page_shift = sh;
     p.scale_mode = cfg->scale_mode;
     p.pdl = (launch_flags & MSA_LAUNCH_PDL) ? 1 : 0;
+#ifdef MSA_CHECKED
+    p.out_hi[0] = p.q_out ? reinterpret_cast<const uint8_t *>(p.q_out) +
+                                num_tokens * (int64_t)cfg->num_q_heads * cfg->head_dim * 2
+                          : nullptr;
+    p.out_hi[1] = p.idx_q_out ? reinterpret_cast<const uint8_t *>(p.idx_q_out) +
+                                    num_tokens * (int64_t)cfg->num_idx_q_heads * cfg->head_dim * 2
+                              : nullptr;
+    for (int ci = 0; ci < 3; ++ci)
+        p.cache_hi[ci] = msa_internal_cache_end(&p.cache[ci].data, ci == 2 ? cfg->num_idx_k_heads
+                                                                           : cfg->num_kv_heads,
+                                                p.cache[ci].num_pages, p.cache[ci].stride_page,
+                                                p.cache[ci].stride_head, p.cache[ci].stride_token,
+                                                p.cache[ci].fp8 ? 1 : 2, cfg->head_dim,
+                                                cfg->page_size);
+#endif
     p.rms_eps = cfg->rms_eps;
     // RoPE frequencies theta^(-2k/rd), evaluated in double and rounded once
     for (int k = 0; k < cfg->rotary_dim / 2; ++k)
@@ -1035,4 +1080,44 @@ msa_status msa_internal_check_cache(const char *name, const msa_cache_desc *c, i
                                     int32_t head_dim, int32_t page_size)
 {
     return check_cache(name, c, heads, head_dim, page_size);
+}
+
+// First byte past the furthest element a write to a cache can reach (nullptr for
+// an absent or empty cache); the checked build's upper bound for its stores.
+const uint8_t *msa_internal_cache_end(uint8_t *const *data, int64_t heads, int64_t num_pages,
+                                      int64_t stride_page, int64_t stride_head,
+                                      int64_t stride_token, int64_t elem_size, int32_t head_dim,
+                                      int32_t page_size)
+{
+    if (!*data || num_pages <= 0 || heads <= 0)
+        return *data;
+    const int64_t last = (num_pages - 1) * stride_page + (heads - 1) * stride_head +
+                         (int64_t)(page_size - 1) * stride_token + head_dim;
+    return *data + last * elem_size;
+}
+
+extern "C" msa_status msa_checked_violations(uint64_t *count, int32_t reset)
+{
+    if (!count)
+        return fail(MSA_ERR_INVALID_ARGUMENT, "count is NULL");
+    *count = 0;
+#ifdef MSA_CHECKED
+    unsigned long long v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpyFromSymbol(&v, g_msa_violations, sizeof v) != cudaSuccess)
+        return fail(MSA_ERR_CUDA, "reading the violation counter failed");
+    uint64_t w = 0;
+    if (msa_internal_projection_violations(&w, reset) != MSA_OK)
+        return fail(MSA_ERR_CUDA, "reading the projection's violation counter failed");
+    if (reset) {
+        const unsigned long long z = 0;
+        if (cudaMemcpyToSymbol(g_msa_violations, &z, sizeof z) != cudaSuccess)
+            return fail(MSA_ERR_CUDA, "resetting the violation counter failed");
+    }
+    *count = (uint64_t)v + w;
+    return MSA_OK;
+#else
+    (void)reset;
+    return fail(MSA_ERR_UNSUPPORTED, "not a checked build (compile with -DMSA_CHECKED)");
+#endif
 }

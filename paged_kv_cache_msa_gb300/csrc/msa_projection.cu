@@ -115,7 +115,30 @@ struct Params {
     int32_t scale_mode;
     float rms_eps;
     float inv_freq[kMaxRotaryHalf];
+#ifdef MSA_CHECKED
+    const uint8_t *out_hi[2];   // first byte past q_out, idx_q_out
+    const uint8_t *cache_hi[3]; // first byte past each cache's reachable extent
+    const uint8_t *rows_hi;     // first byte past rows_out
+#endif
 };
+
+#ifdef MSA_CHECKED
+// Checked build: a global store whose bytes leave its destination's extent is
+// skipped and counted here.
+__device__ unsigned long long g_msa_projection_violations;
+
+__device__ __forceinline__ bool msa_in_range(const void *ptr, int n, const void *lo, const void *hi)
+{
+    const uint8_t *b = static_cast<const uint8_t *>(ptr);
+    if (b >= static_cast<const uint8_t *>(lo) && b + n <= static_cast<const uint8_t *>(hi))
+        return true;
+    atomicAdd(&g_msa_projection_violations, 1ull);
+    return false;
+}
+#define MSA_GUARD(ptr, n, lo, hi) if (!msa_in_range((ptr), (n), (lo), (hi))) {} else
+#else
+#define MSA_GUARD(ptr, n, lo, hi)
+#endif
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -420,6 +443,9 @@ struct Dest {
     uint8_t *row;  // nullptr: nothing is written (padded token, or a cache not taken)
     int fp8;       // 1: E4M3 codes of x * inv; 0: bf16
     float inv;
+#ifdef MSA_CHECKED
+    const uint8_t *lo, *hi;   // the destination's extent
+#endif
 };
 
 template <int D>
@@ -436,6 +462,10 @@ __device__ __forceinline__ Dest make_dest(const Params &p, const Head &hd, int64
         uint16_t *r = hd.sec == 0 ? p.q_out + ((int64_t)t * p.hq + hd.h) * D
                                   : p.idx_q_out + ((int64_t)t * p.hiq + hd.h) * D;
         ds.row = reinterpret_cast<uint8_t *>(r);
+#ifdef MSA_CHECKED
+        ds.lo = reinterpret_cast<const uint8_t *>(hd.sec == 0 ? p.q_out : p.idx_q_out);
+        ds.hi = p.out_hi[hd.sec == 0 ? 0 : 1];
+#endif
         return ds;
     }
     const int ci = hd.sec == 1 ? 0 : hd.sec == 2 ? 1 : 2;
@@ -444,6 +474,10 @@ __device__ __forceinline__ Dest make_dest(const Params &p, const Head &hd, int64
     const CacheArgs &cc = p.cache[ci];
     const int64_t e = pl.page * cc.stride_page + (int64_t)hd.h * cc.stride_head +
                       (int64_t)pl.off * cc.stride_token;
+#ifdef MSA_CHECKED
+    ds.lo = cc.data;
+    ds.hi = p.cache_hi[ci];
+#endif
     if (cc.fp8) {
         const int si = p.scale_mode == MSA_SCALE_PER_HEAD
                            ? (ci == 0 ? hd.h : ci == 1 ? p.hkv + hd.h : 2 * p.hkv + hd.h)
@@ -464,9 +498,11 @@ __device__ __forceinline__ void emit8(const Dest &ds, int d0, const float (&y)[8
         return;
     if (ds.fp8) {
         const float inv = ds.inv;
+        MSA_GUARD(ds.row + d0, 8, ds.lo, ds.hi)
         st_v2(ds.row + d0, pack_e4m3x4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv),
               pack_e4m3x4(y[4] * inv, y[5] * inv, y[6] * inv, y[7] * inv));
     } else {
+        MSA_GUARD(ds.row + 2 * d0, 16, ds.lo, ds.hi)
         st_v4(ds.row + 2 * d0, pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
               pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
     }
@@ -547,6 +583,7 @@ __device__ __forceinline__ void head_fast(const Params &p, const Head &hd, uint3
         uint16_t *dst = p.rows_out + (int64_t)t * p.rows_out_stride + col;
 #pragma unroll
         for (int i = 0; i < D / 8; ++i)
+            MSA_GUARD(dst + 8 * i, 16, p.rows_out, p.rows_hi)
             st_v4(dst + 8 * i, row[4 * i], row[4 * i + 1], row[4 * i + 2], row[4 * i + 3]);
     }
     auto elt = [&](int i) { return (i & 1) ? bf16_hi(row[i >> 1]) : bf16_lo(row[i >> 1]); };
@@ -665,6 +702,7 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, uint32_t taddr, i
                                 (int64_t)(g0 + hh) * D + c;
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
+                    MSA_GUARD(dst + 8 * j, 16, p.rows_out, p.rows_hi)
                     st_v4(dst + 8 * j, bits[4 * j], bits[4 * j + 1], bits[4 * j + 2], bits[4 * j + 3]);
             }
         }
@@ -1158,12 +1196,31 @@ extern "C" msa_status msa_projection_forward(
     fill_cache(p.cache[0], cfg->num_kv_heads > 0 ? k_cache : nullptr);
     fill_cache(p.cache[1], cfg->num_kv_heads > 0 ? v_cache : nullptr);
     fill_cache(p.cache[2], cfg->num_idx_k_heads > 0 ? idx_k_cache : nullptr);
+#ifdef MSA_CHECKED
+    for (int ci = 0; ci < 3; ++ci)
+        p.cache_hi[ci] = msa_internal_cache_end(&p.cache[ci].data, ci == 2 ? cfg->num_idx_k_heads
+                                                                           : cfg->num_kv_heads,
+                                                p.cache[ci].num_pages, p.cache[ci].stride_page,
+                                                p.cache[ci].stride_head, p.cache[ci].stride_token,
+                                                p.cache[ci].fp8 ? 1 : 2, cfg->head_dim,
+                                                cfg->page_size);
+#endif
     p.scales = scales;
     p.rows_out = static_cast<uint16_t *>(rows_out);
     p.rows_out_stride = rows_out_stride;
     p.hidden_scales = hidden_scales;
     p.weight_scales = weight_scales;
     p.status = status;
+#ifdef MSA_CHECKED
+    p.out_hi[0] = q_out ? static_cast<const uint8_t *>(q_out) +
+                              num_tokens * (int64_t)cfg->num_q_heads * cfg->head_dim * 2
+                        : nullptr;
+    p.out_hi[1] = idx_q_out ? static_cast<const uint8_t *>(idx_q_out) +
+                                  num_tokens * (int64_t)cfg->num_idx_q_heads * cfg->head_dim * 2
+                            : nullptr;
+    p.rows_hi = rows_out ? static_cast<const uint8_t *>(rows_out) + num_tokens * rows_out_stride * 2
+                         : nullptr;
+#endif
     p.num_tokens = num_tokens;
     const bool fp8 = operand_dtype == MSA_DTYPE_FP8_E4M3;
     const int es = fp8 ? 1 : 2;
@@ -1247,5 +1304,24 @@ extern "C" msa_status msa_projection_forward(
     if (e != cudaSuccess)
         return fail(MSA_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
     msa_internal_set_detail("");
+    return MSA_OK;
+}
+
+msa_status msa_internal_projection_violations(uint64_t *count, int32_t reset)
+{
+    *count = 0;
+#ifdef MSA_CHECKED
+    unsigned long long v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_msa_projection_violations, sizeof v) != cudaSuccess)
+        return MSA_ERR_CUDA;
+    if (reset) {
+        const unsigned long long z = 0;
+        if (cudaMemcpyToSymbol(g_msa_projection_violations, &z, sizeof z) != cudaSuccess)
+            return MSA_ERR_CUDA;
+    }
+    *count = v;
+#else
+    (void)reset;
+#endif
     return MSA_OK;
 }
