@@ -376,6 +376,53 @@ def indexer_timing(replays: int = 200, calls: int = 20):
             "index_k_tokens_scanned": int(w.kv_len.sum())}
 
 
+def decode_layer_timing(layers: int = 60, replays: int = 50):
+    """The decode layer's MSA hot path at batch 64 (big shapes): the producer, then
+    the indexer on what it wrote (compact index-Q, the index-K cache; contexts
+    U{1..9216}), both with programmatic dependent launch, `layers` layers in one
+    CUDA graph.  Each layer has its own index-K history pool (random codes, on the
+    device); K/V pools are shared by the layers (the producer writes 64 rows)."""
+    import torch
+    from paged_kv_cache_msa_gb300 import binding as B
+    from paged_kv_cache_msa_gb300 import workloads as wl
+    from paged_kv_cache_msa_gb300.device import DecodeLayer, DeviceWorkload
+    w = wl.config2_decode64()
+    first = DeviceWorkload(w)
+    g_cpu = torch.Generator(device="cuda")
+    g_cpu.manual_seed(7)
+    stack = []
+    for l in range(layers):
+        pools = dict(first.pools)
+        pools["idx_k"] = torch.randint(0, 255, first.pools["idx_k"].shape, dtype=torch.uint8,
+                                       device=first.device, generator=g_cpu)
+        stack.append(DecodeLayer(DeviceWorkload(w, pools_on_device=pools), max_blocks_per_seq=144))
+    s = torch.cuda.Stream()
+    out = {}
+    for name, flags in (("pdl", B.MSA_LAUNCH_PDL), ("no_pdl", 0)):
+        with torch.cuda.stream(s):
+            for layer in stack:
+                layer.run(s, flags)
+            s.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for layer in stack:
+                    layer.run(s, flags)
+            for _ in range(3):
+                g.replay()
+            s.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(replays):
+                g.replay()
+            e1.record(s)
+            e1.synchronize()
+        us = 1e3 * e0.elapsed_time(e1) / replays
+        out[name] = {"us_per_step": us, "us_per_layer": us / layers}
+    return {"workload": f"decode batch 64, big shapes, contexts U{{1..9216}}: producer + indexer "
+                        f"(top-16 of 128-token blocks) per layer, {layers} layers in one CUDA graph",
+            "launches_per_layer": 3, **out}
+
+
 def indexer_prefill_timing(reps: int = 5):
     """The indexer of the prefill batch (8 x 8192 causal queries, 8 index heads of
     dim 128, fp8 index-K, top-16 of 128-token blocks): the query-run kernel (tiles
@@ -587,6 +634,7 @@ def run_ours(args):
     if not args.no_decode_step:
         indexer = indexer_timing()
         indexer["prefill"] = indexer_prefill_timing()
+        decode["layer_with_indexer"] = decode_layer_timing()
 
     projection = None
     if not args.no_projection:
@@ -715,6 +763,7 @@ def main():
         build_mod.build()
         out = indexer_timing(replays=max(1, args.steps), calls=20)
         out["prefill"] = indexer_prefill_timing()
+        out["decode_layer"] = decode_layer_timing()
         print(json.dumps(out), flush=True)
         return 0
     return run_ours(args)

@@ -162,3 +162,43 @@ class DeviceProjection:
 
     def rows_to_host(self):
         return self.rows_out.cpu().numpy().view(np.uint16)
+
+
+class DecodeLayer:
+    """One MSA decode layer's hot path on the device: the producer (rows -> compact
+    Q / index-Q, K/V/index-K into the caches) followed by the indexer on what the
+    producer wrote (its compact index-Q and index-K cache), each token's visible
+    history being its position + 1 tokens in its sequence's page-table row."""
+
+    def __init__(self, dw: DeviceWorkload, max_blocks_per_seq: int, block_tokens: int = 128,
+                 topk: int = 16):
+        import torch
+        self.dw = dw
+        w = dw.w
+        s = w.shape
+        assert w.page_table is not None and dw.caches.get("idx_k") is not None
+        P = s["page_size"]
+        self.cfg = B.make_indexer_cfg(s["num_idx_q_heads"], s["head_dim"], P, block_tokens, topk,
+                                      -(-max_blocks_per_seq * P // block_tokens))
+        T = w.num_tokens
+        pt = w.page_table.reshape(w.page_table.shape[0], -1)
+        # the sequence of each token is its slot's table row (logical slots); a padded
+        # token keeps the row of its position in the batch
+        seq = np.where(w.slot_mapping >= 0, w.slot_mapping // (pt.shape[1] * P),
+                       np.arange(T) % pt.shape[0])
+        self.kv_len = _t((w.positions.astype(np.int64) + 1).astype(np.int32), dw.device)
+        self.table_offset = _t((seq * pt.shape[1]).astype(np.int64), dw.device)
+        self.k_scale = dw.scales[2:3] if s.get("scale_mode", 0) == 0 else dw.scales[-1:]
+        self.block_scores = torch.empty((T, self.cfg.max_blocks), dtype=torch.float32,
+                                        device=dw.device)
+        self.topk_ids = torch.empty((T, topk), dtype=torch.int32, device=dw.device)
+
+    def run(self, stream, flags=0):
+        dw = self.dw
+        p = lambda t: int(t.data_ptr())
+        dw.run(B.MSA_LAUNCH_PERSISTENT | (flags & B.MSA_LAUNCH_PDL), stream=stream)
+        B.msa_indexer_forward(self.cfg, dw.w.num_tokens, p(dw.idx_q_out), p(self.kv_len),
+                              p(self.table_offset), p(dw.page_table), dw.page_table.numel(),
+                              dw.caches["idx_k"], p(self.k_scale), p(self.block_scores),
+                              p(self.topk_ids), flags & B.MSA_LAUNCH_PDL,
+                              stream=stream.cuda_stream)

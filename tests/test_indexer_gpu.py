@@ -191,3 +191,36 @@ def test_query_runs_prefill_65536_sampled():
         vals = [s_all[t, i] for i in ids]
         assert len(ids) == min(w.topk, int(nfin[t]))
         assert all(vals[i] >= vals[i + 1] for i in range(len(vals) - 1))
+
+
+def test_decode_layer_producer_then_indexer_in_a_graph():
+    """The producer and the indexer chained as a decode layer (the indexer reads
+    the compact index-Q and the index-K cache the producer just wrote), launched
+    with programmatic dependent launch, 3 layers captured in one CUDA graph: the
+    same bytes as the two kernels launched plainly one after the other."""
+    from paged_kv_cache_msa_gb300 import binding as B
+    from paged_kv_cache_msa_gb300.device import DecodeLayer, DeviceWorkload
+    w = wl.config2_decode64()
+    plain, chained = [], []
+    for _ in range(3):
+        plain.append(DecodeLayer(DeviceWorkload(w), max_blocks_per_seq=144))
+        chained.append(DecodeLayer(DeviceWorkload(w), max_blocks_per_seq=144))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for layer in plain:
+            layer.run(s, 0)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for layer in chained:
+                layer.run(s, B.MSA_LAUNCH_PDL)
+        g.replay()
+        s.synchronize()
+    for a, b in zip(plain, chained):
+        assert torch.equal(a.dw.q_out, b.dw.q_out) and torch.equal(a.dw.idx_q_out, b.dw.idx_q_out)
+        for k in a.dw.pools:
+            assert torch.equal(a.dw.pools[k], b.dw.pools[k])
+        assert torch.equal(a.block_scores, b.block_scores)
+        assert torch.equal(a.topk_ids, b.topk_ids)
+        fin = torch.isfinite(a.block_scores).sum(dim=1)
+        assert int(fin.min()) >= 1      # every token sees at least one scored block
