@@ -555,6 +555,76 @@ def projection_timing(launches: int = 10, warmup: int = 3, num_seqs: int = 8,
     return out
 
 
+def projection_decode_timing(batch: int = 64, calls: int = 20, replays: int = 20):
+    """The projection with the producer in its epilogue on a decode batch (``batch``
+    sequences x 1 token, hidden 6,144 -> 11,392 outputs, big shapes, fp8 caches),
+    bf16 and E4M3 operands, each against its unfused pair (cuBLAS GEMM of the same
+    operand type, then msa_producer_forward).  Every leg is a CUDA graph of
+    ``calls`` launches replayed ``replays`` times; the figure is per launch (for
+    the unfused pair, per GEMM + producer)."""
+    import torch
+    from paged_kv_cache_msa_gb300 import binding as B
+    from paged_kv_cache_msa_gb300 import workloads as wl
+    from paged_kv_cache_msa_gb300.device import DeviceProjection, DeviceWorkload
+    s = torch.cuda.Stream()
+
+    def graph_us(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            fn()
+            s.synchronize()
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(calls):
+                    fn()
+            for _ in range(3):
+                g.replay()
+            s.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(replays):
+                g.replay()
+            e1.record(s)
+            s.synchronize()
+        return 1e3 * e0.elapsed_time(e1) / (calls * replays)
+
+    out = {}
+    for name, dt in (("bf16", wl.DTYPE_BF16), ("e4m3", wl.DTYPE_E4M3)):
+        pw = wl.projection_decode(batch=batch, operand_dtype=dt)
+        dp = DeviceProjection(pw)
+        fused = graph_us(lambda: B.msa_projection_forward(*dp.args(), stream=s.cuda_stream))
+        status = int(dp.status.item())
+        K = pw.hidden_size
+        rows = torch.empty((pw.num_tokens, pw.width), dtype=torch.bfloat16, device=dp.device)
+        try:
+            if dt == wl.DTYPE_E4M3:
+                X = dp.hidden.view(torch.float8_e4m3fn)[:, :K]
+                Wt = dp.weight.view(torch.float8_e4m3fn)[:, :K]
+                one = torch.ones((), dtype=torch.float32, device=dp.device)
+                gemm = graph_us(lambda: torch._scaled_mm(X, Wt.t(), scale_a=one, scale_b=one,
+                                                         out_dtype=torch.bfloat16, out=rows))
+            else:
+                X = dp.hidden.view(torch.bfloat16)[:, :K]
+                Wt = dp.weight.view(torch.bfloat16)[:, :K]
+                gemm = graph_us(lambda: torch.matmul(X, Wt.t(), out=rows))
+        except Exception as e:   # a torch build without the comparator GEMM
+            gemm = None
+            log(f"[bench] decode comparator unavailable: {type(e).__name__}: {e}"[:160])
+        dw = DeviceWorkload(pw.producer, pools_on_device=dp.pools)
+        args = list(dw.args(B.MSA_LAUNCH_PERSISTENT))
+        args[2], args[3] = int(rows.data_ptr()), pw.width
+        prod = graph_us(lambda: B.msa_producer_forward(*args, stream=s.cuda_stream))
+        wbytes = pw.width * K * (1 if dt == wl.DTYPE_E4M3 else 2)
+        out[name] = {"workload": f"decode {batch} tokens, hidden {K} -> {pw.width} outputs, "
+                                 f"{name} operands, fp8 caches",
+                     "us_per_launch": fused, "status": status,
+                     "weight_read_gbs": wbytes / (fused * 1e-6) / 1e9,
+                     "unfused": {"gemm_us": gemm, "producer_us": prod,
+                                 "total_us": None if gemm is None else gemm + prod},
+                     "speedup_vs_unfused": None if gemm is None else (gemm + prod) / fused}
+        del dp, dw
+    return out
+
+
 def run_ours(args):
     import torch
     from paged_kv_cache_msa_gb300 import binding as B
@@ -639,7 +709,8 @@ def run_ours(args):
     projection = None
     if not args.no_projection:
         projection = {"bf16": projection_timing(num_seqs=args.projection_seqs, operand_dtype=0),
-                      "e4m3": projection_timing(num_seqs=args.projection_seqs, operand_dtype=1)}
+                      "e4m3": projection_timing(num_seqs=args.projection_seqs, operand_dtype=1),
+                      "decode_64": projection_decode_timing()}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -754,9 +825,11 @@ def main():
     if args.projection_only:
         from paged_kv_cache_msa_gb300 import build as build_mod
         build_mod.build()
-        print(json.dumps({dt: projection_timing(launches=max(1, args.steps), warmup=args.warmup,
-                                                num_seqs=args.projection_seqs, operand_dtype=i)
-                          for i, dt in enumerate(("bf16", "e4m3"))}), flush=True)
+        out = {dt: projection_timing(launches=max(1, args.steps), warmup=args.warmup,
+                                     num_seqs=args.projection_seqs, operand_dtype=i)
+               for i, dt in enumerate(("bf16", "e4m3"))}
+        out["decode_64"] = projection_decode_timing()
+        print(json.dumps(out), flush=True)
         return 0
     if args.indexer_only:
         from paged_kv_cache_msa_gb300 import build as build_mod

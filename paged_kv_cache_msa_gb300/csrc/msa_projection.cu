@@ -47,6 +47,12 @@
 #include "msa_producer.h"
 #include "msa_projection.h"
 
+#ifndef MSA_PROJ_PREFETCH
+#define MSA_PROJ_PREFETCH 8          // K blocks of weight prefetched into L2 ahead of the ring
+#endif
+#ifndef MSA_PROJ_PREFETCH_MTILES
+#define MSA_PROJ_PREFETCH_MTILES 4   // up to this many 256-token tiles
+#endif
 #ifndef MSA_PROJ_NGROUP
 #define MSA_PROJ_NGROUP 8
 #endif
@@ -107,6 +113,8 @@ struct Params {
     int64_t num_tokens;
     int32_t num_k_blocks;
     int32_t m_tiles, n_tiles, n_group;
+    int32_t split;              // CTAs per cluster sharing an output tile's K (small batches)
+    int32_t prefetch;           // K blocks the weight tile is fetched into L2 ahead (0: none)
     int32_t hq, hkv, hiq, hik, htot;
     int32_t rotary_dim;
     int32_t rope_style;
@@ -236,6 +244,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Bring a box of the tensor into L2 without waiting for it.  Weights read once per
+// launch come from DRAM; a stage's load issued after this prefetch finds them in L2
+// instead of waiting out a DRAM round trip with the ring's few loads in flight.
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap *map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x),
+                 "r"(y)
+                 : "memory");
+}
+
 // Shared-memory matrix descriptor of a K-major operand tile written by TMA with the
 // 128-byte swizzle: rows of 128 bytes, groups of 8 rows 1024 bytes apart.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
@@ -314,6 +332,42 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8])
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Where an epilogue thread's accumulator row lives: this CTA's tensor memory and,
+// with the K dimension split over a cluster, the partial sums the other CTAs of
+// the cluster left in their shared memory ([column / 4][128 rows][4 columns] fp32:
+// a warp's 16-byte reads of four columns cover 512 contiguous bytes).
+struct AccSrc {
+    uint32_t taddr;       // this warp's lanes at the tile's first column
+    int nsplit;           // CTAs whose partial sums add up to the accumulator
+    int row;              // this thread's row (tensor-memory lane)
+    uint32_t part;        // shared-memory offset of the partial sums in every CTA
+};
+
+// 32 accumulator columns [col, col + 32) of this thread's row: the own partial sum
+// plus the other CTAs' in rank order
+__device__ __forceinline__ void acc_ld32(const AccSrc &a, int col, uint32_t (&r)[32])
+{
+    tmem_ld32(a.taddr + (uint32_t)col, r);
+    tmem_wait_ld();
+    for (int s = 1; s < a.nsplit; ++s) {
+        // eight 16-byte loads in flight before any is used
+        const uint32_t base = map_to_rank(a.part, (uint32_t)s) + (uint32_t)((col >> 2) * 128 + a.row) * 16u;
+        float4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(v[j].x), "=f"(v[j].y), "=f"(v[j].z), "=f"(v[j].w)
+                         : "r"(base + (uint32_t)j * 2048u));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + v[j].x);
+            r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + v[j].y);
+            r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + v[j].z);
+            r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + v[j].w);
+        }
+    }
+}
 
 // ---------------------------------------------------------------------------
 // number formats and stores
@@ -524,7 +578,20 @@ __device__ __forceinline__ int norm_index(int sec)
 // by k = rint(a / 2pi), r = a - k * 2pi, with 2pi split into three floats whose
 // first, 6.28125, has 8 significant bits so that k * 6.28125 is exact (Cody and
 // Waite's additive range reduction), and the hardware approximations take r
-// (absolute error about 2^-21 on [-pi, pi]); larger angles use sincosf.
+// (absolute error about 2^-21 on [-pi, pi]); larger angles use sincosf, called
+// out of line: the epilogue unrolls this at every rotated pair of a head, and
+// sincosf's full-range reduction inlined at each of those sites multiplied the
+// epilogue's code several times over.  The epilogue runs once per tile, so its
+// instructions stream through the instruction cache: at small batches, where
+// the epilogue is not hidden behind the next tile's main loop, the inlined copies
+// (never executed) tripled its time.
+__device__ __noinline__ float2 rope_sincos_wide(float a)
+{
+    float s, c;
+    sincosf(a, &s, &c);
+    return make_float2(s, c);
+}
+
 __device__ __forceinline__ void rope_sincos(float a, float *s, float *c)
 {
     if (fabsf(a) < 65536.0f) {
@@ -534,7 +601,9 @@ __device__ __forceinline__ void rope_sincos(float a, float *s, float *c)
         r = fmaf(-k, 1.0253131677018246e-11f, r);
         __sincosf(r, s, c);
     } else {
-        sincosf(a, s, c);
+        const float2 v = rope_sincos_wide(a);
+        *s = v.x;
+        *c = v.y;
     }
 }
 
@@ -543,7 +612,8 @@ __device__ __forceinline__ void rope_sincos(float a, float *s, float *c)
 // is kept in registers; the head's norm weights and per-output scales are held by
 // the lanes of the warp (lane l: dims l, l + 32, ...) and shuffled to every lane.
 template <int D, int ROT>
-__device__ __forceinline__ void head_fast(const Params &p, const Head &hd, uint32_t taddr, int col,
+__device__ __forceinline__ void head_fast(const Params &p, const Head &hd, const AccSrc &src,
+                                          int tcol, int col,
                                           int64_t t, bool live, const Place &pl, int pos,
                                           const RowScale &rs, int lane)
 {
@@ -564,8 +634,7 @@ __device__ __forceinline__ void head_fast(const Params &p, const Head &hd, uint3
 #pragma unroll
     for (int c = 0; c < D; c += 32) {
         uint32_t r[32];
-        tmem_ld32(taddr + (uint32_t)c, r);
-        tmem_wait_ld();
+        acc_ld32(src, tcol + c, r);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             float a = __uint_as_float(r[2 * j]), b = __uint_as_float(r[2 * j + 1]);
@@ -632,9 +701,10 @@ __device__ __forceinline__ void head_fast(const Params &p, const Head &hd, uint3
 // The warp runs the producer on the tile's heads hh with hh % 2 == hgroup (the
 // other epilogue warp of the same tensor-memory lanes takes the rest).
 template <int D>
-__device__ __forceinline__ void epilogue_tile(const Params &p, uint32_t taddr, int n_tile, int64_t t,
-                                              bool live, int hgroup, int lane)
+__device__ __forceinline__ void epilogue_tile(const Params &p, const AccSrc &src, int n_tile,
+                                              int64_t t, bool live, int hgroup, int lane)
 {
+    const uint32_t taddr = src.taddr;
     constexpr int HPT = kBN / D;  // heads per tile
     const int g0 = n_tile * HPT;
 
@@ -661,19 +731,19 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, uint32_t taddr, i
             const Head hd = head_of(p, g0 + hh);
             if (hd.sec < 0)
                 continue;
-            const uint32_t ta = taddr + (uint32_t)(hh * D);
             const int col = col0 + hh * D;
             if (rd == D)
-                head_fast<D, D>(p, hd, ta, col, t, live, pl, pos, rs, lane);
+                head_fast<D, D>(p, hd, src, hh * D, col, t, live, pl, pos, rs, lane);
             else if (rd == D / 2)
-                head_fast<D, D / 2>(p, hd, ta, col, t, live, pl, pos, rs, lane);
+                head_fast<D, D / 2>(p, hd, src, hh * D, col, t, live, pl, pos, rs, lane);
             else
-                head_fast<D, 0>(p, hd, ta, col, t, live, pl, pos, rs, lane);
+                head_fast<D, 0>(p, hd, src, hh * D, col, t, live, pl, pos, rs, lane);
         }
         return;
     }
 
-    // any other RoPE: the accumulator is read twice (norm factor, then values)
+    // any other RoPE: the accumulator is read twice (norm factor, then values);
+    // reached only without a split over K (the host keeps those on the 2-SM kernel)
 
     // pass 1: bf16 row values, optional row store, and each head's norm factor
     float rn[HPT];
@@ -904,7 +974,12 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 tile_coords(p, tile, m, n);
                 const int row_x = m * kPairM + (int)rank * kBM;
                 const int row_w = n * kBN + (int)rank * kHalfN;
+                const int pf = row_w < p.htot * D ? p.prefetch : 0;  // rows past W: nothing to fetch
+                for (int kb = 0; kb < pf && kb < p.num_k_blocks; ++kb)
+                    tma_prefetch_l2(&tmap_w, kb * kBKElems, row_w);
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (pf && kb + pf < p.num_k_blocks)
+                        tma_prefetch_l2(&tmap_w, (kb + pf) * kBKElems, row_w);
                     if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1)) {
                         ok = false;
                         break;
@@ -988,7 +1063,12 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
             }
             tc_fence_after();
             const int64_t t = (int64_t)m * kPairM + (int64_t)rank * kBM + row;
-            epilogue_tile<D>(p, tmem + lane_base + b * kBN, n, t, t < p.num_tokens, hgroup, lane);
+            AccSrc src;
+            src.taddr = tmem + lane_base + b * kBN;
+            src.nsplit = 1;
+            src.row = row;
+            src.part = 0;
+            epilogue_tile<D>(p, src, n, t, t < p.num_tokens, hgroup, lane);
             tc_fence_before();
             __syncwarp();
             if (lane == 0)  // this warp is done reading accumulator b
@@ -1004,6 +1084,207 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
+// small batches: the K dimension split over a cluster
+// ---------------------------------------------------------------------------
+// With a single 128-token tile (num_tokens <= 128) the 2-SM kernel keeps at most
+// one cluster per 256-wide output tile busy, each walking all of K.  Here a
+// cluster of S CTAs takes one output tile and CTA s of it a contiguous S-th of the
+// K blocks, accumulating 128 tokens x 256 outputs in its own tensor memory with the
+// one-SM MMA (tcgen05.mma.cta_group::1, M 128, N 256).  The other CTAs then write
+// their partial sums, column-major, into their shared memory (the ring is free by
+// then) and CTA 0's epilogue adds them in rank order over distributed shared
+// memory before running the producer.  Used for NeoX RoPE over D, D/2 or no dims
+// (the register-resident epilogue); other layouts take the 2-SM kernel.
+
+constexpr int kSplitStages = 4;
+constexpr uint32_t kSplitStageBytes = kTileABytes + 2 * kTileBBytes;  // 128 tokens + 256 weight rows
+constexpr int kSplitDynSmem = kSplitStages * kSplitStageBytes + 1024;
+static_assert(kSplitStages * kSplitStageBytes >= 128u * kBN * 4u, "partial sums fit the ring");
+constexpr uint32_t kIdescShape1 = ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+
+template <bool FP8>
+__device__ __forceinline__ void tc_mma1(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc)
+{
+    if (FP8)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a), "l"(b), "r"((1u << 4) | kIdescShape1), "r"(acc)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a), "l"(b), "r"((1u << 4) | (1u << 7) | (1u << 10) | kIdescShape1), "r"(acc)
+            : "memory");
+}
+
+__device__ __forceinline__ void tc_commit1(uint32_t bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_own(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                             uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kThreads, 1)
+msa_projection_splitk_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                             const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_full[kSplitStages];
+    __shared__ __align__(8) uint64_t bar_empty[kSplitStages];
+    __shared__ __align__(8) uint64_t bar_tfull;
+    __shared__ __align__(8) uint64_t bar_drain;
+    __shared__ uint32_t s_tmem;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const int S = p.split;
+    const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const int n_tile = blockIdx.x / S;
+    const int kb0 = (int)((int64_t)p.num_k_blocks * rank / S);
+    const int kb1 = (int)((int64_t)p.num_k_blocks * (rank + 1) / S);
+    constexpr int kBKElems = FP8 ? kBKBytes : kBKBytes / 2;
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kSplitStages; ++st) {
+            mbar_init(smem_u32(&bar_full[st]), 1);
+            mbar_init(smem_u32(&bar_empty[st]), 1);
+        }
+        mbar_init(smem_u32(&bar_tfull), 1);
+        mbar_init(smem_u32(&bar_drain), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&s_tmem)),
+                     "r"(kBN)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    bool ok = true;
+
+    if (warp == 0) {
+        if (lane == 0) {   // TMA: this CTA's K blocks of the hidden tile and the weight tile
+            uint32_t stage = 0, phase = 0;
+            for (int kb = kb0; kb < kb0 + p.prefetch && kb < kb1; ++kb)
+                tma_prefetch_l2(&tmap_w, kb * kBKElems, n_tile * kBN);
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (p.prefetch && kb + p.prefetch < kb1)
+                    tma_prefetch_l2(&tmap_w, (kb + p.prefetch) * kBKElems, n_tile * kBN);
+                if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t full = smem_u32(&bar_full[stage]);
+                const uint32_t a = ring + stage * kSplitStageBytes;
+                mbar_expect_tx(full, kSplitStageBytes);
+                tma_load_own(a, &tmap_x, kb * kBKElems, 0, full);
+                tma_load_own(a + kTileABytes, &tmap_w, kb * kBKElems, n_tile * kBN, full);
+                if (++stage == kSplitStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) {   // let the copies in flight land before the CTA may exit
+                const uint64_t t0 = globaltimer();
+                while (globaltimer() - t0 < 200000ull) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {   // MMA: the partial sum over this CTA's K blocks
+            uint32_t stage = 0, phase = 0;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait(smem_u32(&bar_full[stage]), phase)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a = ring + stage * kSplitStageBytes;
+                const uint32_t bb = a + kTileABytes;
+#pragma unroll
+                for (int k = 0; k < kBKBytes / 32; ++k)
+                    tc_mma1<FP8>(tmem, sw128_desc(a + 32u * k), sw128_desc(bb + 32u * k),
+                                 (kb > kb0) || (k != 0));
+                tc_commit1(smem_u32(&bar_empty[stage]));
+                if (++stage == kSplitStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            tc_commit1(smem_u32(&bar_tfull));
+            tc_commit1(smem_u32(&bar_drain));
+            if (!mbar_wait(smem_u32(&bar_drain), 0))
+                ok = false;
+        }
+        __syncwarp();
+    } else {
+        // the other CTAs export their partial sums, column-major, into the ring
+        const int quarter = warp & 3, hgroup = (warp - 2) >> 2;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const bool got = mbar_wait(smem_u32(&bar_tfull), 0);
+        if (!__all_sync(0xffffffffu, got))
+            ok = false;
+        tc_fence_after();
+        if (rank > 0 && ok) {
+#pragma unroll
+            for (int c0 = hgroup * (kBN / 2); c0 < (hgroup + 1) * (kBN / 2); c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + (uint32_t)c0, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                     ring + (uint32_t)(((c0 >> 2) + j) * 128 + row) * 16u),
+                                 "r"(r[4 * j]), "r"(r[4 * j + 1]), "r"(r[4 * j + 2]), "r"(r[4 * j + 3])
+                                 : "memory");
+            }
+        }
+    }
+    tc_fence_before();
+    cluster_sync();   // every CTA's partial sums are in place
+    if (rank == 0 && warp >= 2 && ok) {
+        const int quarter = warp & 3, hgroup = (warp - 2) >> 2;
+        const int row = quarter * 32 + lane;
+        tc_fence_after();
+        AccSrc src;
+        src.taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+        src.nsplit = S;
+        src.row = row;
+        src.part = ring;
+        epilogue_tile<D>(p, src, n_tile, row, row < p.num_tokens, hgroup, lane);
+    }
+    if (!ok && p.status)
+        atomicOr(p.status, MSA_STATUS_WAIT_TIMEOUT);
+    tc_fence_before();
+    cluster_sync();   // CTA 0 has read them
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kBN)
                      : "memory");
     }
 }
@@ -1036,6 +1317,8 @@ EncodeTiledFn g_encode = nullptr;
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
     int clusters[4] = {0, 0, 0, 0};  // resident clusters of two CTAs, per kernel variant
+    int split_clusters[4][9] = {};   // resident clusters of S one-SM CTAs (-1: none fits)
+    int sms = 0;
 };
 DeviceInfo g_dev[kMaxDevices];
 
@@ -1248,14 +1531,107 @@ extern "C" msa_status msa_projection_forward(
         p.inv_freq[k] = (float)(1.0 / std::pow((double)cfg->rope_theta,
                                                2.0 * (double)k / (double)cfg->rotary_dim));
 
+    // small batches with the register-resident epilogue: the K dimension split over
+    // a cluster (one CTA per SM), when that keeps more SMs busy
+    const int rdim = cfg->rotary_dim;
+    const bool fast_rope = cfg->rope_style == MSA_ROPE_NEOX && (rdim == D || rdim == D / 2 || rdim == 0);
+    int split = 1;
+    if (num_tokens <= kBM && fast_rope) {
+        int dev0 = 0, sms0 = 0;
+        if (cudaGetDevice(&dev0) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms0, cudaDevAttrMultiProcessorCount, dev0) != cudaSuccess)
+            return fail(MSA_ERR_CUDA, "device query failed");
+        split = sms0 / p.n_tiles;
+        split = split > 8 ? 8 : split;
+        split = split > p.num_k_blocks ? p.num_k_blocks : split;
+        split = split < 1 ? 1 : split;
+    }
+    p.split = split;
+    // weights that each launch reads from DRAM about once (few token tiles): fetched
+    // into L2 a number of K blocks ahead of the ring
+    p.prefetch = (split > 1 || p.m_tiles <= MSA_PROJ_PREFETCH_MTILES) ? MSA_PROJ_PREFETCH : 0;
+
     CUtensorMap mx, mw;
     if (!encode_map(&mx, hidden, num_tokens, hidden_size, hidden_row_stride, kBM, es) ||
-        !encode_map(&mw, weight, W, hidden_size, weight_row_stride, kHalfN, es))
+        !encode_map(&mw, weight, W, hidden_size, weight_row_stride, split > 1 ? kBN : kHalfN, es))
         return fail(MSA_ERR_CUDA, "tensor map encoding failed");
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return fail(MSA_ERR_CUDA, "cudaGetDevice failed");
+    if (split > 1) {
+        const void *sfns[4] = {reinterpret_cast<const void *>(&msa_projection_splitk_kernel<64, false>),
+                               reinterpret_cast<const void *>(&msa_projection_splitk_kernel<128, false>),
+                               reinterpret_cast<const void *>(&msa_projection_splitk_kernel<64, true>),
+                               reinterpret_cast<const void *>(&msa_projection_splitk_kernel<128, true>)};
+        const int si = (D == 128 ? 1 : 0) + (fp8 ? 2 : 0);
+        cudaLaunchConfig_t lc;
+        memset(&lc, 0, sizeof lc);
+        lc.blockDim = dim3(kThreads);
+        lc.dynamicSmemBytes = kSplitDynSmem;
+        lc.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)split;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        int fits;
+        {
+            std::lock_guard<std::mutex> lk(g_mu);
+            fits = g_dev[dev].split_clusters[si][split];
+            if (fits == 0) {
+                int major = 0;
+                if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+                    return fail(MSA_ERR_CUDA, "device query failed");
+                if (major != 10)
+                    return fail(MSA_ERR_UNSUPPORTED, "tcgen05 tensor cores need compute capability 10.x");
+                if (cudaFuncSetAttribute(sfns[si], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSplitDynSmem) != cudaSuccess)
+                    return fail(MSA_ERR_CUDA, "cudaFuncSetAttribute failed");
+                lc.gridDim = dim3((unsigned)split);
+                if (cudaOccupancyMaxActiveClusters(&fits, sfns[si], &lc) != cudaSuccess || fits <= 0) {
+                    (void)cudaGetLastError();
+                    fits = -1;
+                }
+                g_dev[dev].split_clusters[si][split] = fits;
+            }
+        }
+        if (fits < 0) {   // no cluster of this size fits: the 2-SM kernel below
+            split = 1;
+            p.split = 1;
+            if (!encode_map(&mw, weight, W, hidden_size, weight_row_stride, kHalfN, es))
+                return fail(MSA_ERR_CUDA, "tensor map encoding failed");
+        }
+    }
+    if (split > 1) {
+        const void *sfns[4] = {reinterpret_cast<const void *>(&msa_projection_splitk_kernel<64, false>),
+                               reinterpret_cast<const void *>(&msa_projection_splitk_kernel<128, false>),
+                               reinterpret_cast<const void *>(&msa_projection_splitk_kernel<64, true>),
+                               reinterpret_cast<const void *>(&msa_projection_splitk_kernel<128, true>)};
+        const int si = (D == 128 ? 1 : 0) + (fp8 ? 2 : 0);
+        cudaLaunchConfig_t lc;
+        memset(&lc, 0, sizeof lc);
+        lc.gridDim = dim3((unsigned)(p.n_tiles * split));
+        lc.blockDim = dim3(kThreads);
+        lc.dynamicSmemBytes = kSplitDynSmem;
+        lc.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)split;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        void *args[] = {&mx, &mw, &p};
+        if (cudaLaunchKernelExC(&lc, sfns[si], args) != cudaSuccess) {
+            const cudaError_t e = cudaGetLastError();
+            return fail(MSA_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+        }
+        msa_internal_set_detail("");
+        return MSA_OK;
+    }
     const void *fns[4] = {reinterpret_cast<const void *>(&msa_projection_kernel<64, false>),
                           reinterpret_cast<const void *>(&msa_projection_kernel<128, false>),
                           reinterpret_cast<const void *>(&msa_projection_kernel<64, true>),

@@ -285,6 +285,18 @@ def test_no_index_k_cache_and_odd_sections():
 
 
 @pytest.mark.parametrize("dt", OPERANDS, ids=OPERAND_IDS)
+@pytest.mark.parametrize("T,hidden", [(1, 330), (33, 192), (96, 448), (128, 600), (128, 2100)])
+def test_small_batches_split_over_k(T, hidden, dt):
+    """At most 128 tokens with NeoX RoPE: the K blocks are shared out over a cluster
+    of 2 to 8 CTAs whose partial sums one CTA adds up.  The hidden sizes give clusters
+    of every size from 2 to 8 (bf16: ceil(K/64) blocks; E4M3: ceil(K/128)), with a
+    ragged last block, and big heads in every output tile."""
+    pw = _batch(50 + T + hidden, dict(wl.BIG, num_q_heads=6), T, hidden, pad_frac=0.1,
+                hidden_pad=16, weight_pad=16, operand_dtype=dt)
+    check_projection(pw)
+
+
+@pytest.mark.parametrize("dt", OPERANDS, ids=OPERAND_IDS)
 def test_decode_batch_64_hidden_6144(dt):
     """The decode batch (64 tokens, big shapes, hidden 6,144): every output."""
     check_projection(wl.projection_decode(operand_dtype=dt))
