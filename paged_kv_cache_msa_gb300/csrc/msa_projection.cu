@@ -333,6 +333,15 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8])
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Where an epilogue thread's accumulator row lives: this CTA's tensor memory and,
 // with the K dimension split over a cluster, the partial sums the other CTAs of
 // the cluster left in their shared memory ([column / 4][128 rows][4 columns] fp32:
@@ -342,6 +351,8 @@ struct AccSrc {
     int nsplit;           // CTAs whose partial sums add up to the accumulator
     int row;              // this thread's row (tensor-memory lane)
     uint32_t part;        // shared-memory offset of the partial sums in every CTA
+    uint32_t table;       // this warp's lanes at the RoPE table (cos at +k, sin at +64+k),
+                          // when the kernel filled one during the main loop
 };
 
 // 32 accumulator columns [col, col + 32) of this thread's row: the own partial sum
@@ -611,7 +622,7 @@ __device__ __forceinline__ void rope_sincos(float a, float *s, float *c)
 // D/2 or 0).  The accumulator is read from tensor memory once and the bf16 row
 // is kept in registers; the head's norm weights and per-output scales are held by
 // the lanes of the warp (lane l: dims l, l + 32, ...) and shuffled to every lane.
-template <int D, int ROT>
+template <int D, int ROT, bool TABLE>
 __device__ __forceinline__ void head_fast(const Params &p, const Head &hd, const AccSrc &src,
                                           int tcol, int col,
                                           int64_t t, bool live, const Place &pl, int pos,
@@ -675,10 +686,21 @@ __device__ __forceinline__ void head_fast(const Params &p, const Head &hd, const
 #pragma unroll
     for (int k0 = 0; k0 < H; k0 += 8) {
         float yu[8], yv[8];
+        uint32_t ct[8], st[8];
+        if (TABLE) {   // filled by this row's threads while the main loop ran
+            tmem_ld8(src.table + (uint32_t)k0, ct);
+            tmem_ld8(src.table + 64u + (uint32_t)k0, st);
+            tmem_wait_ld();
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             float sn, cs;
-            rope_sincos((float)pos * p.inv_freq[k0 + j], &sn, &cs);
+            if (TABLE) {
+                cs = __uint_as_float(ct[j]);
+                sn = __uint_as_float(st[j]);
+            } else {
+                rope_sincos((float)pos * p.inv_freq[k0 + j], &sn, &cs);
+            }
             const float a = (elt(k0 + j) * rn) * wgt(k0 + j);
             const float b = (elt(k0 + H + j) * rn) * wgt(k0 + H + j);
             yu[j] = fmaf(-b, sn, a * cs);
@@ -700,7 +722,7 @@ __device__ __forceinline__ void head_fast(const Params &p, const Head &hd, const
 // taddr: tensor-memory address of this warp's lanes at the tile's first column.
 // The warp runs the producer on the tile's heads hh with hh % 2 == hgroup (the
 // other epilogue warp of the same tensor-memory lanes takes the rest).
-template <int D>
+template <int D, bool TABLE = false>
 __device__ __forceinline__ void epilogue_tile(const Params &p, const AccSrc &src, int n_tile,
                                               int64_t t, bool live, int hgroup, int lane)
 {
@@ -733,11 +755,11 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const AccSrc &src
                 continue;
             const int col = col0 + hh * D;
             if (rd == D)
-                head_fast<D, D>(p, hd, src, hh * D, col, t, live, pl, pos, rs, lane);
+                head_fast<D, D, TABLE>(p, hd, src, hh * D, col, t, live, pl, pos, rs, lane);
             else if (rd == D / 2)
-                head_fast<D, D / 2>(p, hd, src, hh * D, col, t, live, pl, pos, rs, lane);
+                head_fast<D, D / 2, TABLE>(p, hd, src, hh * D, col, t, live, pl, pos, rs, lane);
             else
-                head_fast<D, 0>(p, hd, src, hh * D, col, t, live, pl, pos, rs, lane);
+                head_fast<D, 0, TABLE>(p, hd, src, hh * D, col, t, live, pl, pos, rs, lane);
         }
         return;
     }
@@ -1066,6 +1088,7 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
             AccSrc src;
             src.taddr = tmem + lane_base + b * kBN;
             src.nsplit = 1;
+            src.table = 0;
             src.row = row;
             src.part = 0;
             epilogue_tile<D>(p, src, n, t, t < p.num_tokens, hgroup, lane);
@@ -1106,6 +1129,10 @@ constexpr uint32_t kSplitStageBytes = kTileABytes + 2 * kTileBBytes;  // 128 tok
 constexpr int kSplitDynSmem = kSplitStages * kSplitStageBytes + 1024;
 static_assert(kSplitStages * kSplitStageBytes >= 128u * kBN * 4u, "partial sums fit the ring");
 constexpr uint32_t kIdescShape1 = ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+// tensor memory: the accumulator in columns [0, 256), CTA 0's RoPE table (cos, sin of
+// up to 64 frequencies per row) in [256, 384); allocations are powers of two
+constexpr uint32_t kSplitTmemCols = 512;
+constexpr uint32_t kTableCol = kBN;
 
 template <bool FP8>
 __device__ __forceinline__ void tc_mma1(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc)
@@ -1175,7 +1202,7 @@ msa_projection_splitk_kernel(const __grid_constant__ CUtensorMap tmap_x,
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(&s_tmem)),
-                     "r"(kBN)
+                     "r"(kSplitTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -1246,6 +1273,26 @@ msa_projection_splitk_kernel(const __grid_constant__ CUtensorMap tmap_x,
         const int quarter = warp & 3, hgroup = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        if (rank == 0 && p.rotary_dim > 0) {
+            // While the main loop runs: this row's RoPE cos / sin, the two warps of a
+            // lane quarter taking half the frequencies each, into tensor memory for
+            // the epilogue (the same angle and evaluation it would make itself)
+            const int H = p.rotary_dim / 2;   // 16, 32 or 64: halves are whole blocks of 8
+            const int pos = row < p.num_tokens ? __ldg(p.positions + row) : 0;
+            for (int k0 = hgroup * (H / 2); k0 < (hgroup + 1) * (H / 2); k0 += 8) {
+                uint32_t ct[8], st[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float sn, cs;
+                    rope_sincos((float)pos * p.inv_freq[k0 + j], &sn, &cs);
+                    ct[j] = __float_as_uint(cs);
+                    st[j] = __float_as_uint(sn);
+                }
+                tmem_st8(tmem + lane_base + kTableCol + (uint32_t)k0, ct);
+                tmem_st8(tmem + lane_base + kTableCol + 64u + (uint32_t)k0, st);
+            }
+            tmem_wait_st();
+        }
         const bool got = mbar_wait(smem_u32(&bar_tfull), 0);
         if (!__all_sync(0xffffffffu, got))
             ok = false;
@@ -1276,7 +1323,8 @@ msa_projection_splitk_kernel(const __grid_constant__ CUtensorMap tmap_x,
         src.nsplit = S;
         src.row = row;
         src.part = ring;
-        epilogue_tile<D>(p, src, n_tile, row, row < p.num_tokens, hgroup, lane);
+        src.table = tmem + ((uint32_t)(quarter * 32) << 16) + kTableCol;
+        epilogue_tile<D, true>(p, src, n_tile, row, row < p.num_tokens, hgroup, lane);
     }
     if (!ok && p.status)
         atomicOr(p.status, MSA_STATUS_WAIT_TIMEOUT);
@@ -1284,7 +1332,8 @@ msa_projection_splitk_kernel(const __grid_constant__ CUtensorMap tmap_x,
     cluster_sync();   // CTA 0 has read them
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kBN)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kSplitTmemCols)
                      : "memory");
     }
 }
