@@ -1119,10 +1119,13 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
 // cluster of S CTAs takes one output tile and CTA s of it a contiguous S-th of the
 // K blocks, accumulating 128 tokens x 256 outputs in its own tensor memory with the
 // one-SM MMA (tcgen05.mma.cta_group::1, M 128, N 256).  The other CTAs then write
-// their partial sums, column-major, into their shared memory (the ring is free by
-// then) and CTA 0's epilogue adds them in rank order over distributed shared
-// memory before running the producer.  Used for NeoX RoPE over D, D/2 or no dims
-// (the register-resident epilogue); other layouts take the 2-SM kernel.
+// their partial sums into their shared memory (the ring is free by then) as
+// [column / 4][128 rows][4 columns] fp32, and CTA 0's epilogue adds them in rank
+// order over distributed shared memory before running the producer.  While the
+// main loop runs, CTA 0's epilogue warps fill a RoPE cos / sin table for their
+// rows in tensor memory (columns 256-383), which the epilogue reads back instead
+// of evaluating the angles after the main loop.  Used for NeoX RoPE over D, D/2
+// or no dims (the register-resident epilogue); other layouts take the 2-SM kernel.
 
 constexpr int kSplitStages = 4;
 constexpr uint32_t kSplitStageBytes = kTileABytes + 2 * kTileBBytes;  // 128 tokens + 256 weight rows
@@ -1269,7 +1272,8 @@ msa_projection_splitk_kernel(const __grid_constant__ CUtensorMap tmap_x,
         }
         __syncwarp();
     } else {
-        // the other CTAs export their partial sums, column-major, into the ring
+        // the other CTAs export their partial sums into the ring, four columns of a
+        // row per 16 bytes
         const int quarter = warp & 3, hgroup = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
