@@ -296,6 +296,18 @@ def test_small_batches_split_over_k(T, hidden, dt):
     check_projection(pw)
 
 
+@pytest.mark.parametrize("T", [40, 200])
+def test_large_positions(T):
+    """Positions in [2^16, 2^24): RoPE angles past 2^16 take the full-range sine and
+    cosine instead of the 2pi reduction.  40 tokens run the split-over-K kernel
+    (whose table is filled during the main loop), 200 the 2-SM kernel."""
+    pw = _batch(60 + T, dict(wl.BIG, num_q_heads=6), T, 384)
+    rng = np.random.default_rng(T)
+    # positions only enter RoPE; the slots were fixed when the batch was built
+    pw.producer.positions[:] = rng.integers(1 << 16, 1 << 24, size=T).astype(np.int32)
+    check_projection(pw)
+
+
 @pytest.mark.parametrize("dt", OPERANDS, ids=OPERAND_IDS)
 def test_decode_batch_64_hidden_6144(dt):
     """The decode batch (64 tokens, big shapes, hidden 6,144): every output."""
