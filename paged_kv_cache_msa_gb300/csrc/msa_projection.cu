@@ -47,8 +47,11 @@
 #include "msa_producer.h"
 #include "msa_projection.h"
 
+// K blocks of weight prefetched into L2 ahead of the ring at small batches (a build-time
+// knob; 0 = off).  Measured at decode 64 / 256 / 1,024 tokens: 8 and 16 blocks ahead were 0-5%
+// slower than none (the weight stream got no faster), so it is off.
 #ifndef MSA_PROJ_PREFETCH
-#define MSA_PROJ_PREFETCH 8          // K blocks of weight prefetched into L2 ahead of the ring
+#define MSA_PROJ_PREFETCH 0
 #endif
 #ifndef MSA_PROJ_PREFETCH_MTILES
 #define MSA_PROJ_PREFETCH_MTILES 4   // up to this many 256-token tiles
