@@ -236,6 +236,32 @@ WORKLOAD_DESC = {
 }
 
 
+def host_cpu() -> dict:
+    """The host the oracle runs on: its core count (the oracle itself uses one) and
+    CPU model, as lscpu or /proc/cpuinfo report them."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            k, _, v = line.partition(":")
+            if k.strip() in ("Model name", "Vendor ID") and v.strip() and model is None:
+                model = v.strip()
+            if k.strip() == "Model name" and v.strip():
+                model = v.strip()
+    except Exception:
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith(("model name", "cpu part")):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except Exception:
+            pass
+    return {"host_cores": os.cpu_count(), "cpu_model": model, "threads_used": 1}
+
+
 # ---------------------------------------------------------------------------
 # the reference arm: the CPU oracle
 # ---------------------------------------------------------------------------
@@ -265,7 +291,8 @@ def run_reference(args):
                    "parallelism": "replicas"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"{sample} consecutive tokens of the workload per step "
-                                   f"(cycling through it), single-threaded C oracle"},
+                                   f"(cycling through it), single-threaded C oracle",
+                         **host_cpu()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -307,6 +334,111 @@ def decode_step_timing(replays: int, big: bool, pdl: bool):
     return {"us_per_step": us_step, "us_per_layer": us_step / 60, "layers": 60,
             "tokens_per_layer": tokens, "launches_per_step": 60,
             "shapes": "big" if big else "tiny", "pdl": pdl, "replays": replays}
+
+
+def empty_graph_floor(nodes: int = 60, replays: int = 1000):
+    """The launch floor of a CUDA graph of ``nodes`` kernel nodes that do next to
+    nothing (a 4-byte fill each): microseconds per replay and per node."""
+    import torch
+    t = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(nodes):
+            t.fill_(1)
+    with torch.cuda.stream(s):
+        for _ in range(20):
+            g.replay()
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(replays):
+            g.replay()
+        e1.record(s)
+        e1.synchronize()
+    us = 1e3 * e0.elapsed_time(e1) / replays
+    return {"nodes": nodes, "us_per_graph": us, "us_per_node": us / nodes,
+            "what": "a graph of 4-byte fill kernels, the cost of a launch inside a graph"}
+
+
+def legacy_write_path_timing(replays: int = 200, layers: int = 60):
+    """The write path the fused producer replaces, as the pages describe it: per
+    cache a division kernel (page), a remainder kernel (in-page offset), an index
+    cast and an index_put scatter into the paged HND cache -- 12 launches per layer
+    for K, V and index-K -- in PyTorch eager ops on the GPU, ``layers`` layers of the
+    decode step (batch 256, tiny shapes, each layer its own caches, physical slots)
+    captured in one CUDA graph.  The values are taken as already encoded (fp8 K/V,
+    bf16 index-K); the fused producer's 60 launches do the norm, RoPE, compact Q /
+    index-Q and encoding as well."""
+    import torch
+    from paged_kv_cache_msa_gb300 import workloads as wl
+    dev = torch.device("cuda")
+    g_rng = torch.Generator(device=dev)
+    g_rng.manual_seed(11)
+    stack = []
+    for l in range(layers):
+        w = wl.config3_decode_step(l)
+        s_, T = w.shape, w.num_tokens
+        D, P = s_["head_dim"], s_["page_size"]
+        pt = w.page_table.reshape(-1).astype(np.int64)
+        # the physical slots the producer's table lookup gives (legacy callers pass these)
+        blk = w.slot_mapping // P
+        phys = np.where(w.slot_mapping >= 0, pt[np.clip(blk, 0, pt.size - 1)] * P + w.slot_mapping % P, -1)
+        assert (phys >= 0).all(), "the decode-step workload has no padded slots"
+        caches = []
+        for key in ("k", "v", "idx_k"):
+            c = w.caches[key]
+            es = c.elem_size()
+            dt = torch.uint8 if es == 1 else torch.int16
+            pool = torch.zeros(c.num_pages * c.num_heads * P * D, dtype=dt, device=dev)
+            view = pool.view(c.num_pages, c.num_heads, P, D).permute(0, 2, 1, 3)   # [pages, P, H, D]
+            vals = torch.randint(0, 120, (T, c.num_heads, D), generator=g_rng, device=dev).to(dt)
+            caches.append((view, vals))
+        stack.append((torch.from_numpy(phys.astype(np.int32)).to(dev), P, caches))
+
+    def layer(slot32, P, caches):
+        for view, vals in caches:
+            page = torch.div(slot32, P, rounding_mode="floor")      # division
+            off = torch.remainder(slot32, P)                         # remainder
+            page64 = page.long()                                     # index cast
+            view.index_put_((page64, off), vals)                     # scatter
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for item in stack:
+            layer(*item)
+        s.synchronize()
+        kernels = None
+        try:
+            from torch.profiler import ProfilerActivity, profile
+            with profile(activities=[ProfilerActivity.CUDA]) as prof:
+                layer(*stack[0])
+                s.synchronize()
+            kernels = sum(1 for e in prof.events() if e.device_type.name == "CUDA"
+                          and not e.name.startswith("Memcpy") and not e.name.startswith("Memset"))
+        except Exception as e:   # the profiler is context only
+            log(f"[bench] kernel count unavailable: {type(e).__name__}: {e}"[:160])
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for item in stack:
+                layer(*item)
+        for _ in range(10):
+            g.replay()
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(replays):
+            g.replay()
+        e1.record(s)
+        e1.synchronize()
+    us = 1e3 * e0.elapsed_time(e1) / replays
+    del g, stack
+    torch.cuda.empty_cache()
+    return {"workload": f"decode step, {layers} layers x 256 tokens, tiny shapes: the legacy write "
+                        f"path (per cache: division, remainder, index cast, index_put) in eager "
+                        f"PyTorch ops, one CUDA graph",
+            "us_per_step": us, "us_per_layer": us / layers,
+            "launches_per_layer_measured": kernels, "launches_per_step_designed": 12 * layers}
 
 
 def graph_launch_us(dw, flags, launches: int, replays: int) -> float:
@@ -698,7 +830,9 @@ def run_ours(args):
     if not args.no_decode_step:
         decode = {"tiny": decode_step_timing(1000, big=False, pdl=True),
                   "tiny_no_pdl": decode_step_timing(1000, big=False, pdl=False),
-                  "big": decode_step_timing(200, big=True, pdl=True)}
+                  "big": decode_step_timing(200, big=True, pdl=True),
+                  "empty_graph_floor": empty_graph_floor(60),
+                  "legacy_write_path": legacy_write_path_timing()}
 
     indexer = None
     if not args.no_decode_step:
@@ -717,7 +851,8 @@ def run_ours(args):
         n, dt = OracleRunner(w).timed(budget_s=args.cpu_budget)
         cpu = {"value": n / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"first {n} of {w.num_tokens} tokens of the same workload "
-                         f"({dt:.1f}s, single-threaded C oracle on the host)"}
+                         f"({dt:.1f}s, single-threaded C oracle on the host)",
+               **host_cpu()}
 
     if rank != 0:
         return 0
@@ -731,24 +866,50 @@ def run_ours(args):
                    "global_batch": w.num_tokens * world, "launch": f"persistent grid {grid}x{block}",
                    "l2": "inputs larger than L2 (1.49 GB of rows per step), no flush",
                    "parallelism": f"replicas x{world}"},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        # the large per-leg records first; the headline figures at the end of the line
+        "projection": projection,
+        "indexer": indexer,
+        "decode_step_detail": decode,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "us_per_launch": kernel_avg_ms * 1e3,
+        "us_per_launch_in_graph": us_graph,
         "hbm_gbs": achieved, "hbm_frac_of_peak": achieved / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "kernel_avg_us": kernel_avg_ms * 1e3},
-        "us_per_launch": kernel_avg_ms * 1e3,
-        "us_per_launch_in_graph": us_graph,
-        "gpu_launches": args.steps,
-        "clocks": clk,
-        "e2e": e2e,
-        "decode_step": decode,
-        "indexer": indexer,
-        "projection": projection,
-        "cpu_baseline": cpu,
+        "decode_step": decode_summary(decode),
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def decode_summary(decode):
+    """The decode-step figures in a few numbers (the full records are in
+    decode_step_detail)."""
+    if not decode:
+        return None
+    t = decode["tiny"]
+    out = {"workload": "60 layers x 256 tokens, tiny shapes, one CUDA graph, PDL",
+           "us_per_layer": t["us_per_layer"], "us_per_step": t["us_per_step"],
+           "launches_per_step": t["launches_per_step"],
+           "us_per_layer_no_pdl": decode["tiny_no_pdl"]["us_per_layer"],
+           "us_per_layer_big_shapes": decode["big"]["us_per_layer"]}
+    f = decode.get("empty_graph_floor")
+    if f:
+        out["empty_graph_us_per_node"] = f["us_per_node"]
+    lw = decode.get("legacy_write_path")
+    if lw:
+        out["legacy_write_path_us_per_step"] = lw["us_per_step"]
+        out["legacy_write_path_launches_per_layer"] = lw["launches_per_layer_measured"]
+    li = decode.get("layer_with_indexer")
+    if li:
+        out["layer_with_indexer_us_per_layer"] = li["pdl"]["us_per_layer"]
+    return out
 
 
 def run_e2e(dw, w, flags, steps, warmup, world, chunk_tokens=8192):
@@ -784,6 +945,7 @@ def run_e2e(dw, w, flags, steps, warmup, world, chunk_tokens=8192):
 
     ms_zero = timed(pipe.run_zero_copy)
     ms_copy = timed(pipe.run)
+    link = pinned_copy_bandwidth(h_qkv, h_q, dw.qkv.device)
     return {"value": w.num_tokens * steps * world / (ms_zero / 1e3), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": ms_zero / steps,
@@ -792,7 +954,40 @@ def run_e2e(dw, w, flags, steps, warmup, world, chunk_tokens=8192):
             "copy_pipeline": {"value": w.num_tokens * steps * world / (ms_copy / 1e3),
                               "ms_per_step": ms_copy / steps,
                               "chunk_tokens": min(chunk_tokens, w.num_tokens),
-                              "api": "HostPipeline.run: chunked cudaMemcpyAsync in, kernel, out"}}
+                              "api": "HostPipeline.run: chunked cudaMemcpyAsync in, kernel, out"},
+            "link": link,
+            "frac_of_copy_link": ((h2d + d2h) / (ms_zero / steps * 1e-3) / 1e9) / link["gbs_both_ways_serial"]}
+
+
+def pinned_copy_bandwidth(h_in, h_out, device, reps: int = 5):
+    """Plain cudaMemcpyAsync of the step's input bytes host -> device and output
+    bytes device -> host (pinned host memory, one copy each, CUDA events): the
+    CPU-GPU link's throughput for exactly the end-to-end step's traffic."""
+    import torch
+    d_in = torch.empty(h_in.shape, dtype=h_in.dtype, device=device)
+    d_out = torch.empty(h_out.shape, dtype=h_out.dtype, device=device)
+    s = torch.cuda.Stream(device=device)
+
+    def timed(fn):
+        with torch.cuda.stream(s):
+            fn()
+            s.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(reps):
+                fn()
+            e1.record(s)
+            e1.synchronize()
+        return e0.elapsed_time(e1) / reps
+    ms_h2d = timed(lambda: d_in.copy_(h_in, non_blocking=True))
+    ms_d2h = timed(lambda: h_out.copy_(d_out, non_blocking=True))
+    b_in = h_in.numel() * h_in.element_size()
+    b_out = h_out.numel() * h_out.element_size()
+    del d_in, d_out
+    return {"h2d_gbs": b_in / (ms_h2d * 1e-3) / 1e9, "d2h_gbs": b_out / (ms_d2h * 1e-3) / 1e9,
+            "h2d_bytes": b_in, "d2h_bytes": b_out,
+            "gbs_both_ways_serial": (b_in + b_out) / ((ms_h2d + ms_d2h) * 1e-3) / 1e9,
+            "what": "one pinned cudaMemcpyAsync each way of the rows in and compact Q out"}
 
 
 def main():

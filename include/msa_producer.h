@@ -78,12 +78,18 @@ typedef enum { MSA_SCALE_PER_TENSOR = 0, MSA_SCALE_PER_HEAD = 1 } msa_scale_mode
 #define MSA_LAUNCH_PERSISTENT 1   /* grid of at most (SMs x resident CTAs) CTAs that
                                      stride over the tokens; otherwise one CTA per token */
 #define MSA_LAUNCH_PDL 2          /* programmatic dependent launch: the kernel may start
-                                     while the previous kernel in the stream finishes.  It
-                                     waits for that kernel before reading qkv and before
-                                     any write; it reads the norm weights, positions, slot
-                                     mapping and page table before waiting, so the kernel
-                                     launched just before it must not write those (stage
-                                     them earlier in the step). */
+                                     while the kernel enqueued just before it on the stream
+                                     (call it P) is still running.  It reads qkv and writes
+                                     anything only after waiting for P; it reads the norm
+                                     weights, positions, slot mapping and page table before
+                                     that wait, so P must not write those.  Every kernel of
+                                     this library lets its dependents start only after its
+                                     own wait, so when P is one of them, or any kernel that
+                                     does the same or was launched without this attribute,
+                                     all kernels enqueued before P have completed by then
+                                     and may write those arrays (stage them earlier in the
+                                     step).  A P that lets its dependents start before its
+                                     own wait extends the rule to the kernels before it. */
 #define MSA_LAUNCH_QUERY_RUNS 4   /* msa_indexer_forward only: the queries come in runs of
                                      one sequence (consecutive queries with the same
                                      table_offset, as in a prefill chunk), so tiles of 8
@@ -244,8 +250,9 @@ typedef struct {
  *                and page_table before waiting for the kernel launched just before it
  *                on the stream (which must therefore not write them); idx_q, the
  *                cache, k_scale and the outputs are touched only after the wait (the
- *                query-run kernel waits before reading anything).  The top-k kernel
- *                lets the next kernel on the stream start likewise.
+ *                query-run kernel waits before reading anything).  Each of the two
+ *                kernels lets the next kernel on the stream start only after its own
+ *                wait (see MSA_LAUNCH_PDL).
  *                MSA_LAUNCH_QUERY_RUNS: see its definition.
  * Errors as for msa_producer_forward; num_queries == 0 launches nothing.
  */

@@ -16,7 +16,7 @@
  *     row[t, j] = bf16_rne( (sum_k hidden[t, k] * weight[j, k]) * sx[t] * sw[j] )
  *
  * with the operands bf16, or FP8 E4M3 with dequantisation scales sx (per token)
- * and sw (per output) -- the pages' "one quantized ... projection"; the sum is
+ * and sw (per output) -- the pages' projection is a quantised one; the sum is
  * accumulated in fp32 on the tensor cores and scaled as (sum * sx[t]) * sw[j] in
  * fp32 -- then exactly what msa_producer_forward
  * does to a row it reads (see msa_producer.h): the same configuration, placement,

@@ -466,8 +466,8 @@ int oracle_indexer(int32_t num_heads, int32_t head_dim, int32_t page_size, int32
 /*
  * The wide projection that feeds the producer ("[None][perf] Fuse MiniMax-M3 QKV
  * and index projection", Description, AFTER diagram: hidden states -> one wider
- * fused GEMM [Q | K | V | index-Q | index-K] -> one fused producer; the change
- * "packs Q, K, V, index-Q, and index-K into one quantized ... projection").
+ * fused GEMM [Q | K | V | index-Q | index-K] -> one fused producer; the five
+ * outputs come from a single quantised projection there).
  *
  *   rows[t, j] = bf16(fp32(hidden_scale[t] * weight_scale[j] *
  *                          sum_k x[t, k] * w[j, k]))            for j < width

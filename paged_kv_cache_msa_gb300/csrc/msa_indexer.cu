@@ -685,10 +685,11 @@ __global__ void __launch_bounds__(kTopkThreads) msa_index_topk_kernel(const __gr
     const int64_t t = blockIdx.x;
     const int n = p.max_blocks;
     int32_t *out = p.topk_ids + t * p.topk;
-    // the next kernel may start its own prologue now; it still waits for this grid
-    // to complete before it reads what this grid writes
-    asm volatile("griddepcontrol.launch_dependents;" :::);
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // The next kernel may start its prologue once this grid has waited: every kernel
+    // before this one has completed by then (see the producer's kernel for why the
+    // signal comes after the wait).
+    asm volatile("griddepcontrol.launch_dependents;" :::);
     const float *row = p.block_scores + t * n;
 
     if (n <= kRankMaxBlocks) {

@@ -5,24 +5,31 @@
 // applies to a row; only where the row comes from differs: here it is the fp32
 // accumulator of a 128-token x 256-output tile in tensor memory, rounded to bf16.
 //
-// Kernel structure: persistent clusters of two CTAs (one per SM), 192 threads each.
-// A cluster computes 256-token x 256-output tiles with the 2-SM MMA: CTA r of the
-// pair holds tokens [128r, 128r + 128) of the tile and weight rows [128r, 128r +
-// 128) of its outputs, and its tensor memory receives the accumulator of its own
-// 128 tokens over all 256 outputs.  Per CTA:
-//   warp 0      TMA producer: 64-element K blocks of its hidden rows and weight
-//               rows into a 7-stage shared-memory ring (128-byte swizzle,
-//               K-major); the copies of both CTAs complete on the leader's barrier
+// Kernel structure: persistent clusters of two CTAs (one per SM), 320 threads
+// each (kThreads = 64 + 32 x 8).  A cluster computes 256-token x 256-output tiles
+// with the 2-SM MMA: CTA r of the pair holds tokens [128r, 128r + 128) of the tile
+// and weight rows [128r, 128r + 128) of its outputs, and its tensor memory
+// receives the accumulator of its own 128 tokens over all 256 outputs.  Per CTA:
+//   warp 0      TMA producer: 128-byte K blocks (64 bf16 or 128 E4M3 elements) of
+//               its hidden rows and weight rows into a 7-stage shared-memory ring
+//               (128-byte swizzle, K-major); the copies of both CTAs complete on
+//               the leader's barrier
 //   warp 1      tensor-memory owner; in the leader CTA (rank 0) one thread issues
-//               tcgen05.mma.cta_group::2 kind::f16 (M 256, N 256, K 16) into one of
-//               two accumulators (2 x 256 columns), so that the epilogue of a tile
-//               overlaps the main loop of the next, and commits to both CTAs
-//   warps 2..5  epilogue: thread r of the four warps owns token row r of its CTA's
-//               half of the tile (tensor-memory lane r) and runs the producer on
-//               the tile's heads
-// Per SM a K block moves 32 KB through shared memory for 128 x 256 x 64 MACs
+//               tcgen05.mma.cta_group::2 (kind::f16 for bf16, kind::f8f6f4 for
+//               E4M3; M 256, N 256) into one of two accumulators (2 x 256 columns),
+//               so that the epilogue of a tile overlaps the main loop of the next,
+//               and commits to both CTAs
+//   warps 2..9  epilogue: warp w reads tensor-memory lane quarter w & 3 (thread
+//               r of it owns token row r of its CTA's half of the tile) and takes
+//               the head group (w - 2) >> 2, so the two warps of a lane quarter
+//               split the tile's heads between them; each runs the producer on
+//               its heads
+// Per SM a K block moves 32 KB through shared memory for 128 x 256 x 64 bf16 MACs
 // (half of what a one-SM 128 x 256 tile needs), which is what lets 7 stages --
 // about 2 us of loads -- be in flight.
+//
+// At most 128 tokens the K dimension is split over a cluster of up to 8 CTAs
+// instead (msa_projection_splitk_kernel, section "small batches" below).
 //
 // Tiles are visited output-group-major: for each group of n_group 256-wide output
 // tiles, every 256-token tile in order, so that the group's weight panels stay in
@@ -1349,6 +1356,62 @@ msa_projection_splitk_kernel(const __grid_constant__ CUtensorMap tmap_x,
 // host side
 // ---------------------------------------------------------------------------
 
+// ---------------------------------------------------------------------------
+// build units
+// ---------------------------------------------------------------------------
+// The eight kernel instantiations below take minutes to compile in one unit, so
+// the build may compile this file several times with MSA_PROJ_UNIT set: unit 0
+// holds the host code alone, unit k = 1..8 the k-th kernel alone (returned by
+// msa_internal_projection_kernel_<k>), and the units compile in parallel.
+// Without MSA_PROJ_UNIT everything is in one unit (the checked build, whose
+// device-side violation counter must live in one module).
+#if defined(MSA_PROJ_UNIT) && defined(MSA_CHECKED)
+#error "the checked build compiles the projection as one unit"
+#endif
+#if !defined(MSA_PROJ_UNIT)
+#define MSA_PROJ_HOST 1
+#elif MSA_PROJ_UNIT == 0
+#define MSA_PROJ_HOST 1
+#else
+#define MSA_PROJ_HOST 0
+#endif
+
+#if MSA_PROJ_HOST
+#if defined(MSA_PROJ_UNIT)
+}  // namespace
+const void *msa_internal_projection_kernel_1();
+const void *msa_internal_projection_kernel_2();
+const void *msa_internal_projection_kernel_3();
+const void *msa_internal_projection_kernel_4();
+const void *msa_internal_projection_kernel_5();
+const void *msa_internal_projection_kernel_6();
+const void *msa_internal_projection_kernel_7();
+const void *msa_internal_projection_kernel_8();
+namespace {
+#endif
+
+// Host address of a kernel: split over K or not; variant v = (D == 128) + 2 * FP8.
+const void *projection_kernel(bool splitk, int v)
+{
+#if defined(MSA_PROJ_UNIT)
+    static const void *(*const get[8])() = {
+        msa_internal_projection_kernel_1, msa_internal_projection_kernel_2,
+        msa_internal_projection_kernel_3, msa_internal_projection_kernel_4,
+        msa_internal_projection_kernel_5, msa_internal_projection_kernel_6,
+        msa_internal_projection_kernel_7, msa_internal_projection_kernel_8};
+    return get[(splitk ? 4 : 0) + v]();
+#else
+    const void *k[8] = {reinterpret_cast<const void *>(&msa_projection_kernel<64, false>),
+                        reinterpret_cast<const void *>(&msa_projection_kernel<128, false>),
+                        reinterpret_cast<const void *>(&msa_projection_kernel<64, true>),
+                        reinterpret_cast<const void *>(&msa_projection_kernel<128, true>),
+                        reinterpret_cast<const void *>(&msa_projection_splitk_kernel<64, false>),
+                        reinterpret_cast<const void *>(&msa_projection_splitk_kernel<128, false>),
+                        reinterpret_cast<const void *>(&msa_projection_splitk_kernel<64, true>),
+                        reinterpret_cast<const void *>(&msa_projection_splitk_kernel<128, true>)};
+    return k[(splitk ? 4 : 0) + v];
+#endif
+}
 msa_status fail(msa_status s, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
 msa_status fail(msa_status s, const char *fmt, ...)
 {
@@ -1616,10 +1679,8 @@ extern "C" msa_status msa_projection_forward(
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return fail(MSA_ERR_CUDA, "cudaGetDevice failed");
     if (split > 1) {
-        const void *sfns[4] = {reinterpret_cast<const void *>(&msa_projection_splitk_kernel<64, false>),
-                               reinterpret_cast<const void *>(&msa_projection_splitk_kernel<128, false>),
-                               reinterpret_cast<const void *>(&msa_projection_splitk_kernel<64, true>),
-                               reinterpret_cast<const void *>(&msa_projection_splitk_kernel<128, true>)};
+        const void *sfns[4] = {projection_kernel(true, 0), projection_kernel(true, 1),
+                               projection_kernel(true, 2), projection_kernel(true, 3)};
         const int si = (D == 128 ? 1 : 0) + (fp8 ? 2 : 0);
         cudaLaunchConfig_t lc;
         memset(&lc, 0, sizeof lc);
@@ -1662,10 +1723,8 @@ extern "C" msa_status msa_projection_forward(
         }
     }
     if (split > 1) {
-        const void *sfns[4] = {reinterpret_cast<const void *>(&msa_projection_splitk_kernel<64, false>),
-                               reinterpret_cast<const void *>(&msa_projection_splitk_kernel<128, false>),
-                               reinterpret_cast<const void *>(&msa_projection_splitk_kernel<64, true>),
-                               reinterpret_cast<const void *>(&msa_projection_splitk_kernel<128, true>)};
+        const void *sfns[4] = {projection_kernel(true, 0), projection_kernel(true, 1),
+                               projection_kernel(true, 2), projection_kernel(true, 3)};
         const int si = (D == 128 ? 1 : 0) + (fp8 ? 2 : 0);
         cudaLaunchConfig_t lc;
         memset(&lc, 0, sizeof lc);
@@ -1688,10 +1747,8 @@ extern "C" msa_status msa_projection_forward(
         msa_internal_set_detail("");
         return MSA_OK;
     }
-    const void *fns[4] = {reinterpret_cast<const void *>(&msa_projection_kernel<64, false>),
-                          reinterpret_cast<const void *>(&msa_projection_kernel<128, false>),
-                          reinterpret_cast<const void *>(&msa_projection_kernel<64, true>),
-                          reinterpret_cast<const void *>(&msa_projection_kernel<128, true>)};
+    const void *fns[4] = {projection_kernel(false, 0), projection_kernel(false, 1),
+                          projection_kernel(false, 2), projection_kernel(false, 3)};
     const int vi = (D == 128 ? 1 : 0) + (fp8 ? 2 : 0);
     const void *fn = fns[vi];
     cudaLaunchConfig_t lc;
@@ -1757,3 +1814,27 @@ msa_status msa_internal_projection_violations(uint64_t *count, int32_t reset)
 #endif
     return MSA_OK;
 }
+
+#else
+}  // namespace
+#endif  // MSA_PROJ_HOST
+
+#if defined(MSA_PROJ_UNIT) && MSA_PROJ_UNIT > 0
+#if MSA_PROJ_UNIT == 1
+const void *msa_internal_projection_kernel_1() { return reinterpret_cast<const void *>(&msa_projection_kernel<64, false>); }
+#elif MSA_PROJ_UNIT == 2
+const void *msa_internal_projection_kernel_2() { return reinterpret_cast<const void *>(&msa_projection_kernel<128, false>); }
+#elif MSA_PROJ_UNIT == 3
+const void *msa_internal_projection_kernel_3() { return reinterpret_cast<const void *>(&msa_projection_kernel<64, true>); }
+#elif MSA_PROJ_UNIT == 4
+const void *msa_internal_projection_kernel_4() { return reinterpret_cast<const void *>(&msa_projection_kernel<128, true>); }
+#elif MSA_PROJ_UNIT == 5
+const void *msa_internal_projection_kernel_5() { return reinterpret_cast<const void *>(&msa_projection_splitk_kernel<64, false>); }
+#elif MSA_PROJ_UNIT == 6
+const void *msa_internal_projection_kernel_6() { return reinterpret_cast<const void *>(&msa_projection_splitk_kernel<128, false>); }
+#elif MSA_PROJ_UNIT == 7
+const void *msa_internal_projection_kernel_7() { return reinterpret_cast<const void *>(&msa_projection_splitk_kernel<64, true>); }
+#elif MSA_PROJ_UNIT == 8
+const void *msa_internal_projection_kernel_8() { return reinterpret_cast<const void *>(&msa_projection_splitk_kernel<128, true>); }
+#endif
+#endif

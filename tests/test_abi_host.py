@@ -352,3 +352,27 @@ def test_projection_malformed_call_is_rejected(lib, over, status):
     a = good_projection(**over)
     assert B.msa_projection_validate(**a) == status, B.last_error_detail()
     assert B.msa_projection_forward(**a, stream=0, check=False) == status
+
+
+def test_build_reuse_is_keyed_on_source_content(tmp_path):
+    """A library on disk is reused only when the digest of its sources, build
+    script, command line and defines matches the one recorded beside it; any
+    change of a source byte or a define makes build() compile again."""
+    build_mod.build()
+    d0 = build_mod.source_digest(())
+    assert build_mod.up_to_date(())
+    assert build_mod.source_digest(("MSA_STAGES=3",)) != d0
+    assert not build_mod.up_to_date(("MSA_STAGES=3",))
+    # a copy of the sources with one byte changed hashes differently
+    src = build_mod.SOURCES[0]
+    saved = list(build_mod.DEPENDENCIES)
+    changed = tmp_path / os.path.basename(src)
+    with open(src, "rb") as f:
+        data = f.read()
+    changed.write_bytes(data + b"\n")
+    try:
+        build_mod.DEPENDENCIES[build_mod.DEPENDENCIES.index(src)] = str(changed)
+        assert build_mod.source_digest(()) != d0
+    finally:
+        build_mod.DEPENDENCIES[:] = saved
+    assert build_mod.source_digest(()) == d0

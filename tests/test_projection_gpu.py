@@ -14,6 +14,12 @@ widened, element by element, by the change the row bound can cause through the
 norm factor, the weight and the RoPE partner; at least 99% of all values must meet
 the unwidened tolerance.  The written cache bytes are checked exactly (two
 sentinel runs).
+
+The epilogue's own producer arithmetic is pinned separately and strictly: the
+oracle producer run on the bf16 rows the kernel itself wrote (rows_out, the values
+the epilogue normalises, rotates and encodes) must match every compact Q / index-Q
+value within 2e-2 + 1e-2*|ref| and every fp8 code within one E4M3 step, with no
+widening and no allowance (``check_epilogue_strict``).
 """
 import numpy as np
 import pytest
@@ -21,7 +27,7 @@ import torch
 
 import oracle
 from gpu_harness import SENTINEL_XOR, check_against_oracle, oracle_written_mask
-from harness import BF16_ATOL, BF16_RTOL, cache_cells, e4m3_ulp_distance, run_oracle
+from harness import BF16_ATOL, BF16_RTOL, cache_cells, compare_bf16, e4m3_ulp_distance, run_oracle
 from paged_kv_cache_msa_gb300 import binding as B
 from paged_kv_cache_msa_gb300 import workloads as wl
 from paged_kv_cache_msa_gb300.device import DeviceProjection
@@ -56,11 +62,14 @@ def _exact_and_acc(pw: wl.ProjectionWorkload, idx):
     return exact, acc
 
 
-def check_rows(got: np.ndarray, pw: wl.ProjectionWorkload, rows: np.ndarray):
-    """The kernel's bf16 rows against the oracle's: at least 99% identical, and
+def check_rows(got: np.ndarray, pw: wl.ProjectionWorkload, rows, idx=None):
+    """The kernel's bf16 rows (of the tokens ``idx``, all by default) against the
+    exact scaled dot products (float64 library matmul of the decoded operands):
     every one within the error of an fp32 accumulation of K products,
-    K * 2^-24 * sum_k |x_k w_k|, plus one bf16 step of the exact value."""
-    exact, acc = _exact_and_acc(pw, np.arange(pw.num_tokens))
+    K * 2^-24 * sum_k |x_k w_k|, plus one bf16 step of the exact value; and, when
+    the oracle's rows are given, at least 99% identical to them."""
+    idx = np.arange(pw.num_tokens) if idx is None else idx
+    exact, acc = _exact_and_acc(pw, idx)
     a = np.abs(exact)
     step = np.where(a > 0, np.exp2(np.floor(np.log2(np.maximum(a, 1e-300))) - 7), 0.0)
     bound = step + acc
@@ -68,7 +77,8 @@ def check_rows(got: np.ndarray, pw: wl.ProjectionWorkload, rows: np.ndarray):
     bad = err > bound
     assert not bad.any(), (f"projection rows: {int(bad.sum())} beyond the fp32 accumulation bound; "
                            f"first at {np.argwhere(bad)[:3].tolist()}")
-    assert (got == rows).mean() > 0.99, "projection rows: more than 1% not exactly rounded"
+    if rows is not None:
+        assert (got == rows).mean() > 0.99, "projection rows: more than 1% not exactly rounded"
 
 
 def oracle_rows(pw: wl.ProjectionWorkload, idx=None) -> np.ndarray:
@@ -204,6 +214,66 @@ def check_values(pw, idx, rows, q_o, iq_o, pools_o, dp):
     assert strict_ok >= 0.99 * total, f"only {strict_ok} of {total} within the producer's tolerance"
 
 
+def _sub_workload(w_p: wl.Workload, idx, rows: np.ndarray, tag: str) -> wl.Workload:
+    """The producer workload restricted to the tokens ``idx`` with the given rows."""
+    meta = dict(w_p.meta)
+    if "valid_mask" in meta:
+        meta["valid_mask"] = meta["valid_mask"][idx]
+    return wl.Workload(w_p.name + tag, w_p.shape, np.ascontiguousarray(rows), rows.shape[1],
+                       w_p.positions[idx].copy(), w_p.slot_mapping[idx].copy(), w_p.page_table,
+                       w_p.weights, w_p.scales, w_p.caches, w_p.pools, w_p.seed, meta)
+
+
+def check_epilogue_strict(pw: wl.ProjectionWorkload, dp: DeviceProjection, idx=None):
+    """The epilogue's producer arithmetic alone, at the producer's own tolerance.
+
+    ``dp`` ran on cache pools filled with the workload's sentinel pattern A and wrote
+    its bf16 rows (rows_out).  The oracle producer runs on exactly those rows for the
+    tokens ``idx`` (all by default); every compact Q / index-Q value of those tokens
+    must lie within 2e-2 + 1e-2*|ref|, every fp8 cache code within one E4M3 step and
+    every bf16 cache value within the Q tolerance -- no widening, no allowance."""
+    w_p = pw.producer
+    T = pw.num_tokens
+    idx = np.arange(T) if idx is None else np.asarray(idx, dtype=np.int64)
+    dev = dp.device
+    it = torch.from_numpy(idx).to(dev)
+    rows_k = dp.rows_out.index_select(0, it).cpu().numpy().view(np.uint16)
+    sub = _sub_workload(w_p, idx, rows_k, "[kernel rows]")
+    q_o, iq_o, pools_o = run_oracle(sub, pools=wl.host_pools(w_p))
+    q_d = dp.dw.q_out.index_select(0, it).cpu().numpy().view(np.uint16)
+    iq_d = dp.dw.idx_q_out.index_select(0, it).cpu().numpy().view(np.uint16)
+    compare_bf16(q_d, q_o, "q_out from the kernel's rows")
+    compare_bf16(iq_d, iq_o, "idx_q_out from the kernel's rows")
+    P = w_p.shape["page_size"]
+    pt = None if w_p.page_table is None else w_p.page_table.reshape(-1)
+    for key in ("k", "v", "idx_k"):
+        c = w_p.caches.get(key)
+        if c is None or c.num_heads == 0:
+            continue
+        pl = [oracle.place(int(ls), P, pt, c.num_pages) for ls in sub.slot_mapping]
+        if not any(x is not None for x in pl):
+            continue
+        cells = cache_cells(w_p, key, pl).reshape(-1)
+        got = dp.pools[c.pool].index_select(0, torch.from_numpy(cells).to(dev)).cpu().numpy()
+        exp = pools_o[c.pool][cells]
+        if c.dtype == wl.DTYPE_E4M3:
+            d = e4m3_ulp_distance(got, exp)
+            assert d.max(initial=0) <= 1, (f"{key} cache from the kernel's rows: "
+                                           f"{int((d > 1).sum())} codes more than one E4M3 step off")
+        else:
+            compare_bf16(got.view(np.uint16), exp.view(np.uint16), f"{key} cache from the kernel's rows")
+
+
+def tile_samples(T: int, seed: int, tile: int = 128) -> np.ndarray:
+    """At least one token of every ``tile``-token tile (a random one), plus the first
+    and last two tokens of the batch and of the first and last tiles."""
+    rng = np.random.default_rng(seed)
+    starts = np.arange(0, T, tile)
+    pick = starts + rng.integers(0, tile, size=starts.shape[0])
+    edges = [0, 1, tile - 1, tile, tile + 1, T - tile - 1, T - tile, T - 2, T - 1]
+    return np.unique(np.clip(np.concatenate([pick, edges]), 0, T - 1))
+
+
 def check_projection(pw: wl.ProjectionWorkload):
     rows = oracle_rows(pw)
     w_rows = pw.with_rows(rows)
@@ -223,6 +293,7 @@ def check_projection(pw: wl.ProjectionWorkload):
                               device_run=device_run, check_cache_values=False)
     assert statuses == [0, 0]
     check_values(pw, np.arange(pw.num_tokens), rows, q_o, iq_o, pools_o, dp)
+    check_epilogue_strict(pw, dp)
 
 
 def _batch(seed, heads, T, hidden, **kw):
@@ -350,13 +421,17 @@ def test_graph_replay_matches_direct_launch():
 def test_prefill_65536_tokens_hidden_6144_sampled(dt):
     """The full-size prefill (65,536 tokens, hidden 6,144, 11,392 outputs): the
     written cache bytes exactly against the oracle's placement of every token
-    (two sentinel runs), and sampled tokens (tile edges, first and last tokens,
-    random ones) element by element against the oracle."""
+    (two sentinel runs), and sampled tokens -- a random one from every 128-token
+    tile, the first and last tokens and tile edges -- element by element against
+    the oracle, end to end and (on the kernel's own rows) strictly."""
     pw = wl.projection_prefill(operand_dtype=dt)
     T = pw.num_tokens
     rng = np.random.default_rng(77)
+    # end to end through the oracle's own rows (about 2 s of oracle work per token)
     idx = np.unique(np.concatenate([[0, 1, 127, 128, 129, 255, 256, T - 129, T - 128, T - 1],
                                     rng.integers(0, T, size=22)]))
+    # one token of every 128-token tile: rows against the exact products, epilogue strictly
+    idx_tiles = tile_samples(T, 78)
     w_p = pw.producer
     host_a = wl.host_pools(w_p)
     dev = torch.device("cuda")
@@ -365,7 +440,7 @@ def test_prefill_65536_tokens_hidden_6144_sampled(dt):
     for xor in (0, SENTINEL_XOR):
         pools = {k: (v ^ xor) for k, v in a_dev.items()}
         start = {k: v.clone() for k, v in pools.items()}
-        dp = DeviceProjection(pw, pools_on_device=pools)
+        dp = DeviceProjection(pw, pools_on_device=pools, rows_out=xor == 0)
         dp.run()
         torch.cuda.synchronize()
         assert int(dp.status.item()) == 0
@@ -385,3 +460,9 @@ def test_prefill_65536_tokens_hidden_6144_sampled(dt):
                       dict(w_p.meta, valid_mask=w_p.meta["valid_mask"][idx]))
     q_o, iq_o, pools_o = run_oracle(sub, pools=wl.host_pools(w_p))
     check_values(pw, idx, rows, q_o, iq_o, pools_o, runs[0][0])
+    # every tile: the kernel's rows within the fp32 accumulation bound of the exact
+    # products, and the epilogue alone, strictly, on the rows the kernel wrote (run A)
+    dp_a = runs[0][0]
+    it = torch.from_numpy(idx_tiles).to(dp_a.device)
+    check_rows(dp_a.rows_out.index_select(0, it).cpu().numpy().view(np.uint16), pw, None, idx_tiles)
+    check_epilogue_strict(pw, dp_a, idx_tiles)
