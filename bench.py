@@ -410,12 +410,17 @@ def legacy_write_path_timing(replays: int = 200, layers: int = 60):
         s.synchronize()
         kernels = None
         try:
+            # kernels of one layer: the device-side kernel records, else the host-side
+            # launch calls of the CUDA runtime
             from torch.profiler import ProfilerActivity, profile
-            with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
                 layer(*stack[0])
                 s.synchronize()
-            kernels = sum(1 for e in prof.events() if e.device_type.name == "CUDA"
-                          and not e.name.startswith("Memcpy") and not e.name.startswith("Memset"))
+            ev = list(prof.events())
+            dev = [e for e in ev if "CUDA" in str(getattr(e, "device_type", ""))
+                   and not e.name.startswith(("Memcpy", "Memset", "cuda"))]
+            api = [e for e in ev if e.name.startswith(("cudaLaunchKernel", "cuLaunchKernel"))]
+            kernels = len(dev) if dev else len(api)
         except Exception as e:   # the profiler is context only
             log(f"[bench] kernel count unavailable: {type(e).__name__}: {e}"[:160])
         g = torch.cuda.CUDAGraph()
@@ -467,9 +472,9 @@ def graph_launch_us(dw, flags, launches: int, replays: int) -> float:
 
 def indexer_timing(replays: int = 200, calls: int = 20):
     """The indexer of the decode-batch-64 layer (64 queries, contexts U{1..9216},
-    8 index heads of dim 128, fp8 index-K): one call = score kernel + top-k kernel;
-    `calls` back-to-back calls captured in a graph, with programmatic dependent
-    launch of the score kernel (and, for comparison, without)."""
+    8 index heads of dim 128, fp8 index-K): one call = one kernel (a cluster of CTAs
+    per query, top-k in the same kernel); `calls` back-to-back calls captured in a
+    graph, with programmatic dependent launch (and, for comparison, without)."""
     import torch
     from paged_kv_cache_msa_gb300 import binding as B
     from paged_kv_cache_msa_gb300 import workloads as wl
@@ -502,7 +507,7 @@ def indexer_timing(replays: int = 200, calls: int = 20):
     peak, _ = peaks()
     return {"workload": "decode batch 64, contexts U{1..9216}, 8 index heads x 128, fp8 index-K, "
                         "top-16 of 128-token blocks",
-            "us_per_call": us, "us_per_call_without_pdl": us_plain, "launches_per_call": 2,
+            "us_per_call": us, "us_per_call_without_pdl": us_plain, "launches_per_call": 1,
             "algorithmic_bytes": alg,
             "gbs": alg / (us * 1e-6) / 1e9, "frac_of_peak": alg / (us * 1e-6) / 1e9 / peak,
             "index_k_tokens_scanned": int(w.kv_len.sum())}
@@ -552,10 +557,10 @@ def decode_layer_timing(layers: int = 60, replays: int = 50):
         out[name] = {"us_per_step": us, "us_per_layer": us / layers}
     return {"workload": f"decode batch 64, big shapes, contexts U{{1..9216}}: producer + indexer "
                         f"(top-16 of 128-token blocks) per layer, {layers} layers in one CUDA graph",
-            "launches_per_layer": 3, **out}
+            "launches_per_layer": 2, **out}
 
 
-def indexer_prefill_timing(reps: int = 5):
+def indexer_prefill_timing(reps: int = 5, num_seqs: int = 8):
     """The indexer of the prefill batch (8 x 8192 causal queries, 8 index heads of
     dim 128, fp8 index-K, top-16 of 128-token blocks): the query-run kernel (tiles
     of 16 queries on the tcgen05 tensor cores) and, for comparison, the per-query
@@ -564,7 +569,7 @@ def indexer_prefill_timing(reps: int = 5):
     from paged_kv_cache_msa_gb300 import binding as B
     from paged_kv_cache_msa_gb300 import workloads as wl
     from paged_kv_cache_msa_gb300.device import DeviceIndexer
-    w = wl.indexer_prefill()
+    w = wl.indexer_prefill(num_seqs=num_seqs)
     dv = DeviceIndexer(w)
     s = torch.cuda.Stream()
 
@@ -587,7 +592,7 @@ def indexer_prefill_timing(reps: int = 5):
     flops = 2.0 * float(w.kv_len.astype(np.int64).sum()) * H * D   # visible (query, key, head) dots
     burst, _, kind = tensor_peaks()
     tf = flops / (us_runs * 1e-6) / 1e12
-    return {"workload": "prefill 8 x 8192 causal queries, 8 index heads x 128, fp8 index-K, "
+    return {"workload": f"prefill {num_seqs} x 8192 causal queries, 8 index heads x 128, fp8 index-K, "
                         "top-16 of 128-token blocks",
             "us_per_call": us_runs, "us_per_call_per_query_kernel": us_plain,
             "queries_per_s": T / (us_runs * 1e-6), "launches_per_call": 2,
@@ -1003,6 +1008,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--indexer-only", action="store_true",
                     help="time only the decode-batch-64 indexer and print its JSON")
+    ap.add_argument("--indexer-prefill-only", action="store_true",
+                    help="time only the prefill (query-run) indexer and print its JSON")
     ap.add_argument("--no-projection", action="store_true",
                     help="skip the projection GEMM + producer leg")
     ap.add_argument("--projection-only", action="store_true",
@@ -1026,11 +1033,17 @@ def main():
         out["decode_64"] = projection_decode_timing()
         print(json.dumps(out), flush=True)
         return 0
+    if args.indexer_prefill_only:
+        from paged_kv_cache_msa_gb300 import build as build_mod
+        build_mod.build()
+        print(json.dumps(indexer_prefill_timing(reps=max(1, args.steps), num_seqs=args.prefill_seqs)),
+              flush=True)
+        return 0
     if args.indexer_only:
         from paged_kv_cache_msa_gb300 import build as build_mod
         build_mod.build()
         out = indexer_timing(replays=max(1, args.steps), calls=20)
-        out["prefill"] = indexer_prefill_timing()
+        out["prefill"] = indexer_prefill_timing(num_seqs=args.prefill_seqs)
         out["decode_layer"] = decode_layer_timing()
         print(json.dumps(out), flush=True)
         return 0

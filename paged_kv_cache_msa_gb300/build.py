@@ -168,6 +168,24 @@ def build_checked(force: bool = False) -> str:
     return CHECKED_LIB_PATH
 
 
+STARVED_LIB_PATH = os.path.join(OUT_DIR, "libmsa_producer_starved.so")
+STARVED_WAIT_LIMIT_NS = 50_000_000
+
+
+def build_starved(force: bool = False) -> str:
+    """Compiles the starved test library (-DMSA_STARVE, every bounded wait limited to
+    STARVED_WAIT_LIMIT_NS): the projection's TMA warps and the query-run indexer's MMA
+    thread issue nothing, so every wait on their barriers runs out with no copy or
+    MMA in flight.  Only the tests of the timeout path load
+    it; the product uses build()."""
+    defs = ("MSA_STARVE", f"MSA_WAIT_LIMIT_NS={STARVED_WAIT_LIMIT_NS}ull")
+    stamp = STARVED_LIB_PATH + ".sha256"
+    digest = source_digest(defs)
+    if force or not _fresh(STARVED_LIB_PATH, stamp, digest):
+        _compile(STARVED_LIB_PATH, stamp, digest, [f"-D{d}" for d in defs])
+    return STARVED_LIB_PATH
+
+
 if __name__ == "__main__":
     defs = [a[2:] for a in sys.argv[1:] if a.startswith("-D")]
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, defines=defs or None))

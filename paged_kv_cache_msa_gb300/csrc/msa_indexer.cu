@@ -38,6 +38,16 @@
 #ifndef MSA_INDEX_GROUPS
 #define MSA_INDEX_GROUPS 4
 #endif
+// 1: query runs take the warp-specialised kernel (msa_index_runs_kernel); 0: the
+// lockstep one (msa_index_tiled_kernel).
+#ifndef MSA_INDEX_RUNS_WS
+#define MSA_INDEX_RUNS_WS 1
+#endif
+// 1: the per-query path is the one-kernel cluster design (msa_index_decode_kernel);
+// 0: the score kernel followed by the top-k kernel.
+#ifndef MSA_INDEX_DECODE_CLUSTER
+#define MSA_INDEX_DECODE_CLUSTER 0
+#endif
 // Resident 128-thread score CTAs per SM the register budget is sized for.
 #ifndef MSA_INDEX_MIN_CTAS
 #define MSA_INDEX_MIN_CTAS 4
@@ -357,7 +367,8 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// true once the phase with the given parity has completed; false after 2 s
+// true once the phase with the given parity has completed; false after the limit
+// (MSA_WAIT_LIMIT_NS, 2 s)
 __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
 {
     if (mbar_try(bar, parity))
@@ -366,7 +377,7 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
     for (uint32_t n = 1;; ++n) {
         if (mbar_try(bar, parity))
             return true;
-        if ((n & 63) == 0 && globaltimer() - t0 > 2000000000ull)
+        if ((n & 63) == 0 && globaltimer() - t0 > MSA_WAIT_LIMIT_NS)
             return false;
     }
 }
@@ -616,7 +627,11 @@ msa_index_tiled_kernel(const __grid_constant__ IndexerParams p)
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncthreads();
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#ifdef MSA_STARVE
+            if (false) {   // the starved test build: no MMA, no commit
+#else
             if (tid == 0) {
+#endif
                 const uint32_t d = tmem + st * kTileKeys;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
@@ -660,6 +675,541 @@ msa_index_tiled_kernel(const __grid_constant__ IndexerParams p)
 }
 
 // ---------------------------------------------------------------------------
+// block scores of query runs, warp-specialised (prefill)
+// ---------------------------------------------------------------------------
+//
+// The scores of msa_index_tiled_kernel, with the MMA operands swapped and the
+// phases pipelined across warps instead of run in lockstep:
+//   A (M = 128)  the 128 keys of a block: FP8 codes converted to f16 (bf16 rows as
+//                they are) by the gather warps and written from registers straight
+//                into tensor memory (tcgen05.st) -- no shared-memory round trip;
+//   B (N = 128)  the tile's query heads (row = query * HP + head), K-major in shared
+//                memory with the 128-byte swizzle, loaded once per tile;
+//   D            fp32 [key, query-head] in tensor memory.
+// The only shared-memory traffic per block is the MMA reading B (32 KB for D = 128).
+// Warps: 0 allocates tensor memory and its lane 0 issues the MMAs; 1-8 gather
+// (warps w and w + 4 share tensor-memory lane quarter w & 3 and take one half of
+// the head dimension each; the rows of the next block are in flight in registers
+// while the current one is converted); 9-16 epilogue, two groups of four that take
+// alternate blocks, group g always reading accumulator g (thread = key of its lane
+// quarter: per query, the max over its heads of the key's scores, masked by the
+// key's page and the query's visible length; then the max over the block's keys,
+// by a shuffle butterfly inside the warp and across the group's four warps through
+// shared memory).  CTAs are persistent over the tiles.  Hand-offs are mbarriers: key
+// stages (A) full / empty, accumulators full / empty, query tiles (B) full / empty.
+// Every wait is bounded: after a timeout the CTA stops issuing copies and MMAs, and
+// the epilogue scores every remaining visible block NaN (never selected).
+
+constexpr int kRunsNSA = 3;            // key stages (A) in tensor memory
+constexpr int kRunsNACC = 2;           // accumulators
+constexpr int kRunsThreads = 17 * 32;  // 1 MMA + 8 gather + 2 x 4 epilogue warps
+constexpr uint32_t kRunsTmemCols = 512;
+constexpr int kRunsDynSmem = 120 * 1024;  // two query tiles; more than half an SM: one CTA per SM
+
+template <int QT>
+__device__ __forceinline__ float butterfly_max(float (&v)[QT], int lane)
+{
+    // after the level with offset o, a lane keeps the half of its values selected by
+    // bit o of its lane id, combined with its partner's copy of that half
+    static_assert(QT == 8 || QT == 16, "queries per tile");
+#pragma unroll
+    for (int o = 16, n = QT; o >= 1; o >>= 1) {
+        if (n > 1) {
+            const bool hi = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < QT / 2; ++i) {
+                if (i < n / 2) {
+                    const float send = hi ? v[i] : v[i + n / 2];
+                    const float keep = hi ? v[i + n / 2] : v[i];
+                    v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
+                }
+            }
+            n /= 2;
+        } else {
+            v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], o));
+        }
+    }
+    return v[0];   // the max of query (lane >> 1) & 15 (QT 16) or (lane >> 2) & 7 (QT 8)
+}
+
+__device__ __forceinline__ void tmem_st32x(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16x(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t *r)
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ void mbar_arrive_local(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// The segments and blocks of a tile, in the order every role walks them: one
+// sequence (table row) at a time, first the one of the lowest unscored query;
+// fn(seg_mask, toff, seg_len, nb) per segment.
+template <int QT, typename Fn>
+__device__ __forceinline__ void for_each_segment(const int32_t *len, const int64_t *toff,
+                                                 int max_blocks, Fn &&fn)
+{
+    constexpr uint32_t all = (QT == 32) ? 0xffffffffu : ((1u << QT) - 1u);
+    uint32_t done = 0;
+    while (done != all) {
+        const int q0 = __ffs(~done & all) - 1;
+        const int64_t to = toff[q0];
+        uint32_t seg = 0;
+        int32_t seg_len = 0;
+#pragma unroll
+        for (int q = 0; q < QT; ++q)
+            if (!((done >> q) & 1) && toff[q] == to) {
+                seg |= 1u << q;
+                seg_len = len[q] > seg_len ? len[q] : seg_len;
+            }
+        int nb = to == INT64_MIN ? 0 : (int)((seg_len + kTileKeys - 1) / kTileKeys);
+        nb = nb > max_blocks ? max_blocks : nb;
+        fn(seg, to, seg_len, nb);
+        done |= seg;
+    }
+}
+
+template <int D, bool FP8, int HP>
+__global__ void __launch_bounds__(kRunsThreads, 1)
+msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
+{
+    constexpr int QT = 128 / HP;                           // queries per tile
+    constexpr uint32_t kBBytes = 128u * D * 2u;            // one query tile (B)
+    constexpr int CH = D / 8;                              // 16-byte chunks of a 2-byte row
+    constexpr uint32_t kACols = D / 2;                     // tensor-memory columns of a key stage
+    constexpr uint32_t kAccCols = 128;
+    constexpr uint32_t kACol0 = kRunsNACC * kAccCols;      // first key-stage column
+    static_assert(kACol0 + kRunsNSA * kACols <= kRunsTmemCols, "tensor memory budget");
+    constexpr uint32_t kIdesc = (1u << 4) | ((FP8 ? 0u : 1u) << 7) | ((FP8 ? 0u : 1u) << 10) |
+                                ((uint32_t)(128 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_tile_full[2], bar_tile_empty[2];
+    __shared__ __align__(8) uint64_t bar_a_full[kRunsNSA], bar_a_empty[kRunsNSA];
+    __shared__ __align__(8) uint64_t bar_acc_full[kRunsNACC], bar_acc_empty[kRunsNACC];
+    __shared__ __align__(8) uint64_t bar_drain;
+    __shared__ int32_t g_len[2][QT];       // gather side's tile metadata (also read by the MMA)
+    __shared__ int64_t g_toff[2][QT];
+    __shared__ int32_t e_len[2][2][QT];    // each epilogue group's own copy
+    __shared__ int64_t e_toff[2][2][QT];
+    __shared__ float s_red[2][2][4][QT];   // [group][block parity][warp][query]
+    __shared__ int s_red_ok[2][2][4];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t bbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const int64_t num_tiles = (p.num_queries + QT - 1) / QT;
+
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(smem_u32(&bar_tile_full[i])));
+            // released by the eight epilogue warps and the MMA thread
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 9;" ::"r"(smem_u32(&bar_tile_empty[i])));
+        }
+        for (int i = 0; i < kRunsNSA; ++i) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(smem_u32(&bar_a_full[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_a_empty[i])));
+        }
+        for (int i = 0; i < kRunsNACC; ++i) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_acc_full[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(smem_u32(&bar_acc_empty[i])));
+        }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_drain)));
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&s_tmem)),
+                     "r"(kRunsTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = s_tmem;
+    volatile int *abort_flag = &s_abort;
+
+    if (warp == 0) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            uint32_t it = 0, tile_it = 0;
+            bool ok = true;
+            for (int64_t ti = blockIdx.x; ti < num_tiles && ok; ti += gridDim.x, ++tile_it) {
+                const uint32_t tb = tile_it & 1;
+                if (*abort_flag || !mbar_wait(smem_u32(&bar_tile_full[tb]), (tile_it >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t bt = bbase + tb * kBBytes;
+                for_each_segment<QT>(g_len[tb], g_toff[tb], p.max_blocks,
+                                     [&](uint32_t, int64_t, int32_t, int nb) {
+                    for (int b = 0; b < nb && ok; ++b, ++it) {
+                        const uint32_t s = it % kRunsNSA, ph = (it / kRunsNSA) & 1;
+                        const uint32_t a = it % kRunsNACC, pa = (it / kRunsNACC) & 1;
+                        if (*abort_flag || !mbar_wait(smem_u32(&bar_a_full[s]), ph) ||
+                            !mbar_wait(smem_u32(&bar_acc_empty[a]), pa ^ 1)) {
+                            ok = false;
+                            break;
+                        }
+                        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                        const uint32_t d = tmem + a * kAccCols;
+#ifndef MSA_STARVE
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            const uint32_t at = tmem + kACol0 + s * kACols + (uint32_t)ks * 8u;
+                            const uint32_t koff = (uint32_t)(ks >> 2) * (128u * 128u) + (uint32_t)(ks & 3) * 32u;
+                            const uint64_t bd = sw128_desc(bt + koff);
+                            asm volatile(
+                                "{\n\t.reg .pred pp;\n\tsetp.ne.b32 pp, %4, 0;\n\t"
+                                "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pp;\n\t}" ::"r"(d),
+                                "r"(at), "l"(bd), "r"(kIdesc), "r"((uint32_t)ks)
+                                : "memory");
+                        }
+                        asm volatile(
+                            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                smem_u32(&bar_a_empty[s]))
+                            : "memory");
+                        asm volatile(
+                            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                smem_u32(&bar_acc_full[a]))
+                            : "memory");
+#else
+                        (void)d;
+#endif
+                    }
+                });
+                if (ok)   // this thread is done with the tile (its MMAs may still run)
+                    mbar_arrive_local(smem_u32(&bar_tile_empty[tb]));
+            }
+            if (!ok)
+                *abort_flag = 1;
+            // every MMA has completed before tensor memory is released
+            asm volatile(
+                "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                    smem_u32(&bar_drain))
+                : "memory");
+            (void)mbar_wait(smem_u32(&bar_drain), 0);
+        }
+        __syncwarp();
+    } else if (warp <= 8) {
+        // ---------------- gather ----------------
+        const int gt = tid - 32;                    // 0..255
+        const int quarter = warp & 3, half = (warp - 1) >> 2;
+        const int key = quarter * 32 + lane;        // tensor-memory lane = key of the block
+        constexpr int NV = FP8 ? D / 32 : D / 16;   // 16-byte pieces of half a key row
+        const uint32_t a_lane = (uint32_t)(quarter * 32) << 16;
+        uint32_t it = 0, tile_it = 0;
+        bool stop = false;
+        for (int64_t ti = blockIdx.x; ti < num_tiles; ti += gridDim.x, ++tile_it) {
+            const uint32_t tb = tile_it & 1;
+            stop = stop || *abort_flag ||
+                   !__any_sync(0xffffffffu, mbar_wait(smem_u32(&bar_tile_empty[tb]), ((tile_it >> 1) & 1) ^ 1));
+            const int64_t t0 = ti * QT;
+            if (!stop && gt < QT) {
+                const int64_t t = t0 + gt;
+                const int32_t len = t < p.num_queries ? __ldg(p.kv_len + t) : 0;
+                g_len[tb][gt] = len > 0 ? len : 0;
+                g_toff[tb][gt] = t < p.num_queries ? __ldg(p.table_offset + t) : INT64_MIN;
+            }
+            {   // the query tile: row r = (query r / HP, head r % HP), this thread's half
+                const int r = gt >> 1, hh = gt & 1;
+                const int q = r / HP, h = r % HP;
+                const int64_t t = t0 + q;
+                const bool real = h < p.heads && t < p.num_queries;
+                const uint16_t *src = p.idx_q + (t * p.heads + h) * D;
+                const uint32_t bt = bbase + tb * kBBytes;
+#pragma unroll
+                for (int c = hh * (CH / 2); c < (hh + 1) * (CH / 2); ++c) {
+                    if (stop)
+                        break;
+                    uint4 v = real ? ldg16(src + 8 * c) : make_uint4(0, 0, 0, 0);
+                    if (FP8) {   // bf16 -> f16 (exact for the normal f16 range)
+                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                        uint32_t o[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            o[k] = f2_to_f16x2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
+                        v = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                    sts128(swz(bt, r, c), v.x, v.y, v.z, v.w);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            // publishes the tile's metadata to every gather thread and takes one stop
+            // decision for all eight gather warps (a warp that stopped on its own,
+            // after a wait ran out, stops them all here)
+            {
+                uint32_t any;
+                asm volatile(
+                    "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, 1, 256, p; selp.u32 %0, 1, 0, q; }"
+                    : "=r"(any)
+                    : "r"((uint32_t)stop)
+                    : "memory");
+                if (any) {
+                    *abort_flag = 1;
+                    break;
+                }
+            }
+            if (lane == 0)
+                mbar_arrive_local(smem_u32(&bar_tile_full[tb]));
+
+            for_each_segment<QT>(g_len[tb], g_toff[tb], p.max_blocks,
+                                 [&](uint32_t, int64_t toff, int32_t seg_len, int nb) {
+                // this thread's half row of key `key` of block bb, fetched into registers
+                auto fetch = [&](int bb, uint4 (&raw)[NV]) {
+                    const int64_t j = (int64_t)bb * kTileKeys + key;
+                    bool okr = bb < nb && j < seg_len;
+                    int64_t page = -1;
+                    if (okr) {
+                        const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
+                        const int64_t ti2 = toff + blk;
+                        page = (ti2 >= 0 && ti2 < p.page_table_len) ? (int64_t)__ldg(p.page_table + ti2) : -1;
+                        okr = page >= 0 && page < p.num_pages;
+                    }
+                    const int64_t off = p.page_shift >= 0 ? (j & (p.page_size - 1)) : j % p.page_size;
+                    const uint8_t *row = okr ? p.kdata + (page * p.stride_page + off * p.stride_token) * (FP8 ? 1 : 2) +
+                                                   (size_t)half * (D / 2) * (FP8 ? 1 : 2)
+                                             : nullptr;
+#pragma unroll
+                    for (int v = 0; v < NV; ++v)
+                        raw[v] = okr ? ldg16(row + 16 * v) : make_uint4(0, 0, 0, 0);
+                };
+                auto store = [&](const uint4 (&raw)[NV]) -> bool {
+                    const uint32_t s = it % kRunsNSA, ph = (it / kRunsNSA) & 1;
+                    if (*abort_flag || !__any_sync(0xffffffffu, mbar_wait(smem_u32(&bar_a_empty[s]), ph ^ 1))) {
+                        *abort_flag = 1;
+                        return false;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    uint32_t w[32];
+                    if (FP8) {
+#pragma unroll
+                        for (int v = 0; v < NV; ++v) {
+                            const uint32_t x[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                w[8 * v + 2 * k] = e4m3x2_to_f16x2(x[k] & 0xFFFF);
+                                w[8 * v + 2 * k + 1] = e4m3x2_to_f16x2(x[k] >> 16);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < NV; ++v) {
+                            w[4 * v] = raw[v].x;
+                            w[4 * v + 1] = raw[v].y;
+                            w[4 * v + 2] = raw[v].z;
+                            w[4 * v + 3] = raw[v].w;
+                        }
+                    }
+                    const uint32_t taddr = tmem + a_lane + kACol0 + s * kACols + (uint32_t)half * (kACols / 2);
+                    if (D == 128)
+                        tmem_st32x(taddr, w);
+                    else
+                        tmem_st16x(taddr, w);
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive_local(smem_u32(&bar_a_full[s]));
+                    ++it;
+                    return true;
+                };
+                if (stop || nb == 0)
+                    return;
+                // two register sets: the rows of block b + 1 are in flight while block b
+                // is converted and stored
+                uint4 ra[NV], rb[NV];
+                fetch(0, ra);
+                if (nb > 1)
+                    fetch(1, rb);
+                for (int b = 0; b < nb; b += 2) {
+                    if (!store(ra)) { stop = true; return; }
+                    if (b + 2 < nb)
+                        fetch(b + 2, ra);
+                    if (b + 1 < nb) {
+                        if (!store(rb)) { stop = true; return; }
+                        if (b + 3 < nb)
+                            fetch(b + 3, rb);
+                    }
+                }
+            });
+        }
+    } else {
+        // ---------------- epilogue: two groups, alternate blocks ----------------
+        const int grp = (warp - 9) >> 2;            // takes the blocks with item parity grp
+        const int et = tid - (9 + 4 * grp) * 32;    // 0..127 within the group
+        const int quarter = warp & 3;
+        const int key = quarter * 32 + lane;
+        const uint32_t d_lane = (uint32_t)(quarter * 32) << 16;
+        const uint32_t acc_col = (uint32_t)grp * kAccCols;   // item parity grp -> accumulator grp
+        const float kscale = FP8 ? __ldg(p.k_scale) : 1.0f;
+        auto group_sync = [&]() {
+            if (grp == 0)
+                asm volatile("bar.sync 2, 128;" ::: "memory");
+            else
+                asm volatile("bar.sync 3, 128;" ::: "memory");
+        };
+        uint32_t it = 0, tile_it = 0;
+        for (int64_t ti = blockIdx.x; ti < num_tiles; ti += gridDim.x, ++tile_it) {
+            const uint32_t tb = tile_it & 1;
+            const int64_t t0 = ti * QT;
+            int32_t *elen = e_len[grp][tb];
+            int64_t *etoff = e_toff[grp][tb];
+            if (et < QT) {
+                const int64_t t = t0 + et;
+                const int32_t len = t < p.num_queries ? __ldg(p.kv_len + t) : 0;
+                elen[et] = len > 0 ? len : 0;
+                etoff[et] = t < p.num_queries ? __ldg(p.table_offset + t) : INT64_MIN;
+            }
+            group_sync();
+            for_each_segment<QT>(elen, etoff, p.max_blocks,
+                                 [&](uint32_t seg, int64_t toff, int32_t, int nb) {
+                int32_t minlen = 0x7fffffff;
+#pragma unroll
+                for (int q = 0; q < QT; ++q)
+                    if ((seg >> q) & 1)
+                        minlen = elen[q] < minlen ? elen[q] : minlen;
+                // this key's table entry for block bb (raw; -1 outside the table)
+                auto entry = [&](int bb) -> int64_t {
+                    const int64_t j = (int64_t)bb * kTileKeys + key;
+                    const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
+                    const int64_t ti2 = toff + blk;
+                    return (ti2 >= 0 && ti2 < p.page_table_len) ? (int64_t)__ldg(p.page_table + ti2) : -1;
+                };
+                int b = ((it & 1) == (uint32_t)grp) ? 0 : 1;     // this group's first block
+                int64_t pg = b < nb ? entry(b) : -1;
+                for (; b < nb; b += 2) {
+                    const uint32_t its = it + (uint32_t)b;          // global item index
+                    const int64_t pg_next = b + 2 < nb ? entry(b + 2) : -1;   // in flight meanwhile
+                    const uint32_t pa = (its / kRunsNACC) & 1;
+                    const int64_t j = (int64_t)b * kTileKeys + key;
+                    const bool kvalid = pg >= 0 && pg < p.num_pages;
+                    bool got = !*abort_flag;
+                    if (got)
+                        got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_acc_full[grp]), pa));
+                    if (!got)
+                        *abort_flag = 1;
+                    float m[QT];
+#pragma unroll
+                    for (int q = 0; q < QT; ++q)
+                        m[q] = -INFINITY;
+                    if (got) {
+                        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                        const bool whole = __all_sync(0xffffffffu, kvalid && j < minlen) && p.heads == HP;
+#pragma unroll
+                        for (int c0 = 0; c0 < 128; c0 += 32) {
+                            uint32_t r[32];
+                            tmem_ld32_nowait(tmem + d_lane + acc_col + (uint32_t)c0, r);
+                            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                            for (int qq = 0; qq < 32 / HP; ++qq) {
+                                const int q = c0 / HP + qq;
+                                float v = -INFINITY;
+#pragma unroll
+                                for (int h = 0; h < HP; ++h)
+                                    if (whole || h < p.heads)
+                                        v = fmaxf(v, __uint_as_float(r[qq * HP + h]));
+                                if (!whole && !(kvalid && j < elen[q]))
+                                    v = -INFINITY;
+                                m[q] = v;
+                            }
+                        }
+                    }
+                    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive_local(smem_u32(&bar_acc_empty[grp]));
+                    const float wm = butterfly_max<QT>(m, lane);
+                    const int qo = QT == 16 ? ((lane >> 1) & 15) : ((lane >> 2) & 7);
+                    const int rp = (int)((its >> 1) & 1);           // this group's block parity
+                    if ((lane & (QT == 16 ? 1 : 3)) == 0)
+                        s_red[grp][rp][quarter][qo] = wm;
+                    if (lane == 0)
+                        s_red_ok[grp][rp][quarter] = got ? 1 : 0;
+                    group_sync();
+                    if (et < QT && ((seg >> et) & 1) && t0 + et < p.num_queries) {
+                        const float *rr = &s_red[grp][rp][0][0];
+                        const float v = fmaxf(fmaxf(rr[et], rr[QT + et]), fmaxf(rr[2 * QT + et], rr[3 * QT + et]));
+                        const int *ok4 = s_red_ok[grp][rp];
+                        const bool all_got = ok4[0] & ok4[1] & ok4[2] & ok4[3];
+                        p.block_scores[(t0 + et) * p.max_blocks + b] =
+                            all_got ? (v > -INFINITY ? v * kscale : -INFINITY) : __int_as_float(0x7fc00000);
+                    }
+                    pg = pg_next;
+                }
+                it += (uint32_t)nb;
+                // blocks the segment's queries do not reach (the two groups share them)
+                const int rest = p.max_blocks - nb;
+                for (int idx = et + 128 * grp; idx < QT * rest; idx += 256) {
+                    const int q = idx / rest, bb = nb + idx % rest;
+                    if ((seg >> q) & 1 && t0 + q < p.num_queries)
+                        p.block_scores[(t0 + q) * p.max_blocks + bb] = -INFINITY;
+                }
+            });
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_local(smem_u32(&bar_tile_empty[tb]));
+        }
+    }
+
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kRunsTmemCols)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
 // top-k block ids
 // ---------------------------------------------------------------------------
 // (a, ia) ranks before (b, ib): higher score first, lower id among equals.
@@ -671,43 +1221,33 @@ __device__ __forceinline__ bool ranks_before(float a, int ia, float b, int ib)
 constexpr int kTopkThreads = 128;
 constexpr int kRankMaxBlocks = 1024;   // rows up to this many blocks are ranked in shared memory
 
-// One CTA per query.  Short rows: the row is staged in shared memory and every
-// finite entry counts the entries ranked before it (all threads in parallel);
-// entries with rank < topk write their id at that rank.  Long rows: warp 0 takes
-// topk rounds, each an arg-max over the entries ranked after the previous pick.
-// Under programmatic dependent launch the kernel waits for the score kernel
-// before reading its output.
-__global__ void __launch_bounds__(kTopkThreads) msa_index_topk_kernel(const __grid_constant__ IndexerParams p)
+// Top-k ids of one row of n block scores, by the kTopkThreads threads of a CTA.
+// Short rows (n <= kRankMaxBlocks) are ranked in shared memory s_row: every finite
+// entry counts the entries ranked before it, all threads in parallel, and entries
+// with rank < topk write their id at that rank.  When `staged`, s_row already holds
+// the row; otherwise it is read from `row`.  Long rows: warp 0 takes topk rounds,
+// each an arg-max over the entries ranked after the previous pick, reading `row`.
+__device__ __forceinline__ void topk_row(const float *row, float *s_row, int *s_nfin, bool staged,
+                                         int n, int topk, int32_t *out)
 {
-    __shared__ __align__(16) float s_row[kRankMaxBlocks];
-    __shared__ int s_nfin;
     const int tid = threadIdx.x, lane = tid & 31;
-    const int64_t t = blockIdx.x;
-    const int n = p.max_blocks;
-    int32_t *out = p.topk_ids + t * p.topk;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    // The next kernel may start its prologue once this grid has waited: every kernel
-    // before this one has completed by then (see the producer's kernel for why the
-    // signal comes after the wait).
-    asm volatile("griddepcontrol.launch_dependents;" :::);
-    const float *row = p.block_scores + t * n;
-
     if (n <= kRankMaxBlocks) {
         if (tid == 0)
-            s_nfin = 0;
+            *s_nfin = 0;
         __syncthreads();
         int nfin = 0;
         const int npad = (n + 3) & ~3;
         for (int b = tid; b < npad; b += kTopkThreads) {
-            const float v = b < n ? row[b] : -INFINITY;
-            s_row[b] = v;
+            const float v = b < n ? (staged ? s_row[b] : row[b]) : -INFINITY;
+            if (!staged || b >= n)
+                s_row[b] = v;
             nfin += (v > -INFINITY) ? 1 : 0;   // NaN and -inf are not candidates
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             nfin += __shfl_xor_sync(0xffffffffu, nfin, o);
         if (lane == 0)
-            atomicAdd(&s_nfin, nfin);
+            atomicAdd(s_nfin, nfin);
         __syncthreads();
         const float4 *r4 = reinterpret_cast<const float4 *>(s_row);
         for (int b = tid; b < n; b += kTopkThreads) {
@@ -723,10 +1263,10 @@ __global__ void __launch_bounds__(kTopkThreads) msa_index_topk_kernel(const __gr
                 rank += (w.z > v || (w.z == v && u + 2 < b)) ? 1 : 0;
                 rank += (w.w > v || (w.w == v && u + 3 < b)) ? 1 : 0;
             }
-            if (rank < p.topk)
+            if (rank < topk)
                 out[rank] = b;
         }
-        for (int r = s_nfin + tid; r < p.topk; r += kTopkThreads)
+        for (int r = *s_nfin + tid; r < topk; r += kTopkThreads)
             out[r] = -1;
         return;
     }
@@ -736,7 +1276,7 @@ __global__ void __launch_bounds__(kTopkThreads) msa_index_topk_kernel(const __gr
     float prev_s = INFINITY;
     int prev_i = -1;
     int r = 0;
-    for (; r < p.topk; ++r) {
+    for (; r < topk; ++r) {
         float bs = -INFINITY;
         int bi = -1;
         for (int b = lane; b < n; b += 32) {
@@ -766,8 +1306,267 @@ __global__ void __launch_bounds__(kTopkThreads) msa_index_topk_kernel(const __gr
         prev_s = bs;
         prev_i = bi;
     }
-    for (int rr = r + 1 + lane; rr < p.topk; rr += 32)
+    for (int rr = r + 1 + lane; rr < topk; rr += 32)
         out[rr] = -1;
+}
+
+// One CTA per query, after a score kernel; under programmatic dependent launch it
+// waits for the score kernel before reading its output.
+__global__ void __launch_bounds__(kTopkThreads) msa_index_topk_kernel(const __grid_constant__ IndexerParams p)
+{
+    __shared__ __align__(16) float s_row[kRankMaxBlocks];
+    __shared__ int s_nfin;
+    const int64_t t = blockIdx.x;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // The next kernel may start its prologue once this grid has waited: every kernel
+    // before this one has completed by then (see the producer's kernel for why the
+    // signal comes after the wait).
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+    topk_row(p.block_scores + t * p.max_blocks, s_row, &s_nfin, false, p.max_blocks, p.topk,
+             p.topk_ids + t * p.topk);
+}
+
+// ---------------------------------------------------------------------------
+// decode: a cluster of CTAs per query, top-k in the same kernel
+// ---------------------------------------------------------------------------
+//
+// The per-query scores of msa_index_score_kernel, restructured so that the history
+// read is not a chain of dependent loads: each query gets a cluster of CS CTAs
+// (host-chosen so that the grid fills the GPU once) that share out its blocks, CTA r
+// warp w taking blocks (k * CS + r) * 4 + w; a warp stages the index-K rows of its
+// blocks into shared memory with cp.async in rounds of kDecRoundBytes (two rounds in
+// flight, rows fetched through the page table, 16-byte pieces, 4 rows per
+// instruction), and scores each round from shared memory with the same mma.sync
+// contraction.  Every block score goes to block_scores and, over distributed shared
+// memory, to CTA 0 of the cluster; after one cluster barrier CTA 0 selects the top-k
+// from its shared memory.  No global scratch, one kernel per call, no wait on a flag
+// (cp.async.wait_group and the hardware cluster barrier cannot spin).
+
+constexpr int kDecRoundBytes = 8192;   // bytes of rows per warp per round
+constexpr int kDecThreads = 128;
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kDecThreads, 2)
+msa_index_decode_kernel(const __grid_constant__ IndexerParams p)
+{
+    constexpr int KS = D / 16;                  // mma k-steps
+    constexpr int ES = FP8 ? 1 : 2;
+    constexpr int ROWB = D * ES;                // bytes of an index-K row
+    constexpr int CPT = ROWB / 16;              // 16-byte pieces per row
+    constexpr int RT = kDecRoundBytes / ROWB;   // rows per round
+    constexpr int NWL = FP8 ? (D / 4) / 16 : (D / 4) / 8;   // 16-byte words per lane and token
+    static_assert(RT % 8 == 0 && (RT * CPT) % 32 == 0, "round geometry");
+    extern __shared__ __align__(16) uint8_t s_stage[];    // [4 warps][2][kDecRoundBytes]
+    __shared__ __align__(16) float s_q[16][D];
+    __shared__ __align__(16) uint4 s_af[KS][32];
+    __shared__ __align__(16) float s_row[kRankMaxBlocks];   // CTA 0: the query's block scores
+    __shared__ int s_nfin;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, i = lane & 3;
+    uint32_t cs, rank;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(cs));
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    const int64_t t = (int64_t)blockIdx.x / cs;
+    const int H = p.heads;
+    const int bt = p.block_tokens;
+    const int n = p.max_blocks;
+    const bool staged = n <= kRankMaxBlocks;
+    // the cluster's CTAs must all be running before one writes another's shared memory
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+
+    // metadata first (read before waiting on the previous kernel under PDL)
+    const int32_t len_raw = __ldg(p.kv_len + t);
+    const int64_t tbase = __ldg(p.table_offset + t);
+    const int64_t L = len_raw > 0 ? (int64_t)len_raw : 0;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+
+    // the query's heads (rows >= H zero) and the A fragments, as in the score kernel
+    constexpr int NCH = 16 * D / 8, CPTQ = (NCH + kDecThreads - 1) / kDecThreads;
+    uint4 qraw[CPTQ];
+#pragma unroll
+    for (int u = 0; u < CPTQ; ++u) {
+        const int ch = tid + u * kDecThreads;
+        const int h = ch * 8 / D;
+        qraw[u] = (ch < NCH && h < H) ? ldg16(p.idx_q + (t * H + h) * D + (ch * 8) % D)
+                                      : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < CPTQ; ++u) {
+        const int ch = tid + u * kDecThreads;
+        if (ch < NCH) {
+            float *dst = &s_q[ch * 8 / D][(ch * 8) % D];
+            const uint32_t wv[4] = {qraw[u].x, qraw[u].y, qraw[u].z, qraw[u].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                dst[2 * k] = __uint_as_float(wv[k] << 16);
+                dst[2 * k + 1] = __uint_as_float(wv[k] & 0xFFFF0000u);
+            }
+        }
+    }
+    __syncthreads();
+    for (int st = warp; st < KS; st += 4) {
+        const int d = i * (D / 4) + 4 * st;
+        const float *r0 = &s_q[g][d], *r1 = &s_q[g + 8][d];
+        uint4 f;
+        if (FP8) {
+            f.x = f2_to_f16x2(r0[0], r0[1]);
+            f.y = f2_to_f16x2(r1[0], r1[1]);
+            f.z = f2_to_f16x2(r0[2], r0[3]);
+            f.w = f2_to_f16x2(r1[2], r1[3]);
+        } else {
+            f.x = f2_to_bf16x2(r0[0], r0[1]);
+            f.y = f2_to_bf16x2(r1[0], r1[1]);
+            f.z = f2_to_bf16x2(r0[2], r0[3]);
+            f.w = f2_to_bf16x2(r1[2], r1[3]);
+        }
+        s_af[st][lane] = f;
+    }
+    __syncthreads();
+    const bool row0_real = g < H, row1_real = g + 8 < H;
+    const float kscale = FP8 ? __ldg(p.k_scale) : 1.0f;
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA is running
+    const uint32_t srow0 = smem_u32(&s_row[0]);
+
+    // this warp's work: rounds of RT tokens over its blocks, flattened
+    const int rpb = (bt + RT - 1) / RT;                   // rounds per block
+    const int64_t stride_b = (int64_t)cs * 4;
+    const int64_t my_first = (int64_t)rank * 4 + warp;
+    const int64_t my_blocks = my_first < n ? (n - 1 - my_first) / stride_b + 1 : 0;
+    const int64_t tasks = my_blocks * rpb;
+    const uint32_t buf0 = smem_u32(s_stage) + (uint32_t)warp * 2u * kDecRoundBytes;
+
+    // The page of token j (-1: no row).  `entry` caches, one per lane, the table
+    // entries of the 32 logical pages from `blk0` on (the staging side and the
+    // scoring side keep their own); every lane of the warp calls this together.
+    auto page_of = [&](int64_t j, int64_t blk0, int64_t entry) -> int64_t {
+        const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
+        const int64_t rel = blk - blk0;
+        const long long e_sh = __shfl_sync(0xffffffffu, (long long)entry, (int)(rel & 31));
+        int64_t e;
+        if (rel >= 0 && rel < 32) {
+            e = e_sh;
+        } else {
+            const int64_t ti = tbase + blk;
+            e = (ti >= 0 && ti < p.page_table_len) ? (int64_t)__ldg(p.page_table + ti) : -1;
+        }
+        return (e >= 0 && e < p.num_pages) ? e : -1;
+    };
+    auto lane_entry_of = [&](int64_t blk0) -> int64_t {
+        const int64_t ti = tbase + blk0 + lane;
+        return (ti >= 0 && ti < p.page_table_len) ? (int64_t)__ldg(p.page_table + ti) : -1;
+    };
+    auto first_page_block = [&](int64_t b) -> int64_t {
+        const int64_t bj0 = b * bt;
+        return p.page_shift >= 0 ? (bj0 >> p.page_shift) : bj0 / p.page_size;
+    };
+    auto task_range = [&](int64_t task, int64_t &b, int64_t &j0, int64_t &j1) {
+        b = my_first + (task / rpb) * stride_b;
+        const int64_t bj0 = b * bt, bj1 = (bj0 + bt < L) ? bj0 + bt : L;
+        j0 = bj0 + (task % rpb) * RT;
+        j1 = (j0 + RT < bj1) ? j0 + RT : bj1;   // empty when j0 >= bj1
+    };
+    int64_t iss_blk0 = -1, iss_entry = -1;   // the staging side's table cache
+    // cp.async of the rows of task `task` into buffer `bsel`, then a commit (an empty
+    // group past the last task)
+    auto issue = [&](int64_t task, int bsel) {
+        if (task < tasks) {
+            int64_t b, j0, j1;
+            task_range(task, b, j0, j1);
+            const int64_t blk0 = first_page_block(b);
+            if (blk0 != iss_blk0) {
+                iss_entry = lane_entry_of(blk0);
+                iss_blk0 = blk0;
+            }
+            const uint32_t dst = buf0 + (uint32_t)bsel * kDecRoundBytes;
+            const int64_t nt = j1 > j0 ? j1 - j0 : 0;
+            for (int c = lane; c < RT * CPT; c += 32) {   // RT * CPT is a multiple of 32
+                const int r = c / CPT, piece = c % CPT;
+                const int64_t j = j0 + r;
+                const int64_t page = page_of(j, blk0, iss_entry);
+                if (r < nt && page >= 0) {
+                    const int64_t off = p.page_shift >= 0 ? (j & (p.page_size - 1)) : j % p.page_size;
+                    const uint8_t *src = p.kdata + (page * p.stride_page + off * p.stride_token) * ES + 16 * piece;
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + (uint32_t)(r * ROWB + 16 * piece)),
+                                 "l"(src)
+                                 : "memory");
+                }
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    int64_t cmp_blk0 = -1, cmp_entry = -1;   // the scoring side's table cache
+
+    issue(0, 0);
+    issue(1, 1);
+    float best = -INFINITY;
+    for (int64_t task = 0; task < tasks; ++task) {
+        const int bsel = (int)(task & 1);
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+        __syncwarp();
+        int64_t b, j0, j1;
+        task_range(task, b, j0, j1);
+        if (task % rpb == 0)
+            best = -INFINITY;
+        const int64_t blk0 = first_page_block(b);
+        if (blk0 != cmp_blk0) {
+            cmp_entry = lane_entry_of(blk0);
+            cmp_blk0 = blk0;
+        }
+        const uint32_t src0 = buf0 + (uint32_t)bsel * kDecRoundBytes;
+        for (int64_t jb = j0; jb < j1; jb += 8) {
+            // lane (g, i): token jb + g, its quarter i of the row, from shared memory
+            const int64_t j = jb + g;
+            const int64_t pg = page_of(j, blk0, cmp_entry);
+            const bool ok = j < j1 && pg >= 0;
+            uint4 w[NWL];
+            const uint32_t a0 = src0 + (uint32_t)((j - j0) * ROWB) + (uint32_t)(i * (D / 4) * ES);
+#pragma unroll
+            for (int v = 0; v < NWL; ++v)
+                w[v] = ok ? lds128(a0 + 16u * v) : make_uint4(0, 0, 0, 0);
+            float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const uint32_t *words = reinterpret_cast<const uint32_t *>(w);
+#pragma unroll
+            for (int st = 0; st < KS; ++st) {
+                const uint4 f = s_af[st][lane];
+                const uint32_t a[4] = {f.x, f.y, f.z, f.w};
+                if (FP8)
+                    mma_f16(c, a, e4m3x2_to_f16x2(words[st] & 0xFFFF), e4m3x2_to_f16x2(words[st] >> 16));
+                else
+                    mma_bf16(c, a, words[2 * st], words[2 * st + 1]);
+            }
+            float m0 = fmaxf(row0_real ? c[0] : -INFINITY, row1_real ? c[2] : -INFINITY);
+            float m1 = fmaxf(row0_real ? c[1] : -INFINITY, row1_real ? c[3] : -INFINITY);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+                m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+            }
+            const bool ok0 = __shfl_sync(0xffffffffu, ok, 8 * i);
+            const bool ok1 = __shfl_sync(0xffffffffu, ok, 8 * i + 4);
+            float m = fmaxf(ok0 ? m0 : -INFINITY, ok1 ? m1 : -INFINITY);
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            best = fmaxf(best, m);
+        }
+        __syncwarp();   // every lane is done reading the buffer before it is refilled
+        issue(task + 2, bsel);
+        if (task % rpb == rpb - 1 && lane == 0) {   // the block is complete
+            const float v = best > -INFINITY ? best * kscale : -INFINITY;
+            p.block_scores[t * n + b] = v;
+            if (staged) {
+                uint32_t remote;
+                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(srow0 + 4u * (uint32_t)b), "r"(0));
+                asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+            }
+        }
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    // every block score is in CTA 0's shared memory (and in block_scores)
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (rank == 0)
+        topk_row(p.block_scores + t * n, s_row, &s_nfin, staged, n, p.topk, p.topk_ids + t * p.topk);
 }
 
 // ---------------------------------------------------------------------------
@@ -895,25 +1694,93 @@ extern "C" msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t nu
     sc.stream = stream;
     if (tiled) {
         const int D = cfg->head_dim;
-        const int qt = cfg->num_heads <= 8 ? 16 : 8;
+        const bool hp8 = cfg->num_heads <= 8;
+        const int qt = hp8 ? 16 : 8;
+        int major = 0, dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return fail(MSA_ERR_CUDA, "device query failed");
+        if (major != 10)
+            return fail(MSA_ERR_UNSUPPORTED, "query runs need tcgen05 tensor cores (compute capability 10.x)");
+        const int64_t tiles = (num_queries + qt - 1) / qt;
+#if MSA_INDEX_RUNS_WS
+        const int smem = kRunsDynSmem;
+        const void *fns[8] = {
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<64, false, 8>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<64, false, 16>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<64, true, 8>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<64, true, 16>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, false, 8>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, false, 16>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, true, 8>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, true, 16>)};
+        score_fn = fns[(D == 128 ? 4 : 0) + (p.fp8 ? 2 : 0) + (hp8 ? 0 : 1)];
+        sc.gridDim = dim3((unsigned)(tiles < sms ? tiles : sms));   // persistent, one CTA per SM
+        sc.blockDim = dim3(kRunsThreads);
+#else
         const int smem = 3 * 128 * D * 2 + 1024;
         score_fn = D == 128 ? (p.fp8 ? reinterpret_cast<const void *>(&msa_index_tiled_kernel<128, true>)
                                      : reinterpret_cast<const void *>(&msa_index_tiled_kernel<128, false>))
                             : (p.fp8 ? reinterpret_cast<const void *>(&msa_index_tiled_kernel<64, true>)
                                      : reinterpret_cast<const void *>(&msa_index_tiled_kernel<64, false>));
+        sc.gridDim = dim3((unsigned)tiles);
+        sc.blockDim = dim3(kTileThreads);
+#endif
         if (cudaFuncSetAttribute(score_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
             cudaSuccess)
             return fail(MSA_ERR_CUDA, "cudaFuncSetAttribute failed");
-        int major = 0, dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
-            return fail(MSA_ERR_CUDA, "device query failed");
-        if (major != 10)
-            return fail(MSA_ERR_UNSUPPORTED, "query runs need tcgen05 tensor cores (compute capability 10.x)");
-        sc.gridDim = dim3((unsigned)((num_queries + qt - 1) / qt));
-        sc.blockDim = dim3(kTileThreads);
         sc.dynamicSmemBytes = (size_t)smem;
     }
+#if MSA_INDEX_DECODE_CLUSTER
+    if (!tiled) {
+        // one kernel: a cluster of CTAs per query, top-k in CTA 0 of each cluster
+        const int D = cfg->head_dim;
+        const void *fn = D == 128 ? (p.fp8 ? reinterpret_cast<const void *>(&msa_index_decode_kernel<128, true>)
+                                           : reinterpret_cast<const void *>(&msa_index_decode_kernel<128, false>))
+                                  : (p.fp8 ? reinterpret_cast<const void *>(&msa_index_decode_kernel<64, true>)
+                                           : reinterpret_cast<const void *>(&msa_index_decode_kernel<64, false>));
+        const int smem = 4 * 2 * kDecRoundBytes;
+        int dev = 0, sms = 0, per_sm = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return fail(MSA_ERR_CUDA, "device query failed");
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kDecThreads, smem) != cudaSuccess ||
+            per_sm <= 0)
+            return fail(MSA_ERR_CUDA, "occupancy query failed");
+        // the largest cluster (1..8 CTAs per query, no more than the query's blocks
+        // need) with which the grid fits on the GPU in one wave
+        int64_t cs = ((int64_t)sms * per_sm) / num_queries;
+        const int64_t need = (cfg->max_blocks + 3) / 4;
+        cs = cs > need ? need : cs;
+        cs = cs > 8 ? 8 : (cs < 1 ? 1 : cs);
+        cudaLaunchConfig_t dc;
+        memset(&dc, 0, sizeof dc);
+        dc.gridDim = dim3((unsigned)(num_queries * cs));
+        dc.blockDim = dim3(kDecThreads);
+        dc.dynamicSmemBytes = (size_t)smem;
+        dc.stream = stream;
+        cudaLaunchAttribute dattr[2];
+        dattr[0].id = cudaLaunchAttributeClusterDimension;
+        dattr[0].val.clusterDim.x = (unsigned)cs;
+        dattr[0].val.clusterDim.y = 1;
+        dattr[0].val.clusterDim.z = 1;
+        int na = 1;
+        if (p.pdl) {
+            dattr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            dattr[1].val.programmaticStreamSerializationAllowed = 1;
+            na = 2;
+        }
+        dc.attrs = dattr;
+        dc.numAttrs = na;
+        void *dargs[] = {&p};
+        const cudaError_t de = cudaLaunchKernelExC(&dc, fn, dargs);
+        if (de != cudaSuccess)
+            return fail(MSA_ERR_CUDA, "decode kernel launch failed: %s", cudaGetErrorString(de));
+        return MSA_OK;
+    }
+#endif
     cudaLaunchAttribute sattr[1];
     if (p.pdl) {
         sattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -3,6 +3,20 @@
 
 #include "msa_producer.h"
 
+// Time limit of every bounded wait in the kernels (mbarrier waits), in
+// nanoseconds of %globaltimer.  A build-time knob: the starved test build (below)
+// sets a short one.
+#ifndef MSA_WAIT_LIMIT_NS
+#define MSA_WAIT_LIMIT_NS 2000000000ull
+#endif
+
+// MSA_STARVE (the starved test build only, never the product): the projection's
+// TMA warps and the query-run indexer's MMA thread issue nothing, so that every
+// wait on their barriers runs out; the tests check that each kernel then stops
+// (the projection without writing, the indexer scoring what it could not finish
+// NaN), reports the timeout and frees its tensor memory.  No copy or MMA is in
+// flight when the waits give up.
+
 // Records a detail message for msa_last_error_detail() on this thread.
 void msa_internal_set_detail(const char *msg);
 

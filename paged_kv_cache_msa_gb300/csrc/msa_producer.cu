@@ -33,7 +33,8 @@
 //     decoupled, so their memory and shuffle latencies overlap.
 //   * No wait on another CTA, flag or mbarrier exists, so nothing can spin.
 //     With programmatic dependent launch the kernel reads its constants and the
-//     first group's metadata before waiting for the previous kernel.
+//     first group's metadata before waiting for the previous kernel, and lets the
+//     next kernel start only after that wait.
 
 #include "msa_producer.h"
 #include "msa_internal.h"
@@ -56,6 +57,16 @@
 #define MSA_STAGES 2
 #endif
 
+// 1: under programmatic dependent launch the next kernel may start as soon as this
+// one begins; 0: only once this one has waited for its own predecessor.
+#ifndef MSA_PDL_EARLY_TRIGGER
+#define MSA_PDL_EARLY_TRIGGER 0
+#endif
+// Unroll factor of the loop over a token's head-row passes (1: not unrolled).
+#ifndef MSA_PASS_UNROLL
+#define MSA_PASS_UNROLL 2
+#endif
+
 // Tokens whose placement and rotary table are prepared together (one barrier each).
 #ifndef MSA_GROUP
 #define MSA_GROUP 8
@@ -67,6 +78,7 @@ constexpr int kMaxRotaryHalf = 64;       // rotary_dim / 2 <= head_dim / 2 <= 64
 constexpr int kMaxHeadScales = 256;      // per-head scale mode: 2*Hkv + Hik <= 256
 constexpr int kStages = MSA_STAGES;
 constexpr int kGroup = MSA_GROUP;        // tokens per metadata group (one barrier each)
+constexpr int kPassUnroll = MSA_PASS_UNROLL;
 constexpr int kMaxRowBytes = 96 * 1024;  // widest token row the shared-memory ring takes
 
 struct CacheArgs {
@@ -250,43 +262,294 @@ __device__ __forceinline__ TokenMeta place(const Params &p, long long ls, long l
 }
 
 // ---------------------------------------------------------------------------
-// the producer kernel
+// the per-token compute (shared by both kernels)
 // ---------------------------------------------------------------------------
 //
 // D   head_dim (64 or 128): a head row is L = D/16 lanes of 2 x 8 elements
-// NT  threads per CTA (a multiple of 32)
+// NT  compute threads per CTA (a multiple of 32)
+
+// Which 2 x 8 elements of a head row a lane holds, and its first head row.
+struct LaneGeom {
+    int q;           // lane position inside its head rows
+    int row0;        // first head row of this thread
+    int npass;       // passes over the token's head rows (uniform across the warp)
+    int aoff, boff;  // element offsets of piece A and piece B in the head row
+    bool pair;       // NeoX: piece B holds the rotate-half partners of piece A
+    bool rot_a, rot_b;  // GPT-J: piece A / B lies inside the rotary dims
+};
+
+template <int D, int NT>
+__device__ __forceinline__ LaneGeom lane_geom(const Params &p, int tid)
+{
+    constexpr int L = D / 16;
+    constexpr int RPP = NT / L;
+    LaneGeom g;
+    const int warp = tid >> 5;
+    g.q = tid % L;
+    g.row0 = tid / L;
+    const int warp_row0 = (warp * 32) / L;
+    g.npass = p.htot > warp_row0 ? (p.htot - warp_row0 + RPP - 1) / RPP : 0;
+    const int rd = p.rotary_dim;
+    const int half = rd / 2;
+    g.pair = g.rot_a = g.rot_b = false;
+    if (p.rope_style == MSA_ROPE_NEOX) {
+        if (16 * g.q < rd) {          // rotated: dims k and k + rd/2 (k = 8q .. 8q+7)
+            g.aoff = 8 * g.q;
+            g.boff = 8 * g.q + half;
+            g.pair = true;
+        } else {                      // pass-through dims [rd, D)
+            g.aoff = rd + 16 * (g.q - rd / 16);
+            g.boff = g.aoff + 8;
+        }
+    } else {                          // GPT-J: pairs (2k, 2k+1) inside each piece
+        g.aoff = 16 * g.q;
+        g.boff = g.aoff + 8;
+        g.rot_a = g.aoff < rd;
+        g.rot_b = g.boff < rd;
+    }
+    return g;
+}
+
+// Every head row of token t that this thread takes part in: load its two pieces
+// from the staged row at shared address srow, RMSNorm (all but V), RoPE, then the
+// compact Q / index-Q store or the cache encode and scatter.
+template <int D, int NT>
+__device__ __forceinline__ void token_rows(const Params &p, const LaneGeom &g, uint32_t srow,
+                                           const TokenMeta &meta, const float *cos_row,
+                                           const float *sin_row, const float (*s_w)[D], int64_t t)
+{
+    constexpr int L = D / 16;
+    constexpr int RPP = NT / L;
+    const int htot = p.htot;
+    const int e_k = p.hq, e_v = p.hq + p.hkv, e_iq = p.hq + 2 * p.hkv;
+    const int e_ik = e_iq + p.hiq;
+    const int aoff = g.aoff, boff = g.boff;
+    uint16_t *q_tok = p.q_out + (int64_t)t * p.hq * D;
+    uint16_t *iq_tok = p.idx_q_out + (int64_t)t * p.hiq * D;
+
+#pragma unroll kPassUnroll
+    for (int pass = 0; pass < g.npass; ++pass) {
+        const int hr = g.row0 + pass * RPP;
+        const bool active = hr < htot;
+
+        // y holds piece A in y[0..3] and piece B in y[4..7], as element pairs
+        float2 y[8];
+        if (active) {
+            const uint4 ra = lds128(srow + 2u * (uint32_t)(hr * D + aoff));
+            const uint4 rb = lds128(srow + 2u * (uint32_t)(hr * D + boff));
+            y[0] = unpack2(ra.x); y[1] = unpack2(ra.y);
+            y[2] = unpack2(ra.z); y[3] = unpack2(ra.w);
+            y[4] = unpack2(rb.x); y[5] = unpack2(rb.y);
+            y[6] = unpack2(rb.z); y[7] = unpack2(rb.w);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                y[j] = f2(0.0f);
+        }
+
+        float2 ss2 = __fmul2_rn(y[0], y[0]);
+#pragma unroll
+        for (int j = 1; j < 8; ++j)
+            ss2 = __ffma2_rn(y[j], y[j], ss2);
+        float ss = ss2.x + ss2.y;
+#pragma unroll
+        for (int o = 1; o < L; o <<= 1)
+            ss += __shfl_xor_sync(0xffffffffu, ss, o, L);
+        if (!active)
+            continue;
+
+        // section of this head row: 0 Q, 1 K, 2 V, 3 idx-Q, 4 idx-K
+        int sec, h;
+        if (hr < e_k) { sec = 0; h = hr; }
+        else if (hr < e_v) { sec = 1; h = hr - e_k; }
+        else if (hr < e_iq) { sec = 2; h = hr - e_v; }
+        else if (hr < e_ik) { sec = 3; h = hr - e_iq; }
+        else { sec = 4; h = hr - e_ik; }
+
+        if (sec != 2) {
+            const int widx = sec == 0 ? 0 : sec == 1 ? 1 : sec == 3 ? 2 : 3;
+            const float2 r2 = f2(rsqrtf(fmaf(ss, 1.0f / (float)D, p.rms_eps)));
+            {
+                const float4 w0 = *reinterpret_cast<const float4 *>(&s_w[widx][aoff]);
+                const float4 w1 = *reinterpret_cast<const float4 *>(&s_w[widx][aoff + 4]);
+                y[0] = __fmul2_rn(__fmul2_rn(y[0], r2), make_float2(w0.x, w0.y));
+                y[1] = __fmul2_rn(__fmul2_rn(y[1], r2), make_float2(w0.z, w0.w));
+                y[2] = __fmul2_rn(__fmul2_rn(y[2], r2), make_float2(w1.x, w1.y));
+                y[3] = __fmul2_rn(__fmul2_rn(y[3], r2), make_float2(w1.z, w1.w));
+            }
+            {
+                const float4 w0 = *reinterpret_cast<const float4 *>(&s_w[widx][boff]);
+                const float4 w1 = *reinterpret_cast<const float4 *>(&s_w[widx][boff + 4]);
+                y[4] = __fmul2_rn(__fmul2_rn(y[4], r2), make_float2(w0.x, w0.y));
+                y[5] = __fmul2_rn(__fmul2_rn(y[5], r2), make_float2(w0.z, w0.w));
+                y[6] = __fmul2_rn(__fmul2_rn(y[6], r2), make_float2(w1.x, w1.y));
+                y[7] = __fmul2_rn(__fmul2_rn(y[7], r2), make_float2(w1.z, w1.w));
+            }
+            if (g.pair) {
+                // u' = u c - v s, v' = v c + u s, with u in piece A and v in piece B;
+                // pair j of each piece is at frequencies 8q + 2j, 8q + 2j + 1
+                const float4 c0 = *reinterpret_cast<const float4 *>(cos_row);
+                const float4 c1 = *reinterpret_cast<const float4 *>(cos_row + 4);
+                const float4 s0 = *reinterpret_cast<const float4 *>(sin_row);
+                const float4 s1 = *reinterpret_cast<const float4 *>(sin_row + 4);
+                const float2 cs[4] = {make_float2(c0.x, c0.y), make_float2(c0.z, c0.w),
+                                      make_float2(c1.x, c1.y), make_float2(c1.z, c1.w)};
+                const float2 sn[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w),
+                                      make_float2(s1.x, s1.y), make_float2(s1.z, s1.w)};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 u = y[j], v = y[4 + j];
+                    y[j] = __ffma2_rn(v, make_float2(-sn[j].x, -sn[j].y), __fmul2_rn(u, cs[j]));
+                    y[4 + j] = __ffma2_rn(u, sn[j], __fmul2_rn(v, cs[j]));
+                }
+            } else if (g.rot_a || g.rot_b) {
+                // GPT-J: (y[2m], y[2m+1]) at frequency 8q + m (piece A), 8q + 4 + m (B)
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    if (m < 4 ? g.rot_a : g.rot_b) {
+                        const float c = cos_row[m], sn = sin_row[m];
+                        const float u = y[m].x, v = y[m].y;
+                        y[m] = make_float2(u * c - v * sn, v * c + u * sn);
+                    }
+                }
+            }
+        }
+
+        if (sec == 0 || sec == 3) {
+            uint16_t *dst = sec == 0 ? q_tok + h * D : iq_tok + h * D;
+#ifdef MSA_CHECKED
+            const void *lo = sec == 0 ? (const void *)p.q_out : (const void *)p.idx_q_out;
+            const void *hi = p.out_hi[sec == 0 ? 0 : 1];
+#endif
+            MSA_GUARD(dst + aoff, 16, lo, hi) st_v4(dst + aoff, pack_bf16x8(y));
+            MSA_GUARD(dst + boff, 16, lo, hi) st_v4(dst + boff, pack_bf16x8(y + 4));
+        } else {
+            const int ci = sec == 1 ? 0 : sec == 2 ? 1 : 2;
+            if (!((meta.valid >> ci) & 1))
+                continue;
+            const CacheArgs &cc = p.cache[ci];
+            const int64_t e = meta.page * cc.stride_page + (int64_t)h * cc.stride_head +
+                              (int64_t)meta.off * cc.stride_token;
+            if (cc.fp8) {
+                const int si = p.scale_mode == MSA_SCALE_PER_HEAD
+                                   ? (ci == 0 ? h : ci == 1 ? p.hkv + h : 2 * p.hkv + h)
+                                   : ci;
+                const float2 inv = f2(__frcp_rn(__ldg(p.scales + si)));
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    y[j] = __fmul2_rn(y[j], inv);
+                uint8_t *dst = cc.data + e;
+                MSA_GUARD(dst + aoff, 8, cc.data, p.cache_hi[ci])
+                st_v2(dst + aoff, pack_e4m3x4(y[0], y[1]), pack_e4m3x4(y[2], y[3]));
+                MSA_GUARD(dst + boff, 8, cc.data, p.cache_hi[ci])
+                st_v2(dst + boff, pack_e4m3x4(y[4], y[5]), pack_e4m3x4(y[6], y[7]));
+            } else {
+                uint16_t *dst = reinterpret_cast<uint16_t *>(cc.data) + e;
+                MSA_GUARD(dst + aoff, 16, cc.data, p.cache_hi[ci])
+                st_v4(dst + aoff, pack_bf16x8(y));
+                MSA_GUARD(dst + boff, 16, cc.data, p.cache_hi[ci])
+                st_v4(dst + boff, pack_bf16x8(y + 4));
+            }
+        }
+    }
+}
+
+// The per-token metadata pipeline, shared by both kernels.  Tokens are taken in
+// groups of kGroup; the placement and rotary table of group g + 1 are computed at
+// the end of group g into the other half of a double-buffered shared table.
+// Thread j < kGroup owns token j of every group: the slot and page-table entry of
+// the group whose metadata is computed next (loaded a group earlier), and the slot
+// of the group after that.  Table entry e = tid + m*NT is (token e / half,
+// frequency e % half); its position is loaded a group early.
+template <int NT>
+struct MetaPipe {
+    static constexpr int ME = kGroup * kMaxRotaryHalf / NT;  // table entries per thread
+    long long ls_n = -1, pte_n = -1, ls_nn = -1;
+    int pos_n[ME];
+
+    __device__ __forceinline__ long long load_slot(const Params &p, int64_t t0, int64_t G,
+                                                   int64_t ntok, int64_t i) const
+    {
+        return i < ntok ? __ldg(p.slots + t0 + i * G) : -1;
+    }
+    __device__ __forceinline__ void load_positions(const Params &p, int tid, int64_t t0, int64_t G,
+                                                   int64_t ntok, int64_t gbase)
+    {
+        const int half = p.rotary_dim / 2;
+#pragma unroll
+        for (int m = 0; m < ME; ++m) {
+            const int e = tid + m * NT;
+            const int64_t i = gbase + (half > 0 ? e / half : 0);
+            pos_n[m] = (half > 0 && e < kGroup * half && i < ntok) ? __ldg(p.positions + t0 + i * G) : 0;
+        }
+    }
+    __device__ __forceinline__ void start(const Params &p, int tid, int64_t t0, int64_t G, int64_t ntok)
+    {
+        if (tid < kGroup) {
+            ls_n = load_slot(p, t0, G, ntok, tid);
+            pte_n = table_entry(p, ls_n);
+            ls_nn = load_slot(p, t0, G, ntok, kGroup + tid);
+        }
+        load_positions(p, tid, t0, G, ntok, 0);
+    }
+    __device__ __forceinline__ void compute(const Params &p, int tid, int64_t ntok, int64_t gbase,
+                                            TokenMeta (*s_meta)[kGroup],
+                                            float (*s_cs)[kGroup][2][kMaxRotaryHalf], int b)
+    {
+        const int half = p.rotary_dim / 2;
+        if (tid < kGroup)
+            s_meta[b][tid] = place(p, ls_n, pte_n);
+#pragma unroll
+        for (int m = 0; m < ME; ++m) {
+            const int e = tid + m * NT;
+            if (half > 0 && e < kGroup * half && gbase + e / half < ntok) {
+                const int j = e / half, k = e % half;
+                float sn, c;
+                sincosf((float)pos_n[m] * p.inv_freq[k], &sn, &c);
+                s_cs[b][j][0][k] = c;
+                s_cs[b][j][1][k] = sn;
+            }
+        }
+    }
+    __device__ __forceinline__ void prefetch(const Params &p, int tid, int64_t t0, int64_t G,
+                                             int64_t ntok, int64_t gbase)
+    {
+        if (tid < kGroup) {
+            ls_n = ls_nn;
+            pte_n = table_entry(p, ls_n);
+            ls_nn = load_slot(p, t0, G, ntok, gbase + kGroup + tid);
+        }
+        load_positions(p, tid, t0, G, ntok, gbase);
+    }
+};
+
+// ---------------------------------------------------------------------------
+// the producer kernel, rows staged by the compute threads (cp.async)
+// ---------------------------------------------------------------------------
 //
 // A CTA takes the tokens blockIdx.x + i * gridDim.x, i = 0, 1, ...  in groups of
-// kGroup.  The metadata of group g + 1 is computed at the end of group g into the
-// other half of a double-buffered shared table and published by group g + 1's
-// single barrier.
+// kGroup.  Each thread copies the 16-byte pieces of the rows that it later reads
+// into a kStages-deep shared-memory ring, one token ahead.
 template <int D, int NT>
 __global__ void __launch_bounds__(NT, MSA_MIN_CTAS_PER_SM * 256 / NT)
 msa_producer_kernel(const __grid_constant__ Params p)
 {
     constexpr int L = D / 16;
     constexpr int RPP = NT / L;                       // head rows per pass
-    constexpr int ME = kGroup * kMaxRotaryHalf / NT;  // table entries per thread
     static_assert(NT % 32 == 0 && 32 % L == 0, "a head row must sit inside one warp");
-    static_assert(kGroup <= NT && ME * NT == kGroup * kMaxRotaryHalf, "group geometry");
+    static_assert(kGroup <= NT && MetaPipe<NT>::ME * NT == kGroup * kMaxRotaryHalf, "group geometry");
 
     extern __shared__ __align__(128) uint8_t s_rows[];  // kStages x row_bytes
     __shared__ __align__(16) float s_w[4][D];
     __shared__ __align__(16) float s_cs[2][kGroup][2][kMaxRotaryHalf];  // [buf][token][cos|sin][k]
     __shared__ __align__(16) TokenMeta s_meta[2][kGroup];
 
-    // The next kernel in the stream may be scheduled right away: it still waits for
-    // this grid to complete before touching what this grid writes.
+#if MSA_PDL_EARLY_TRIGGER
     asm volatile("griddepcontrol.launch_dependents;" :::);
-
+#endif
     const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int q = tid % L;          // lane position inside its head rows
-    const int row0 = tid / L;       // first head row of this thread
+    const LaneGeom g = lane_geom<D, NT>(p, tid);
     const int htot = p.htot;
-    // passes this warp makes (uniform across the warp, so shuffles stay converged)
-    const int warp_row0 = (warp * 32) / L;
-    const int npass = htot > warp_row0 ? (htot - warp_row0 + RPP - 1) / RPP : 0;
 
     // constants (may be read before waiting on the previous kernel): loaded into
     // registers now, stored to shared memory once the other loads are in flight
@@ -307,80 +570,15 @@ msa_producer_kernel(const __grid_constant__ Params p)
     const int64_t ntok = (T - t0 + G - 1) / G;  // tokens of this CTA
     auto token = [&](int64_t i) { return t0 + i * G; };
 
-    // ---- lane geometry: which 2 x 8 elements of a head row this lane holds ----
-    const int rd = p.rotary_dim;
-    const int half = rd / 2;
-    const bool neox = p.rope_style == MSA_ROPE_NEOX;
-    int aoff, boff;
-    bool pair = false, rot_a = false, rot_b = false;
-    if (neox) {
-        if (16 * q < rd) {            // rotated: dims k and k + rd/2 (k = 8q .. 8q+7)
-            aoff = 8 * q;
-            boff = 8 * q + half;
-            pair = true;
-        } else {                      // pass-through dims [rd, D)
-            aoff = rd + 16 * (q - rd / 16);
-            boff = aoff + 8;
-        }
-    } else {                          // GPT-J: pairs (2k, 2k+1) inside each piece
-        aoff = 16 * q;
-        boff = aoff + 8;
-        rot_a = aoff < rd;
-        rot_b = boff < rd;
-    }
-
-    const int e_k = p.hq, e_v = p.hq + p.hkv, e_iq = p.hq + 2 * p.hkv;
-    const int e_ik = e_iq + p.hiq;
-
     const uint32_t rows_base = smem_addr(s_rows);
     auto stage_row = [&](int64_t tok, int stage) {
         const uint16_t *src = p.qkv + tok * p.row_stride;
         const uint32_t dst = rows_base + (uint32_t)stage * (uint32_t)p.row_bytes;
-        for (int hr = row0; hr < htot; hr += RPP) {
+        for (int hr = g.row0; hr < htot; hr += RPP) {
             const int e = hr * D;
-            cp_async16(dst + 2u * (uint32_t)(e + aoff), src + e + aoff);
-            cp_async16(dst + 2u * (uint32_t)(e + boff), src + e + boff);
+            cp_async16(dst + 2u * (uint32_t)(e + g.aoff), src + e + g.aoff);
+            cp_async16(dst + 2u * (uint32_t)(e + g.boff), src + e + g.boff);
         }
-    };
-
-    // ---- metadata pipeline ----
-    // Thread j < kGroup owns token j of every group: the slot and page-table entry
-    // of the group whose metadata is computed next (loaded a group earlier), and
-    // the slot of the group after that.  Table entry e = tid + m*NT is
-    // (token e / half, frequency e % half); its position is loaded a group early.
-    long long ls_n = -1, pte_n = -1, ls_nn = -1;
-    int pos_n[ME];
-    auto load_slot = [&](int64_t i) -> long long { return i < ntok ? __ldg(p.slots + token(i)) : -1; };
-    auto load_positions = [&](int64_t gbase) {
-#pragma unroll
-        for (int m = 0; m < ME; ++m) {
-            const int e = tid + m * NT;
-            const int64_t i = gbase + (half > 0 ? e / half : 0);
-            pos_n[m] = (half > 0 && e < kGroup * half && i < ntok) ? __ldg(p.positions + token(i)) : 0;
-        }
-    };
-    auto compute_meta = [&](int64_t gbase, int b) {
-        if (tid < kGroup)
-            s_meta[b][tid] = place(p, ls_n, pte_n);
-#pragma unroll
-        for (int m = 0; m < ME; ++m) {
-            const int e = tid + m * NT;
-            if (half > 0 && e < kGroup * half && gbase + e / half < ntok) {
-                const int j = e / half, k = e % half;
-                float s, c;
-                sincosf((float)pos_n[m] * p.inv_freq[k], &s, &c);
-                s_cs[b][j][0][k] = c;
-                s_cs[b][j][1][k] = s;
-            }
-        }
-    };
-    auto prefetch_meta = [&](int64_t gbase) {  // for the group starting at gbase
-        if (tid < kGroup) {
-            ls_n = ls_nn;
-            pte_n = table_entry(p, ls_n);
-            ls_nn = load_slot(gbase + kGroup + tid);
-        }
-        load_positions(gbase);
     };
     auto stage_first_rows = [&]() {
 #pragma unroll
@@ -391,22 +589,17 @@ msa_producer_kernel(const __grid_constant__ Params p)
         }
     };
 
+    MetaPipe<NT> meta;
     // ---- prologue ----
     // Under programmatic dependent launch the first group's metadata is computed
-    // before waiting on the previous kernel (positions, slots and the page table
-    // must not be written by the kernel launched just before this one) and the rows
-    // are read after it.  Otherwise the rows are requested first, so that their
-    // latency overlaps the metadata's dependent loads.
+    // before waiting on the previous kernel and the rows are read after it.
+    // Otherwise the rows are requested first, so that their latency overlaps the
+    // metadata's dependent loads.
     if (!p.pdl)
         stage_first_rows();
-    if (tid < kGroup) {
-        ls_n = load_slot(tid);
-        pte_n = table_entry(p, ls_n);
-        ls_nn = load_slot(kGroup + tid);
-    }
-    load_positions(0);
-    compute_meta(0, 0);
-    prefetch_meta(kGroup);
+    meta.start(p, tid, t0, G, ntok);
+    meta.compute(p, tid, ntok, 0, s_meta, s_cs, 0);
+    meta.prefetch(p, tid, t0, G, ntok, kGroup);
 #pragma unroll
     for (int m = 0; m < NW; ++m) {
         const int i = tid + m * NT;
@@ -415,6 +608,13 @@ msa_producer_kernel(const __grid_constant__ Params p)
     }
 
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // The next kernel in the stream may start once every CTA has passed this point
+    // (or exited).  Signalling only after the wait means that every kernel enqueued
+    // before this one has completed by then, so a dependent that reads its inputs
+    // before its own wait sees the writes of all of them (this kernel's excepted).
+#if !MSA_PDL_EARLY_TRIGGER
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+#endif
     if (p.pdl)
         stage_first_rows();
 
@@ -425,153 +625,21 @@ msa_producer_kernel(const __grid_constant__ Params p)
 
         const int64_t gend = gn < ntok ? gn : ntok;
         for (int64_t i = g0; i < gend; ++i) {
-            const int64_t t = token(i);
             const int jt = (int)(i - g0);
-
-            // rows of the token kStages-1 ahead
-            {
+            {   // rows of the token kStages-1 ahead
                 const int64_t ip = i + kStages - 1;
                 if (ip < ntok)
                     stage_row(token(ip), (int)(ip % kStages));
                 cp_async_commit();
             }
-            const TokenMeta meta = s_meta[buf][jt];
-            const float *cos_row = &s_cs[buf][jt][0][8 * q];
-            const float *sin_row = &s_cs[buf][jt][1][8 * q];
-
-            cp_async_wait<kStages - 1>();  // this thread's pieces of token t have landed
+            cp_async_wait<kStages - 1>();  // this thread's pieces of token i have landed
             const uint32_t srow = rows_base + (uint32_t)(i % kStages) * (uint32_t)p.row_bytes;
-            uint16_t *q_tok = p.q_out + (int64_t)t * p.hq * D;
-            uint16_t *iq_tok = p.idx_q_out + (int64_t)t * p.hiq * D;
-
-            for (int pass = 0; pass < npass; ++pass) {
-                const int hr = row0 + pass * RPP;
-                const bool active = hr < htot;
-
-                // y holds piece A in y[0..3] and piece B in y[4..7], as element pairs
-                float2 y[8];
-                if (active) {
-                    const uint4 ra = lds128(srow + 2u * (uint32_t)(hr * D + aoff));
-                    const uint4 rb = lds128(srow + 2u * (uint32_t)(hr * D + boff));
-                    y[0] = unpack2(ra.x); y[1] = unpack2(ra.y);
-                    y[2] = unpack2(ra.z); y[3] = unpack2(ra.w);
-                    y[4] = unpack2(rb.x); y[5] = unpack2(rb.y);
-                    y[6] = unpack2(rb.z); y[7] = unpack2(rb.w);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        y[j] = f2(0.0f);
-                }
-
-                float2 ss2 = __fmul2_rn(y[0], y[0]);
-#pragma unroll
-                for (int j = 1; j < 8; ++j)
-                    ss2 = __ffma2_rn(y[j], y[j], ss2);
-                float ss = ss2.x + ss2.y;
-#pragma unroll
-                for (int o = 1; o < L; o <<= 1)
-                    ss += __shfl_xor_sync(0xffffffffu, ss, o, L);
-                if (!active)
-                    continue;
-
-                // section of this head row: 0 Q, 1 K, 2 V, 3 idx-Q, 4 idx-K
-                int sec, h;
-                if (hr < e_k) { sec = 0; h = hr; }
-                else if (hr < e_v) { sec = 1; h = hr - e_k; }
-                else if (hr < e_iq) { sec = 2; h = hr - e_v; }
-                else if (hr < e_ik) { sec = 3; h = hr - e_iq; }
-                else { sec = 4; h = hr - e_ik; }
-
-                if (sec != 2) {
-                    const int widx = sec == 0 ? 0 : sec == 1 ? 1 : sec == 3 ? 2 : 3;
-                    const float2 r2 = f2(rsqrtf(fmaf(ss, 1.0f / (float)D, p.rms_eps)));
-                    {
-                        const float4 w0 = *reinterpret_cast<const float4 *>(&s_w[widx][aoff]);
-                        const float4 w1 = *reinterpret_cast<const float4 *>(&s_w[widx][aoff + 4]);
-                        y[0] = __fmul2_rn(__fmul2_rn(y[0], r2), make_float2(w0.x, w0.y));
-                        y[1] = __fmul2_rn(__fmul2_rn(y[1], r2), make_float2(w0.z, w0.w));
-                        y[2] = __fmul2_rn(__fmul2_rn(y[2], r2), make_float2(w1.x, w1.y));
-                        y[3] = __fmul2_rn(__fmul2_rn(y[3], r2), make_float2(w1.z, w1.w));
-                    }
-                    {
-                        const float4 w0 = *reinterpret_cast<const float4 *>(&s_w[widx][boff]);
-                        const float4 w1 = *reinterpret_cast<const float4 *>(&s_w[widx][boff + 4]);
-                        y[4] = __fmul2_rn(__fmul2_rn(y[4], r2), make_float2(w0.x, w0.y));
-                        y[5] = __fmul2_rn(__fmul2_rn(y[5], r2), make_float2(w0.z, w0.w));
-                        y[6] = __fmul2_rn(__fmul2_rn(y[6], r2), make_float2(w1.x, w1.y));
-                        y[7] = __fmul2_rn(__fmul2_rn(y[7], r2), make_float2(w1.z, w1.w));
-                    }
-                    if (pair) {
-                        // u' = u c - v s, v' = v c + u s, with u in piece A and v in piece B;
-                        // pair j of each piece is at frequencies 8q + 2j, 8q + 2j + 1
-                        const float4 c0 = *reinterpret_cast<const float4 *>(cos_row);
-                        const float4 c1 = *reinterpret_cast<const float4 *>(cos_row + 4);
-                        const float4 s0 = *reinterpret_cast<const float4 *>(sin_row);
-                        const float4 s1 = *reinterpret_cast<const float4 *>(sin_row + 4);
-                        const float2 cs[4] = {make_float2(c0.x, c0.y), make_float2(c0.z, c0.w),
-                                              make_float2(c1.x, c1.y), make_float2(c1.z, c1.w)};
-                        const float2 sn[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w),
-                                              make_float2(s1.x, s1.y), make_float2(s1.z, s1.w)};
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const float2 u = y[j], v = y[4 + j];
-                            y[j] = __ffma2_rn(v, make_float2(-sn[j].x, -sn[j].y), __fmul2_rn(u, cs[j]));
-                            y[4 + j] = __ffma2_rn(u, sn[j], __fmul2_rn(v, cs[j]));
-                        }
-                    } else if (rot_a || rot_b) {
-                        // GPT-J: (y[2m], y[2m+1]) at frequency 8q + m (piece A), 8q + 4 + m (B)
-#pragma unroll
-                        for (int m = 0; m < 8; ++m) {
-                            if (m < 4 ? rot_a : rot_b) {
-                                const float c = cos_row[m], sn = sin_row[m];
-                                const float u = y[m].x, v = y[m].y;
-                                y[m] = make_float2(u * c - v * sn, v * c + u * sn);
-                            }
-                        }
-                    }
-                }
-
-                if (sec == 0 || sec == 3) {
-                    uint16_t *dst = sec == 0 ? q_tok + h * D : iq_tok + h * D;
-#ifdef MSA_CHECKED
-                    const void *lo = sec == 0 ? (const void *)p.q_out : (const void *)p.idx_q_out;
-                    const void *hi = p.out_hi[sec == 0 ? 0 : 1];
-#endif
-                    MSA_GUARD(dst + aoff, 16, lo, hi) st_v4(dst + aoff, pack_bf16x8(y));
-                    MSA_GUARD(dst + boff, 16, lo, hi) st_v4(dst + boff, pack_bf16x8(y + 4));
-                } else {
-                    const int ci = sec == 1 ? 0 : sec == 2 ? 1 : 2;
-                    if (!((meta.valid >> ci) & 1))
-                        continue;
-                    const CacheArgs &cc = p.cache[ci];
-                    const int64_t e = meta.page * cc.stride_page + (int64_t)h * cc.stride_head +
-                                      (int64_t)meta.off * cc.stride_token;
-                    if (cc.fp8) {
-                        const int si = p.scale_mode == MSA_SCALE_PER_HEAD
-                                           ? (ci == 0 ? h : ci == 1 ? p.hkv + h : 2 * p.hkv + h)
-                                           : ci;
-                        const float2 inv = f2(__frcp_rn(__ldg(p.scales + si)));
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            y[j] = __fmul2_rn(y[j], inv);
-                        uint8_t *dst = cc.data + e;
-                        MSA_GUARD(dst + aoff, 8, cc.data, p.cache_hi[ci])
-                        st_v2(dst + aoff, pack_e4m3x4(y[0], y[1]), pack_e4m3x4(y[2], y[3]));
-                        MSA_GUARD(dst + boff, 8, cc.data, p.cache_hi[ci])
-                        st_v2(dst + boff, pack_e4m3x4(y[4], y[5]), pack_e4m3x4(y[6], y[7]));
-                    } else {
-                        uint16_t *dst = reinterpret_cast<uint16_t *>(cc.data) + e;
-                        MSA_GUARD(dst + aoff, 16, cc.data, p.cache_hi[ci])
-                        st_v4(dst + aoff, pack_bf16x8(y));
-                        MSA_GUARD(dst + boff, 16, cc.data, p.cache_hi[ci])
-                        st_v4(dst + boff, pack_bf16x8(y + 4));
-                    }
-                }
-            }
+            token_rows<D, NT>(p, g, srow, s_meta[buf][jt], &s_cs[buf][jt][0][8 * g.q],
+                              &s_cs[buf][jt][1][8 * g.q], s_w, token(i));
         }
         if (gn < ntok) {  // the next group's metadata, into the other buffer
-            compute_meta(gn, buf ^ 1);
-            prefetch_meta(gn + kGroup);
+            meta.compute(p, tid, ntok, gn, s_meta, s_cs, buf ^ 1);
+            meta.prefetch(p, tid, t0, G, ntok, gn + kGroup);
         }
     }
     cp_async_wait<0>();
@@ -826,7 +894,8 @@ msa_status launch_shape(const msa_producer_cfg *cfg, int64_t T, int32_t flags, V
                         int *grid, int *smem)
 {
     *v = pick_variant(cfg);
-    *smem = (int)(kStages * htot_of(cfg) * cfg->head_dim * 2);
+    const int64_t row_bytes = htot_of(cfg) * cfg->head_dim * 2;
+    *smem = (int)(kStages * row_bytes);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return fail(MSA_ERR_CUDA, "cudaGetDevice failed");
@@ -853,9 +922,9 @@ msa_status launch_shape(const msa_producer_cfg *cfg, int64_t T, int32_t flags, V
         di.sms = sms;
     }
     if (*smem > max_dyn)
-        return fail(MSA_ERR_UNSUPPORTED, "a row of %d bytes does not fit the shared-memory ring",
-                    *smem / kStages);
-    if (!(flags & MSA_LAUNCH_PERSISTENT)) {
+        return fail(MSA_ERR_UNSUPPORTED, "a row of %lld bytes does not fit the shared-memory ring",
+                    (long long)row_bytes);
+    if (!(flags & MSA_LAUNCH_PERSISTENT)) {   // one token per CTA
         *grid = (int)(T < 0x7fffffff ? T : 0x7fffffff);
         return MSA_OK;
     }

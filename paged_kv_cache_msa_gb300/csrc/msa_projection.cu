@@ -86,7 +86,7 @@ constexpr uint32_t kStageBytes = kTileABytes + kTileBBytes;  // per CTA
 constexpr int kDynSmem = kStages * kStageBytes + 1024;        // + alignment slack for the ring
 constexpr uint32_t kTmemCols = 2 * kBN;
 constexpr int kMaxRotaryHalf = 64;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+constexpr unsigned long long kWaitLimitNs = MSA_WAIT_LIMIT_NS;
 
 // tcgen05 instruction descriptors: fp32 accumulator (bits 4-5 = 1), A and B formats
 // at bits 7-9 and 10-12 (kind::f16: 1 = bf16; kind::f8f6f4: 0 = E4M3), both K-major
@@ -999,7 +999,11 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
 
     if (warp == 0) {
         // ---------------- TMA producer (both CTAs) ----------------
+#ifdef MSA_STARVE
+        if (false) {   // the starved test build: no copy is ever issued
+#else
         if (lane == 0) {
+#endif
             uint32_t stage = 0, phase = 0;
             for (int64_t tile = cluster_id; tile < num_tiles && ok; tile += num_clusters) {
                 int m, n;
@@ -1192,6 +1196,7 @@ msa_projection_splitk_kernel(const __grid_constant__ CUtensorMap tmap_x,
     __shared__ __align__(8) uint64_t bar_tfull;
     __shared__ __align__(8) uint64_t bar_drain;
     __shared__ uint32_t s_tmem;
+    __shared__ uint32_t s_fail;   // a wait of this CTA ran out: its partial sum is not valid
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1210,6 +1215,7 @@ msa_projection_splitk_kernel(const __grid_constant__ CUtensorMap tmap_x,
         }
         mbar_init(smem_u32(&bar_tfull), 1);
         mbar_init(smem_u32(&bar_drain), 1);
+        s_fail = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -1226,7 +1232,11 @@ msa_projection_splitk_kernel(const __grid_constant__ CUtensorMap tmap_x,
     bool ok = true;
 
     if (warp == 0) {
+#ifdef MSA_STARVE
+        if (false) {   // the starved test build: no copy is ever issued
+#else
         if (lane == 0) {   // TMA: this CTA's K blocks of the hidden tile and the weight tile
+#endif
             uint32_t stage = 0, phase = 0;
             for (int kb = kb0; kb < kb0 + p.prefetch && kb < kb1; ++kb)
                 tma_prefetch_l2(&tmap_w, kb * kBKElems, n_tile * kBN);
@@ -1326,9 +1336,27 @@ msa_projection_splitk_kernel(const __grid_constant__ CUtensorMap tmap_x,
             }
         }
     }
+    // A wait that ran out anywhere in the cluster (a copy, an MMA or the accumulator
+    // that never completed) leaves some partial sum invalid -- the MMA thread still
+    // commits the accumulator barrier after a timeout, so the epilogue warps cannot
+    // see it from their own wait -- and then no CTA may run the epilogue: each CTA
+    // flags its failure before the cluster barrier, and CTA 0 reads every flag.
+    if (!ok)
+        *(volatile uint32_t *)&s_fail = 1u;
     tc_fence_before();
-    cluster_sync();   // every CTA's partial sums are in place
-    if (rank == 0 && warp >= 2 && ok) {
+    cluster_sync();   // every CTA's partial sums (and failure flags) are in place
+    bool all_ok = ok;
+    if (rank == 0 && warp >= 2) {
+        for (int r = 0; r < S; ++r) {
+            uint32_t f;
+            asm volatile("ld.shared::cluster.u32 %0, [%1];"
+                         : "=r"(f)
+                         : "r"(map_to_rank(smem_u32(&s_fail), (uint32_t)r))
+                         : "memory");
+            all_ok = all_ok && f == 0u;
+        }
+    }
+    if (rank == 0 && warp >= 2 && all_ok) {
         const int quarter = warp & 3, hgroup = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;
         tc_fence_after();

@@ -337,3 +337,4 @@ def test_pdl_chain_reads_metadata_written_launches_back():
                 assert e4m3_ulp_distance(pools_d[name][m], pools_o[name][m]).max(initial=0) <= 1
             else:
                 compare_bf16(pools_d[name][m].view(np.uint16), pools_o[name][m].view(np.uint16), name)
+
