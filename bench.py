@@ -329,10 +329,11 @@ def decode_step_timing(replays: int, big: bool, pdl: bool):
         e1.synchronize()
     us_step = 1e3 * e0.elapsed_time(e1) / replays
     tokens = layers[0].w.num_tokens
+    nodes = graph_kernel_nodes(lambda: [dw.run(flags, stream=s) for dw in layers], s)
     del g, layers
     torch.cuda.empty_cache()
     return {"us_per_step": us_step, "us_per_layer": us_step / 60, "layers": 60,
-            "tokens_per_layer": tokens, "launches_per_step": 60,
+            "tokens_per_layer": tokens, "launches_per_step": 60, "kernel_nodes_in_graph": nodes,
             "shapes": "big" if big else "tiny", "pdl": pdl, "replays": replays}
 
 
@@ -360,6 +361,34 @@ def empty_graph_floor(nodes: int = 60, replays: int = 1000):
     us = 1e3 * e0.elapsed_time(e1) / replays
     return {"nodes": nodes, "us_per_graph": us, "us_per_node": us / nodes,
             "what": "a graph of 4-byte fill kernels, the cost of a launch inside a graph"}
+
+
+def graph_kernel_nodes(fn, stream):
+    """Kernel nodes of a CUDA graph captured from fn() on `stream`: the number of
+    kernels fn launches (counted through the driver's graph API), or None."""
+    import ctypes
+    import torch
+    try:
+        g = torch.cuda.CUDAGraph(keep_graph=True)
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        h = ctypes.c_void_p(g.raw_cuda_graph())
+        cu = ctypes.CDLL("libcuda.so.1")
+        n = ctypes.c_size_t(0)
+        if cu.cuGraphGetNodes(h, None, ctypes.byref(n)) != 0:
+            return None
+        nodes = (ctypes.c_void_p * max(1, n.value))()
+        if cu.cuGraphGetNodes(h, nodes, ctypes.byref(n)) != 0:
+            return None
+        kernels, t = 0, ctypes.c_int(-1)
+        for i in range(n.value):
+            if cu.cuGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(t)) == 0 and t.value == 0:
+                kernels += 1   # CU_GRAPH_NODE_TYPE_KERNEL
+        del g
+        return kernels
+    except Exception as e:   # context only
+        log(f"[bench] kernel count unavailable: {type(e).__name__}: {e}"[:160])
+        return None
 
 
 def legacy_write_path_timing(replays: int = 200, layers: int = 60):
@@ -408,21 +437,7 @@ def legacy_write_path_timing(replays: int = 200, layers: int = 60):
         for item in stack:
             layer(*item)
         s.synchronize()
-        kernels = None
-        try:
-            # kernels of one layer: the device-side kernel records, else the host-side
-            # launch calls of the CUDA runtime
-            from torch.profiler import ProfilerActivity, profile
-            with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
-                layer(*stack[0])
-                s.synchronize()
-            ev = list(prof.events())
-            dev = [e for e in ev if "CUDA" in str(getattr(e, "device_type", ""))
-                   and not e.name.startswith(("Memcpy", "Memset", "cuda"))]
-            api = [e for e in ev if e.name.startswith(("cudaLaunchKernel", "cuLaunchKernel"))]
-            kernels = len(dev) if dev else len(api)
-        except Exception as e:   # the profiler is context only
-            log(f"[bench] kernel count unavailable: {type(e).__name__}: {e}"[:160])
+        kernels = graph_kernel_nodes(lambda: layer(*stack[0]), s)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
             for item in stack:
@@ -472,9 +487,9 @@ def graph_launch_us(dw, flags, launches: int, replays: int) -> float:
 
 def indexer_timing(replays: int = 200, calls: int = 20):
     """The indexer of the decode-batch-64 layer (64 queries, contexts U{1..9216},
-    8 index heads of dim 128, fp8 index-K): one call = one kernel (a cluster of CTAs
-    per query, top-k in the same kernel); `calls` back-to-back calls captured in a
-    graph, with programmatic dependent launch (and, for comparison, without)."""
+    8 index heads of dim 128, fp8 index-K): one call = score kernel + top-k kernel;
+    `calls` back-to-back calls captured in a graph, with programmatic dependent
+    launch of the score kernel (and, for comparison, without)."""
     import torch
     from paged_kv_cache_msa_gb300 import binding as B
     from paged_kv_cache_msa_gb300 import workloads as wl
@@ -507,7 +522,7 @@ def indexer_timing(replays: int = 200, calls: int = 20):
     peak, _ = peaks()
     return {"workload": "decode batch 64, contexts U{1..9216}, 8 index heads x 128, fp8 index-K, "
                         "top-16 of 128-token blocks",
-            "us_per_call": us, "us_per_call_without_pdl": us_plain, "launches_per_call": 1,
+            "us_per_call": us, "us_per_call_without_pdl": us_plain, "launches_per_call": 2,
             "algorithmic_bytes": alg,
             "gbs": alg / (us * 1e-6) / 1e9, "frac_of_peak": alg / (us * 1e-6) / 1e9 / peak,
             "index_k_tokens_scanned": int(w.kv_len.sum())}
@@ -557,7 +572,7 @@ def decode_layer_timing(layers: int = 60, replays: int = 50):
         out[name] = {"us_per_step": us, "us_per_layer": us / layers}
     return {"workload": f"decode batch 64, big shapes, contexts U{{1..9216}}: producer + indexer "
                         f"(top-16 of 128-token blocks) per layer, {layers} layers in one CUDA graph",
-            "launches_per_layer": 2, **out}
+            "launches_per_layer": 3, **out}
 
 
 def indexer_prefill_timing(reps: int = 5, num_seqs: int = 8):

@@ -78,18 +78,17 @@ typedef enum { MSA_SCALE_PER_TENSOR = 0, MSA_SCALE_PER_HEAD = 1 } msa_scale_mode
 #define MSA_LAUNCH_PERSISTENT 1   /* grid of at most (SMs x resident CTAs) CTAs that
                                      stride over the tokens; otherwise one CTA per token */
 #define MSA_LAUNCH_PDL 2          /* programmatic dependent launch: the kernel may start
-                                     while the kernel enqueued just before it on the stream
-                                     (call it P) is still running.  It reads qkv and writes
-                                     anything only after waiting for P; it reads the norm
-                                     weights, positions, slot mapping and page table before
-                                     that wait, so P must not write those.  Every kernel of
-                                     this library lets its dependents start only after its
-                                     own wait, so when P is one of them, or any kernel that
-                                     does the same or was launched without this attribute,
-                                     all kernels enqueued before P have completed by then
-                                     and may write those arrays (stage them earlier in the
-                                     step).  A P that lets its dependents start before its
-                                     own wait extends the rule to the kernels before it. */
+                                     before the kernels enqueued ahead of it on the stream
+                                     have completed.  It reads qkv and writes anything only
+                                     after waiting for them; it reads the norm weights,
+                                     positions, slot mapping and page table before that
+                                     wait.  The producer lets the next kernel start as soon
+                                     as it begins, so a run of launches with this flag may
+                                     be in flight together: those four arrays must not be
+                                     written by any kernel enqueued after the last kernel
+                                     of the stream launched without programmatic dependent
+                                     launch.  Stage them with plain launches (a copy) before
+                                     the run, e.g. once at the start of a decode step. */
 #define MSA_LAUNCH_QUERY_RUNS 4   /* msa_indexer_forward only: the queries come in runs of
                                      one sequence (consecutive queries with the same
                                      table_offset, as in a prefill chunk), so tiles of 8
@@ -245,14 +244,14 @@ typedef struct {
  * k_scale        device fp32 [1]: dequantisation scale of an FP8 cache (NULL for bf16).
  * block_scores   device fp32 [num_queries, max_blocks], written in full.
  * topk_ids       device int32 [num_queries, topk].
- * launch_flags   MSA_LAUNCH_PDL: the score kernel is launched with programmatic
- *                dependent launch; the per-query kernel reads kv_len, table_offset
- *                and page_table before waiting for the kernel launched just before it
- *                on the stream (which must therefore not write them); idx_q, the
- *                cache, k_scale and the outputs are touched only after the wait (the
- *                query-run kernel waits before reading anything).  Each of the two
- *                kernels lets the next kernel on the stream start only after its own
- *                wait (see MSA_LAUNCH_PDL).
+ * launch_flags   MSA_LAUNCH_PDL: the indexer's first kernel is launched with
+ *                programmatic dependent launch; the per-query path reads kv_len,
+ *                table_offset and page-table entries before waiting for the kernels
+ *                ahead of it on the stream (the rule of MSA_LAUNCH_PDL applies to
+ *                them); idx_q, the cache, k_scale and the outputs are touched only
+ *                after the wait (the query-run kernel waits before reading anything).
+ *                The indexer's kernels let the next kernel on the stream start only
+ *                after their own wait.
  *                MSA_LAUNCH_QUERY_RUNS: see its definition.
  * Errors as for msa_producer_forward; num_queries == 0 launches nothing.
  */

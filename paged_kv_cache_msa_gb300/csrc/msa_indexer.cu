@@ -43,11 +43,6 @@
 #ifndef MSA_INDEX_RUNS_WS
 #define MSA_INDEX_RUNS_WS 1
 #endif
-// 1: the per-query path is the one-kernel cluster design (msa_index_decode_kernel);
-// 0: the score kernel followed by the top-k kernel.
-#ifndef MSA_INDEX_DECODE_CLUSTER
-#define MSA_INDEX_DECODE_CLUSTER 0
-#endif
 // Resident 128-thread score CTAs per SM the register budget is sized for.
 #ifndef MSA_INDEX_MIN_CTAS
 #define MSA_INDEX_MIN_CTAS 4
@@ -289,19 +284,28 @@ __global__ void __launch_bounds__(kScoreWarps * 32, MSA_INDEX_MIN_CTAS) msa_inde
                     w[u][v] = ok ? ldg16(row + i * (D / 4) + 8 * v) : make_uint4(0, 0, 0, 0);
             }
         }
+        // the k-steps are issued step-major over the NG groups, so that consecutive
+        // mma.sync are independent (group-major order would chain each on the last)
+        float cc[NG][4];
+#pragma unroll
+        for (int u = 0; u < NG; ++u)
+            cc[u][0] = cc[u][1] = cc[u][2] = cc[u][3] = 0.0f;
+#pragma unroll
+        for (int st = 0; st < KS; ++st) {
+            const uint4 f = s_af[st][lane];
+            const uint32_t a[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+            for (int u = 0; u < NG; ++u) {
+                const uint32_t *words = reinterpret_cast<const uint32_t *>(w[u]);
+                if (FP8)
+                    mma_f16(cc[u], a, e4m3x2_to_f16x2(words[st] & 0xFFFF), e4m3x2_to_f16x2(words[st] >> 16));
+                else
+                    mma_bf16(cc[u], a, words[2 * st], words[2 * st + 1]);
+            }
+        }
 #pragma unroll
         for (int u = 0; u < NG; ++u) {
-            float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const uint32_t *words = reinterpret_cast<const uint32_t *>(w[u]);
-#pragma unroll
-            for (int st = 0; st < KS; ++st) {
-                const uint4 f = s_af[st][lane];
-                const uint32_t a[4] = {f.x, f.y, f.z, f.w};
-                if (FP8)
-                    mma_f16(c, a, e4m3x2_to_f16x2(words[st] & 0xFFFF), e4m3x2_to_f16x2(words[st] >> 16));
-                else
-                    mma_bf16(c, a, words[2 * st], words[2 * st + 1]);
-            }
+            const float *c = cc[u];
             // columns 2i, 2i+1: max over the real heads (rows g, g+8 across lane groups)
             float m0 = fmaxf(row0_real ? c[0] : -INFINITY, row1_real ? c[2] : -INFINITY);
             float m1 = fmaxf(row0_real ? c[1] : -INFINITY, row1_real ? c[3] : -INFINITY);
@@ -380,6 +384,12 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
         if ((n & 63) == 0 && globaltimer() - t0 > MSA_WAIT_LIMIT_NS)
             return false;
     }
+}
+
+// mbar_wait with the common case (the phase has already completed) inline
+__device__ __forceinline__ bool mbar_wait_fast(uint32_t bar, uint32_t parity)
+{
+    return mbar_try(bar, parity) || mbar_wait(bar, parity);
 }
 
 // K-major operand tile in the 128-byte swizzle layout: 16-byte chunk c of row r (of
@@ -882,7 +892,7 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
             bool ok = true;
             for (int64_t ti = blockIdx.x; ti < num_tiles && ok; ti += gridDim.x, ++tile_it) {
                 const uint32_t tb = tile_it & 1;
-                if (*abort_flag || !mbar_wait(smem_u32(&bar_tile_full[tb]), (tile_it >> 1) & 1)) {
+                if (*abort_flag || !mbar_wait_fast(smem_u32(&bar_tile_full[tb]), (tile_it >> 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -892,8 +902,8 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
                     for (int b = 0; b < nb && ok; ++b, ++it) {
                         const uint32_t s = it % kRunsNSA, ph = (it / kRunsNSA) & 1;
                         const uint32_t a = it % kRunsNACC, pa = (it / kRunsNACC) & 1;
-                        if (*abort_flag || !mbar_wait(smem_u32(&bar_a_full[s]), ph) ||
-                            !mbar_wait(smem_u32(&bar_acc_empty[a]), pa ^ 1)) {
+                        if (*abort_flag || !mbar_wait_fast(smem_u32(&bar_a_full[s]), ph) ||
+                            !mbar_wait_fast(smem_u32(&bar_acc_empty[a]), pa ^ 1)) {
                             ok = false;
                             break;
                         }
@@ -934,7 +944,7 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
                 "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                     smem_u32(&bar_drain))
                 : "memory");
-            (void)mbar_wait(smem_u32(&bar_drain), 0);
+            (void)mbar_wait_fast(smem_u32(&bar_drain), 0);
         }
         __syncwarp();
     } else if (warp <= 8) {
@@ -949,7 +959,7 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
         for (int64_t ti = blockIdx.x; ti < num_tiles; ti += gridDim.x, ++tile_it) {
             const uint32_t tb = tile_it & 1;
             stop = stop || *abort_flag ||
-                   !__any_sync(0xffffffffu, mbar_wait(smem_u32(&bar_tile_empty[tb]), ((tile_it >> 1) & 1) ^ 1));
+                   !__any_sync(0xffffffffu, mbar_wait_fast(smem_u32(&bar_tile_empty[tb]), ((tile_it >> 1) & 1) ^ 1));
             const int64_t t0 = ti * QT;
             if (!stop && gt < QT) {
                 const int64_t t = t0 + gt;
@@ -957,12 +967,14 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
                 g_len[tb][gt] = len > 0 ? len : 0;
                 g_toff[tb][gt] = t < p.num_queries ? __ldg(p.table_offset + t) : INT64_MIN;
             }
-            {   // the query tile: row r = (query r / HP, head r % HP), this thread's half
+            {   // the query tile: row r = (query r / HP, head r % HP), this thread's half.
+                // Rows of heads past num_heads repeat head 0, so that the max over a
+                // query's HP columns equals the max over its real heads.
                 const int r = gt >> 1, hh = gt & 1;
                 const int q = r / HP, h = r % HP;
                 const int64_t t = t0 + q;
-                const bool real = h < p.heads && t < p.num_queries;
-                const uint16_t *src = p.idx_q + (t * p.heads + h) * D;
+                const bool real = t < p.num_queries;
+                const uint16_t *src = p.idx_q + (t * p.heads + (h < p.heads ? h : 0)) * D;
                 const uint32_t bt = bbase + tb * kBBytes;
 #pragma unroll
                 for (int c = hh * (CH / 2); c < (hh + 1) * (CH / 2); ++c) {
@@ -1022,7 +1034,7 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
                 };
                 auto store = [&](const uint4 (&raw)[NV]) -> bool {
                     const uint32_t s = it % kRunsNSA, ph = (it / kRunsNSA) & 1;
-                    if (*abort_flag || !__any_sync(0xffffffffu, mbar_wait(smem_u32(&bar_a_empty[s]), ph ^ 1))) {
+                    if (*abort_flag || !__any_sync(0xffffffffu, mbar_wait_fast(smem_u32(&bar_a_empty[s]), ph ^ 1))) {
                         *abort_flag = 1;
                         return false;
                     }
@@ -1132,7 +1144,7 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
                     const bool kvalid = pg >= 0 && pg < p.num_pages;
                     bool got = !*abort_flag;
                     if (got)
-                        got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_acc_full[grp]), pa));
+                        got = __all_sync(0xffffffffu, mbar_wait_fast(smem_u32(&bar_acc_full[grp]), pa));
                     if (!got)
                         *abort_flag = 1;
                     float m[QT];
@@ -1141,7 +1153,7 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
                         m[q] = -INFINITY;
                     if (got) {
                         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                        const bool whole = __all_sync(0xffffffffu, kvalid && j < minlen) && p.heads == HP;
+                        // the max over a query's HP columns (padded heads repeat head 0)
 #pragma unroll
                         for (int c0 = 0; c0 < 128; c0 += 32) {
                             uint32_t r[32];
@@ -1149,16 +1161,24 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
                             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
                             for (int qq = 0; qq < 32 / HP; ++qq) {
-                                const int q = c0 / HP + qq;
-                                float v = -INFINITY;
+                                float x[HP];
 #pragma unroll
                                 for (int h = 0; h < HP; ++h)
-                                    if (whole || h < p.heads)
-                                        v = fmaxf(v, __uint_as_float(r[qq * HP + h]));
-                                if (!whole && !(kvalid && j < elen[q]))
-                                    v = -INFINITY;
-                                m[q] = v;
+                                    x[h] = __uint_as_float(r[qq * HP + h]);
+#pragma unroll
+                                for (int w2 = HP / 2; w2 > 0; w2 >>= 1)
+#pragma unroll
+                                    for (int h = 0; h < w2; ++h)
+                                        x[h] = fmaxf(x[h], x[h + w2]);
+                                m[c0 / HP + qq] = x[0];
                             }
+                        }
+                        // keys without a page, or not visible to a query, take no part
+                        if (!__all_sync(0xffffffffu, kvalid && j < minlen)) {
+#pragma unroll
+                            for (int q = 0; q < QT; ++q)
+                                if (!(kvalid && j < elen[q]))
+                                    m[q] = -INFINITY;
                         }
                     }
                     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -1327,249 +1347,6 @@ __global__ void __launch_bounds__(kTopkThreads) msa_index_topk_kernel(const __gr
 }
 
 // ---------------------------------------------------------------------------
-// decode: a cluster of CTAs per query, top-k in the same kernel
-// ---------------------------------------------------------------------------
-//
-// The per-query scores of msa_index_score_kernel, restructured so that the history
-// read is not a chain of dependent loads: each query gets a cluster of CS CTAs
-// (host-chosen so that the grid fills the GPU once) that share out its blocks, CTA r
-// warp w taking blocks (k * CS + r) * 4 + w; a warp stages the index-K rows of its
-// blocks into shared memory with cp.async in rounds of kDecRoundBytes (two rounds in
-// flight, rows fetched through the page table, 16-byte pieces, 4 rows per
-// instruction), and scores each round from shared memory with the same mma.sync
-// contraction.  Every block score goes to block_scores and, over distributed shared
-// memory, to CTA 0 of the cluster; after one cluster barrier CTA 0 selects the top-k
-// from its shared memory.  No global scratch, one kernel per call, no wait on a flag
-// (cp.async.wait_group and the hardware cluster barrier cannot spin).
-
-constexpr int kDecRoundBytes = 8192;   // bytes of rows per warp per round
-constexpr int kDecThreads = 128;
-
-template <int D, bool FP8>
-__global__ void __launch_bounds__(kDecThreads, 2)
-msa_index_decode_kernel(const __grid_constant__ IndexerParams p)
-{
-    constexpr int KS = D / 16;                  // mma k-steps
-    constexpr int ES = FP8 ? 1 : 2;
-    constexpr int ROWB = D * ES;                // bytes of an index-K row
-    constexpr int CPT = ROWB / 16;              // 16-byte pieces per row
-    constexpr int RT = kDecRoundBytes / ROWB;   // rows per round
-    constexpr int NWL = FP8 ? (D / 4) / 16 : (D / 4) / 8;   // 16-byte words per lane and token
-    static_assert(RT % 8 == 0 && (RT * CPT) % 32 == 0, "round geometry");
-    extern __shared__ __align__(16) uint8_t s_stage[];    // [4 warps][2][kDecRoundBytes]
-    __shared__ __align__(16) float s_q[16][D];
-    __shared__ __align__(16) uint4 s_af[KS][32];
-    __shared__ __align__(16) float s_row[kRankMaxBlocks];   // CTA 0: the query's block scores
-    __shared__ int s_nfin;
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, i = lane & 3;
-    uint32_t cs, rank;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(cs));
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
-    const int64_t t = (int64_t)blockIdx.x / cs;
-    const int H = p.heads;
-    const int bt = p.block_tokens;
-    const int n = p.max_blocks;
-    const bool staged = n <= kRankMaxBlocks;
-    // the cluster's CTAs must all be running before one writes another's shared memory
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-
-    // metadata first (read before waiting on the previous kernel under PDL)
-    const int32_t len_raw = __ldg(p.kv_len + t);
-    const int64_t tbase = __ldg(p.table_offset + t);
-    const int64_t L = len_raw > 0 ? (int64_t)len_raw : 0;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" :::);
-
-    // the query's heads (rows >= H zero) and the A fragments, as in the score kernel
-    constexpr int NCH = 16 * D / 8, CPTQ = (NCH + kDecThreads - 1) / kDecThreads;
-    uint4 qraw[CPTQ];
-#pragma unroll
-    for (int u = 0; u < CPTQ; ++u) {
-        const int ch = tid + u * kDecThreads;
-        const int h = ch * 8 / D;
-        qraw[u] = (ch < NCH && h < H) ? ldg16(p.idx_q + (t * H + h) * D + (ch * 8) % D)
-                                      : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int u = 0; u < CPTQ; ++u) {
-        const int ch = tid + u * kDecThreads;
-        if (ch < NCH) {
-            float *dst = &s_q[ch * 8 / D][(ch * 8) % D];
-            const uint32_t wv[4] = {qraw[u].x, qraw[u].y, qraw[u].z, qraw[u].w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                dst[2 * k] = __uint_as_float(wv[k] << 16);
-                dst[2 * k + 1] = __uint_as_float(wv[k] & 0xFFFF0000u);
-            }
-        }
-    }
-    __syncthreads();
-    for (int st = warp; st < KS; st += 4) {
-        const int d = i * (D / 4) + 4 * st;
-        const float *r0 = &s_q[g][d], *r1 = &s_q[g + 8][d];
-        uint4 f;
-        if (FP8) {
-            f.x = f2_to_f16x2(r0[0], r0[1]);
-            f.y = f2_to_f16x2(r1[0], r1[1]);
-            f.z = f2_to_f16x2(r0[2], r0[3]);
-            f.w = f2_to_f16x2(r1[2], r1[3]);
-        } else {
-            f.x = f2_to_bf16x2(r0[0], r0[1]);
-            f.y = f2_to_bf16x2(r1[0], r1[1]);
-            f.z = f2_to_bf16x2(r0[2], r0[3]);
-            f.w = f2_to_bf16x2(r1[2], r1[3]);
-        }
-        s_af[st][lane] = f;
-    }
-    __syncthreads();
-    const bool row0_real = g < H, row1_real = g + 8 < H;
-    const float kscale = FP8 ? __ldg(p.k_scale) : 1.0f;
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA is running
-    const uint32_t srow0 = smem_u32(&s_row[0]);
-
-    // this warp's work: rounds of RT tokens over its blocks, flattened
-    const int rpb = (bt + RT - 1) / RT;                   // rounds per block
-    const int64_t stride_b = (int64_t)cs * 4;
-    const int64_t my_first = (int64_t)rank * 4 + warp;
-    const int64_t my_blocks = my_first < n ? (n - 1 - my_first) / stride_b + 1 : 0;
-    const int64_t tasks = my_blocks * rpb;
-    const uint32_t buf0 = smem_u32(s_stage) + (uint32_t)warp * 2u * kDecRoundBytes;
-
-    // The page of token j (-1: no row).  `entry` caches, one per lane, the table
-    // entries of the 32 logical pages from `blk0` on (the staging side and the
-    // scoring side keep their own); every lane of the warp calls this together.
-    auto page_of = [&](int64_t j, int64_t blk0, int64_t entry) -> int64_t {
-        const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
-        const int64_t rel = blk - blk0;
-        const long long e_sh = __shfl_sync(0xffffffffu, (long long)entry, (int)(rel & 31));
-        int64_t e;
-        if (rel >= 0 && rel < 32) {
-            e = e_sh;
-        } else {
-            const int64_t ti = tbase + blk;
-            e = (ti >= 0 && ti < p.page_table_len) ? (int64_t)__ldg(p.page_table + ti) : -1;
-        }
-        return (e >= 0 && e < p.num_pages) ? e : -1;
-    };
-    auto lane_entry_of = [&](int64_t blk0) -> int64_t {
-        const int64_t ti = tbase + blk0 + lane;
-        return (ti >= 0 && ti < p.page_table_len) ? (int64_t)__ldg(p.page_table + ti) : -1;
-    };
-    auto first_page_block = [&](int64_t b) -> int64_t {
-        const int64_t bj0 = b * bt;
-        return p.page_shift >= 0 ? (bj0 >> p.page_shift) : bj0 / p.page_size;
-    };
-    auto task_range = [&](int64_t task, int64_t &b, int64_t &j0, int64_t &j1) {
-        b = my_first + (task / rpb) * stride_b;
-        const int64_t bj0 = b * bt, bj1 = (bj0 + bt < L) ? bj0 + bt : L;
-        j0 = bj0 + (task % rpb) * RT;
-        j1 = (j0 + RT < bj1) ? j0 + RT : bj1;   // empty when j0 >= bj1
-    };
-    int64_t iss_blk0 = -1, iss_entry = -1;   // the staging side's table cache
-    // cp.async of the rows of task `task` into buffer `bsel`, then a commit (an empty
-    // group past the last task)
-    auto issue = [&](int64_t task, int bsel) {
-        if (task < tasks) {
-            int64_t b, j0, j1;
-            task_range(task, b, j0, j1);
-            const int64_t blk0 = first_page_block(b);
-            if (blk0 != iss_blk0) {
-                iss_entry = lane_entry_of(blk0);
-                iss_blk0 = blk0;
-            }
-            const uint32_t dst = buf0 + (uint32_t)bsel * kDecRoundBytes;
-            const int64_t nt = j1 > j0 ? j1 - j0 : 0;
-            for (int c = lane; c < RT * CPT; c += 32) {   // RT * CPT is a multiple of 32
-                const int r = c / CPT, piece = c % CPT;
-                const int64_t j = j0 + r;
-                const int64_t page = page_of(j, blk0, iss_entry);
-                if (r < nt && page >= 0) {
-                    const int64_t off = p.page_shift >= 0 ? (j & (p.page_size - 1)) : j % p.page_size;
-                    const uint8_t *src = p.kdata + (page * p.stride_page + off * p.stride_token) * ES + 16 * piece;
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + (uint32_t)(r * ROWB + 16 * piece)),
-                                 "l"(src)
-                                 : "memory");
-                }
-            }
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    };
-    int64_t cmp_blk0 = -1, cmp_entry = -1;   // the scoring side's table cache
-
-    issue(0, 0);
-    issue(1, 1);
-    float best = -INFINITY;
-    for (int64_t task = 0; task < tasks; ++task) {
-        const int bsel = (int)(task & 1);
-        asm volatile("cp.async.wait_group 1;" ::: "memory");
-        __syncwarp();
-        int64_t b, j0, j1;
-        task_range(task, b, j0, j1);
-        if (task % rpb == 0)
-            best = -INFINITY;
-        const int64_t blk0 = first_page_block(b);
-        if (blk0 != cmp_blk0) {
-            cmp_entry = lane_entry_of(blk0);
-            cmp_blk0 = blk0;
-        }
-        const uint32_t src0 = buf0 + (uint32_t)bsel * kDecRoundBytes;
-        for (int64_t jb = j0; jb < j1; jb += 8) {
-            // lane (g, i): token jb + g, its quarter i of the row, from shared memory
-            const int64_t j = jb + g;
-            const int64_t pg = page_of(j, blk0, cmp_entry);
-            const bool ok = j < j1 && pg >= 0;
-            uint4 w[NWL];
-            const uint32_t a0 = src0 + (uint32_t)((j - j0) * ROWB) + (uint32_t)(i * (D / 4) * ES);
-#pragma unroll
-            for (int v = 0; v < NWL; ++v)
-                w[v] = ok ? lds128(a0 + 16u * v) : make_uint4(0, 0, 0, 0);
-            float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const uint32_t *words = reinterpret_cast<const uint32_t *>(w);
-#pragma unroll
-            for (int st = 0; st < KS; ++st) {
-                const uint4 f = s_af[st][lane];
-                const uint32_t a[4] = {f.x, f.y, f.z, f.w};
-                if (FP8)
-                    mma_f16(c, a, e4m3x2_to_f16x2(words[st] & 0xFFFF), e4m3x2_to_f16x2(words[st] >> 16));
-                else
-                    mma_bf16(c, a, words[2 * st], words[2 * st + 1]);
-            }
-            float m0 = fmaxf(row0_real ? c[0] : -INFINITY, row1_real ? c[2] : -INFINITY);
-            float m1 = fmaxf(row0_real ? c[1] : -INFINITY, row1_real ? c[3] : -INFINITY);
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-                m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-            }
-            const bool ok0 = __shfl_sync(0xffffffffu, ok, 8 * i);
-            const bool ok1 = __shfl_sync(0xffffffffu, ok, 8 * i + 4);
-            float m = fmaxf(ok0 ? m0 : -INFINITY, ok1 ? m1 : -INFINITY);
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            best = fmaxf(best, m);
-        }
-        __syncwarp();   // every lane is done reading the buffer before it is refilled
-        issue(task + 2, bsel);
-        if (task % rpb == rpb - 1 && lane == 0) {   // the block is complete
-            const float v = best > -INFINITY ? best * kscale : -INFINITY;
-            p.block_scores[t * n + b] = v;
-            if (staged) {
-                uint32_t remote;
-                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(srow0 + 4u * (uint32_t)b), "r"(0));
-                asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
-            }
-        }
-    }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    // every block score is in CTA 0's shared memory (and in block_scores)
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-    if (rank == 0)
-        topk_row(p.block_scores + t * n, s_row, &s_nfin, staged, n, p.topk, p.topk_ids + t * p.topk);
-}
-
-// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 
@@ -1732,55 +1509,6 @@ extern "C" msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t nu
             return fail(MSA_ERR_CUDA, "cudaFuncSetAttribute failed");
         sc.dynamicSmemBytes = (size_t)smem;
     }
-#if MSA_INDEX_DECODE_CLUSTER
-    if (!tiled) {
-        // one kernel: a cluster of CTAs per query, top-k in CTA 0 of each cluster
-        const int D = cfg->head_dim;
-        const void *fn = D == 128 ? (p.fp8 ? reinterpret_cast<const void *>(&msa_index_decode_kernel<128, true>)
-                                           : reinterpret_cast<const void *>(&msa_index_decode_kernel<128, false>))
-                                  : (p.fp8 ? reinterpret_cast<const void *>(&msa_index_decode_kernel<64, true>)
-                                           : reinterpret_cast<const void *>(&msa_index_decode_kernel<64, false>));
-        const int smem = 4 * 2 * kDecRoundBytes;
-        int dev = 0, sms = 0, per_sm = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return fail(MSA_ERR_CUDA, "device query failed");
-        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kDecThreads, smem) != cudaSuccess ||
-            per_sm <= 0)
-            return fail(MSA_ERR_CUDA, "occupancy query failed");
-        // the largest cluster (1..8 CTAs per query, no more than the query's blocks
-        // need) with which the grid fits on the GPU in one wave
-        int64_t cs = ((int64_t)sms * per_sm) / num_queries;
-        const int64_t need = (cfg->max_blocks + 3) / 4;
-        cs = cs > need ? need : cs;
-        cs = cs > 8 ? 8 : (cs < 1 ? 1 : cs);
-        cudaLaunchConfig_t dc;
-        memset(&dc, 0, sizeof dc);
-        dc.gridDim = dim3((unsigned)(num_queries * cs));
-        dc.blockDim = dim3(kDecThreads);
-        dc.dynamicSmemBytes = (size_t)smem;
-        dc.stream = stream;
-        cudaLaunchAttribute dattr[2];
-        dattr[0].id = cudaLaunchAttributeClusterDimension;
-        dattr[0].val.clusterDim.x = (unsigned)cs;
-        dattr[0].val.clusterDim.y = 1;
-        dattr[0].val.clusterDim.z = 1;
-        int na = 1;
-        if (p.pdl) {
-            dattr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            dattr[1].val.programmaticStreamSerializationAllowed = 1;
-            na = 2;
-        }
-        dc.attrs = dattr;
-        dc.numAttrs = na;
-        void *dargs[] = {&p};
-        const cudaError_t de = cudaLaunchKernelExC(&dc, fn, dargs);
-        if (de != cudaSuccess)
-            return fail(MSA_ERR_CUDA, "decode kernel launch failed: %s", cudaGetErrorString(de));
-        return MSA_OK;
-    }
-#endif
     cudaLaunchAttribute sattr[1];
     if (p.pdl) {
         sattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -736,6 +736,10 @@ template <int D, bool TABLE = false>
 __device__ __forceinline__ void epilogue_tile(const Params &p, const AccSrc &src, int n_tile,
                                               int64_t t, bool live, int hgroup, int lane)
 {
+    // a warp whose 32 rows are all past the last token has nothing to read or write
+    // (a partial last token tile; at decode sizes half the tile)
+    if (!__any_sync(0xffffffffu, live))
+        return;
     const uint32_t taddr = src.taddr;
     constexpr int HPT = kBN / D;  // heads per tile
     const int g0 = n_tile * HPT;
@@ -1297,10 +1301,11 @@ msa_projection_splitk_kernel(const __grid_constant__ CUtensorMap tmap_x,
         const int quarter = warp & 3, hgroup = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        if (rank == 0 && p.rotary_dim > 0) {
+        if (rank == 0 && p.rotary_dim > 0 && __any_sync(0xffffffffu, row < p.num_tokens)) {
             // While the main loop runs: this row's RoPE cos / sin, the two warps of a
             // lane quarter taking half the frequencies each, into tensor memory for
-            // the epilogue (the same angle and evaluation it would make itself)
+            // the epilogue (the same angle and evaluation it would make itself); a
+            // warp whose rows are all past the last token skips it
             const int H = p.rotary_dim / 2;   // 16, 32 or 64: halves are whole blocks of 8
             const int pos = row < p.num_tokens ? __ldg(p.positions + row) : 0;
             for (int k0 = hgroup * (H / 2); k0 < (hgroup + 1) * (H / 2); k0 += 8) {
@@ -1321,7 +1326,8 @@ msa_projection_splitk_kernel(const __grid_constant__ CUtensorMap tmap_x,
         if (!__all_sync(0xffffffffu, got))
             ok = false;
         tc_fence_after();
-        if (rank > 0 && ok) {
+        if (rank > 0 && ok && __any_sync(0xffffffffu, row < p.num_tokens)) {
+            // (rows past the last token are never read back)
 #pragma unroll
             for (int c0 = hgroup * (kBN / 2); c0 < (hgroup + 1) * (kBN / 2); c0 += 32) {
                 uint32_t r[32];

@@ -59,6 +59,12 @@ def test_indexer_block_sizes_topk_and_pages(bt, topk, P):
                                  topk=topk, page_size=P))
 
 
+def test_indexer_rows_longer_than_the_shared_ranking():
+    """More than 1,024 blocks per query (40,000 tokens in blocks of 32): the top-k is
+    taken from block_scores in global memory instead of the shared-memory ranking."""
+    _check(wl.make_indexer_batch("long_rows", 95, [40000, 100, 33000], block_tokens=32, topk=16))
+
+
 def test_indexer_table_holes_and_padded_pages():
     w = wl.make_indexer_batch("holes", 97, [700, 1500, 64], page_pad_bytes=256)
     pt = np.array(w.page_table, copy=True)

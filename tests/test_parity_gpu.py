@@ -269,17 +269,16 @@ def test_sixty_layer_decode_step_in_one_graph():
                 compare_bf16(pools_d[name][m].view(np.uint16), pools_o[name][m].view(np.uint16), name)
 
 
-def test_pdl_chain_reads_metadata_written_launches_back():
+def test_pdl_chain_reads_metadata_staged_launches_back():
     """Under programmatic dependent launch the producer reads its positions and slots
-    before waiting on the kernel enqueued just before it, and every kernel of the
-    library lets its dependents start only after its own wait.  Per layer, in one
-    CUDA graph: a copy kernel stages the layer's slots, the indexer (score and
-    top-k kernels, both launched with PDL) writes the int32 array that this layer's
-    producer takes as its positions, another layer's producer runs (PDL), then this
-    layer's producer (PDL).  Its metadata was thus written two and more launches
-    back, the positions by one of the library's own PDL kernels.  The buffers start
-    as stale values (slots -1, positions 0x7fff); every layer must match the oracle
-    run on the final positions and slots."""
+    before waiting on the kernels ahead of it, and lets the next kernel start at once,
+    so a run of such launches may be in flight together; the metadata must be staged
+    by kernels launched without programmatic dependent launch before the run.  Per
+    layer, in one CUDA graph: copy kernels stage the layer's positions and slots, the
+    indexer runs (its kernels launched with PDL), another layer's producer runs
+    (PDL), then this layer's producer (PDL): the metadata it reads first was written
+    two and more launches back.  The buffers start stale (slots -1, positions 0x7fff);
+    every layer must match the oracle."""
     from harness import e4m3_ulp_distance
     from gpu_harness import oracle_written_mask
     from paged_kv_cache_msa_gb300.device import DeviceIndexer
@@ -290,44 +289,32 @@ def test_pdl_chain_reads_metadata_written_launches_back():
     dos = [DeviceWorkload(w) for w in others]
     iw = wl.indexer_decode64()
     ix = DeviceIndexer(iw)
-    T = layers[0].num_tokens
-    assert ix.topk_ids.numel() >= T
     slot_src = [dw.slots.clone() for dw in dws]
-    pos_bufs = [torch.empty_like(ix.topk_ids) for _ in range(n_layers)]
+    pos_src = [dw.positions.clone() for dw in dws]
     s = torch.cuda.Stream()
-    p = lambda t: int(t.data_ptr())
     flags = PERSISTENT | B.MSA_LAUNCH_PDL
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
-        for dw, do, src, pb in zip(dws, dos, slot_src, pos_bufs):
-            dw.slots.copy_(src)
-            assert B.msa_indexer_forward(ix.cfg, iw.idx_q.shape[0], p(ix.idx_q), p(ix.kv_len),
-                                         p(ix.table_offset), p(ix.page_table),
-                                         ix.page_table.numel(), ix.cache, p(ix.k_scale),
-                                         p(ix.block_scores), p(pb), B.MSA_LAUNCH_PDL,
-                                         stream=s.cuda_stream) == B.MSA_OK
+        for dw, do, ss, ps in zip(dws, dos, slot_src, pos_src):
+            dw.slots.copy_(ss)
+            dw.positions.copy_(ps)
+            ix.run(stream=s, launch_flags=B.MSA_LAUNCH_PDL)
             do.run(flags, stream=s)
-            args = list(dw.args(flags))
-            args[4] = p(pb)                      # positions: the top-k kernel's output
-            assert B.msa_producer_forward(*args, stream=s.cuda_stream) == B.MSA_OK
-    for dw, pb in zip(dws, pos_bufs):
+            dw.run(flags, stream=s)
+    for dw in dws:
         dw.slots.fill_(-1)
-        pb.fill_(0x7FFF)
+        dw.positions.fill_(0x7FFF)
     torch.cuda.synchronize()
     g.replay()
     torch.cuda.synchronize()
-    for w, dw, pb in zip(layers, dws, pos_bufs):
-        pos = pb.reshape(-1)[:T].cpu().numpy().astype(np.int32)
-        assert (pos != 0x7FFF).all() and (pos < iw.max_blocks).all()
-        w2 = wl.Workload(w.name + "[chained]", w.shape, w.qkv, w.row_stride, pos, w.slot_mapping,
-                         w.page_table, w.weights, w.scales, w.caches, w.pools, w.seed, w.meta)
-        sent = wl.host_pools(w2)
-        q_o, iq_o, pools_o = run_oracle(w2)
+    for w, dw in zip(layers, dws):
+        sent = wl.host_pools(w)
+        q_o, iq_o, pools_o = run_oracle(w)
         q_d, iq_d = dw.outputs_to_host()
         compare_bf16(q_d, q_o, f"{w.name} q_out")
         compare_bf16(iq_d, iq_o, f"{w.name} idx_q_out")
-        masks = oracle_written_mask(w2)
+        masks = oracle_written_mask(w)
         pools_d = dw.pools_to_host()
         for name in w.pools:
             m = masks[name]
@@ -337,4 +324,3 @@ def test_pdl_chain_reads_metadata_written_launches_back():
                 assert e4m3_ulp_distance(pools_d[name][m], pools_o[name][m]).max(initial=0) <= 1
             else:
                 compare_bf16(pools_d[name][m].view(np.uint16), pools_o[name][m].view(np.uint16), name)
-
