@@ -38,11 +38,6 @@
 #ifndef MSA_INDEX_GROUPS
 #define MSA_INDEX_GROUPS 4
 #endif
-// 1: query runs take the warp-specialised kernel (msa_index_runs_kernel); 0: the
-// lockstep one (msa_index_tiled_kernel).
-#ifndef MSA_INDEX_RUNS_WS
-#define MSA_INDEX_RUNS_WS 1
-#endif
 // Resident 128-thread score CTAs per SM the register budget is sized for.
 #ifndef MSA_INDEX_MIN_CTAS
 #define MSA_INDEX_MIN_CTAS 4
@@ -328,25 +323,8 @@ __global__ void __launch_bounds__(kScoreWarps * 32, MSA_INDEX_MIN_CTAS) msa_inde
 }
 
 // ---------------------------------------------------------------------------
-// block scores of query runs on the tcgen05 tensor cores (prefill)
+// tensor-core and barrier helpers of the query-run kernel
 // ---------------------------------------------------------------------------
-//
-// When queries come in runs of one sequence (a prefill chunk), the queries of a run
-// share every index-K block they see, so a CTA takes a tile of QT consecutive
-// queries and scores them together: the tile's query heads are the 128 rows of the
-// MMA (row = query * HP + head, HP = 8 or 16 rows per query, QT = 128 / HP) and a
-// block of 128 keys is its 128 columns, with K = head_dim; fp32 accumulators in
-// tensor memory.  Per block the CTA gathers the keys' rows through the page table
-// into shared memory (E4M3 codes become f16 exactly, with the query rounded to f16
-// as in the per-query kernel; bf16 rows stay bf16), one thread issues the D/16
-// tcgen05.mma (M 128, N 128), and while the tensor cores work on that block the
-// threads read the previous block's accumulator (two accumulators, 2 x 128
-// columns): thread r owns row r, takes the max over the keys visible to its query
-// (key < kv_len, page inside the table and the cache), then the max over its
-// query's heads by shuffles.  Keys with no valid page, and heads past num_heads,
-// take no part.  A tile whose queries belong to several sequences (different
-// table rows) is scored one sequence at a time.  Every mbarrier wait is bounded;
-// a block whose wait ran out is scored NaN (never selected).
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -416,287 +394,28 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
     return d;
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-constexpr int kTileThreads = 128;
 constexpr int kTileKeys = 128;   // keys per MMA tile: the 128-token blocks of the pages
-
-template <int D, bool FP8>
-__global__ void __launch_bounds__(kTileThreads, 2)
-msa_index_tiled_kernel(const __grid_constant__ IndexerParams p)
-{
-    constexpr uint32_t kOperandBytes = 128u * D * 2u;   // one 128-row f16/bf16 tile
-    constexpr int CH = D / 8;                           // 16-byte chunks of a 2-byte row
-    // idesc: fp32 accumulator; A and B f16 (FP8 cache) or bf16; K-major; N 128, M 128
-    constexpr uint32_t kIdesc = (1u << 4) | ((FP8 ? 0u : 1u) << 7) | ((FP8 ? 0u : 1u) << 10) |
-                                ((uint32_t)(kTileKeys >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_mma[2];
-    __shared__ uint32_t s_tmem;
-    __shared__ int64_t s_toff[16];
-    __shared__ int32_t s_len[16];
-    // keys of a block with a valid page (bit j of word w: key 32w + j), for the last
-    // four blocks: block i's mask is written before the barrier of iteration i and
-    // read in its epilogue, which some warps may still run while others write
-    // block i + 2's
-    __shared__ uint32_t s_kmask[4][4];
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int HP = p.heads <= 8 ? 8 : 16;
-    const int QT = 128 / HP;
-    const int64_t t0 = (int64_t)blockIdx.x * QT;
-    const uint32_t opA = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    const uint32_t opB0 = opA + kOperandBytes;
-
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (tid < QT) {
-        const int64_t t = t0 + tid;
-        const int32_t len = t < p.num_queries ? __ldg(p.kv_len + t) : 0;
-        s_len[tid] = len > 0 ? len : 0;
-        s_toff[tid] = t < p.num_queries ? __ldg(p.table_offset + t) : INT64_MIN;
-    }
-    if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_mma[0])));
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_mma[1])));
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(&s_tmem)),
-                     "r"(2 * kTileKeys)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    // the query tile: row tid = (query tid / HP, head tid % HP); absent rows zero
-    {
-        const int q = tid / HP, h = tid % HP;
-        const int64_t t = t0 + q;
-        const bool real = h < p.heads && t < p.num_queries;
-        const uint16_t *src = p.idx_q + (t * p.heads + h) * D;
-#pragma unroll
-        for (int c = 0; c < CH; ++c) {
-            uint4 v = real ? ldg16(src + 8 * c) : make_uint4(0, 0, 0, 0);
-            if (FP8) {   // bf16 -> f16 (exact for the normal f16 range)
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                uint32_t o[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    o[k] = f2_to_f16x2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
-                v = make_uint4(o[0], o[1], o[2], o[3]);
-            }
-            sts128(swz(opA, tid, c), v.x, v.y, v.z, v.w);
-        }
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const uint32_t tmem = s_tmem;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const float kscale = FP8 ? __ldg(p.k_scale) : 1.0f;
-
-    // this thread's row in the epilogue
-    const int eq = tid / HP, eh = tid % HP;
-    const int64_t et = t0 + eq;
-
-    uint32_t done = 0;             // queries of the tile already scored (bit q)
-    const uint32_t all = (1u << QT) - 1u;
-    uint32_t iter = 0;             // blocks issued so far (phases of the two barriers)
-    while (done != all) {
-        // the next sequence: the table row of the first query not yet scored
-        const int q0 = __ffs(~done & all) - 1;
-        const int64_t toff = s_toff[q0];
-        uint32_t seg = 0;
-        int32_t seg_len = 0;
-        for (int q = 0; q < QT; ++q)
-            if (!((done >> q) & 1) && s_toff[q] == toff) {
-                seg |= 1u << q;
-                seg_len = s_len[q] > seg_len ? s_len[q] : seg_len;
-            }
-        const bool absent = toff == INT64_MIN;     // queries past num_queries
-        int nb = absent ? 0 : (seg_len + kTileKeys - 1) / kTileKeys;
-        if (nb > p.max_blocks)
-            nb = p.max_blocks;
-        const bool mine = (seg >> eq) & 1;
-
-        auto epilogue = [&](int b, uint32_t it) {
-            const uint32_t st = it & 1;
-            const bool got = mbar_wait(smem_u32(&bar_mma[st]), (it >> 1) & 1);
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const int32_t len = s_len[eq];
-            const uint32_t *km = s_kmask[it & 3];
-            // every key of the block valid and visible to this query: no masking
-            const bool whole = (km[0] & km[1] & km[2] & km[3]) == 0xffffffffu &&
-                               (b + 1) * kTileKeys <= len;
-            float m = -INFINITY;
-#pragma unroll
-            for (int c0 = 0; c0 < kTileKeys; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_base + st * kTileKeys + c0, r);
-                float v[32];
-                if (whole) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        v[j] = __uint_as_float(r[j]);
-                } else {
-                    const uint32_t valid = km[c0 >> 5];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int key = b * kTileKeys + c0 + j;
-                        v[j] = (((valid >> j) & 1) && key < len) ? __uint_as_float(r[j]) : -INFINITY;
-                    }
-                }
-                // a tree, not a chain: five dependent steps instead of 32
-#pragma unroll
-                for (int w = 16; w > 0; w >>= 1)
-#pragma unroll
-                    for (int j = 0; j < w; ++j)
-                        v[j] = fmaxf(v[j], v[j + w]);
-                m = fmaxf(m, v[0]);
-            }
-            if (eh >= p.heads)
-                m = -INFINITY;
-            for (int o = 1; o < HP; o <<= 1)
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            if (eh == 0 && mine && et < p.num_queries)
-                p.block_scores[et * p.max_blocks + b] =
-                    got ? (m > -INFINITY ? m * kscale : -INFINITY) : __int_as_float(0x7fc00000);
-            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        };
-
-        // Key row tid of each block is fetched ahead: its page-table entry two blocks
-        // ahead, its row one block ahead, so that both latencies overlap the MMAs and
-        // the previous block's epilogue.
-        constexpr int NV = FP8 ? D / 16 : CH;   // 16-byte pieces of a key row
-        auto table_entry = [&](int bb) -> int64_t {
-            const int64_t j = (int64_t)bb * kTileKeys + tid;
-            if (bb >= nb || j >= seg_len)
-                return -1;
-            const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
-            const int64_t ti = toff + blk;
-            return (ti >= 0 && ti < p.page_table_len) ? (int64_t)__ldg(p.page_table + ti) : -1;
-        };
-        uint4 raw[NV];
-        bool raw_ok = false;
-        auto fetch_row = [&](int bb, int64_t page) {
-            const int64_t j = (int64_t)bb * kTileKeys + tid;
-            raw_ok = bb < nb && j < seg_len && page >= 0 && page < p.num_pages;
-            const int64_t off = p.page_shift >= 0 ? (j & (p.page_size - 1)) : j % p.page_size;
-            const uint8_t *row =
-                raw_ok ? p.kdata + (page * p.stride_page + off * p.stride_token) * (FP8 ? 1 : 2)
-                       : nullptr;
-#pragma unroll
-            for (int v = 0; v < NV; ++v)
-                raw[v] = raw_ok ? ldg16(row + 16 * v) : make_uint4(0, 0, 0, 0);
-        };
-        int64_t page_next = table_entry(1);
-        fetch_row(0, table_entry(0));
-
-        for (int b = 0; b < nb; ++b, ++iter) {
-            const uint32_t st = iter & 1;
-            const uint32_t opB = opB0 + st * kOperandBytes;
-            const int64_t page_after = table_entry(b + 2);
-            const uint32_t vmask = __ballot_sync(0xffffffffu, raw_ok);
-            if (lane == 0)
-                s_kmask[iter & 3][warp] = vmask;
-            if (FP8) {
-#pragma unroll
-                for (int c = 0; c < D / 16; ++c) {   // 16 codes -> two f16 chunks
-                    const uint32_t w[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
-                    uint32_t h[8];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        h[2 * k] = e4m3x2_to_f16x2(w[k] & 0xFFFF);
-                        h[2 * k + 1] = e4m3x2_to_f16x2(w[k] >> 16);
-                    }
-                    sts128(swz(opB, tid, 2 * c), h[0], h[1], h[2], h[3]);
-                    sts128(swz(opB, tid, 2 * c + 1), h[4], h[5], h[6], h[7]);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < CH; ++c)
-                    sts128(swz(opB, tid, c), raw[c].x, raw[c].y, raw[c].z, raw[c].w);
-            }
-            if (b + 1 < nb)
-                fetch_row(b + 1, page_next);
-            page_next = page_after;
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            __syncthreads();
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-#ifdef MSA_STARVE
-            if (false) {   // the starved test build: no MMA, no commit
-#else
-            if (tid == 0) {
-#endif
-                const uint32_t d = tmem + st * kTileKeys;
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t koff = (uint32_t)(ks >> 2) * (128u * 128u) + (uint32_t)(ks & 3) * 32u;
-                    const uint64_t ad = sw128_desc(opA + koff), bd = sw128_desc(opB + koff);
-                    asm volatile(
-                        "{\n\t.reg .pred pp;\n\tsetp.ne.b32 pp, %4, 0;\n\t"
-                        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pp;\n\t}" ::"r"(d),
-                        "l"(ad), "l"(bd), "r"(kIdesc), "r"((uint32_t)ks)
-                        : "memory");
-                }
-                asm volatile(
-                    "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                        smem_u32(&bar_mma[st]))
-                    : "memory");
-            }
-            __syncwarp();
-            if (b > 0)
-                epilogue(b - 1, iter - 1);   // overlaps the MMAs just issued
-        }
-        if (nb > 0)
-            epilogue(nb - 1, iter - 1);
-        // blocks the sequence's queries do not reach
-        for (int idx = tid; idx < QT * (p.max_blocks - nb); idx += kTileThreads) {
-            const int q = idx / (p.max_blocks - nb), b = nb + idx % (p.max_blocks - nb);
-            if ((seg >> q) & 1 && t0 + q < p.num_queries)
-                p.block_scores[(t0 + q) * p.max_blocks + b] = -INFINITY;
-        }
-        done |= seg;
-        __syncthreads();   // s_kmask and the operand tiles are reused by the next sequence
-    }
-    asm volatile("griddepcontrol.launch_dependents;" :::);
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
-    if (warp == 0) {
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(2 * kTileKeys)
-                     : "memory");
-    }
-}
 
 // ---------------------------------------------------------------------------
 // block scores of query runs, warp-specialised (prefill)
 // ---------------------------------------------------------------------------
 //
-// The scores of msa_index_tiled_kernel, with the MMA operands swapped and the
-// phases pipelined across warps instead of run in lockstep:
+// When queries come in runs of one sequence (a prefill chunk), the queries of a run
+// share every index-K block they see, so a CTA scores a tile of QT consecutive
+// queries (QT = 128 / HP, HP = 8 rows per query for up to 8 heads, else 16) against
+// each 128-token block at once on the tcgen05 tensor cores; a tile whose queries
+// belong to several sequences (different table rows) is scored one sequence at a
+// time.  The FP8 keys become f16 exactly and the queries are rounded to f16, as in
+// the per-query kernel; bf16 stays bf16.  The operands:
 //   A (M = 128)  the 128 keys of a block: FP8 codes converted to f16 (bf16 rows as
 //                they are) by the gather warps and written from registers straight
 //                into tensor memory (tcgen05.st) -- no shared-memory round trip;
 //   B (N = 128)  the tile's query heads (row = query * HP + head), K-major in shared
 //                memory with the 128-byte swizzle, loaded once per tile;
 //   D            fp32 [key, query-head] in tensor memory.
-// The only shared-memory traffic per block is the MMA reading B (32 KB for D = 128).
+// The only shared-memory traffic per block is the MMA reading B (32 KB for D = 128);
+// the earlier arrangement (queries as A, keys gathered into shared memory as B, the
+// CTA's phases in lockstep) needed 96 KB per block and ran at 0.27 of the bf16 peak.
 // Warps: 0 allocates tensor memory and its lane 0 issues the MMAs; 1-8 gather
 // (warps w and w + 4 share tensor-memory lane quarter w & 3 and take one half of
 // the head dimension each; the rows of the next block are in flight in registers
@@ -742,20 +461,6 @@ __device__ __forceinline__ float butterfly_max(float (&v)[QT], int lane)
     return v[0];   // the max of query (lane >> 1) & 15 (QT 16) or (lane >> 2) & 7 (QT 8)
 }
 
-__device__ __forceinline__ void tmem_st32x(uint32_t taddr, const uint32_t (&r)[32])
-{
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-        "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-
 __device__ __forceinline__ void tmem_st16x(uint32_t taddr, const uint32_t (&r)[32])
 {
     asm volatile(
@@ -779,15 +484,6 @@ __device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t *r)
           "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t a)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(a));
-    return v;
 }
 
 __device__ __forceinline__ void mbar_arrive_local(uint32_t bar)
@@ -1039,31 +735,34 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
                         return false;
                     }
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    uint32_t w[32];
-                    if (FP8) {
+                    const uint32_t taddr = tmem + a_lane + kACol0 + s * kACols + (uint32_t)half * (kACols / 2);
+                    // 16 columns (32 elements) at a time, to keep few registers live
 #pragma unroll
-                        for (int v = 0; v < NV; ++v) {
-                            const uint32_t x[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
+                    for (int q16 = 0; q16 < (int)(kACols / 2) / 16; ++q16) {
+                        uint32_t w[32];
+                        if (FP8) {   // two 16-code pieces -> 16 f16x2 words
 #pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                w[8 * v + 2 * k] = e4m3x2_to_f16x2(x[k] & 0xFFFF);
-                                w[8 * v + 2 * k + 1] = e4m3x2_to_f16x2(x[k] >> 16);
+                            for (int vv = 0; vv < 2; ++vv) {
+                                const uint4 rv = raw[2 * q16 + vv];
+                                const uint32_t x[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) {
+                                    w[8 * vv + 2 * k] = e4m3x2_to_f16x2(x[k] & 0xFFFF);
+                                    w[8 * vv + 2 * k + 1] = e4m3x2_to_f16x2(x[k] >> 16);
+                                }
+                            }
+                        } else {     // four 8-element pieces are 16 bf16x2 words already
+#pragma unroll
+                            for (int vv = 0; vv < 4; ++vv) {
+                                const uint4 rv = raw[4 * q16 + vv];
+                                w[4 * vv] = rv.x;
+                                w[4 * vv + 1] = rv.y;
+                                w[4 * vv + 2] = rv.z;
+                                w[4 * vv + 3] = rv.w;
                             }
                         }
-                    } else {
-#pragma unroll
-                        for (int v = 0; v < NV; ++v) {
-                            w[4 * v] = raw[v].x;
-                            w[4 * v + 1] = raw[v].y;
-                            w[4 * v + 2] = raw[v].z;
-                            w[4 * v + 3] = raw[v].w;
-                        }
+                        tmem_st16x(taddr + 16u * (uint32_t)q16, w);
                     }
-                    const uint32_t taddr = tmem + a_lane + kACol0 + s * kACols + (uint32_t)half * (kACols / 2);
-                    if (D == 128)
-                        tmem_st32x(taddr, w);
-                    else
-                        tmem_st16x(taddr, w);
                     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
                     __syncwarp();
@@ -1481,7 +1180,6 @@ extern "C" msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t nu
         if (major != 10)
             return fail(MSA_ERR_UNSUPPORTED, "query runs need tcgen05 tensor cores (compute capability 10.x)");
         const int64_t tiles = (num_queries + qt - 1) / qt;
-#if MSA_INDEX_RUNS_WS
         const int smem = kRunsDynSmem;
         const void *fns[8] = {
             reinterpret_cast<const void *>(&msa_index_runs_kernel<64, false, 8>),
@@ -1495,15 +1193,6 @@ extern "C" msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t nu
         score_fn = fns[(D == 128 ? 4 : 0) + (p.fp8 ? 2 : 0) + (hp8 ? 0 : 1)];
         sc.gridDim = dim3((unsigned)(tiles < sms ? tiles : sms));   // persistent, one CTA per SM
         sc.blockDim = dim3(kRunsThreads);
-#else
-        const int smem = 3 * 128 * D * 2 + 1024;
-        score_fn = D == 128 ? (p.fp8 ? reinterpret_cast<const void *>(&msa_index_tiled_kernel<128, true>)
-                                     : reinterpret_cast<const void *>(&msa_index_tiled_kernel<128, false>))
-                            : (p.fp8 ? reinterpret_cast<const void *>(&msa_index_tiled_kernel<64, true>)
-                                     : reinterpret_cast<const void *>(&msa_index_tiled_kernel<64, false>));
-        sc.gridDim = dim3((unsigned)tiles);
-        sc.blockDim = dim3(kTileThreads);
-#endif
         if (cudaFuncSetAttribute(score_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
             cudaSuccess)
             return fail(MSA_ERR_CUDA, "cudaFuncSetAttribute failed");
