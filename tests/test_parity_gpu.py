@@ -162,6 +162,18 @@ def test_per_head_scales():
     check_against_oracle(w, PERSISTENT)
 
 
+def test_per_head_scales_many_tokens_per_cta():
+    """Per-head scales when each CTA of the persistent grid has many tokens (about 40):
+    the kernel then takes the caches' reciprocal scales from a per-CTA table instead of
+    computing them per head row; 40 prefill sequences of 456 tokens."""
+    rng = np.random.default_rng(18)
+    seq_positions = [list(range(int(s0), int(s0) + 456)) for s0 in rng.integers(0, 4000, size=40)]
+    w = wl.make_batch("per_head_many", 18, wl.BIG, seq_positions, max_blocks=72, num_pages=40 * 72,
+                      scale_mode=1, pad_frac=0.05)
+    w.scales = rng.uniform(0.01, 0.2, size=w.scales.shape).astype(np.float32)
+    check_against_oracle(w, PERSISTENT)
+
+
 def test_saturation_with_small_scale_and_outliers():
     w = _small(9, heads=wl.BIG, T_seqs=20, outlier_frac=0.05, scale=0.002)
     check_against_oracle(w, PERSISTENT)
