@@ -158,12 +158,12 @@ __global__ void __launch_bounds__(kScoreWarps * 32, MSA_INDEX_MIN_CTAS) msa_inde
     const int64_t tbase = __ldg(p.table_offset + t);
     const int64_t L = len_raw > 0 ? (int64_t)len_raw : 0;
     const int64_t cta_j0 = (int64_t)((int64_t)blockIdx.x % cpq) * kScoreWarps * p.block_tokens;
-    if (cta_j0 >= L) {   // every block of this CTA is past the visible tokens
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-        if (lane == 0 && b < p.max_blocks)
-            p.block_scores[t * p.max_blocks + b] = -INFINITY;
+    // Every block of this CTA is past the visible tokens: nothing to score, and the
+    // top-k kernel writes these blocks' -inf, so the CTA leaves at once -- before the
+    // wait, freeing its slot for the CTAs with work (the grid is sized for the
+    // longest history).
+    if (cta_j0 >= L)
         return;
-    }
     // This warp's block, and its page-table entries, one per lane, requested before
     // the query (when the block spans at most 32 pages; otherwise each token looks
     // its page up itself).
@@ -1036,13 +1036,28 @@ __global__ void __launch_bounds__(kTopkThreads) msa_index_topk_kernel(const __gr
     __shared__ __align__(16) float s_row[kRankMaxBlocks];
     __shared__ int s_nfin;
     const int64_t t = blockIdx.x;
+    const int n = p.max_blocks;
+    // blocks from nb on hold no visible token: the per-query score kernel does not
+    // write them (its CTAs past the history leave at once), this kernel does
+    const int32_t len_raw = __ldg(p.kv_len + t);
+    const int64_t L = len_raw > 0 ? (int64_t)len_raw : 0;
+    const int64_t nb64 = (L + p.block_tokens - 1) / p.block_tokens;
+    const int nb = nb64 < n ? (int)nb64 : n;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // The next kernel may start its prologue once this grid has waited: every kernel
     // before this one has completed by then (see the producer's kernel for why the
     // signal comes after the wait).
     asm volatile("griddepcontrol.launch_dependents;" :::);
-    topk_row(p.block_scores + t * p.max_blocks, s_row, &s_nfin, false, p.max_blocks, p.topk,
-             p.topk_ids + t * p.topk);
+    float *row = p.block_scores + t * n;
+    for (int b = nb + (int)threadIdx.x; b < n; b += kTopkThreads)
+        row[b] = -INFINITY;
+    if (n <= kRankMaxBlocks) {   // stage the row, with -inf past the history
+        for (int b = threadIdx.x; b < n; b += kTopkThreads)
+            s_row[b] = b < nb ? row[b] : -INFINITY;
+    } else {
+        __syncthreads();   // the -inf above is in place before warp 0 reads the row
+    }
+    topk_row(row, s_row, &s_nfin, n <= kRankMaxBlocks, n, p.topk, p.topk_ids + t * p.topk);
 }
 
 // ---------------------------------------------------------------------------
