@@ -583,65 +583,78 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
 
     if (warp == 0) {
         // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            uint32_t it = 0, tile_it = 0;
-            bool ok = true;
-            for (int64_t ti = blockIdx.x; ti < num_tiles && ok; ti += gridDim.x, ++tile_it) {
-                const uint32_t tb = tile_it & 1;
-                if (*abort_flag || !mbar_wait_fast(smem_u32(&bar_tile_full[tb]), (tile_it >> 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t bt = bbase + tb * kBBytes;
-                for_each_segment<QT>(g_len[tb], g_toff[tb], p.max_blocks,
-                                     [&](uint32_t, int64_t, int32_t, int nb) {
-                    for (int b = 0; b < nb && ok; ++b, ++it) {
-                        const uint32_t s = it % kRunsNSA, ph = (it / kRunsNSA) & 1;
-                        const uint32_t a = it % kRunsNACC, pa = (it / kRunsNACC) & 1;
-                        if (*abort_flag || !mbar_wait_fast(smem_u32(&bar_a_full[s]), ph) ||
-                            !mbar_wait_fast(smem_u32(&bar_acc_empty[a]), pa ^ 1)) {
-                            ok = false;
-                            break;
-                        }
-                        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                        const uint32_t d = tmem + a * kAccCols;
-#ifndef MSA_STARVE
-#pragma unroll
-                        for (int ks = 0; ks < D / 16; ++ks) {
-                            const uint32_t at = tmem + kACol0 + s * kACols + (uint32_t)ks * 8u;
-                            const uint32_t koff = (uint32_t)(ks >> 2) * (128u * 128u) + (uint32_t)(ks & 3) * 32u;
-                            const uint64_t bd = sw128_desc(bt + koff);
-                            asm volatile(
-                                "{\n\t.reg .pred pp;\n\tsetp.ne.b32 pp, %4, 0;\n\t"
-                                "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pp;\n\t}" ::"r"(d),
-                                "r"(at), "l"(bd), "r"(kIdesc), "r"((uint32_t)ks)
-                                : "memory");
-                        }
-                        asm volatile(
-                            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                smem_u32(&bar_a_empty[s]))
-                            : "memory");
-                        asm volatile(
-                            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                smem_u32(&bar_acc_full[a]))
-                            : "memory");
-#else
-                        (void)d;
-#endif
-                    }
-                });
-                if (ok)   // this thread is done with the tile (its MMAs may still run)
-                    mbar_arrive_local(smem_u32(&bar_tile_empty[tb]));
+        // The whole warp runs the loop, so that the operands stay warp-uniform, and
+        // one elected lane issues each tcgen05 instruction; every wait result and
+        // abort-flag read is made warp-uniform before it steers control flow.
+        uint32_t tile_it = 0;
+        uint32_t s = 0, ph = 0, a = 0, pa = 0;   // key stage and accumulator of the next block, with parities
+        bool ok = true;
+        for (int64_t ti = blockIdx.x; ti < num_tiles && ok; ti += gridDim.x, ++tile_it) {
+            const uint32_t tb = tile_it & 1;
+            if (__any_sync(0xffffffffu, *abort_flag != 0) ||
+                !__all_sync(0xffffffffu, mbar_wait_fast(smem_u32(&bar_tile_full[tb]), (tile_it >> 1) & 1))) {
+                ok = false;
+                break;
             }
-            if (!ok)
-                *abort_flag = 1;
-            // every MMA has completed before tensor memory is released
-            asm volatile(
-                "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                    smem_u32(&bar_drain))
-                : "memory");
-            (void)mbar_wait_fast(smem_u32(&bar_drain), 0);
+            // the query tile's B descriptors, one per K step
+            const uint32_t bt = bbase + tb * kBBytes;
+            uint64_t bd[D / 16];
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+                bd[ks] = sw128_desc(bt + (uint32_t)(ks >> 2) * (128u * 128u) + (uint32_t)(ks & 3) * 32u);
+            for_each_segment<QT>(g_len[tb], g_toff[tb], p.max_blocks,
+                                 [&](uint32_t, int64_t, int32_t, int nb) {
+                for (int b = 0; b < nb && ok; ++b) {
+                    // the abort flag is read only when a stage or accumulator is not
+                    // ready yet: the ready path stays short
+                    if (!__all_sync(0xffffffffu, mbar_try(smem_u32(&bar_a_full[s]), ph) &&
+                                                     mbar_try(smem_u32(&bar_acc_empty[a]), pa ^ 1)) &&
+                        (__any_sync(0xffffffffu, *abort_flag != 0) ||
+                         !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_a_full[s]), ph) &&
+                                                      mbar_wait(smem_u32(&bar_acc_empty[a]), pa ^ 1)))) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t d = tmem + a * kAccCols;
+#ifndef MSA_STARVE
+                    const uint32_t at0 = tmem + kACol0 + s * kACols;
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        asm volatile(
+                            "{\n\t.reg .pred pp, pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
+                            "setp.ne.b32 pp, %4, 0;\n\t"
+                            "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pp;\n\t}" ::"r"(d),
+                            "r"(at0 + (uint32_t)ks * 8u), "l"(bd[ks]), "r"(kIdesc), "r"((uint32_t)ks)
+                            : "memory");
+                    }
+                    asm volatile(
+                        "{\n\t.reg .pred pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
+                        "@pe tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t"
+                        "@pe tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];\n\t}" ::"r"(
+                            smem_u32(&bar_a_empty[s])),
+                        "r"(smem_u32(&bar_acc_full[a]))
+                        : "memory");
+#else
+                    (void)d;
+#endif
+                    if (++s == (uint32_t)kRunsNSA) { s = 0; ph ^= 1u; }
+                    if (++a == (uint32_t)kRunsNACC) { a = 0; pa ^= 1u; }
+                }
+            });
+            __syncwarp();
+            if (ok && lane == 0)   // this warp is done with the tile (its MMAs may still run)
+                mbar_arrive_local(smem_u32(&bar_tile_empty[tb]));
         }
+        if (!ok && lane == 0)
+            *abort_flag = 1;
+        // every MMA has completed before tensor memory is released
+        asm volatile(
+            "{\n\t.reg .pred pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
+            "@pe tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+                smem_u32(&bar_drain))
+            : "memory");
+        (void)mbar_wait_fast(smem_u32(&bar_drain), 0);
         __syncwarp();
     } else if (warp <= 8) {
         // ---------------- gather ----------------
