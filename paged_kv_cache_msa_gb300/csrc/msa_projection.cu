@@ -343,51 +343,18 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8])
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
-                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-                 : "memory");
-}
 
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// Where an epilogue thread's accumulator row lives: this CTA's tensor memory and,
-// with the K dimension split over a cluster, the partial sums the other CTAs of
-// the cluster left in their shared memory ([column / 4][128 rows][4 columns] fp32:
-// a warp's 16-byte reads of four columns cover 512 contiguous bytes).
+// Where an epilogue thread's accumulator row lives: this CTA's tensor memory.
 struct AccSrc {
     uint32_t taddr;       // this warp's lanes at the tile's first column
-    int nsplit;           // CTAs whose partial sums add up to the accumulator
-    int row;              // this thread's row (tensor-memory lane)
-    uint32_t part;        // shared-memory offset of the partial sums in every CTA
-    uint32_t table;       // this warp's lanes at the RoPE table (cos at +k, sin at +64+k),
-                          // when the kernel filled one during the main loop
 };
 
-// 32 accumulator columns [col, col + 32) of this thread's row: the own partial sum
-// plus the other CTAs' in rank order
+// 32 accumulator columns [col, col + 32) of this thread's row
 __device__ __forceinline__ void acc_ld32(const AccSrc &a, int col, uint32_t (&r)[32])
 {
     tmem_ld32(a.taddr + (uint32_t)col, r);
     tmem_wait_ld();
-    for (int s = 1; s < a.nsplit; ++s) {
-        // eight 16-byte loads in flight before any is used
-        const uint32_t base = map_to_rank(a.part, (uint32_t)s) + (uint32_t)((col >> 2) * 128 + a.row) * 16u;
-        float4 v[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(v[j].x), "=f"(v[j].y), "=f"(v[j].z), "=f"(v[j].w)
-                         : "r"(base + (uint32_t)j * 2048u));
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + v[j].x);
-            r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + v[j].y);
-            r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + v[j].z);
-            r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + v[j].w);
-        }
-    }
 }
 
 // ---------------------------------------------------------------------------
@@ -523,9 +490,20 @@ struct Dest {
 #endif
 };
 
+// the reciprocal of the cache scale of a K, V or index-K head
+__device__ __forceinline__ float cache_inv_scale(const Params &p, const Head &hd)
+{
+    const int ci = hd.sec == 1 ? 0 : hd.sec == 2 ? 1 : 2;
+    const int si = p.scale_mode == MSA_SCALE_PER_HEAD
+                       ? (ci == 0 ? hd.h : ci == 1 ? p.hkv + hd.h : 2 * p.hkv + hd.h)
+                       : ci;
+    return __frcp_rn(__ldg(p.scales + si));
+}
+
+// inv_pre: that reciprocal when the caller has it already (negative: read it here)
 template <int D>
 __device__ __forceinline__ Dest make_dest(const Params &p, const Head &hd, int64_t t, bool live,
-                                          const Place &pl)
+                                          const Place &pl, float inv_pre = -1.0f)
 {
     Dest ds;
     ds.row = nullptr;
@@ -554,12 +532,9 @@ __device__ __forceinline__ Dest make_dest(const Params &p, const Head &hd, int64
     ds.hi = p.cache_hi[ci];
 #endif
     if (cc.fp8) {
-        const int si = p.scale_mode == MSA_SCALE_PER_HEAD
-                           ? (ci == 0 ? hd.h : ci == 1 ? p.hkv + hd.h : 2 * p.hkv + hd.h)
-                           : ci;
         ds.row = cc.data + e;
         ds.fp8 = 1;
-        ds.inv = __frcp_rn(__ldg(p.scales + si));
+        ds.inv = inv_pre >= 0.0f ? inv_pre : cache_inv_scale(p, hd);
     } else {
         ds.row = cc.data + 2 * e;
     }
@@ -632,7 +607,7 @@ __device__ __forceinline__ void rope_sincos(float a, float *s, float *c)
 // D/2 or 0).  The accumulator is read from tensor memory once and the bf16 row
 // is kept in registers; the head's norm weights and per-output scales are held by
 // the lanes of the warp (lane l: dims l, l + 32, ...) and shuffled to every lane.
-template <int D, int ROT, bool TABLE>
+template <int D, int ROT>
 __device__ __forceinline__ void head_fast(const Params &p, const Head &hd, const AccSrc &src,
                                           int tcol, int col,
                                           int64_t t, bool live, const Place &pl, int pos,
@@ -696,21 +671,10 @@ __device__ __forceinline__ void head_fast(const Params &p, const Head &hd, const
 #pragma unroll
     for (int k0 = 0; k0 < H; k0 += 8) {
         float yu[8], yv[8];
-        uint32_t ct[8], st[8];
-        if (TABLE) {   // filled by this row's threads while the main loop ran
-            tmem_ld8(src.table + (uint32_t)k0, ct);
-            tmem_ld8(src.table + 64u + (uint32_t)k0, st);
-            tmem_wait_ld();
-        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             float sn, cs;
-            if (TABLE) {
-                cs = __uint_as_float(ct[j]);
-                sn = __uint_as_float(st[j]);
-            } else {
-                rope_sincos((float)pos * p.inv_freq[k0 + j], &sn, &cs);
-            }
+            rope_sincos((float)pos * p.inv_freq[k0 + j], &sn, &cs);
             const float a = (elt(k0 + j) * rn) * wgt(k0 + j);
             const float b = (elt(k0 + H + j) * rn) * wgt(k0 + H + j);
             yu[j] = fmaf(-b, sn, a * cs);
@@ -732,7 +696,7 @@ __device__ __forceinline__ void head_fast(const Params &p, const Head &hd, const
 // taddr: tensor-memory address of this warp's lanes at the tile's first column.
 // The warp runs the producer on the tile's heads hh with hh % 2 == hgroup (the
 // other epilogue warp of the same tensor-memory lanes takes the rest).
-template <int D, bool TABLE = false>
+template <int D>
 __device__ __forceinline__ void epilogue_tile(const Params &p, const AccSrc &src, int n_tile,
                                               int64_t t, bool live, int hgroup, int lane)
 {
@@ -769,11 +733,11 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const AccSrc &src
                 continue;
             const int col = col0 + hh * D;
             if (rd == D)
-                head_fast<D, D, TABLE>(p, hd, src, hh * D, col, t, live, pl, pos, rs, lane);
+                head_fast<D, D>(p, hd, src, hh * D, col, t, live, pl, pos, rs, lane);
             else if (rd == D / 2)
-                head_fast<D, D / 2, TABLE>(p, hd, src, hh * D, col, t, live, pl, pos, rs, lane);
+                head_fast<D, D / 2>(p, hd, src, hh * D, col, t, live, pl, pos, rs, lane);
             else
-                head_fast<D, 0, TABLE>(p, hd, src, hh * D, col, t, live, pl, pos, rs, lane);
+                head_fast<D, 0>(p, hd, src, hh * D, col, t, live, pl, pos, rs, lane);
         }
         return;
     }
@@ -1105,10 +1069,6 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
             const int64_t t = (int64_t)m * kPairM + (int64_t)rank * kBM + row;
             AccSrc src;
             src.taddr = tmem + lane_base + b * kBN;
-            src.nsplit = 1;
-            src.table = 0;
-            src.row = row;
-            src.part = 0;
             epilogue_tile<D>(p, src, n, t, t < p.num_tokens, hgroup, lane);
             tc_fence_before();
             __syncwarp();
@@ -1136,24 +1096,23 @@ msa_projection_kernel(const __grid_constant__ CUtensorMap tmap_x,
 // one cluster per 256-wide output tile busy, each walking all of K.  Here a
 // cluster of S CTAs takes one output tile and CTA s of it a contiguous S-th of the
 // K blocks, accumulating 128 tokens x 256 outputs in its own tensor memory with the
-// one-SM MMA (tcgen05.mma.cta_group::1, M 128, N 256).  The other CTAs then write
-// their partial sums into their shared memory (the ring is free by then) as
-// [column / 4][128 rows][4 columns] fp32, and CTA 0's epilogue adds them in rank
-// order over distributed shared memory before running the producer.  While the
-// main loop runs, CTA 0's epilogue warps fill a RoPE cos / sin table for their
-// rows in tensor memory (columns 256-383), which the epilogue reads back instead
-// of evaluating the angles after the main loop.  Used for NeoX RoPE over D, D/2
-// or no dims (the register-resident epilogue); other layouts take the 2-SM kernel.
+// one-SM MMA (tcgen05.mma.cta_group::1, M 128, N 256).  Every CTA then writes its
+// partial sum into its shared memory (the ring is free by then), and the
+// producer epilogue of the tile is spread over the epilogue warps of all S CTAs,
+// each (token, head) row taken by a group of lanes that add the S partial sums in
+// rank order over distributed shared memory (splitk_epilogue).  Used for NeoX RoPE
+// over D, D/2 or no dims; other layouts take the 2-SM kernel.
 
 constexpr int kSplitStages = 4;
 constexpr uint32_t kSplitStageBytes = kTileABytes + 2 * kTileBBytes;  // 128 tokens + 256 weight rows
 constexpr int kSplitDynSmem = kSplitStages * kSplitStageBytes + 1024;
-static_assert(kSplitStages * kSplitStageBytes >= 128u * kBN * 4u, "partial sums fit the ring");
+// an exported partial sum: 128 rows of 256 fp32 columns, rows 16 bytes further apart
+// than their length so that both the export (a thread per row) and the epilogue's
+// reads (lanes along a row) hit distinct banks
+constexpr uint32_t kPartRowBytes = kBN * 4u + 16u;
+static_assert(kSplitStages * kSplitStageBytes >= 128u * kPartRowBytes, "partial sums fit the ring");
 constexpr uint32_t kIdescShape1 = ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-// tensor memory: the accumulator in columns [0, 256), CTA 0's RoPE table (cos, sin of
-// up to 64 frequencies per row) in [256, 384); allocations are powers of two
-constexpr uint32_t kSplitTmemCols = 512;
-constexpr uint32_t kTableCol = kBN;
+constexpr uint32_t kSplitTmemCols = kBN;   // the accumulator
 
 template <bool FP8>
 __device__ __forceinline__ void tc_mma1(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc)
@@ -1189,6 +1148,174 @@ __device__ __forceinline__ void tma_load_own(uint32_t dst, const CUtensorMap *ma
         : "memory");
 }
 
+// The epilogue of a tile whose K dimension was split over the cluster's S CTAs,
+// spread over every epilogue warp of the cluster.  Item i = (token t, head hh of
+// the tile) goes to a group of D / 8 lanes; lane u of the group holds dims
+// [8u, 8u + 8) of the head row.  Its accumulator is the sum, in rank order, of the
+// partial sums the S CTAs exported to their shared memory; the sum of squares of
+// the rounded bf16 row is a shuffle reduction over the group, and the NeoX partner
+// of a rotated dim (k and k + rd/2) sits rd/16 lanes away.  What the items read
+// besides the partial sums was staged in this CTA's shared memory during the main
+// loop: per token its position, placement and hidden scale; per tile column its
+// norm weight and per-output scale; per head of the tile its cache scale's
+// reciprocal.
+struct SplitStage {
+    int pos[kBM];
+    Place place[kBM];
+    float sx[kBM];
+    float nw[kBN];     // norm weight of the column's head (1: V, or no weight)
+    float sw[kBN];     // per-output scale (1: none, or past the outputs)
+    float dinv[8];     // per head of the tile (negative: not an fp8 cache head)
+    float freq[kMaxRotaryHalf];   // RoPE frequencies: the lanes of a warp index them apart, which
+                       // the kernel-parameter bank would serve one address at a time
+};
+
+// dry: one pass that reads only this CTA's own shared memory and stores nothing,
+// run by the idle epilogue warps during the main loop so that the epilogue's code
+// is in the instruction caches when the real passes come (they run once per
+// launch, on SMs whose caches hold only the main loop).  Out of line, so that both
+// calls run the same instructions.
+template <int D>
+__device__ __noinline__ void splitk_epilogue(const Params &p, uint32_t part, int S, uint32_t self,
+                                             int n_tile, const SplitStage &st, int worker,
+                                             int nworkers, int lane, bool dry)
+{
+    constexpr int LPI = D / 8;          // lanes per item
+    constexpr int IPW = 32 / LPI;       // items per warp and pass
+    constexpr int HPT = kBN / D;        // heads per tile
+    const int c = 8 * (lane % LPI);     // this lane's first dim of the head row
+    const int g0 = n_tile * HPT;
+    const int col0 = n_tile * kBN;
+    const int total = p.num_tokens * HPT;
+    const int rd = p.rotary_dim, half = rd / 2;
+    const bool any_scale = p.hidden_scales || p.weight_scales;
+    // every lane runs every pass (the shuffles need the whole warp); a lane past the
+    // last item computes on row 0 and stores nothing.  The partial sums of ranks
+    // 0..3 for the next pass are loaded while the current pass computes.
+    const int stride = nworkers * IPW;
+    auto item_off = [&](int b) -> uint32_t {
+        const int i = b + lane / LPI;
+        const int t = i < total ? i / HPT : 0, hh = i < total ? i % HPT : 0;
+        return (uint32_t)t * kPartRowBytes + (uint32_t)(hh * D + c) * 4u;
+    };
+    auto load8 = [&](uint32_t off, int r, float4 (&v)[2]) {
+        const uint32_t a = map_to_rank(part + off, dry ? self : (uint32_t)r);
+        asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(v[0].x), "=f"(v[0].y), "=f"(v[0].z), "=f"(v[0].w)
+                     : "r"(a));
+        asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(v[1].x), "=f"(v[1].y), "=f"(v[1].z), "=f"(v[1].w)
+                     : "r"(a + 16u));
+    };
+    float4 nx[4][2];
+    if (worker * IPW < total) {
+        const uint32_t off = item_off(worker * IPW);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (k < S)
+                load8(off, k, nx[k]);
+    }
+    for (int base = worker * IPW; base < total; base += stride) {
+        const int i = base + lane / LPI;
+        const bool on = i < total;
+        const bool store = on && !dry;
+        const int t = on ? i / HPT : 0, hh = on ? i % HPT : 0;
+        Head hd = head_of(p, g0 + hh);
+        if (!on)
+            hd.sec = -1;
+        const int tc = hh * D + c, col = col0 + tc;
+        const bool normed = hd.sec >= 0 && hd.sec != 2;
+
+        // the accumulator: the partial sums in rank order
+        float4 cur[4][2];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            cur[k][0] = nx[k][0];
+            cur[k][1] = nx[k][1];
+        }
+        if (!dry && base + stride < total) {
+            const uint32_t off = item_off(base + stride);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (k < S)
+                    load8(off, k, nx[k]);
+        }
+        float acc[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (k < S) {
+                const float x[8] = {cur[k][0].x, cur[k][0].y, cur[k][0].z, cur[k][0].w,
+                                    cur[k][1].x, cur[k][1].y, cur[k][1].z, cur[k][1].w};
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    acc[j] = k == 0 ? x[j] : acc[j] + x[j];
+            }
+        }
+        for (int r = 4; r < S; ++r) {
+            float4 v[2];
+            load8(item_off(base), r, v);
+            const float x[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                acc[j] += x[j];
+        }
+
+        // the bf16 row (dequantised accumulator, rounded) and its sum of squares
+        const float sx = st.sx[t];
+        uint32_t bits[4];
+        float e[8];
+        float ss = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+            float a = acc[j], b = acc[j + 1];
+            if (any_scale) {
+                a = (a * sx) * st.sw[tc + j];
+                b = (b * sx) * st.sw[tc + j + 1];
+            }
+            bits[j / 2] = pack_bf16x2(a, b);
+            e[j] = bf16_lo(bits[j / 2]);
+            e[j + 1] = bf16_hi(bits[j / 2]);
+            ss = fmaf(e[j], e[j], ss);
+            ss = fmaf(e[j + 1], e[j + 1], ss);
+        }
+        if (p.rows_out && store && hd.sec >= 0) {
+            uint16_t *dst = p.rows_out + (int64_t)t * p.rows_out_stride + col;
+            MSA_GUARD(dst, 16, p.rows_out, p.rows_hi)
+            st_v4(dst, bits[0], bits[1], bits[2], bits[3]);
+        }
+#pragma unroll
+        for (int m = 1; m < LPI; m <<= 1)
+            ss += __shfl_xor_sync(0xffffffffu, ss, m);
+        const float rn = rsqrtf(fmaf(ss, 1.0f / (float)D, p.rms_eps));
+
+        // norm (Q, K, idx-Q, idx-K), then NeoX RoPE over the first rd dims
+        float y[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            y[j] = normed ? (e[j] * rn) * st.nw[tc + j] : e[j];
+        if (rd > 0) {
+            float px[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                px[j] = __shfl_xor_sync(0xffffffffu, y[j], half / 8);
+            if (normed && c < rd) {
+                const bool first = c < half;
+                const int kb = first ? c : c - half;
+                const int pos = st.pos[t];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float sn, cs;
+                    rope_sincos((float)pos * st.freq[kb + j], &sn, &cs);
+                    y[j] = first ? fmaf(-px[j], sn, y[j] * cs) : fmaf(px[j], sn, y[j] * cs);
+                }
+            }
+        }
+        emit8(make_dest<D>(p, hd, t, store, st.place[t], st.dinv[hh]), c, y);
+        if (dry)
+            break;
+    }
+}
+
 template <int D, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
 msa_projection_splitk_kernel(const __grid_constant__ CUtensorMap tmap_x,
@@ -1201,6 +1328,7 @@ msa_projection_splitk_kernel(const __grid_constant__ CUtensorMap tmap_x,
     __shared__ __align__(8) uint64_t bar_drain;
     __shared__ uint32_t s_tmem;
     __shared__ uint32_t s_fail;   // a wait of this CTA ran out: its partial sum is not valid
+    __shared__ SplitStage s_st;   // what the epilogue reads besides the partial sums
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1296,47 +1424,64 @@ msa_projection_splitk_kernel(const __grid_constant__ CUtensorMap tmap_x,
         }
         __syncwarp();
     } else {
-        // the other CTAs export their partial sums into the ring, four columns of a
-        // row per 16 bytes
+        // Every CTA exports its partial sum into the ring (free once the accumulator
+        // is complete), as [row][256 columns] fp32 rows kPartRowBytes apart.  Before
+        // that, while the main loop runs, the epilogue warps stage what this CTA's
+        // share of the epilogue reads: one warp per lane quarter the metadata of its
+        // 32 tokens, the other four the tile's per-column and per-head values.
         const int quarter = warp & 3, hgroup = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        if (rank == 0 && p.rotary_dim > 0 && __any_sync(0xffffffffu, row < p.num_tokens)) {
-            // While the main loop runs: this row's RoPE cos / sin, the two warps of a
-            // lane quarter taking half the frequencies each, into tensor memory for
-            // the epilogue (the same angle and evaluation it would make itself); a
-            // warp whose rows are all past the last token skips it
-            const int H = p.rotary_dim / 2;   // 16, 32 or 64: halves are whole blocks of 8
-            const int pos = row < p.num_tokens ? __ldg(p.positions + row) : 0;
-            for (int k0 = hgroup * (H / 2); k0 < (hgroup + 1) * (H / 2); k0 += 8) {
-                uint32_t ct[8], st[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    float sn, cs;
-                    rope_sincos((float)pos * p.inv_freq[k0 + j], &sn, &cs);
-                    ct[j] = __float_as_uint(cs);
-                    st[j] = __float_as_uint(sn);
-                }
-                tmem_st8(tmem + lane_base + kTableCol + (uint32_t)k0, ct);
-                tmem_st8(tmem + lane_base + kTableCol + 64u + (uint32_t)k0, st);
+        if (hgroup == 0) {
+            Place pl;
+            pl.page = -1;
+            pl.off = 0;
+            pl.valid = 0;
+            int pos = 0;
+            float sx = 1.0f;
+            if (row < p.num_tokens) {
+                pos = __ldg(p.positions + row);
+                pl = place_token(p, __ldg(p.slots + row));
+                if (p.hidden_scales)
+                    sx = __ldg(p.hidden_scales + row);
             }
-            tmem_wait_st();
+            s_st.pos[row] = pos;
+            s_st.place[row] = pl;
+            s_st.sx[row] = sx;
+        } else {
+            constexpr int HPT = kBN / D;
+            for (int tc = row; tc < kBN; tc += kBM) {
+                const int hh = tc / D;
+                const Head hd = head_of(p, n_tile * HPT + hh);
+                const bool normed = hd.sec >= 0 && hd.sec != 2;
+                s_st.nw[tc] = normed ? norm_weight(p.norm_w[norm_index(hd.sec)], tc % D) : 1.0f;
+                s_st.sw[tc] = (p.weight_scales && hd.sec >= 0) ? __ldg(p.weight_scales + n_tile * kBN + tc) : 1.0f;
+            }
+            if (row < p.rotary_dim / 2)
+                s_st.freq[row] = p.inv_freq[row];
+            if (row < HPT) {
+                const Head hd = head_of(p, n_tile * HPT + row);
+                const int ci = hd.sec == 1 ? 0 : hd.sec == 2 ? 1 : hd.sec == 4 ? 2 : -1;
+                s_st.dinv[row] = (ci >= 0 && p.cache[ci].data && p.cache[ci].fp8) ? cache_inv_scale(p, hd) : -1.0f;
+            }
         }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpilogueWarps) : "memory");   // staged
+        splitk_epilogue<D>(p, ring, S, rank, n_tile, s_st, warp - 2, kEpilogueWarps, lane, true);
         const bool got = mbar_wait(smem_u32(&bar_tfull), 0);
         if (!__all_sync(0xffffffffu, got))
             ok = false;
         tc_fence_after();
-        if (rank > 0 && ok && __any_sync(0xffffffffu, row < p.num_tokens)) {
+        if (ok && __any_sync(0xffffffffu, row < p.num_tokens)) {
             // (rows past the last token are never read back)
 #pragma unroll
             for (int c0 = hgroup * (kBN / 2); c0 < (hgroup + 1) * (kBN / 2); c0 += 32) {
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_base + (uint32_t)c0, r);
                 tmem_wait_ld();
+                const uint32_t dst = ring + (uint32_t)row * kPartRowBytes + (uint32_t)c0 * 4u;
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                     ring + (uint32_t)(((c0 >> 2) + j) * 128 + row) * 16u),
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 16u * (uint32_t)j),
                                  "r"(r[4 * j]), "r"(r[4 * j + 1]), "r"(r[4 * j + 2]), "r"(r[4 * j + 3])
                                  : "memory");
             }
@@ -1351,33 +1496,26 @@ msa_projection_splitk_kernel(const __grid_constant__ CUtensorMap tmap_x,
         *(volatile uint32_t *)&s_fail = 1u;
     tc_fence_before();
     cluster_sync();   // every CTA's partial sums (and failure flags) are in place
-    bool all_ok = ok;
-    if (rank == 0 && warp >= 2) {
+    {
+        // every warp of the cluster reads every CTA's flag (loads issued together), so
+        // the cluster agrees, and takes a share of the epilogue
+        uint32_t fails = ok ? 0u : 1u;
         for (int r = 0; r < S; ++r) {
             uint32_t f;
             asm volatile("ld.shared::cluster.u32 %0, [%1];"
                          : "=r"(f)
                          : "r"(map_to_rank(smem_u32(&s_fail), (uint32_t)r))
                          : "memory");
-            all_ok = all_ok && f == 0u;
+            fails |= f;
         }
-    }
-    if (rank == 0 && warp >= 2 && all_ok) {
-        const int quarter = warp & 3, hgroup = (warp - 2) >> 2;
-        const int row = quarter * 32 + lane;
-        tc_fence_after();
-        AccSrc src;
-        src.taddr = tmem + ((uint32_t)(quarter * 32) << 16);
-        src.nsplit = S;
-        src.row = row;
-        src.part = ring;
-        src.table = tmem + ((uint32_t)(quarter * 32) << 16) + kTableCol;
-        epilogue_tile<D, true>(p, src, n_tile, row, row < p.num_tokens, hgroup, lane);
+        if (__all_sync(0xffffffffu, fails == 0u))
+            splitk_epilogue<D>(p, ring, S, rank, n_tile, s_st, warp * S + (int)rank,
+                               (kThreads / 32) * S, lane, false);
     }
     if (!ok && p.status)
         atomicOr(p.status, MSA_STATUS_WAIT_TIMEOUT);
     tc_fence_before();
-    cluster_sync();   // CTA 0 has read them
+    cluster_sync();   // no CTA reads another's partial sums any more
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
