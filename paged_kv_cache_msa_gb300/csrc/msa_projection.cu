@@ -1170,15 +1170,9 @@ struct SplitStage {
                        // the kernel-parameter bank would serve one address at a time
 };
 
-// dry: one pass that reads only this CTA's own shared memory and stores nothing,
-// run by the idle epilogue warps during the main loop so that the epilogue's code
-// is in the instruction caches when the real passes come (they run once per
-// launch, on SMs whose caches hold only the main loop).  Out of line, so that both
-// calls run the same instructions.
 template <int D>
-__device__ __noinline__ void splitk_epilogue(const Params &p, uint32_t part, int S, uint32_t self,
-                                             int n_tile, const SplitStage &st, int worker,
-                                             int nworkers, int lane, bool dry)
+__device__ __forceinline__ void splitk_epilogue(const Params &p, uint32_t part, int S, int n_tile,
+                                                const SplitStage &st, int worker, int nworkers, int lane)
 {
     constexpr int LPI = D / 8;          // lanes per item
     constexpr int IPW = 32 / LPI;       // items per warp and pass
@@ -1190,74 +1184,42 @@ __device__ __noinline__ void splitk_epilogue(const Params &p, uint32_t part, int
     const int rd = p.rotary_dim, half = rd / 2;
     const bool any_scale = p.hidden_scales || p.weight_scales;
     // every lane runs every pass (the shuffles need the whole warp); a lane past the
-    // last item computes on row 0 and stores nothing.  The partial sums of ranks
-    // 0..3 for the next pass are loaded while the current pass computes.
+    // last item computes on row 0 and stores nothing
     const int stride = nworkers * IPW;
-    auto item_off = [&](int b) -> uint32_t {
-        const int i = b + lane / LPI;
-        const int t = i < total ? i / HPT : 0, hh = i < total ? i % HPT : 0;
-        return (uint32_t)t * kPartRowBytes + (uint32_t)(hh * D + c) * 4u;
-    };
-    auto load8 = [&](uint32_t off, int r, float4 (&v)[2]) {
-        const uint32_t a = map_to_rank(part + off, dry ? self : (uint32_t)r);
-        asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(v[0].x), "=f"(v[0].y), "=f"(v[0].z), "=f"(v[0].w)
-                     : "r"(a));
-        asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(v[1].x), "=f"(v[1].y), "=f"(v[1].z), "=f"(v[1].w)
-                     : "r"(a + 16u));
-    };
-    float4 nx[4][2];
-    if (worker * IPW < total) {
-        const uint32_t off = item_off(worker * IPW);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            if (k < S)
-                load8(off, k, nx[k]);
-    }
     for (int base = worker * IPW; base < total; base += stride) {
         const int i = base + lane / LPI;
         const bool on = i < total;
-        const bool store = on && !dry;
         const int t = on ? i / HPT : 0, hh = on ? i % HPT : 0;
         Head hd = head_of(p, g0 + hh);
         if (!on)
             hd.sec = -1;
         const int tc = hh * D + c, col = col0 + tc;
         const bool normed = hd.sec >= 0 && hd.sec != 2;
-
-        // the accumulator: the partial sums in rank order
-        float4 cur[4][2];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            cur[k][0] = nx[k][0];
-            cur[k][1] = nx[k][1];
-        }
-        if (!dry && base + stride < total) {
-            const uint32_t off = item_off(base + stride);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                if (k < S)
-                    load8(off, k, nx[k]);
-        }
+        // the accumulator: the partial sums in rank order, four ranks' loads in flight
         float acc[8];
+        const uint32_t off = (uint32_t)t * kPartRowBytes + (uint32_t)tc * 4u;
+        for (int r0 = 0; r0 < S; r0 += 4) {
+            float4 v[4][2];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            if (k < S) {
-                const float x[8] = {cur[k][0].x, cur[k][0].y, cur[k][0].z, cur[k][0].w,
-                                    cur[k][1].x, cur[k][1].y, cur[k][1].z, cur[k][1].w};
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    acc[j] = k == 0 ? x[j] : acc[j] + x[j];
+            for (int k = 0; k < 4; ++k) {
+                if (r0 + k < S) {
+                    const uint32_t a = map_to_rank(part + off, (uint32_t)(r0 + k));
+                    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                 : "=f"(v[k][0].x), "=f"(v[k][0].y), "=f"(v[k][0].z), "=f"(v[k][0].w) : "r"(a));
+                    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                 : "=f"(v[k][1].x), "=f"(v[k][1].y), "=f"(v[k][1].z), "=f"(v[k][1].w) : "r"(a + 16u));
+                }
             }
-        }
-        for (int r = 4; r < S; ++r) {
-            float4 v[2];
-            load8(item_off(base), r, v);
-            const float x[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                acc[j] += x[j];
+            for (int k = 0; k < 4; ++k) {
+                if (r0 + k < S) {
+                    const float x[8] = {v[k][0].x, v[k][0].y, v[k][0].z, v[k][0].w,
+                                        v[k][1].x, v[k][1].y, v[k][1].z, v[k][1].w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        acc[j] = (r0 + k == 0) ? x[j] : acc[j] + x[j];
+                }
+            }
         }
 
         // the bf16 row (dequantised accumulator, rounded) and its sum of squares
@@ -1278,7 +1240,7 @@ __device__ __noinline__ void splitk_epilogue(const Params &p, uint32_t part, int
             ss = fmaf(e[j], e[j], ss);
             ss = fmaf(e[j + 1], e[j + 1], ss);
         }
-        if (p.rows_out && store && hd.sec >= 0) {
+        if (p.rows_out && hd.sec >= 0) {
             uint16_t *dst = p.rows_out + (int64_t)t * p.rows_out_stride + col;
             MSA_GUARD(dst, 16, p.rows_out, p.rows_hi)
             st_v4(dst, bits[0], bits[1], bits[2], bits[3]);
@@ -1310,9 +1272,7 @@ __device__ __noinline__ void splitk_epilogue(const Params &p, uint32_t part, int
                 }
             }
         }
-        emit8(make_dest<D>(p, hd, t, store, st.place[t], st.dinv[hh]), c, y);
-        if (dry)
-            break;
+        emit8(make_dest<D>(p, hd, t, on, st.place[t], st.dinv[hh]), c, y);
     }
 }
 
@@ -1465,8 +1425,6 @@ msa_projection_splitk_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 s_st.dinv[row] = (ci >= 0 && p.cache[ci].data && p.cache[ci].fp8) ? cache_inv_scale(p, hd) : -1.0f;
             }
         }
-        asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpilogueWarps) : "memory");   // staged
-        splitk_epilogue<D>(p, ring, S, rank, n_tile, s_st, warp - 2, kEpilogueWarps, lane, true);
         const bool got = mbar_wait(smem_u32(&bar_tfull), 0);
         if (!__all_sync(0xffffffffu, got))
             ok = false;
@@ -1496,8 +1454,8 @@ msa_projection_splitk_kernel(const __grid_constant__ CUtensorMap tmap_x,
         *(volatile uint32_t *)&s_fail = 1u;
     tc_fence_before();
     cluster_sync();   // every CTA's partial sums (and failure flags) are in place
-    {
-        // every warp of the cluster reads every CTA's flag (loads issued together), so
+    if (warp >= 2) {
+        // every epilogue warp reads every CTA's flag (the loads issued together), so
         // the cluster agrees, and takes a share of the epilogue
         uint32_t fails = ok ? 0u : 1u;
         for (int r = 0; r < S; ++r) {
@@ -1509,8 +1467,7 @@ msa_projection_splitk_kernel(const __grid_constant__ CUtensorMap tmap_x,
             fails |= f;
         }
         if (__all_sync(0xffffffffu, fails == 0u))
-            splitk_epilogue<D>(p, ring, S, rank, n_tile, s_st, warp * S + (int)rank,
-                               (kThreads / 32) * S, lane, false);
+            splitk_epilogue<D>(p, ring, S, n_tile, s_st, (warp - 2) * S + (int)rank, 8 * S, lane);
     }
     if (!ok && p.status)
         atomicOr(p.status, MSA_STATUS_WAIT_TIMEOUT);
