@@ -499,11 +499,11 @@ def indexer_timing(replays: int = 200, calls: int = 20):
     s = torch.cuda.Stream()
     torch.cuda.synchronize()
 
-    def graph_us(flags):
+    def graph_us(flags, fused=False):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
             for _ in range(calls):
-                dv.run(stream=s, launch_flags=flags)
+                dv.run(stream=s, launch_flags=flags, fused=fused)
         with torch.cuda.stream(s):
             for _ in range(3):
                 g.replay()
@@ -518,11 +518,16 @@ def indexer_timing(replays: int = 200, calls: int = 20):
 
     us_plain = graph_us(0)
     us = graph_us(B.MSA_LAUNCH_PDL)
+    us_fused = graph_us(B.MSA_LAUNCH_PDL, fused=True)
     alg = w.algorithmic_bytes()
     peak, _ = peaks()
     return {"workload": "decode batch 64, contexts U{1..9216}, 8 index heads x 128, fp8 index-K, "
                         "top-16 of 128-token blocks",
             "us_per_call": us, "us_per_call_without_pdl": us_plain, "launches_per_call": 2,
+            "single_launch": {"entry": "msa_indexer_forward_fused", "us_per_call": us_fused,
+                              "launches_per_call": 1,
+                              "gbs": alg / (us_fused * 1e-6) / 1e9,
+                              "frac_of_peak": alg / (us_fused * 1e-6) / 1e9 / peaks()[0]},
             "algorithmic_bytes": alg,
             "gbs": alg / (us * 1e-6) / 1e9, "frac_of_peak": alg / (us * 1e-6) / 1e9 / peak,
             "index_k_tokens_scanned": int(w.kv_len.sum())}
@@ -550,15 +555,16 @@ def decode_layer_timing(layers: int = 60, replays: int = 50):
         stack.append(DecodeLayer(DeviceWorkload(w, pools_on_device=pools), max_blocks_per_seq=144))
     s = torch.cuda.Stream()
     out = {}
-    for name, flags in (("pdl", B.MSA_LAUNCH_PDL), ("no_pdl", 0)):
+    for name, flags, fused in (("pdl", B.MSA_LAUNCH_PDL, False), ("no_pdl", 0, False),
+                               ("pdl_single_launch_indexer", B.MSA_LAUNCH_PDL, True)):
         with torch.cuda.stream(s):
             for layer in stack:
-                layer.run(s, flags)
+                layer.run(s, flags, fused=fused)
             s.synchronize()
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=s):
                 for layer in stack:
-                    layer.run(s, flags)
+                    layer.run(s, flags, fused=fused)
             for _ in range(3):
                 g.replay()
             s.synchronize()
@@ -569,7 +575,8 @@ def decode_layer_timing(layers: int = 60, replays: int = 50):
             e1.record(s)
             e1.synchronize()
         us = 1e3 * e0.elapsed_time(e1) / replays
-        out[name] = {"us_per_step": us, "us_per_layer": us / layers}
+        out[name] = {"us_per_step": us, "us_per_layer": us / layers,
+                     "launches_per_layer": 2 if fused else 3}
     return {"workload": f"decode batch 64, big shapes, contexts U{{1..9216}}: producer + indexer "
                         f"(top-16 of 128-token blocks) per layer, {layers} layers in one CUDA graph",
             "launches_per_layer": 3, **out}

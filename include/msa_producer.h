@@ -263,6 +263,33 @@ msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t num_queries, 
                                cudaStream_t stream);
 
 /*
+ * msa_indexer_forward in a single launch: the same scores, block scores and top-k
+ * ids (bit for bit), with the top-k taken inside the per-query score kernel instead
+ * of a second kernel.  Each of the query's CTAs that scores blocks counts itself in
+ * counters[t] once its block scores are stored; the CTA that arrives last resets
+ * counters[t] to zero and ranks the query's row.
+ *
+ * counters       device int32 [num_queries], caller-owned scratch: every entry must
+ *                be 0 on entry, and a launch that runs to completion leaves every
+ *                entry 0 again, so one buffer zeroed once serves any number of
+ *                launches issued one after another on a stream (or replayed in a
+ *                graph).  Launches that may run at the same time need separate
+ *                buffers.  4-byte aligned.
+ * launch_flags   as for msa_indexer_forward; with MSA_LAUNCH_QUERY_RUNS the
+ *                query-run kernel and the top-k kernel run as there, and counters is
+ *                not touched.
+ * Other arguments and errors as for msa_indexer_forward; counters NULL is
+ * MSA_ERR_INVALID_ARGUMENT, misaligned MSA_ERR_MISALIGNED.  One kernel is enqueued
+ * on `stream`; the library allocates nothing.
+ */
+msa_status msa_indexer_forward_fused(const msa_indexer_cfg *cfg, int64_t num_queries,
+                                     const void *idx_q, const int32_t *kv_len,
+                                     const int64_t *table_offset, const int32_t *page_table,
+                                     int64_t page_table_len, const msa_cache_desc *idx_k_cache,
+                                     const float *k_scale, float *block_scores, int32_t *topk_ids,
+                                     int32_t *counters, int32_t launch_flags, cudaStream_t stream);
+
+/*
  * Device address at which the GPU of the current device reaches host memory
  * `host_ptr` (pinned, mapped host memory; on Grace-Blackwell the GPU reads and
  * writes it over NVLink-C2C).  Sets *device_ptr and returns MSA_OK when the

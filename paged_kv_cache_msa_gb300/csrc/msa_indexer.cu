@@ -69,6 +69,7 @@ struct IndexerParams {
     int32_t topk;
     int32_t max_blocks;
     int32_t pdl;                    // launched with programmatic dependent launch
+    int32_t *counters;              // [T] arrivals per query (single launch), else nullptr
 };
 
 __device__ __forceinline__ uint4 ldg16(const void *p)
@@ -135,7 +136,159 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
     return h2;
 }
 
+// (a, ia) ranks before (b, ib): higher score first, lower id among equals.
+__device__ __forceinline__ bool ranks_before(float a, int ia, float b, int ib)
+{
+    return a > b || (a == b && ia < ib);
+}
+
+constexpr int kTopkThreads = 128;
+constexpr int kRankMaxBlocks = 1024;   // rows up to this many blocks are ranked in shared memory
+
+// Top-k ids of one row of n block scores, by the kTopkThreads threads of a CTA.
+// The row is read from global memory through L2 (ld.global.cg): in the single-launch
+// indexer it holds scores that other CTAs of the same kernel wrote.
+// Short rows (n <= kRankMaxBlocks) are ranked in shared memory s_row: every finite
+// entry counts the entries ranked before it, all threads in parallel, and entries
+// with rank < topk write their id at that rank.  When `staged`, s_row already holds
+// the row; otherwise it is read from `row`.  Long rows: warp 0 takes topk rounds,
+// each an arg-max over the entries ranked after the previous pick, reading `row`.
+__device__ __forceinline__ void topk_row(const float *row, float *s_row, int *s_nfin, bool staged,
+                                         int n, int topk, int32_t *out)
+{
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (n <= kRankMaxBlocks) {
+        if (tid == 0)
+            *s_nfin = 0;
+        __syncthreads();
+        int nfin = 0;
+        const int npad = (n + 3) & ~3;
+        for (int b = tid; b < npad; b += kTopkThreads) {
+            const float v = b < n ? (staged ? s_row[b] : __ldcg(row + b)) : -INFINITY;
+            if (!staged || b >= n)
+                s_row[b] = v;
+            nfin += (v > -INFINITY) ? 1 : 0;   // NaN and -inf are not candidates
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            nfin += __shfl_xor_sync(0xffffffffu, nfin, o);
+        if (lane == 0)
+            atomicAdd(s_nfin, nfin);
+        __syncthreads();
+        const float4 *r4 = reinterpret_cast<const float4 *>(s_row);
+        for (int b = tid; b < n; b += kTopkThreads) {
+            const float v = s_row[b];
+            if (!(v > -INFINITY))
+                continue;
+            int rank = 0;
+            for (int u4 = 0; u4 < npad / 4; ++u4) {
+                const float4 w = r4[u4];
+                const int u = 4 * u4;
+                rank += (w.x > v || (w.x == v && u < b)) ? 1 : 0;
+                rank += (w.y > v || (w.y == v && u + 1 < b)) ? 1 : 0;
+                rank += (w.z > v || (w.z == v && u + 2 < b)) ? 1 : 0;
+                rank += (w.w > v || (w.w == v && u + 3 < b)) ? 1 : 0;
+            }
+            if (rank < topk)
+                out[rank] = b;
+        }
+        for (int r = *s_nfin + tid; r < topk; r += kTopkThreads)
+            out[r] = -1;
+        return;
+    }
+
+    if (tid >= 32)
+        return;
+    float prev_s = INFINITY;
+    int prev_i = -1;
+    int r = 0;
+    for (; r < topk; ++r) {
+        float bs = -INFINITY;
+        int bi = -1;
+        for (int b = lane; b < n; b += 32) {
+            const float v = __ldcg(row + b);
+            if (!(v > -INFINITY))
+                continue;
+            if (!ranks_before(prev_s, prev_i, v, b))
+                continue;
+            if (bi < 0 || ranks_before(v, b, bs, bi)) {
+                bs = v;
+                bi = b;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (oi >= 0 && (bi < 0 || ranks_before(os, oi, bs, bi))) {
+                bs = os;
+                bi = oi;
+            }
+        }
+        if (lane == 0)
+            out[r] = bi;
+        if (bi < 0)
+            break;
+        prev_s = bs;
+        prev_i = bi;
+    }
+    for (int rr = r + 1 + lane; rr < topk; rr += 32)
+        out[rr] = -1;
+}
+
 constexpr int kScoreWarps = 4;   // blocks per CTA (one per warp)
+static_assert(kTopkThreads == kScoreWarps * 32, "a score CTA runs the top-k of the single launch");
+
+// The single-launch indexer's top-k: every CTA of query t that scored blocks counts
+// itself in counters[t] after its block scores are stored and fenced; the CTA that
+// arrives last (the count of such CTAs follows from the query's length) resets the
+// counter to zero for the next launch and ranks the row as the top-k kernel would,
+// writing -inf past the visible history.  A query without visible tokens has no
+// such CTA: its first CTA takes the row alone.  s_row: shared memory for up to
+// kRankMaxBlocks scores (the score kernel's query staging, free by then).
+__device__ __forceinline__ void fused_topk(const IndexerParams &p, int64_t t, int64_t L, int64_t cpq,
+                                           float *s_row)
+{
+    __shared__ int s_last, s_nfin;
+    __syncthreads();   // every warp of this CTA has stored its block score
+    if (threadIdx.x == 0) {
+        const int64_t span = (int64_t)kScoreWarps * p.block_tokens;
+        const int64_t live = (L + span - 1) / span;   // CTAs of the query with blocks to score
+        const int n_live = (int)(live < cpq ? live : cpq);
+        int last = 1;
+        if (n_live > 0) {
+            // release: this CTA's block scores (ordered before by the barrier) are
+            // visible to whoever acquires the count; acquire: the last CTA sees every
+            // other CTA's
+            int old;
+            asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                         : "=r"(old)
+                         : "l"(p.counters + t)
+                         : "memory");
+            last = old == n_live - 1;
+            if (last)
+                p.counters[t] = 0;
+        }
+        s_last = last;
+    }
+    __syncthreads();
+    if (!s_last)
+        return;
+    const int n = p.max_blocks;
+    const int64_t nb64 = (L + p.block_tokens - 1) / p.block_tokens;
+    const int nb = nb64 < n ? (int)nb64 : n;
+    float *row = p.block_scores + t * n;
+    for (int b = nb + (int)threadIdx.x; b < n; b += kTopkThreads)
+        row[b] = -INFINITY;
+    if (n <= kRankMaxBlocks) {   // stage the row, with -inf past the history
+        for (int b = threadIdx.x; b < n; b += kTopkThreads)
+            s_row[b] = b < nb ? __ldcg(row + b) : -INFINITY;
+    } else {
+        __syncthreads();   // the -inf above is in place before warp 0 reads the row
+    }
+    topk_row(row, s_row, &s_nfin, n <= kRankMaxBlocks, n, p.topk, p.topk_ids + t * p.topk);
+}
+
 
 template <int D, bool FP8>
 __global__ void __launch_bounds__(kScoreWarps * 32, MSA_INDEX_MIN_CTAS) msa_index_score_kernel(const __grid_constant__ IndexerParams p)
@@ -159,10 +312,12 @@ __global__ void __launch_bounds__(kScoreWarps * 32, MSA_INDEX_MIN_CTAS) msa_inde
     const int64_t L = len_raw > 0 ? (int64_t)len_raw : 0;
     const int64_t cta_j0 = (int64_t)((int64_t)blockIdx.x % cpq) * kScoreWarps * p.block_tokens;
     // Every block of this CTA is past the visible tokens: nothing to score, and the
-    // top-k kernel writes these blocks' -inf, so the CTA leaves at once -- before the
-    // wait, freeing its slot for the CTAs with work (the grid is sized for the
-    // longest history).
-    if (cta_j0 >= L)
+    // top-k writes these blocks' -inf, so the CTA leaves at once -- before the wait,
+    // freeing its slot for the CTAs with work (the grid is sized for the longest
+    // history).  In the single launch, a query without visible tokens has its first
+    // CTA stay to write its row and ids.
+    const int cta = (int)((int64_t)blockIdx.x % cpq);
+    if (cta_j0 >= L && !(p.counters && L == 0 && cta == 0))
         return;
     // This warp's block, and its page-table entries, one per lane, requested before
     // the query (when the block spans at most 32 pages; otherwise each token looks
@@ -228,98 +383,100 @@ __global__ void __launch_bounds__(kScoreWarps * 32, MSA_INDEX_MIN_CTAS) msa_inde
         s_af[st][lane] = f;
     }
     __syncthreads();
-    if (b >= p.max_blocks)
-        return;
-    const bool row0_real = g < H, row1_real = g + 8 < H;
-    if (lane_page >= p.num_pages)
-        lane_page = -1;
+    if (b < p.max_blocks) {
+        const bool row0_real = g < H, row1_real = g + 8 < H;
+        if (lane_page >= p.num_pages)
+            lane_page = -1;
 
 
-    constexpr int NG = MSA_INDEX_GROUPS;        // token groups whose rows are in flight together
-    constexpr int NWL = FP8 ? (D / 4) / 16 : (D / 4) / 8;   // 16-byte loads per lane and token
-    float best = -INFINITY;
-    for (int64_t jb = j0; jb < jend; jb += 8 * NG) {
-        uint4 w[NG][NWL];
-        bool okg[NG];
-#pragma unroll
-        for (int u = 0; u < NG; ++u) {
-            // this lane loads token g of group u; its columns are tokens 2i, 2i+1
-            const int64_t j = jb + 8 * u + g;
-            bool ok = j < jend;
-            int64_t page = -1;
-            if (ok) {
-                const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
-                if (!pages_in_lanes) {
-                    const int64_t ti = tbase + blk;
-                    if (ti >= 0 && ti < p.page_table_len) {
-                        const int64_t pg = __ldg(p.page_table + ti);
-                        page = (pg >= 0 && pg < p.num_pages) ? pg : -1;
-                    }
-                }
-                (void)blk;
-            }
-            if (pages_in_lanes) {
-                const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
-                const int src = (int)(blk - blk0) & 31;
-                const long long pg = __shfl_sync(0xffffffffu, (long long)lane_page, src);
-                page = ok ? pg : -1;
-            }
-            ok = ok && page >= 0;
-            okg[u] = ok;
-            const int64_t off = p.page_shift >= 0 ? (j & (p.page_size - 1)) : j % p.page_size;
-            const int64_t e = ok ? page * p.stride_page + off * p.stride_token : 0;
-            if (FP8) {
-#pragma unroll
-                for (int v = 0; v < NWL; ++v)
-                    w[u][v] = ok ? ldg16(p.kdata + e + i * (D / 4) + 16 * v) : make_uint4(0, 0, 0, 0);
-            } else {
-                const uint16_t *row = reinterpret_cast<const uint16_t *>(p.kdata) + e;
-#pragma unroll
-                for (int v = 0; v < NWL; ++v)
-                    w[u][v] = ok ? ldg16(row + i * (D / 4) + 8 * v) : make_uint4(0, 0, 0, 0);
-            }
-        }
-        // the k-steps are issued step-major over the NG groups, so that consecutive
-        // mma.sync are independent (group-major order would chain each on the last)
-        float cc[NG][4];
-#pragma unroll
-        for (int u = 0; u < NG; ++u)
-            cc[u][0] = cc[u][1] = cc[u][2] = cc[u][3] = 0.0f;
-#pragma unroll
-        for (int st = 0; st < KS; ++st) {
-            const uint4 f = s_af[st][lane];
-            const uint32_t a[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
+        constexpr int NG = MSA_INDEX_GROUPS;        // token groups whose rows are in flight together
+        constexpr int NWL = FP8 ? (D / 4) / 16 : (D / 4) / 8;   // 16-byte loads per lane and token
+        float best = -INFINITY;
+        for (int64_t jb = j0; jb < jend; jb += 8 * NG) {
+            uint4 w[NG][NWL];
+            bool okg[NG];
+    #pragma unroll
             for (int u = 0; u < NG; ++u) {
-                const uint32_t *words = reinterpret_cast<const uint32_t *>(w[u]);
-                if (FP8)
-                    mma_f16(cc[u], a, e4m3x2_to_f16x2(words[st] & 0xFFFF), e4m3x2_to_f16x2(words[st] >> 16));
-                else
-                    mma_bf16(cc[u], a, words[2 * st], words[2 * st + 1]);
+                // this lane loads token g of group u; its columns are tokens 2i, 2i+1
+                const int64_t j = jb + 8 * u + g;
+                bool ok = j < jend;
+                int64_t page = -1;
+                if (ok) {
+                    const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
+                    if (!pages_in_lanes) {
+                        const int64_t ti = tbase + blk;
+                        if (ti >= 0 && ti < p.page_table_len) {
+                            const int64_t pg = __ldg(p.page_table + ti);
+                            page = (pg >= 0 && pg < p.num_pages) ? pg : -1;
+                        }
+                    }
+                    (void)blk;
+                }
+                if (pages_in_lanes) {
+                    const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
+                    const int src = (int)(blk - blk0) & 31;
+                    const long long pg = __shfl_sync(0xffffffffu, (long long)lane_page, src);
+                    page = ok ? pg : -1;
+                }
+                ok = ok && page >= 0;
+                okg[u] = ok;
+                const int64_t off = p.page_shift >= 0 ? (j & (p.page_size - 1)) : j % p.page_size;
+                const int64_t e = ok ? page * p.stride_page + off * p.stride_token : 0;
+                if (FP8) {
+    #pragma unroll
+                    for (int v = 0; v < NWL; ++v)
+                        w[u][v] = ok ? ldg16(p.kdata + e + i * (D / 4) + 16 * v) : make_uint4(0, 0, 0, 0);
+                } else {
+                    const uint16_t *row = reinterpret_cast<const uint16_t *>(p.kdata) + e;
+    #pragma unroll
+                    for (int v = 0; v < NWL; ++v)
+                        w[u][v] = ok ? ldg16(row + i * (D / 4) + 8 * v) : make_uint4(0, 0, 0, 0);
+                }
+            }
+            // the k-steps are issued step-major over the NG groups, so that consecutive
+            // mma.sync are independent (group-major order would chain each on the last)
+            float cc[NG][4];
+    #pragma unroll
+            for (int u = 0; u < NG; ++u)
+                cc[u][0] = cc[u][1] = cc[u][2] = cc[u][3] = 0.0f;
+    #pragma unroll
+            for (int st = 0; st < KS; ++st) {
+                const uint4 f = s_af[st][lane];
+                const uint32_t a[4] = {f.x, f.y, f.z, f.w};
+    #pragma unroll
+                for (int u = 0; u < NG; ++u) {
+                    const uint32_t *words = reinterpret_cast<const uint32_t *>(w[u]);
+                    if (FP8)
+                        mma_f16(cc[u], a, e4m3x2_to_f16x2(words[st] & 0xFFFF), e4m3x2_to_f16x2(words[st] >> 16));
+                    else
+                        mma_bf16(cc[u], a, words[2 * st], words[2 * st + 1]);
+                }
+            }
+    #pragma unroll
+            for (int u = 0; u < NG; ++u) {
+                const float *c = cc[u];
+                // columns 2i, 2i+1: max over the real heads (rows g, g+8 across lane groups)
+                float m0 = fmaxf(row0_real ? c[0] : -INFINITY, row1_real ? c[2] : -INFINITY);
+                float m1 = fmaxf(row0_real ? c[1] : -INFINITY, row1_real ? c[3] : -INFINITY);
+    #pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+                    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+                }
+                // a column counts only if its token was loaded (lane 8i loaded token 2i)
+                const bool ok0 = __shfl_sync(0xffffffffu, okg[u], 8 * i);
+                const bool ok1 = __shfl_sync(0xffffffffu, okg[u], 8 * i + 4);
+                float m = fmaxf(ok0 ? m0 : -INFINITY, ok1 ? m1 : -INFINITY);
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                best = fmaxf(best, m);
             }
         }
-#pragma unroll
-        for (int u = 0; u < NG; ++u) {
-            const float *c = cc[u];
-            // columns 2i, 2i+1: max over the real heads (rows g, g+8 across lane groups)
-            float m0 = fmaxf(row0_real ? c[0] : -INFINITY, row1_real ? c[2] : -INFINITY);
-            float m1 = fmaxf(row0_real ? c[1] : -INFINITY, row1_real ? c[3] : -INFINITY);
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-                m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-            }
-            // a column counts only if its token was loaded (lane 8i loaded token 2i)
-            const bool ok0 = __shfl_sync(0xffffffffu, okg[u], 8 * i);
-            const bool ok1 = __shfl_sync(0xffffffffu, okg[u], 8 * i + 4);
-            float m = fmaxf(ok0 ? m0 : -INFINITY, ok1 ? m1 : -INFINITY);
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            best = fmaxf(best, m);
-        }
+        if (lane == 0)
+            p.block_scores[t * p.max_blocks + b] = best * (FP8 ? __ldg(p.k_scale) : 1.0f);
     }
-    if (lane == 0)
-        p.block_scores[t * p.max_blocks + b] = best * (FP8 ? __ldg(p.k_scale) : 1.0f);
+    if (p.counters)
+        fused_topk(p, t, L, cpq, &s_q[0][0]);
 }
 
 // ---------------------------------------------------------------------------
@@ -944,104 +1101,6 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
 // ---------------------------------------------------------------------------
 // top-k block ids
 // ---------------------------------------------------------------------------
-// (a, ia) ranks before (b, ib): higher score first, lower id among equals.
-__device__ __forceinline__ bool ranks_before(float a, int ia, float b, int ib)
-{
-    return a > b || (a == b && ia < ib);
-}
-
-constexpr int kTopkThreads = 128;
-constexpr int kRankMaxBlocks = 1024;   // rows up to this many blocks are ranked in shared memory
-
-// Top-k ids of one row of n block scores, by the kTopkThreads threads of a CTA.
-// Short rows (n <= kRankMaxBlocks) are ranked in shared memory s_row: every finite
-// entry counts the entries ranked before it, all threads in parallel, and entries
-// with rank < topk write their id at that rank.  When `staged`, s_row already holds
-// the row; otherwise it is read from `row`.  Long rows: warp 0 takes topk rounds,
-// each an arg-max over the entries ranked after the previous pick, reading `row`.
-__device__ __forceinline__ void topk_row(const float *row, float *s_row, int *s_nfin, bool staged,
-                                         int n, int topk, int32_t *out)
-{
-    const int tid = threadIdx.x, lane = tid & 31;
-    if (n <= kRankMaxBlocks) {
-        if (tid == 0)
-            *s_nfin = 0;
-        __syncthreads();
-        int nfin = 0;
-        const int npad = (n + 3) & ~3;
-        for (int b = tid; b < npad; b += kTopkThreads) {
-            const float v = b < n ? (staged ? s_row[b] : row[b]) : -INFINITY;
-            if (!staged || b >= n)
-                s_row[b] = v;
-            nfin += (v > -INFINITY) ? 1 : 0;   // NaN and -inf are not candidates
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            nfin += __shfl_xor_sync(0xffffffffu, nfin, o);
-        if (lane == 0)
-            atomicAdd(s_nfin, nfin);
-        __syncthreads();
-        const float4 *r4 = reinterpret_cast<const float4 *>(s_row);
-        for (int b = tid; b < n; b += kTopkThreads) {
-            const float v = s_row[b];
-            if (!(v > -INFINITY))
-                continue;
-            int rank = 0;
-            for (int u4 = 0; u4 < npad / 4; ++u4) {
-                const float4 w = r4[u4];
-                const int u = 4 * u4;
-                rank += (w.x > v || (w.x == v && u < b)) ? 1 : 0;
-                rank += (w.y > v || (w.y == v && u + 1 < b)) ? 1 : 0;
-                rank += (w.z > v || (w.z == v && u + 2 < b)) ? 1 : 0;
-                rank += (w.w > v || (w.w == v && u + 3 < b)) ? 1 : 0;
-            }
-            if (rank < topk)
-                out[rank] = b;
-        }
-        for (int r = *s_nfin + tid; r < topk; r += kTopkThreads)
-            out[r] = -1;
-        return;
-    }
-
-    if (tid >= 32)
-        return;
-    float prev_s = INFINITY;
-    int prev_i = -1;
-    int r = 0;
-    for (; r < topk; ++r) {
-        float bs = -INFINITY;
-        int bi = -1;
-        for (int b = lane; b < n; b += 32) {
-            const float v = row[b];
-            if (!(v > -INFINITY))
-                continue;
-            if (!ranks_before(prev_s, prev_i, v, b))
-                continue;
-            if (bi < 0 || ranks_before(v, b, bs, bi)) {
-                bs = v;
-                bi = b;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float os = __shfl_xor_sync(0xffffffffu, bs, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (oi >= 0 && (bi < 0 || ranks_before(os, oi, bs, bi))) {
-                bs = os;
-                bi = oi;
-            }
-        }
-        if (lane == 0)
-            out[r] = bi;
-        if (bi < 0)
-            break;
-        prev_s = bs;
-        prev_i = bi;
-    }
-    for (int rr = r + 1 + lane; rr < topk; rr += 32)
-        out[rr] = -1;
-}
-
 // One CTA per query, after a score kernel; under programmatic dependent launch it
 // waits for the score kernel before reading its output.
 __global__ void __launch_bounds__(kTopkThreads) msa_index_topk_kernel(const __grid_constant__ IndexerParams p)
@@ -1141,21 +1200,15 @@ msa_status validate(const msa_indexer_cfg *cfg, int64_t T, const void *idx_q, co
     return MSA_OK;
 }
 
-}  // namespace
-
-extern "C" msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t num_queries,
-                                          const void *idx_q, const int32_t *kv_len,
-                                          const int64_t *table_offset, const int32_t *page_table,
-                                          int64_t page_table_len, const msa_cache_desc *idx_k_cache,
-                                          const float *k_scale, float *block_scores,
-                                          int32_t *topk_ids, int32_t launch_flags,
-                                          cudaStream_t stream)
+// The launches of both entry points; counters != nullptr: the per-query kernel takes
+// the top-k itself (the query-run path keeps its top-k kernel).
+msa_status indexer_launch(const msa_indexer_cfg *cfg, int64_t num_queries, const void *idx_q,
+                          const int32_t *kv_len, const int64_t *table_offset,
+                          const int32_t *page_table, int64_t page_table_len,
+                          const msa_cache_desc *idx_k_cache, const float *k_scale,
+                          float *block_scores, int32_t *topk_ids, int32_t *counters,
+                          int32_t launch_flags, cudaStream_t stream)
 {
-    msa_status s = validate(cfg, num_queries, idx_q, kv_len, table_offset, page_table,
-                            page_table_len, idx_k_cache, k_scale, block_scores, topk_ids,
-                            launch_flags);
-    if (s != MSA_OK || num_queries == 0)
-        return s;
     IndexerParams p;
     memset(&p, 0, sizeof p);
     p.idx_q = static_cast<const uint16_t *>(idx_q);
@@ -1233,10 +1286,14 @@ extern "C" msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t nu
         sc.attrs = sattr;
         sc.numAttrs = 1;
     }
+    if (!tiled)
+        p.counters = counters;
     void *sargs[] = {&p};
     cudaError_t e = cudaLaunchKernelExC(&sc, score_fn, sargs);
     if (e != cudaSuccess)
         return fail(MSA_ERR_CUDA, "score kernel launch failed: %s", cudaGetErrorString(e));
+    if (p.counters)
+        return MSA_OK;
     // top-k: one CTA per query, launched programmatically dependent on the scores
     cudaLaunchConfig_t lc;
     memset(&lc, 0, sizeof lc);
@@ -1253,4 +1310,47 @@ extern "C" msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t nu
     if (e != cudaSuccess)
         return fail(MSA_ERR_CUDA, "top-k kernel launch failed: %s", cudaGetErrorString(e));
     return MSA_OK;
+}
+
+}  // namespace
+
+extern "C" msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t num_queries,
+                                          const void *idx_q, const int32_t *kv_len,
+                                          const int64_t *table_offset, const int32_t *page_table,
+                                          int64_t page_table_len, const msa_cache_desc *idx_k_cache,
+                                          const float *k_scale, float *block_scores,
+                                          int32_t *topk_ids, int32_t launch_flags,
+                                          cudaStream_t stream)
+{
+    msa_status s = validate(cfg, num_queries, idx_q, kv_len, table_offset, page_table,
+                            page_table_len, idx_k_cache, k_scale, block_scores, topk_ids,
+                            launch_flags);
+    if (s != MSA_OK || num_queries == 0)
+        return s;
+    return indexer_launch(cfg, num_queries, idx_q, kv_len, table_offset, page_table, page_table_len,
+                          idx_k_cache, k_scale, block_scores, topk_ids, nullptr, launch_flags, stream);
+}
+
+extern "C" msa_status msa_indexer_forward_fused(const msa_indexer_cfg *cfg, int64_t num_queries,
+                                                const void *idx_q, const int32_t *kv_len,
+                                                const int64_t *table_offset,
+                                                const int32_t *page_table, int64_t page_table_len,
+                                                const msa_cache_desc *idx_k_cache,
+                                                const float *k_scale, float *block_scores,
+                                                int32_t *topk_ids, int32_t *counters,
+                                                int32_t launch_flags, cudaStream_t stream)
+{
+    msa_status s = validate(cfg, num_queries, idx_q, kv_len, table_offset, page_table,
+                            page_table_len, idx_k_cache, k_scale, block_scores, topk_ids,
+                            launch_flags);
+    if (s != MSA_OK)
+        return s;
+    if (!counters)
+        return fail(MSA_ERR_INVALID_ARGUMENT, "counters is NULL");
+    if (reinterpret_cast<uintptr_t>(counters) % 4)
+        return fail(MSA_ERR_MISALIGNED, "counters is misaligned");
+    if (num_queries == 0)
+        return MSA_OK;
+    return indexer_launch(cfg, num_queries, idx_q, kv_len, table_offset, page_table, page_table_len,
+                          idx_k_cache, k_scale, block_scores, topk_ids, counters, launch_flags, stream);
 }

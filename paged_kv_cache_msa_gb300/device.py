@@ -99,20 +99,25 @@ class DeviceIndexer:
         self.k_scale = torch.tensor([w.k_scale], dtype=torch.float32, device=self.device)
         self.block_scores = torch.empty((T, w.max_blocks), dtype=torch.float32, device=self.device)
         self.topk_ids = torch.empty((T, w.topk), dtype=torch.int32, device=self.device)
+        self.counters = torch.zeros((T,), dtype=torch.int32, device=self.device)
         c = w.cache
         self.cache = B.make_cache(self.pool.data_ptr() + c.offset, c.dtype, c.num_pages, 1,
                                   c.stride_page, c.stride_head, c.stride_token)
 
-    def run(self, stream=None, launch_flags=0):
+    def run(self, stream=None, launch_flags=0, fused=False):
+        """msa_indexer_forward, or with ``fused`` msa_indexer_forward_fused on this
+        indexer's zeroed per-query counters."""
         import torch
         if stream is None:
             stream = torch.cuda.current_stream(self.device)
         p = lambda t: int(t.data_ptr())
-        return B.msa_indexer_forward(self.cfg, self.w.idx_q.shape[0], p(self.idx_q), p(self.kv_len),
-                                     p(self.table_offset), p(self.page_table),
-                                     self.page_table.numel(), self.cache, p(self.k_scale),
-                                     p(self.block_scores), p(self.topk_ids), launch_flags,
-                                     stream=stream.cuda_stream)
+        args = (self.cfg, self.w.idx_q.shape[0], p(self.idx_q), p(self.kv_len),
+                p(self.table_offset), p(self.page_table), self.page_table.numel(), self.cache,
+                p(self.k_scale), p(self.block_scores), p(self.topk_ids))
+        if fused:
+            return B.msa_indexer_forward_fused(*args, p(self.counters), launch_flags,
+                                               stream=stream.cuda_stream)
+        return B.msa_indexer_forward(*args, launch_flags, stream=stream.cuda_stream)
 
 
 class DeviceProjection:
@@ -192,13 +197,19 @@ class DecodeLayer:
         self.block_scores = torch.empty((T, self.cfg.max_blocks), dtype=torch.float32,
                                         device=dw.device)
         self.topk_ids = torch.empty((T, topk), dtype=torch.int32, device=dw.device)
+        self.counters = torch.zeros((T,), dtype=torch.int32, device=dw.device)
 
-    def run(self, stream, flags=0):
+    def run(self, stream, flags=0, fused=False):
+        """The producer, then the indexer on what it wrote (with ``fused``, the
+        single-launch indexer on this layer's zeroed counters)."""
         dw = self.dw
         p = lambda t: int(t.data_ptr())
         dw.run(B.MSA_LAUNCH_PERSISTENT | (flags & B.MSA_LAUNCH_PDL), stream=stream)
-        B.msa_indexer_forward(self.cfg, dw.w.num_tokens, p(dw.idx_q_out), p(self.kv_len),
-                              p(self.table_offset), p(dw.page_table), dw.page_table.numel(),
-                              dw.caches["idx_k"], p(self.k_scale), p(self.block_scores),
-                              p(self.topk_ids), flags & B.MSA_LAUNCH_PDL,
-                              stream=stream.cuda_stream)
+        args = (self.cfg, dw.w.num_tokens, p(dw.idx_q_out), p(self.kv_len), p(self.table_offset),
+                p(dw.page_table), dw.page_table.numel(), dw.caches["idx_k"], p(self.k_scale),
+                p(self.block_scores), p(self.topk_ids))
+        if fused:
+            B.msa_indexer_forward_fused(*args, p(self.counters), flags & B.MSA_LAUNCH_PDL,
+                                        stream=stream.cuda_stream)
+        else:
+            B.msa_indexer_forward(*args, flags & B.MSA_LAUNCH_PDL, stream=stream.cuda_stream)

@@ -286,6 +286,20 @@ def test_indexer_host_checks(lib, over, status):
     # rejected calls (and an empty one) return before touching the GPU
     got = B.msa_indexer_forward(**a, stream=0, check=False)
     assert got == status, (B.status_string(got), B.last_error_detail())
+    # the single-launch entry checks the same arguments the same way
+    got = B.msa_indexer_forward_fused(**a, counters=BASE + 30 * 2**32, stream=0, check=False)
+    assert got == status, (B.status_string(got), B.last_error_detail())
+
+
+@pytest.mark.parametrize("counters,status", [
+    (None, B.MSA_ERR_INVALID_ARGUMENT),
+    (BASE + 30 * 2**32 + 2, B.MSA_ERR_MISALIGNED),
+])
+def test_indexer_fused_counter_checks(lib, counters, status):
+    for nq in (64, 0):   # the counters are checked before an empty call returns
+        a = good_indexer_call(num_queries=nq)
+        got = B.msa_indexer_forward_fused(**a, counters=counters, stream=0, check=False)
+        assert got == status, (B.status_string(got), B.last_error_detail())
 
 
 # ---------------------------------------------------------------------------
