@@ -290,6 +290,37 @@ msa_status msa_indexer_forward_fused(const msa_indexer_cfg *cfg, int64_t num_que
                                      int32_t *counters, int32_t launch_flags, cudaStream_t stream);
 
 /*
+ * msa_indexer_forward_fused_noalloc -- msa_indexer_forward_fused on per-query
+ * counters that the library owns instead of the caller: a file-scope device array
+ * of 65,536 int32 per device.  No counterpart in the source pages; it exists for
+ * callers that cannot allocate device memory on the call path -- a runtime whose
+ * allocator does not reach this library (a plain C host, a plugin handed only
+ * pointers to its inputs and outputs), or a step being assembled where an
+ * allocation would be a synchronising call.  Neither this function nor its kernel
+ * allocates anything.
+ *
+ * The first call on a device looks the array's address up (cudaGetSymbolAddress,
+ * its status checked) and zeroes it with cudaMemsetAsync on `stream`, ordered
+ * before that call's launch; make that first call outside stream capture.  Later
+ * calls only launch.  The array is shared by every call on the device: calls that
+ * may run at the same time (on different streams without an ordering between them)
+ * race on the counters and give wrong ids -- order them, or give each its own
+ * counters through msa_indexer_forward_fused.  A launch that does not run to
+ * completion can leave counters nonzero for the calls after it.
+ *
+ * Arguments, results and errors as for msa_indexer_forward_fused without
+ * `counters`; num_queries above 65,536 is MSA_ERR_UNSUPPORTED (checked on the host,
+ * before any device call).
+ */
+msa_status msa_indexer_forward_fused_noalloc(const msa_indexer_cfg *cfg, int64_t num_queries,
+                                             const void *idx_q, const int32_t *kv_len,
+                                             const int64_t *table_offset, const int32_t *page_table,
+                                             int64_t page_table_len,
+                                             const msa_cache_desc *idx_k_cache, const float *k_scale,
+                                             float *block_scores, int32_t *topk_ids,
+                                             int32_t launch_flags, cudaStream_t stream);
+
+/*
  * Device address at which the GPU of the current device reaches host memory
  * `host_ptr` (pinned, mapped host memory; on Grace-Blackwell the GPU reads and
  * writes it over NVLink-C2C).  Sets *device_ptr and returns MSA_OK when the

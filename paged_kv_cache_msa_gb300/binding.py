@@ -33,7 +33,8 @@ MSA_LAUNCH_QUERY_RUNS = 4
 
 # every function the header declares
 EXPORTED = ("msa_producer_forward", "msa_producer_validate", "msa_producer_launch_shape",
-            "msa_indexer_forward", "msa_indexer_forward_fused", "msa_host_buffer_device_address",
+            "msa_indexer_forward", "msa_indexer_forward_fused", "msa_indexer_forward_fused_noalloc",
+            "msa_host_buffer_device_address",
             "msa_status_string",
             "msa_last_error_detail", "msa_projection_forward", "msa_projection_validate",
             "msa_checked_violations")
@@ -126,6 +127,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.msa_indexer_forward_fused.argtypes = [ctypes.POINTER(MsaIndexerCfg), i64, vp, vp, vp, vp,
                                                 i64, cachep, vp, vp, vp, vp, i32, vp]
         L.msa_indexer_forward_fused.restype = ctypes.c_int
+        L.msa_indexer_forward_fused_noalloc.argtypes = [ctypes.POINTER(MsaIndexerCfg), i64, vp, vp,
+                                                        vp, vp, i64, cachep, vp, vp, vp, i32, vp]
+        L.msa_indexer_forward_fused_noalloc.restype = ctypes.c_int
         proj = [cfgp, i64, vp, i64, i64, vp, i64, ctypes.c_int, vp, vp, vp, vp, vp, i64, vp, vp,
                 vp, vp, vp, vp, cachep, cachep, cachep, vp, vp, i64, vp]
         L.msa_projection_forward.argtypes = proj + [vp]
@@ -301,6 +305,21 @@ def msa_indexer_forward_fused(cfg, num_queries, idx_q, kv_len, table_offset, pag
                                          block_scores, topk_ids, counters, int(launch_flags), stream)
     if check and s != MSA_OK:
         raise MsaError(s, "msa_indexer_forward_fused", last_error_detail())
+    return s
+
+
+def msa_indexer_forward_fused_noalloc(cfg, num_queries, idx_q, kv_len, table_offset, page_table,
+                                      page_table_len, idx_k_cache, k_scale, block_scores,
+                                      topk_ids, launch_flags=0, stream=0, check=True) -> int:
+    """The single-launch C entry point on the library's own counters; pointers are
+    integers or None.  Raises MsaError unless the call returns MSA_OK (``check=False``
+    returns the status)."""
+    s = load().msa_indexer_forward_fused_noalloc(
+        ctypes.byref(cfg) if cfg is not None else None, int(num_queries), idx_q, kv_len,
+        table_offset, page_table, int(page_table_len), _ref(idx_k_cache), k_scale, block_scores,
+        topk_ids, int(launch_flags), stream)
+    if check and s != MSA_OK:
+        raise MsaError(s, "msa_indexer_forward_fused_noalloc", last_error_detail())
     return s
 
 

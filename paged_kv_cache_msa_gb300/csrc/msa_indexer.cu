@@ -33,6 +33,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 // Groups of 8 tokens whose index-K rows a warp has in flight at once.
 #ifndef MSA_INDEX_GROUPS
@@ -1351,6 +1352,68 @@ extern "C" msa_status msa_indexer_forward_fused(const msa_indexer_cfg *cfg, int6
         return fail(MSA_ERR_MISALIGNED, "counters is misaligned");
     if (num_queries == 0)
         return MSA_OK;
+    return indexer_launch(cfg, num_queries, idx_q, kv_len, table_offset, page_table, page_table_len,
+                          idx_k_cache, k_scale, block_scores, topk_ids, counters, launch_flags, stream);
+}
+
+// ---------------------------------------------------------------------------
+// msa_indexer_forward_fused_noalloc: the single-launch indexer on counters this
+// library owns (a file-scope device array), for callers that cannot allocate
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int64_t kNoAllocQueries = 65536;   // counters in the library's array
+
+// one counter per query; all zero between launches (each launch that runs to
+// completion leaves them zero)
+static __device__ __align__(256) int32_t g_noalloc_counters[kNoAllocQueries];
+
+std::mutex g_noalloc_mu;
+int32_t *g_noalloc_ptr[64];   // the array's address on each device, once looked up and cleared
+
+}  // namespace
+
+extern "C" msa_status msa_indexer_forward_fused_noalloc(const msa_indexer_cfg *cfg,
+                                                        int64_t num_queries, const void *idx_q,
+                                                        const int32_t *kv_len,
+                                                        const int64_t *table_offset,
+                                                        const int32_t *page_table,
+                                                        int64_t page_table_len,
+                                                        const msa_cache_desc *idx_k_cache,
+                                                        const float *k_scale, float *block_scores,
+                                                        int32_t *topk_ids, int32_t launch_flags,
+                                                        cudaStream_t stream)
+{
+    msa_status s = validate(cfg, num_queries, idx_q, kv_len, table_offset, page_table,
+                            page_table_len, idx_k_cache, k_scale, block_scores, topk_ids,
+                            launch_flags);
+    if (s != MSA_OK)
+        return s;
+    if (num_queries > kNoAllocQueries)
+        return fail(MSA_ERR_UNSUPPORTED, "num_queries %lld is above the %lld counters of the library",
+                    (long long)num_queries, (long long)kNoAllocQueries);
+    if (num_queries == 0)
+        return MSA_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return fail(MSA_ERR_CUDA, "cudaGetDevice failed");
+    int32_t *counters = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        if (!g_noalloc_ptr[dev]) {
+            // first use on this device: the array's address, and every counter zeroed
+            // (stream-ordered before this call's launch)
+            void *a = nullptr;
+            cudaError_t e = cudaGetSymbolAddress(&a, g_noalloc_counters);
+            if (e != cudaSuccess)
+                return fail(MSA_ERR_CUDA, "cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
+            e = cudaMemsetAsync(a, 0, sizeof(g_noalloc_counters), stream);
+            if (e != cudaSuccess)
+                return fail(MSA_ERR_CUDA, "clearing the counters failed: %s", cudaGetErrorString(e));
+            g_noalloc_ptr[dev] = static_cast<int32_t *>(a);
+        }
+        counters = g_noalloc_ptr[dev];
+    }
     return indexer_launch(cfg, num_queries, idx_q, kv_len, table_offset, page_table, page_table_len,
                           idx_k_cache, k_scale, block_scores, topk_ids, counters, launch_flags, stream);
 }
