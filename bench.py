@@ -936,6 +936,9 @@ def decode_summary(decode):
     li = decode.get("layer_with_indexer")
     if li:
         out["layer_with_indexer_us_per_layer"] = li["pdl"]["us_per_layer"]
+        if "pdl_single_launch_indexer" in li:
+            out["layer_with_single_launch_indexer_us_per_layer"] = \
+                li["pdl_single_launch_indexer"]["us_per_layer"]
     return out
 
 
