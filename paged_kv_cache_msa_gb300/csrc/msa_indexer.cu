@@ -71,6 +71,7 @@ struct IndexerParams {
     int32_t max_blocks;
     int32_t pdl;                    // launched with programmatic dependent launch
     int32_t *counters;              // [T] arrivals per query (single launch), else nullptr
+    int32_t topk_rows;              // queries per CTA of the several-rows top-k kernel
 };
 
 __device__ __forceinline__ uint4 ldg16(const void *p)
@@ -1133,6 +1134,81 @@ __global__ void __launch_bounds__(kTopkThreads) msa_index_topk_kernel(const __gr
     topk_row(row, s_row, &s_nfin, n <= kRankMaxBlocks, n, p.topk, p.topk_ids + t * p.topk);
 }
 
+constexpr int kTopkRowsMax = 16;            // queries per CTA of the several-rows kernel
+constexpr int64_t kTopkRowsMinQueries = 2048;  // batches that take it (each CTA then does more)
+
+// The top-k of topk_rows consecutive queries per CTA, for large batches of short
+// rows (topk_rows x max_blocks <= kRankMaxBlocks): the CTA writes -inf past each
+// query's history, stages the rows (contiguous in block_scores) together, and every
+// finite entry counts the entries of its row ranked before it, all rows at once --
+// the rule of topk_row; ranks past a row's finite entries take -1.  One CTA per
+// query would leave each of them mostly waiting on its loads, in dozens of waves.
+__global__ void __launch_bounds__(kTopkThreads) msa_index_topk_rows_kernel(const __grid_constant__ IndexerParams p)
+{
+    __shared__ __align__(16) float s_row[kRankMaxBlocks];
+    __shared__ int s_nb[kTopkRowsMax], s_nfin[kTopkRowsMax];
+    const int n = p.max_blocks, topk = p.topk, tid = threadIdx.x;
+    const int64_t q0 = (int64_t)blockIdx.x * p.topk_rows;
+    const int64_t left = p.num_queries - q0;
+    const int nq = left < p.topk_rows ? (int)left : p.topk_rows;
+    if (tid < nq) {
+        const int32_t len_raw = __ldg(p.kv_len + q0 + tid);
+        const int64_t L = len_raw > 0 ? (int64_t)len_raw : 0;
+        const int64_t nb64 = (L + p.block_tokens - 1) / p.block_tokens;
+        s_nb[tid] = nb64 < n ? (int)nb64 : n;
+        s_nfin[tid] = 0;
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+    __syncthreads();
+    float *rows = p.block_scores + q0 * n;
+    for (int idx = tid; idx < nq * n; idx += kTopkThreads) {
+        const int r = idx / n, b = idx - r * n;
+        float v = -INFINITY;
+        if (b < s_nb[r])
+            v = rows[idx];
+        else
+            rows[idx] = -INFINITY;
+        s_row[idx] = v;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < nq * n; idx += kTopkThreads) {
+        const float v = s_row[idx];
+        if (!(v > -INFINITY))   // NaN and -inf are not candidates
+            continue;
+        const int r = idx / n, b = idx - r * n;
+        atomicAdd(&s_nfin[r], 1);
+        const float *row = s_row + r * n;
+        int rank = 0;
+        // entries past the row's history are -inf and never rank before a candidate
+        const int nb = s_nb[r];
+        if ((n & 3) == 0) {   // rows start on 16-byte boundaries: four entries a load
+            const float4 *r4 = reinterpret_cast<const float4 *>(row);
+            for (int u4 = 0; u4 < (nb + 3) / 4; ++u4) {
+                const float4 w = r4[u4];
+                const int u = 4 * u4;
+                rank += (w.x > v || (w.x == v && u < b)) ? 1 : 0;
+                rank += (w.y > v || (w.y == v && u + 1 < b)) ? 1 : 0;
+                rank += (w.z > v || (w.z == v && u + 2 < b)) ? 1 : 0;
+                rank += (w.w > v || (w.w == v && u + 3 < b)) ? 1 : 0;
+            }
+        } else {
+            for (int u = 0; u < nb; ++u) {
+                const float w = row[u];
+                rank += (w > v || (w == v && u < b)) ? 1 : 0;
+            }
+        }
+        if (rank < topk)
+            p.topk_ids[(q0 + r) * topk + rank] = b;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < nq * topk; idx += kTopkThreads) {
+        const int r = idx / topk, k = idx - r * topk;
+        if (k >= s_nfin[r])
+            p.topk_ids[(q0 + r) * topk + k] = -1;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -1295,10 +1371,17 @@ msa_status indexer_launch(const msa_indexer_cfg *cfg, int64_t num_queries, const
         return fail(MSA_ERR_CUDA, "score kernel launch failed: %s", cudaGetErrorString(e));
     if (p.counters)
         return MSA_OK;
-    // top-k: one CTA per query, launched programmatically dependent on the scores
+    // top-k: one CTA per query (several short rows per CTA in large batches),
+    // launched programmatically dependent on the scores
+    int rows = 1;
+    if (num_queries >= kTopkRowsMinQueries && 2 * cfg->max_blocks <= kRankMaxBlocks) {
+        rows = kRankMaxBlocks / cfg->max_blocks;
+        rows = rows > kTopkRowsMax ? kTopkRowsMax : rows;
+    }
+    p.topk_rows = rows;
     cudaLaunchConfig_t lc;
     memset(&lc, 0, sizeof lc);
-    lc.gridDim = dim3((unsigned)num_queries);
+    lc.gridDim = dim3((unsigned)((num_queries + rows - 1) / rows));
     lc.blockDim = dim3(kTopkThreads);
     lc.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1307,7 +1390,9 @@ msa_status indexer_launch(const msa_indexer_cfg *cfg, int64_t num_queries, const
     lc.attrs = attr;
     lc.numAttrs = 1;
     void *args[] = {&p};
-    e = cudaLaunchKernelExC(&lc, reinterpret_cast<const void *>(&msa_index_topk_kernel), args);
+    e = cudaLaunchKernelExC(&lc, rows > 1 ? reinterpret_cast<const void *>(&msa_index_topk_rows_kernel)
+                                          : reinterpret_cast<const void *>(&msa_index_topk_kernel),
+                            args);
     if (e != cudaSuccess)
         return fail(MSA_ERR_CUDA, "top-k kernel launch failed: %s", cudaGetErrorString(e));
     return MSA_OK;

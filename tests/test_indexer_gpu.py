@@ -153,6 +153,29 @@ def test_query_runs_table_holes_and_topk_sizes():
     _check(w, flags=_runs())
 
 
+@pytest.mark.parametrize("lens,heads", [
+    ([9000, 5, 300, 0, 4000, 128], 8),
+    ([70000, 300, 0], 8),                  # 547 blocks a row: past the shared ranking's short rows
+    ([70000, 66000, 10, 0], 12),           # 8 queries a tile
+], ids=["mixed", "long_rows", "long_rows_12_heads"])
+def test_query_runs_long_and_empty_histories(lens, heads):
+    """The query-run kernel on one query per sequence, with long and empty histories,
+    against the oracle."""
+    w = wl.make_indexer_batch(f"runs_rank_{heads}_{len(lens)}", 520 + len(lens) + heads, lens,
+                              heads=heads, topk=16)
+    _check(w, flags=_runs())
+
+
+@pytest.mark.parametrize("flags", [0, 4], ids=["per_query", "query_runs"])
+@pytest.mark.parametrize("seqs,topk", [([2100], 16), ([1100, 1000, 300], 64)])
+def test_top_k_of_several_rows_per_cta(flags, seqs, topk):
+    """Batches of 2,048 queries and more with short rows take the top-k kernel that
+    ranks up to 16 rows per CTA: against the oracle, through both score kernels
+    (including rows past a query's history, written -inf by the top-k kernel)."""
+    _check(wl.make_indexer_prefill(f"rows_{len(seqs)}_{topk}", 540 + len(seqs), seqs, topk=topk),
+           flags=flags)
+
+
 def test_query_runs_match_the_per_query_kernel():
     """The same prefill batch through both score kernels: the block scores agree to
     fp32 accumulation error and the -inf pattern is identical."""
