@@ -902,7 +902,10 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
                 };
                 auto store = [&](const uint4 (&raw)[NV]) -> bool {
                     const uint32_t s = it % kRunsNSA, ph = (it / kRunsNSA) & 1;
-                    if (*abort_flag || !__any_sync(0xffffffffu, mbar_wait_fast(smem_u32(&bar_a_empty[s]), ph ^ 1))) {
+                    // the abort flag is read only when the stage is not free yet
+                    if (!__all_sync(0xffffffffu, mbar_try(smem_u32(&bar_a_empty[s]), ph ^ 1)) &&
+                        (__any_sync(0xffffffffu, *abort_flag != 0) ||
+                         !__any_sync(0xffffffffu, mbar_wait(smem_u32(&bar_a_empty[s]), ph ^ 1)))) {
                         *abort_flag = 1;
                         return false;
                     }
@@ -979,6 +982,7 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
                 asm volatile("bar.sync 3, 128;" ::: "memory");
         };
         uint32_t it = 0, tile_it = 0;
+        bool aborted = false;
         for (int64_t ti = blockIdx.x; ti < num_tiles; ti += gridDim.x, ++tile_it) {
             const uint32_t tb = tile_it & 1;
             const int64_t t0 = ti * QT;
@@ -1013,11 +1017,21 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
                     const uint32_t pa = (its / kRunsNACC) & 1;
                     const int64_t j = (int64_t)b * kTileKeys + key;
                     const bool kvalid = pg >= 0 && pg < p.num_pages;
-                    bool got = !*abort_flag;
-                    if (got)
-                        got = __all_sync(0xffffffffu, mbar_wait_fast(smem_u32(&bar_acc_full[grp]), pa));
-                    if (!got)
-                        *abort_flag = 1;
+                    // The abort flag is read only when the accumulator is not ready yet:
+                    // after an abort the MMA completes no further phase, so the first
+                    // wait that follows fails and sees the flag, and `aborted` keeps
+                    // every later block from trying (a later try could find an older
+                    // phase of the same parity complete).
+                    bool got = false;
+                    if (!aborted) {
+                        got = __all_sync(0xffffffffu, mbar_try(smem_u32(&bar_acc_full[grp]), pa));
+                        if (!got && !__any_sync(0xffffffffu, *abort_flag != 0))
+                            got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_acc_full[grp]), pa));
+                        if (!got) {
+                            aborted = true;
+                            *abort_flag = 1;
+                        }
+                    }
                     float m[QT];
 #pragma unroll
                     for (int q = 0; q < QT; ++q)
