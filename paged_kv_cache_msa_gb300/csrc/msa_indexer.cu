@@ -575,7 +575,8 @@ constexpr int kTileKeys = 128;   // keys per MMA tile: the 128-token blocks of t
 // The only shared-memory traffic per block is the MMA reading B (32 KB for D = 128);
 // the earlier arrangement (queries as A, keys gathered into shared memory as B, the
 // CTA's phases in lockstep) needed 96 KB per block and ran at 0.27 of the bf16 peak.
-// Warps: 0 allocates tensor memory and its lane 0 issues the MMAs; 1-8 gather
+// Warps: 0 allocates tensor memory and issues the MMAs (the whole warp runs the
+// loop, one elected lane issues each tcgen05 instruction); 1-8 gather
 // (warps w and w + 4 share tensor-memory lane quarter w & 3 and take one half of
 // the head dimension each; the rows of the next block are in flight in registers
 // while the current one is converted); 9-16 epilogue, two groups of four that take
