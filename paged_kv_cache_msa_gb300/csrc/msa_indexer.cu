@@ -131,6 +131,24 @@ __device__ __forceinline__ uint32_t f2_to_bf16x2(float lo, float hi)
     return d;
 }
 
+// (x0, x1) -> two E4M3 codes, x0 in the low byte; round to nearest even, saturating
+__device__ __forceinline__ uint32_t e4m3x2_from_f32(float x0, float x1)
+{
+    unsigned short c;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(x1), "f"(x0));
+    return (uint32_t)c;
+}
+
+// an f16 pair -> (low half, high half) as floats
+__device__ __forceinline__ float2 f16x2_to_f2(uint32_t h2)
+{
+    float lo, hi;
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; cvt.f32.f16 %0, l; cvt.f32.f16 %1, h; }"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h2));
+    return make_float2(lo, hi);
+}
+
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
 {
     uint32_t h2;
@@ -683,9 +701,12 @@ __global__ void __launch_bounds__(kRunsThreads, 1)
 msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
 {
     constexpr int QT = 128 / HP;                           // queries per tile
-    constexpr uint32_t kBBytes = 128u * D * 2u;            // one query tile (B)
+    // E4M3 keys of 128 dims: the MMA takes them as stored (kind::f8f6f4, A = the raw
+    // codes in tensor memory) against each query split into two E4M3 halves
+    constexpr bool F8 = FP8 && D == 128;
+    constexpr uint32_t kBBytes = 128u * D * 2u;            // one query tile (B): f16/bf16, or E4M3 hi | lo
     constexpr int CH = D / 8;                              // 16-byte chunks of a 2-byte row
-    constexpr uint32_t kACols = D / 2;                     // tensor-memory columns of a key stage
+    constexpr uint32_t kACols = F8 ? D / 4 : D / 2;        // tensor-memory columns of a key stage
     constexpr uint32_t kAccCols = 128;
     constexpr uint32_t kACol0 = kRunsNACC * kAccCols;      // first key-stage column
     static_assert(kACol0 + kRunsNSA * kACols <= kRunsTmemCols, "tensor memory budget");
@@ -696,6 +717,7 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
     __shared__ __align__(8) uint64_t bar_a_full[kRunsNSA], bar_a_empty[kRunsNSA];
     __shared__ __align__(8) uint64_t bar_acc_full[kRunsNACC], bar_acc_empty[kRunsNACC];
     __shared__ __align__(8) uint64_t bar_drain;
+    __shared__ float s_qinv[2][QT];        // E4M3 split: 2^-e of each query's scale
     __shared__ int32_t g_len[2][QT];       // gather side's tile metadata (also read by the MMA)
     __shared__ int64_t g_toff[2][QT];
     __shared__ int32_t e_len[2][2][QT];    // each epilogue group's own copy
@@ -781,12 +803,20 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
                     const uint32_t at0 = tmem + kACol0 + s * kACols;
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
-                        asm volatile(
-                            "{\n\t.reg .pred pp, pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
-                            "setp.ne.b32 pp, %4, 0;\n\t"
-                            "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pp;\n\t}" ::"r"(d),
-                            "r"(at0 + (uint32_t)ks * 8u), "l"(bd[ks]), "r"(kIdesc), "r"((uint32_t)ks)
-                            : "memory");
+                        if (F8)   // K steps 0-3 against the hi halves, 4-7 against the lo halves
+                            asm volatile(
+                                "{\n\t.reg .pred pp, pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
+                                "setp.ne.b32 pp, %4, 0;\n\t"
+                                "@pe tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, pp;\n\t}" ::"r"(d),
+                                "r"(at0 + (uint32_t)(ks & 3) * 8u), "l"(bd[ks]), "r"(kIdesc), "r"((uint32_t)ks)
+                                : "memory");
+                        else
+                            asm volatile(
+                                "{\n\t.reg .pred pp, pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
+                                "setp.ne.b32 pp, %4, 0;\n\t"
+                                "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pp;\n\t}" ::"r"(d),
+                                "r"(at0 + (uint32_t)ks * 8u), "l"(bd[ks]), "r"(kIdesc), "r"((uint32_t)ks)
+                                : "memory");
                     }
                     asm volatile(
                         "{\n\t.reg .pred pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
@@ -845,6 +875,59 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
                 const bool real = t < p.num_queries;
                 const uint16_t *src = p.idx_q + (t * p.heads + (h < p.heads ? h : 0)) * D;
                 const uint32_t bt = bbase + tb * kBBytes;
+                if (F8) {
+                    // The query in two E4M3 halves: x * 2^e = hi + lo, e chosen so that the
+                    // query's largest |x| (over its heads and dims) lands in [128, 256), hi
+                    // = x * 2^e rounded to E4M3 and lo = the remainder rounded to E4M3 (the
+                    // sum is exact unless an element is below 2^-2 after scaling).  Byte d
+                    // of a tile row is dim d: hi in the first 16 KB, lo in the second.
+                    uint4 v[CH / 2];
+                    float amax = 0.0f;
+#pragma unroll
+                    for (int k = 0; k < CH / 2; ++k) {
+                        v[k] = (real && !stop) ? ldg16(src + 8 * (hh * (CH / 2) + k)) : make_uint4(0, 0, 0, 0);
+                        const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[j] << 16)),
+                                                     fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+                    }
+#pragma unroll
+                    for (int o = 1; o < 2 * HP; o <<= 1)   // the query's 2 * HP threads are consecutive lanes
+                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                    int e = 0;
+                    if (amax > 0.0f) {
+                        e = 7 - ((int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127);   // 7 - floor(log2 amax)
+                        e = e > 126 ? 126 : e;
+                    }
+                    const float sc = __int_as_float((e + 127) << 23);   // 2^e, e in [-120, 126]
+                    if (h == 0 && hh == 0)
+                        s_qinv[tb][q] = __int_as_float((127 - e) << 23);
+                    uint32_t hw[16], lw[16];
+#pragma unroll
+                    for (int k = 0; k < CH / 2; ++k) {   // 8 dims a chunk -> 2 words of hi, 2 of lo
+                        const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+                        for (int j = 0; j < 4; j += 2) {
+                            const float x0 = __uint_as_float(w[j] << 16) * sc, x1 = __uint_as_float(w[j] & 0xFFFF0000u) * sc;
+                            const float x2 = __uint_as_float(w[j + 1] << 16) * sc,
+                                        x3 = __uint_as_float(w[j + 1] & 0xFFFF0000u) * sc;
+                            const uint32_t h01 = e4m3x2_from_f32(x0, x1), h23 = e4m3x2_from_f32(x2, x3);
+                            const float2 d01 = f16x2_to_f2(e4m3x2_to_f16x2(h01)), d23 = f16x2_to_f2(e4m3x2_to_f16x2(h23));
+                            hw[2 * k + j / 2] = h01 | (h23 << 16);
+                            lw[2 * k + j / 2] = e4m3x2_from_f32(x0 - d01.x, x1 - d01.y) |
+                                                (e4m3x2_from_f32(x2 - d23.x, x3 - d23.y) << 16);
+                        }
+                    }
+                    if (!stop) {
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            sts128(swz(bt, r, 4 * hh + m), hw[4 * m], hw[4 * m + 1], hw[4 * m + 2], hw[4 * m + 3]);
+                            sts128(swz(bt + 16384u, r, 4 * hh + m), lw[4 * m], lw[4 * m + 1], lw[4 * m + 2],
+                                   lw[4 * m + 3]);
+                        }
+                    }
+                } else
 #pragma unroll
                 for (int c = hh * (CH / 2); c < (hh + 1) * (CH / 2); ++c) {
                     if (stop)
@@ -916,7 +999,7 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
 #pragma unroll
                     for (int q16 = 0; q16 < (int)(kACols / 2) / 16; ++q16) {
                         uint32_t w[32];
-                        if (FP8) {   // two 16-code pieces -> 16 f16x2 words
+                        if (FP8 && !F8) {   // two 16-code pieces -> 16 f16x2 words
 #pragma unroll
                             for (int vv = 0; vv < 2; ++vv) {
                                 const uint4 rv = raw[2 * q16 + vv];
@@ -927,7 +1010,7 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
                                     w[8 * vv + 2 * k + 1] = e4m3x2_to_f16x2(x[k] >> 16);
                                 }
                             }
-                        } else {     // four 8-element pieces are 16 bf16x2 words already
+                        } else {     // four pieces are 16 words already (bf16 pairs or E4M3 quads)
 #pragma unroll
                             for (int vv = 0; vv < 4; ++vv) {
                                 const uint4 rv = raw[4 * q16 + vv];
@@ -994,6 +1077,18 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
                 const int32_t len = t < p.num_queries ? __ldg(p.kv_len + t) : 0;
                 elen[et] = len > 0 ? len : 0;
                 etoff[et] = t < p.num_queries ? __ldg(p.table_offset + t) : INT64_MIN;
+            }
+            if (F8 && !aborted) {
+                // the query scales s_qinv[tb] are written before the gather releases the
+                // tile; the tile is not reused before this group releases it
+                const uint32_t par = (tile_it >> 1) & 1;
+                bool ok = __all_sync(0xffffffffu, mbar_try(smem_u32(&bar_tile_full[tb]), par));
+                if (!ok && !__any_sync(0xffffffffu, *abort_flag != 0))
+                    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_tile_full[tb]), par));
+                if (!ok) {
+                    aborted = true;
+                    *abort_flag = 1;
+                }
             }
             group_sync();
             for_each_segment<QT>(elen, etoff, p.max_blocks,
@@ -1084,8 +1179,9 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
                         const float v = fmaxf(fmaxf(rr[et], rr[QT + et]), fmaxf(rr[2 * QT + et], rr[3 * QT + et]));
                         const int *ok4 = s_red_ok[grp][rp];
                         const bool all_got = ok4[0] & ok4[1] & ok4[2] & ok4[3];
+                        const float sc = F8 ? kscale * s_qinv[tb][et] : kscale;
                         p.block_scores[(t0 + et) * p.max_blocks + b] =
-                            all_got ? (v > -INFINITY ? v * kscale : -INFINITY) : __int_as_float(0x7fc00000);
+                            all_got ? (v > -INFINITY ? v * sc : -INFINITY) : __int_as_float(0x7fc00000);
                     }
                     pg = pg_next;
                 }
