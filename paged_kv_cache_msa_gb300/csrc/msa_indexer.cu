@@ -72,6 +72,7 @@ struct IndexerParams {
     int32_t pdl;                    // launched with programmatic dependent launch
     int32_t *counters;              // [T] arrivals per query (single launch), else nullptr
     int32_t topk_rows;              // queries per CTA of the several-rows top-k kernel
+    int64_t rows_per_page;          // stride_page / stride_token (query runs with TMA key rows)
 };
 
 __device__ __forceinline__ uint4 ldg16(const void *p)
@@ -608,10 +609,13 @@ constexpr int kTileKeys = 128;   // keys per MMA tile: the 128-token blocks of t
 // the epilogue scores every remaining visible block NaN (never selected).
 
 constexpr int kRunsNSA = 3;            // key stages (A) in tensor memory
+constexpr int kRunsNSATma = 8;         // key stages (A) in shared memory (TMA path): one per gather warp
 constexpr int kRunsNACC = 2;           // accumulators
 constexpr int kRunsThreads = 17 * 32;  // 1 MMA + 8 gather + 2 x 4 epilogue warps
 constexpr uint32_t kRunsTmemCols = 512;
 constexpr int kRunsDynSmem = 120 * 1024;  // two query tiles; more than half an SM: one CTA per SM
+constexpr int kRunsStageBytes = 128 * 128;  // one key stage in shared memory: 128 rows of 128 E4M3 codes
+constexpr int kRunsDynSmemTma = 1024 + 2 * 128 * 128 * 2 + kRunsNSATma * kRunsStageBytes;
 
 template <int QT>
 __device__ __forceinline__ float butterfly_max(float (&v)[QT], int lane)
@@ -669,6 +673,24 @@ __device__ __forceinline__ void mbar_arrive_local(uint32_t bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Four rows of a byte-row tensor map (one-row boxes of 128 bytes, 128-byte swizzle)
+// into four consecutive 128-byte rows of shared memory; the bytes are counted on `bar`.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, const int32_t (&row)[4],
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(map), "r"(0), "r"(row[0]), "r"(row[1]), "r"(row[2]), "r"(row[3]), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
 // The segments and blocks of a tile, in the order every role walks them: one
 // sequence (table row) at a time, first the one of the lowest unscored query;
 // fn(seg_mask, toff, seg_len, nb) per segment.
@@ -696,25 +718,30 @@ __device__ __forceinline__ void for_each_segment(const int32_t *len, const int64
     }
 }
 
-template <int D, bool FP8, int HP>
+template <int D, bool FP8, int HP, bool TMA>
 __global__ void __launch_bounds__(kRunsThreads, 1)
-msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
+msa_index_runs_kernel(const __grid_constant__ IndexerParams p, const __grid_constant__ CUtensorMap kmap)
 {
     constexpr int QT = 128 / HP;                           // queries per tile
     // E4M3 keys of 128 dims: the MMA takes them as stored (kind::f8f6f4, A = the raw
     // codes in tensor memory) against each query split into two E4M3 halves
     constexpr bool F8 = FP8 && D == 128;
+    // TMA: the key rows go to shared memory (tile::gather4 copies) and the MMA reads
+    // them from there; otherwise the gather warps load them and store them to tensor
+    // memory
+    static_assert(!TMA || F8, "TMA key rows: E4M3 keys of 128 dims");
+    constexpr int NSA = TMA ? kRunsNSATma : kRunsNSA;
     constexpr uint32_t kBBytes = 128u * D * 2u;            // one query tile (B): f16/bf16, or E4M3 hi | lo
     constexpr int CH = D / 8;                              // 16-byte chunks of a 2-byte row
     constexpr uint32_t kACols = F8 ? D / 4 : D / 2;        // tensor-memory columns of a key stage
     constexpr uint32_t kAccCols = 128;
     constexpr uint32_t kACol0 = kRunsNACC * kAccCols;      // first key-stage column
-    static_assert(kACol0 + kRunsNSA * kACols <= kRunsTmemCols, "tensor memory budget");
+    static_assert(TMA || kACol0 + NSA * kACols <= kRunsTmemCols, "tensor memory budget");
     constexpr uint32_t kIdesc = (1u << 4) | ((FP8 ? 0u : 1u) << 7) | ((FP8 ? 0u : 1u) << 10) |
                                 ((uint32_t)(128 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_tile_full[2], bar_tile_empty[2];
-    __shared__ __align__(8) uint64_t bar_a_full[kRunsNSA], bar_a_empty[kRunsNSA];
+    __shared__ __align__(8) uint64_t bar_a_full[NSA], bar_a_empty[NSA];
     __shared__ __align__(8) uint64_t bar_acc_full[kRunsNACC], bar_acc_empty[kRunsNACC];
     __shared__ __align__(8) uint64_t bar_drain;
     __shared__ float s_qinv[2][QT];        // E4M3 split: 2^-e of each query's scale
@@ -729,6 +756,7 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t bbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t abase = bbase + 2u * kBBytes;   // TMA key stages, 1024-byte aligned
     const int64_t num_tiles = (p.num_queries + QT - 1) / QT;
 
     if (tid == 0) {
@@ -737,8 +765,11 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
             // released by the eight epilogue warps and the MMA thread
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 9;" ::"r"(smem_u32(&bar_tile_empty[i])));
         }
-        for (int i = 0; i < kRunsNSA; ++i) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(smem_u32(&bar_a_full[i])));
+        for (int i = 0; i < NSA; ++i) {
+            // the eight gather warps' tensor-memory stores, or one expect-tx arrival
+            // and the copies' bytes
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&bar_a_full[i])),
+                         "r"(TMA ? 1 : 8));
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_a_empty[i])));
         }
         for (int i = 0; i < kRunsNACC; ++i) {
@@ -803,7 +834,15 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
                     const uint32_t at0 = tmem + kACol0 + s * kACols;
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
-                        if (F8)   // K steps 0-3 against the hi halves, 4-7 against the lo halves
+                        if (TMA)   // A from shared memory; K steps 0-3 against hi, 4-7 against lo
+                            asm volatile(
+                                "{\n\t.reg .pred pp, pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
+                                "setp.ne.b32 pp, %4, 0;\n\t"
+                                "@pe tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, pp;\n\t}" ::"r"(d),
+                                "l"(sw128_desc(abase + s * (uint32_t)kRunsStageBytes + (uint32_t)(ks & 3) * 32u)),
+                                "l"(bd[ks]), "r"(kIdesc), "r"((uint32_t)ks)
+                                : "memory");
+                        else if (F8)   // K steps 0-3 against the hi halves, 4-7 against the lo halves
                             asm volatile(
                                 "{\n\t.reg .pred pp, pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
                                 "setp.ne.b32 pp, %4, 0;\n\t"
@@ -828,7 +867,7 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
 #else
                     (void)d;
 #endif
-                    if (++s == (uint32_t)kRunsNSA) { s = 0; ph ^= 1u; }
+                    if (++s == (uint32_t)NSA) { s = 0; ph ^= 1u; }
                     if (++a == (uint32_t)kRunsNACC) { a = 0; pa ^= 1u; }
                 }
             });
@@ -849,6 +888,8 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
     } else if (warp <= 8) {
         // ---------------- gather ----------------
         const int gt = tid - 32;                    // 0..255
+        const int gw = warp - 1;                    // TMA path: this warp's key stage
+        uint32_t uses = 0;                          // TMA path: blocks this warp has issued
         const int quarter = warp & 3, half = (warp - 1) >> 2;
         const int key = quarter * 32 + lane;        // tensor-memory lane = key of the block
         constexpr int NV = FP8 ? D / 32 : D / 16;   // 16-byte pieces of half a key row
@@ -963,6 +1004,50 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
             if (lane == 0)
                 mbar_arrive_local(smem_u32(&bar_tile_full[tb]));
 
+            if constexpr (TMA) {
+                // Warp gw issues the blocks whose item index is gw mod 8, each into its own
+                // stage gw: lane l gathers the rows of keys 4l .. 4l + 3 with one
+                // tile::gather4 copy.  Keys without a row (past the segment's history, no
+                // page) read row 0 of the cache; the epilogue masks them.
+                for_each_segment<QT>(g_len[tb], g_toff[tb], p.max_blocks,
+                                     [&](uint32_t, int64_t toff, int32_t seg_len, int nb) {
+                    if (stop)
+                        return;
+                    for (int b = (int)(((uint32_t)gw - it) & 7u); b < nb; b += 8) {
+                        const uint32_t par = (uses & 1u) ^ 1u;
+                        const uint32_t empty = smem_u32(&bar_a_empty[gw]), full = smem_u32(&bar_a_full[gw]);
+                        if (!__all_sync(0xffffffffu, mbar_try(empty, par)) &&
+                            (__any_sync(0xffffffffu, *abort_flag != 0) ||
+                             !__all_sync(0xffffffffu, mbar_wait(empty, par)))) {
+                            *abort_flag = 1;
+                            stop = true;
+                            return;
+                        }
+                        int32_t row[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int64_t j = (int64_t)b * kTileKeys + 4 * lane + k;
+                            row[k] = 0;
+                            if (j < seg_len) {
+                                const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
+                                const int64_t off = p.page_shift >= 0 ? (j & (p.page_size - 1)) : j % p.page_size;
+                                const int64_t ti2 = toff + blk;
+                                const int64_t page =
+                                    (ti2 >= 0 && ti2 < p.page_table_len) ? (int64_t)__ldg(p.page_table + ti2) : -1;
+                                if (page >= 0 && page < p.num_pages)
+                                    row[k] = (int32_t)(page * p.rows_per_page + off);
+                            }
+                        }
+                        if (lane == 0)
+                            mbar_expect_tx(full, (uint32_t)kRunsStageBytes);
+                        __syncwarp();
+                        tma_gather4(abase + (uint32_t)gw * (uint32_t)kRunsStageBytes + (uint32_t)lane * 512u, &kmap,
+                                    row, full);
+                        ++uses;
+                    }
+                    it += (uint32_t)nb;
+                });
+            } else
             for_each_segment<QT>(g_len[tb], g_toff[tb], p.max_blocks,
                                  [&](uint32_t, int64_t toff, int32_t seg_len, int nb) {
                 // this thread's half row of key `key` of block bb, fetched into registers
@@ -985,7 +1070,7 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
                         raw[v] = okr ? ldg16(row + 16 * v) : make_uint4(0, 0, 0, 0);
                 };
                 auto store = [&](const uint4 (&raw)[NV]) -> bool {
-                    const uint32_t s = it % kRunsNSA, ph = (it / kRunsNSA) & 1;
+                    const uint32_t s = it % NSA, ph = (it / NSA) & 1;
                     // the abort flag is read only when the stage is not free yet
                     if (!__all_sync(0xffffffffu, mbar_try(smem_u32(&bar_a_empty[s]), ph ^ 1)) &&
                         (__any_sync(0xffffffffu, *abort_flag != 0) ||
@@ -1050,6 +1135,10 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
                 }
             });
         }
+        // TMA path: this warp's copies have landed before the CTA can finish (they
+        // complete whether or not the MMA consumes them)
+        if (TMA && uses > 0)
+            (void)__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_a_full[gw]), (uses - 1u) & 1u));
     } else {
         // ---------------- epilogue: two groups, alternate blocks ----------------
         const int grp = (warp - 9) >> 2;            // takes the blocks with item parity grp
@@ -1432,6 +1521,8 @@ msa_status indexer_launch(const msa_indexer_cfg *cfg, int64_t num_queries, const
                      : reinterpret_cast<const void *>(&msa_index_score_kernel<128, false>))
             : (p.fp8 ? reinterpret_cast<const void *>(&msa_index_score_kernel<64, true>)
                      : reinterpret_cast<const void *>(&msa_index_score_kernel<64, false>));
+    alignas(64) CUtensorMap kmap;   // the key rows, for query runs on E4M3 keys of 128 dims
+    memset(&kmap, 0, sizeof kmap);
     cudaLaunchConfig_t sc;
     memset(&sc, 0, sizeof sc);
     sc.gridDim = dim3((unsigned)(num_queries * cpq));
@@ -1449,17 +1540,32 @@ msa_status indexer_launch(const msa_indexer_cfg *cfg, int64_t num_queries, const
         if (major != 10)
             return fail(MSA_ERR_UNSUPPORTED, "query runs need tcgen05 tensor cores (compute capability 10.x)");
         const int64_t tiles = (num_queries + qt - 1) / qt;
-        const int smem = kRunsDynSmem;
-        const void *fns[8] = {
-            reinterpret_cast<const void *>(&msa_index_runs_kernel<64, false, 8>),
-            reinterpret_cast<const void *>(&msa_index_runs_kernel<64, false, 16>),
-            reinterpret_cast<const void *>(&msa_index_runs_kernel<64, true, 8>),
-            reinterpret_cast<const void *>(&msa_index_runs_kernel<64, true, 16>),
-            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, false, 8>),
-            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, false, 16>),
-            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, true, 8>),
-            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, true, 16>)};
-        score_fn = fns[(D == 128 ? 4 : 0) + (p.fp8 ? 2 : 0) + (hp8 ? 0 : 1)];
+        // E4M3 keys of 128 dims whose rows lie on one grid (each page a whole number of
+        // token strides, 16-byte aligned): the key rows are gathered by TMA
+        bool tma = false;
+        if (p.fp8 && D == 128 && p.num_pages >= 1 && p.stride_token > 0 && p.stride_page % p.stride_token == 0 &&
+            (reinterpret_cast<uintptr_t>(p.kdata) & 15u) == 0) {
+            const int64_t rpp = p.stride_page / p.stride_token;
+            const int64_t rows = (p.num_pages - 1) * rpp + cfg->page_size;
+            if (rpp >= cfg->page_size && rows < ((int64_t)1 << 31) &&
+                msa_internal_encode_byte_rows(&kmap, p.kdata, rows, p.stride_token)) {
+                tma = true;
+                p.rows_per_page = rpp;
+            }
+        }
+        const int smem = tma ? kRunsDynSmemTma : kRunsDynSmem;
+        const void *fns[10] = {
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<64, false, 8, false>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<64, false, 16, false>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<64, true, 8, false>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<64, true, 16, false>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, false, 8, false>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, false, 16, false>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, true, 8, false>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, true, 16, false>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, true, 8, true>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, true, 16, true>)};
+        score_fn = tma ? fns[8 + (hp8 ? 0 : 1)] : fns[(D == 128 ? 4 : 0) + (p.fp8 ? 2 : 0) + (hp8 ? 0 : 1)];
         sc.gridDim = dim3((unsigned)(tiles < sms ? tiles : sms));   // persistent, one CTA per SM
         sc.blockDim = dim3(kRunsThreads);
         if (cudaFuncSetAttribute(score_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
@@ -1476,7 +1582,7 @@ msa_status indexer_launch(const msa_indexer_cfg *cfg, int64_t num_queries, const
     }
     if (!tiled)
         p.counters = counters;
-    void *sargs[] = {&p};
+    void *sargs[] = {&p, &kmap};   // the per-query kernel takes p alone
     cudaError_t e = cudaLaunchKernelExC(&sc, score_fn, sargs);
     if (e != cudaSuccess)
         return fail(MSA_ERR_CUDA, "score kernel launch failed: %s", cudaGetErrorString(e));

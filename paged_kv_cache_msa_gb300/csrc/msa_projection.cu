@@ -1673,6 +1673,11 @@ msa_status validate(const msa_producer_cfg *cfg, int64_t num_tokens, const void 
 
 }  // namespace
 
+bool msa_internal_encode_byte_rows(CUtensorMap *m, const void *base, int64_t rows, int64_t stride_bytes)
+{
+    return encode_map(m, base, rows, kBKBytes, stride_bytes, 1, 1);
+}
+
 extern "C" msa_status msa_projection_validate(
     const msa_producer_cfg *cfg, int64_t num_tokens, const void *hidden, int64_t hidden_size,
     int64_t hidden_row_stride, const void *weight, int64_t weight_row_stride,

@@ -144,6 +144,18 @@ def test_query_runs_interleaved_sequences_and_pages(P):
     _check(w, flags=_runs())
 
 
+@pytest.mark.parametrize("P,pad", [(64, 128), (96, 0), (16, 384), (64, 16)],
+                         ids=["unused_rows_between_pages", "page_96", "page_16_padded", "off_the_row_grid"])
+def test_query_runs_key_row_layouts(P, pad):
+    """E4M3 keys of 128 dims: pages that span a whole number of token rows take the
+    TMA row gather (with unused rows between pages, and a page size that is not a
+    power of two); padding off the row grid takes the register gather.  Both against
+    the oracle."""
+    w = wl.make_indexer_prefill(f"rows{P}_{pad}", 560 + P + pad, [700, 333, 129], page_size=P,
+                                page_pad_bytes=pad)
+    _check(w, flags=_runs())
+
+
 def test_query_runs_table_holes_and_topk_sizes():
     w = wl.make_indexer_prefill("holes_runs", 501, [700, 260], topk=3)
     pt = np.array(w.page_table, copy=True)
