@@ -73,6 +73,7 @@ struct IndexerParams {
     int32_t *counters;              // [T] arrivals per query (single launch), else nullptr
     int32_t topk_rows;              // queries per CTA of the several-rows top-k kernel
     int64_t rows_per_page;          // stride_page / stride_token (query runs with TMA key rows)
+    int32_t box_rows;               // rows of the key-row tensor map's box: a page, 128, or 1 (gather4)
 };
 
 __device__ __forceinline__ uint4 ldg16(const void *p)
@@ -609,13 +610,14 @@ constexpr int kTileKeys = 128;   // keys per MMA tile: the 128-token blocks of t
 // the epilogue scores every remaining visible block NaN (never selected).
 
 constexpr int kRunsNSA = 3;            // key stages (A) in tensor memory
-constexpr int kRunsNSATma = 8;         // key stages (A) in shared memory (TMA path): one per gather warp
+constexpr int kRunsNSATma = 8;         // key stages (B) in shared memory (TMA kernel): one per gather warp
 constexpr int kRunsNACC = 2;           // accumulators
 constexpr int kRunsThreads = 17 * 32;  // 1 MMA + 8 gather + 2 x 4 epilogue warps
 constexpr uint32_t kRunsTmemCols = 512;
 constexpr int kRunsDynSmem = 120 * 1024;  // two query tiles; more than half an SM: one CTA per SM
 constexpr int kRunsStageBytes = 128 * 128;  // one key stage in shared memory: 128 rows of 128 E4M3 codes
-constexpr int kRunsDynSmemTma = 1024 + 2 * 128 * 128 * 2 + kRunsNSATma * kRunsStageBytes;
+constexpr int kRunsDynSmemTma = 1024 + 2 * 2 * 128 * 128 + kRunsNSATma * kRunsStageBytes;
+constexpr int kRunsTmaThreads = 26 * 32;  // 2 MMA + 8 gather + 4 x 4 epilogue warps
 
 template <int QT>
 __device__ __forceinline__ float butterfly_max(float (&v)[QT], int lane)
@@ -685,6 +687,17 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// A box of consecutive rows of a byte-row tensor map from row `row` into shared
+// memory; the bytes are counted on `bar`.
+__device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap *map, int32_t row, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(map), "r"(0), "r"(row), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
@@ -718,25 +731,21 @@ __device__ __forceinline__ void for_each_segment(const int32_t *len, const int64
     }
 }
 
-template <int D, bool FP8, int HP, bool TMA>
+template <int D, bool FP8, int HP>
 __global__ void __launch_bounds__(kRunsThreads, 1)
-msa_index_runs_kernel(const __grid_constant__ IndexerParams p, const __grid_constant__ CUtensorMap kmap)
+msa_index_runs_kernel(const __grid_constant__ IndexerParams p)
 {
     constexpr int QT = 128 / HP;                           // queries per tile
     // E4M3 keys of 128 dims: the MMA takes them as stored (kind::f8f6f4, A = the raw
     // codes in tensor memory) against each query split into two E4M3 halves
     constexpr bool F8 = FP8 && D == 128;
-    // TMA: the key rows go to shared memory (tile::gather4 copies) and the MMA reads
-    // them from there; otherwise the gather warps load them and store them to tensor
-    // memory
-    static_assert(!TMA || F8, "TMA key rows: E4M3 keys of 128 dims");
-    constexpr int NSA = TMA ? kRunsNSATma : kRunsNSA;
+    constexpr int NSA = kRunsNSA;
     constexpr uint32_t kBBytes = 128u * D * 2u;            // one query tile (B): f16/bf16, or E4M3 hi | lo
     constexpr int CH = D / 8;                              // 16-byte chunks of a 2-byte row
     constexpr uint32_t kACols = F8 ? D / 4 : D / 2;        // tensor-memory columns of a key stage
     constexpr uint32_t kAccCols = 128;
     constexpr uint32_t kACol0 = kRunsNACC * kAccCols;      // first key-stage column
-    static_assert(TMA || kACol0 + NSA * kACols <= kRunsTmemCols, "tensor memory budget");
+    static_assert(kACol0 + NSA * kACols <= kRunsTmemCols, "tensor memory budget");
     constexpr uint32_t kIdesc = (1u << 4) | ((FP8 ? 0u : 1u) << 7) | ((FP8 ? 0u : 1u) << 10) |
                                 ((uint32_t)(128 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
     extern __shared__ uint8_t smem_raw[];
@@ -756,7 +765,6 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p, const __grid_cons
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t bbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    const uint32_t abase = bbase + 2u * kBBytes;   // TMA key stages, 1024-byte aligned
     const int64_t num_tiles = (p.num_queries + QT - 1) / QT;
 
     if (tid == 0) {
@@ -766,10 +774,7 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p, const __grid_cons
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 9;" ::"r"(smem_u32(&bar_tile_empty[i])));
         }
         for (int i = 0; i < NSA; ++i) {
-            // the eight gather warps' tensor-memory stores, or one expect-tx arrival
-            // and the copies' bytes
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&bar_a_full[i])),
-                         "r"(TMA ? 1 : 8));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(smem_u32(&bar_a_full[i])));
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_a_empty[i])));
         }
         for (int i = 0; i < kRunsNACC; ++i) {
@@ -834,15 +839,7 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p, const __grid_cons
                     const uint32_t at0 = tmem + kACol0 + s * kACols;
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
-                        if (TMA)   // A from shared memory; K steps 0-3 against hi, 4-7 against lo
-                            asm volatile(
-                                "{\n\t.reg .pred pp, pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
-                                "setp.ne.b32 pp, %4, 0;\n\t"
-                                "@pe tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, pp;\n\t}" ::"r"(d),
-                                "l"(sw128_desc(abase + s * (uint32_t)kRunsStageBytes + (uint32_t)(ks & 3) * 32u)),
-                                "l"(bd[ks]), "r"(kIdesc), "r"((uint32_t)ks)
-                                : "memory");
-                        else if (F8)   // K steps 0-3 against the hi halves, 4-7 against the lo halves
+                        if (F8)   // K steps 0-3 against the hi halves, 4-7 against the lo halves
                             asm volatile(
                                 "{\n\t.reg .pred pp, pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
                                 "setp.ne.b32 pp, %4, 0;\n\t"
@@ -888,8 +885,6 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p, const __grid_cons
     } else if (warp <= 8) {
         // ---------------- gather ----------------
         const int gt = tid - 32;                    // 0..255
-        const int gw = warp - 1;                    // TMA path: this warp's key stage
-        uint32_t uses = 0;                          // TMA path: blocks this warp has issued
         const int quarter = warp & 3, half = (warp - 1) >> 2;
         const int key = quarter * 32 + lane;        // tensor-memory lane = key of the block
         constexpr int NV = FP8 ? D / 32 : D / 16;   // 16-byte pieces of half a key row
@@ -1004,50 +999,6 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p, const __grid_cons
             if (lane == 0)
                 mbar_arrive_local(smem_u32(&bar_tile_full[tb]));
 
-            if constexpr (TMA) {
-                // Warp gw issues the blocks whose item index is gw mod 8, each into its own
-                // stage gw: lane l gathers the rows of keys 4l .. 4l + 3 with one
-                // tile::gather4 copy.  Keys without a row (past the segment's history, no
-                // page) read row 0 of the cache; the epilogue masks them.
-                for_each_segment<QT>(g_len[tb], g_toff[tb], p.max_blocks,
-                                     [&](uint32_t, int64_t toff, int32_t seg_len, int nb) {
-                    if (stop)
-                        return;
-                    for (int b = (int)(((uint32_t)gw - it) & 7u); b < nb; b += 8) {
-                        const uint32_t par = (uses & 1u) ^ 1u;
-                        const uint32_t empty = smem_u32(&bar_a_empty[gw]), full = smem_u32(&bar_a_full[gw]);
-                        if (!__all_sync(0xffffffffu, mbar_try(empty, par)) &&
-                            (__any_sync(0xffffffffu, *abort_flag != 0) ||
-                             !__all_sync(0xffffffffu, mbar_wait(empty, par)))) {
-                            *abort_flag = 1;
-                            stop = true;
-                            return;
-                        }
-                        int32_t row[4];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int64_t j = (int64_t)b * kTileKeys + 4 * lane + k;
-                            row[k] = 0;
-                            if (j < seg_len) {
-                                const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
-                                const int64_t off = p.page_shift >= 0 ? (j & (p.page_size - 1)) : j % p.page_size;
-                                const int64_t ti2 = toff + blk;
-                                const int64_t page =
-                                    (ti2 >= 0 && ti2 < p.page_table_len) ? (int64_t)__ldg(p.page_table + ti2) : -1;
-                                if (page >= 0 && page < p.num_pages)
-                                    row[k] = (int32_t)(page * p.rows_per_page + off);
-                            }
-                        }
-                        if (lane == 0)
-                            mbar_expect_tx(full, (uint32_t)kRunsStageBytes);
-                        __syncwarp();
-                        tma_gather4(abase + (uint32_t)gw * (uint32_t)kRunsStageBytes + (uint32_t)lane * 512u, &kmap,
-                                    row, full);
-                        ++uses;
-                    }
-                    it += (uint32_t)nb;
-                });
-            } else
             for_each_segment<QT>(g_len[tb], g_toff[tb], p.max_blocks,
                                  [&](uint32_t, int64_t toff, int32_t seg_len, int nb) {
                 // this thread's half row of key `key` of block bb, fetched into registers
@@ -1135,10 +1086,6 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p, const __grid_cons
                 }
             });
         }
-        // TMA path: this warp's copies have landed before the CTA can finish (they
-        // complete whether or not the MMA consumes them)
-        if (TMA && uses > 0)
-            (void)__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_a_full[gw]), (uses - 1u) & 1u));
     } else {
         // ---------------- epilogue: two groups, alternate blocks ----------------
         const int grp = (warp - 9) >> 2;            // takes the blocks with item parity grp
@@ -1281,6 +1228,497 @@ msa_index_runs_kernel(const __grid_constant__ IndexerParams p, const __grid_cons
                     const int q = idx / rest, bb = nb + idx % rest;
                     if ((seg >> q) & 1 && t0 + q < p.num_queries)
                         p.block_scores[(t0 + q) * p.max_blocks + bb] = -INFINITY;
+                }
+            });
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_local(smem_u32(&bar_tile_empty[tb]));
+        }
+    }
+
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kRunsTmemCols)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
+// block scores of query runs on E4M3 keys of 128 dims, key rows gathered by TMA
+// ---------------------------------------------------------------------------
+//
+// The tiles and segments of msa_index_runs_kernel, with the operands the other way
+// round and both in shared memory (128-byte swizzle, K-major):
+//   A (M = 128)  the tile's query heads (row = query * HP + head), each query split
+//                into E4M3 halves hi | lo under a power-of-two scale (K steps 0-3
+//                read hi, 4-7 lo), written once per tile by the gather warps;
+//   B (N = 128)  the block's 128 key rows as stored (E4M3 codes), gathered into a
+//                key stage by tile::gather4 copies (no register staging);
+//   D            fp32 [query head, key] in tensor memory: four accumulators, block i
+//                in accumulator i mod 4.
+// Warps: 0 and 25 issue the MMAs of the even and the odd blocks (one elected lane of
+// the whole warp issues; one warp's waits overlap the other's MMAs); 1-8 gather: the
+// query tile, then key stage w - 1 each, filled with the blocks whose item index is
+// w - 1 mod 8 (lane l gathers keys 4l .. 4l + 3); 9-24 epilogue, four groups of four,
+// group g reading accumulator g.  Each barrier phase is waited on by one warp or
+// group that also waited on the phase before it (a parity wait two phases ahead would
+// see the older phase complete): stage s is consumed by MMA warp s mod 2 and
+// accumulator a issued by MMA warp a mod 2 and read by epilogue group a.  An epilogue thread holds one query head's row of D: the
+// max over the block's visible keys in registers, then over the query's HP heads by
+// shuffles, and the query's head-0 lane writes the block score.  Key validity (a page
+// in range) is a 128-bit mask each epilogue warp builds by ballot; keys past a
+// query's history are cut by its length.
+template <int HP>
+__global__ void __launch_bounds__(kRunsTmaThreads, 1)
+msa_index_runs_tma_kernel(const __grid_constant__ IndexerParams p, const __grid_constant__ CUtensorMap kmap)
+{
+    constexpr int QT = 128 / HP;                           // queries per tile
+    constexpr int NSA = kRunsNSATma;
+    constexpr int NACC = 4;
+    constexpr uint32_t kAccCols = 128;
+    constexpr uint32_t kQBytes = 2u * 128u * 128u;         // one query tile: hi atom | lo atom
+    static_assert(NACC * kAccCols <= kRunsTmemCols, "tensor memory budget");
+    // E4M3 x E4M3 -> fp32, both K-major, N = 128, M = 128
+    constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(128 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_tile_full[2], bar_tile_empty[2];
+    __shared__ __align__(8) uint64_t bar_k_full[NSA], bar_k_empty[NSA];
+    __shared__ __align__(8) uint64_t bar_acc_full[NACC], bar_acc_empty[NACC];
+    __shared__ __align__(8) uint64_t bar_drain;
+    __shared__ float s_qinv[2][QT];        // 2^-e of each query's scale
+    __shared__ float s_amax[2][QT];        // max |x| of each query over one half of the dims
+    __shared__ int32_t g_len[2][QT];       // gather side's tile metadata (also read by the MMA)
+    __shared__ int64_t g_toff[2][QT];
+    __shared__ int32_t e_len[4][2][QT];    // each epilogue group's own copy
+    __shared__ int64_t e_toff[4][2][QT];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t qbase = (smem_u32(smem_raw) + 1023u) & ~1023u;   // two query tiles, 1024-byte aligned
+    const uint32_t kbase = qbase + 2u * kQBytes;                     // the key stages
+    const int64_t num_tiles = (p.num_queries + QT - 1) / QT;
+
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(smem_u32(&bar_tile_full[i])));
+            // released by the sixteen epilogue warps and the two MMA warps
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 18;" ::"r"(smem_u32(&bar_tile_empty[i])));
+        }
+        for (int i = 0; i < NSA; ++i) {
+            // one expect-tx arrival and the copies' bytes; the MMA's commit
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_k_full[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_k_empty[i])));
+        }
+        for (int i = 0; i < NACC; ++i) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_acc_full[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(smem_u32(&bar_acc_empty[i])));
+        }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 2;" ::"r"(smem_u32(&bar_drain)));
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&s_tmem)),
+                     "r"(kRunsTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = s_tmem;
+    volatile int *abort_flag = &s_abort;
+
+    if (warp == 0 || warp == 25) {
+        // ---------------- MMA issuers: warp 0 the even blocks, warp 25 the odd ones ----------------
+        const uint32_t g = warp == 0 ? 0u : 1u;
+        uint32_t tile_it = 0, it = 0;
+        bool ok = true;
+        for (int64_t ti = blockIdx.x; ti < num_tiles && ok; ti += gridDim.x, ++tile_it) {
+            const uint32_t tb = tile_it & 1;
+            if (__any_sync(0xffffffffu, *abort_flag != 0) ||
+                !__all_sync(0xffffffffu, mbar_wait_fast(smem_u32(&bar_tile_full[tb]), (tile_it >> 1) & 1))) {
+                ok = false;
+                break;
+            }
+            const uint64_t qd = sw128_desc(qbase + tb * kQBytes);
+            for_each_segment<QT>(g_len[tb], g_toff[tb], p.max_blocks,
+                                 [&](uint32_t, int64_t, int32_t, int nb) {
+                for (int b = (int)((g ^ it) & 1u); b < nb && ok; b += 2) {
+                    const uint32_t its = it + (uint32_t)b;   // global item index
+                    const uint32_t s = its % (uint32_t)NSA, ph = (its / (uint32_t)NSA) & 1u;
+                    const uint32_t a = its % (uint32_t)NACC, pa = (its / (uint32_t)NACC) & 1u;
+                    if (!__all_sync(0xffffffffu, mbar_try(smem_u32(&bar_k_full[s]), ph) &&
+                                                     mbar_try(smem_u32(&bar_acc_empty[a]), pa ^ 1)) &&
+                        (__any_sync(0xffffffffu, *abort_flag != 0) ||
+                         !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_k_full[s]), ph) &&
+                                                      mbar_wait(smem_u32(&bar_acc_empty[a]), pa ^ 1)))) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t d = tmem + a * kAccCols;
+#ifndef MSA_STARVE
+                    const uint64_t kd = sw128_desc(kbase + s * (uint32_t)kRunsStageBytes);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)   // K steps 0-3: hi x keys, 4-7: lo x keys (32 bytes each)
+                        asm volatile(
+                            "{\n\t.reg .pred pp, pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
+                            "setp.ne.b32 pp, %4, 0;\n\t"
+                            "@pe tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, pp;\n\t}" ::"r"(d),
+                            "l"(qd + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2)), "l"(kd + (uint64_t)((ks & 3) * 2)),
+                            "r"(kIdesc), "r"((uint32_t)ks)
+                            : "memory");
+                    asm volatile(
+                        "{\n\t.reg .pred pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
+                        "@pe tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t"
+                        "@pe tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];\n\t}" ::"r"(
+                            smem_u32(&bar_k_empty[s])),
+                        "r"(smem_u32(&bar_acc_full[a]))
+                        : "memory");
+#else
+                    (void)d;
+#endif
+                }
+                it += (uint32_t)nb;
+            });
+            __syncwarp();
+            if (ok && lane == 0)   // this warp is done with the tile (its MMAs may still run)
+                mbar_arrive_local(smem_u32(&bar_tile_empty[tb]));
+        }
+        if (!ok && lane == 0)
+            *abort_flag = 1;
+        // every MMA of both warps has completed before tensor memory is released
+        asm volatile(
+            "{\n\t.reg .pred pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
+            "@pe tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+                smem_u32(&bar_drain))
+            : "memory");
+        (void)mbar_wait_fast(smem_u32(&bar_drain), 0);
+        __syncwarp();
+    } else if (warp <= 8) {
+        // ---------------- gather: query tiles into tensor memory, key rows by TMA ----------------
+        const int gt = tid - 32;                    // 0..255
+        const int gw = warp - 1;                    // this warp's key stage
+        const int quarter = warp & 3, half = (warp - 1) >> 2;
+        const int r = quarter * 32 + lane;          // tensor-memory lane = query-tile row
+        const int q = r / HP, h = r % HP;
+        uint32_t it = 0, tile_it = 0, uses = 0;
+        bool stop = false;
+        for (int64_t ti = blockIdx.x; ti < num_tiles; ti += gridDim.x, ++tile_it) {
+            const uint32_t tb = tile_it & 1;
+            stop = stop || *abort_flag ||
+                   !__any_sync(0xffffffffu, mbar_wait_fast(smem_u32(&bar_tile_empty[tb]), ((tile_it >> 1) & 1) ^ 1));
+            const int64_t t0 = ti * QT;
+            if (gt == 0 && ti + gridDim.x < num_tiles) {
+                // the next tile's query rows (contiguous) into L2 while this tile runs
+                const int64_t n0 = (ti + gridDim.x) * QT;
+                const int64_t nq = p.num_queries - n0 < QT ? p.num_queries - n0 : QT;
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.idx_q + n0 * p.heads * 128),
+                             "r"((uint32_t)(nq * p.heads * 256))
+                             : "memory");
+            }
+            if (!stop && gt < QT) {
+                const int64_t t = t0 + gt;
+                const int32_t len = t < p.num_queries ? __ldg(p.kv_len + t) : 0;
+                g_len[tb][gt] = len > 0 ? len : 0;
+                g_toff[tb][gt] = t < p.num_queries ? __ldg(p.table_offset + t) : INT64_MIN;
+            }
+            {
+                // Row r = (query q, head h), this warp's half of the dims.  Rows of heads
+                // past num_heads repeat head 0, so that the max over a query's HP rows
+                // equals the max over its real heads.  x * 2^e = hi + lo with e chosen so
+                // that the query's largest |x| (over its heads and dims) lies in
+                // [128, 256), hi = x * 2^e rounded to E4M3, lo = the remainder rounded
+                // to E4M3 (exact unless an element is below 2^-2 after scaling).
+                const int64_t t = t0 + q;
+                const bool real = t < p.num_queries && !stop;
+                const uint16_t *src = p.idx_q + (t * p.heads + (h < p.heads ? h : 0)) * 128 + half * 64;
+                uint4 v[8];
+                float amax = 0.0f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    v[k] = real ? ldg16(src + 8 * k) : make_uint4(0, 0, 0, 0);
+                    const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[j] << 16)),
+                                                 fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+                }
+#pragma unroll
+                for (int o = 1; o < HP; o <<= 1)   // the query's HP rows are consecutive lanes
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                if (h == 0)
+                    s_amax[half][q] = amax;
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                amax = fmaxf(s_amax[0][q], s_amax[1][q]);
+                int e = 0;
+                if (amax > 0.0f) {
+                    e = 7 - ((int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127);   // 7 - floor(log2 amax)
+                    e = e > 126 ? 126 : e;
+                }
+                const float sc = __int_as_float((e + 127) << 23);   // 2^e, e in [-120, 126]
+                if (h == 0 && half == 0)
+                    s_qinv[tb][q] = __int_as_float((127 - e) << 23);
+                uint32_t hw[16], lw[16];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {   // 8 dims a chunk -> 2 words of hi, 2 of lo
+                    const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+                    for (int j = 0; j < 4; j += 2) {
+                        const float x0 = __uint_as_float(w[j] << 16) * sc, x1 = __uint_as_float(w[j] & 0xFFFF0000u) * sc;
+                        const float x2 = __uint_as_float(w[j + 1] << 16) * sc,
+                                    x3 = __uint_as_float(w[j + 1] & 0xFFFF0000u) * sc;
+                        const uint32_t h01 = e4m3x2_from_f32(x0, x1), h23 = e4m3x2_from_f32(x2, x3);
+                        const float2 d01 = f16x2_to_f2(e4m3x2_to_f16x2(h01)), d23 = f16x2_to_f2(e4m3x2_to_f16x2(h23));
+                        hw[2 * k + j / 2] = h01 | (h23 << 16);
+                        lw[2 * k + j / 2] = e4m3x2_from_f32(x0 - d01.x, x1 - d01.y) |
+                                            (e4m3x2_from_f32(x2 - d23.x, x3 - d23.y) << 16);
+                    }
+                }
+                if (!stop) {
+                    // 64 dims = 16-byte chunks 4 half .. 4 half + 3 of row r, hi atom and lo atom
+                    const uint32_t bt = qbase + tb * kQBytes;
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        sts128(swz(bt, r, 4 * half + m), hw[4 * m], hw[4 * m + 1], hw[4 * m + 2], hw[4 * m + 3]);
+                        sts128(swz(bt + 16384u, r, 4 * half + m), lw[4 * m], lw[4 * m + 1], lw[4 * m + 2],
+                               lw[4 * m + 3]);
+                    }
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            // publishes the tile's metadata to every gather thread and takes one stop
+            // decision for all eight gather warps
+            {
+                uint32_t any;
+                asm volatile(
+                    "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, 1, 256, p; selp.u32 %0, 1, 0, q; }"
+                    : "=r"(any)
+                    : "r"((uint32_t)stop)
+                    : "memory");
+                if (any) {
+                    *abort_flag = 1;
+                    break;
+                }
+            }
+            if (lane == 0)
+                mbar_arrive_local(smem_u32(&bar_tile_full[tb]));
+
+            // Key rows.  When pages are whole boxes of p.box_rows rows (a page size that
+            // divides 128, or a multiple of 128), lane l < 128 / box_rows copies box l of
+            // the block with one tiled copy; otherwise lane l gathers keys 4l .. 4l + 3
+            // with one tile::gather4 copy.  A box or key without a page, or wholly past
+            // the segment's history, reads from row 0 of the cache; the epilogue masks
+            // it.  The next block's page entries load while the stage wait runs.
+            const int BR = p.box_rows;
+            for_each_segment<QT>(g_len[tb], g_toff[tb], p.max_blocks,
+                                 [&](uint32_t, int64_t toff, int32_t seg_len, int nb) {
+                if (stop)
+                    return;
+                // the first key of this lane's box (k = 0), or its key k, in block bb
+                auto key_of = [&](int bb, int k) -> int64_t {
+                    return (int64_t)bb * kTileKeys + (BR > 1 ? (int64_t)lane * BR : (int64_t)(4 * lane + k));
+                };
+                auto entries = [&](int bb, int32_t (&e)[4]) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int64_t j = key_of(bb, k);
+                        e[k] = -1;
+                        if (bb < nb && j < seg_len && (BR > 1 ? (k == 0 && lane * BR < kTileKeys) : true)) {
+                            const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
+                            const int64_t ti2 = toff + blk;
+                            if (ti2 >= 0 && ti2 < p.page_table_len)
+                                e[k] = __ldg(p.page_table + ti2);
+                        }
+                    }
+                };
+                int b = (int)(((uint32_t)gw - it) & 7u);
+                int32_t ec[4];
+                entries(b, ec);
+                for (; b < nb; b += 8) {
+                    int32_t en[4];
+                    entries(b + 8, en);
+                    int32_t row[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int64_t j = key_of(b, k);
+                        const int64_t off = p.page_shift >= 0 ? (j & (p.page_size - 1)) : j % p.page_size;
+                        row[k] = (ec[k] >= 0 && (int64_t)ec[k] < p.num_pages)
+                                     ? (int32_t)((int64_t)ec[k] * p.rows_per_page + off)
+                                     : 0;
+                    }
+                    const uint32_t par = (uses & 1u) ^ 1u;
+                    const uint32_t empty = smem_u32(&bar_k_empty[gw]), full = smem_u32(&bar_k_full[gw]);
+                    if (!__all_sync(0xffffffffu, mbar_try(empty, par)) &&
+                        (__any_sync(0xffffffffu, *abort_flag != 0) ||
+                         !__all_sync(0xffffffffu, mbar_wait(empty, par)))) {
+                        *abort_flag = 1;
+                        stop = true;
+                        return;
+                    }
+                    if (lane == 0)
+                        mbar_expect_tx(full, (uint32_t)kRunsStageBytes);
+                    __syncwarp();
+                    const uint32_t st = kbase + (uint32_t)gw * (uint32_t)kRunsStageBytes;
+                    if (BR > 1) {
+                        if (lane * BR < kTileKeys)
+                            tma_load_rows(st + (uint32_t)(lane * BR) * 128u, &kmap, row[0], full);
+                    } else {
+                        tma_gather4(st + (uint32_t)lane * 512u, &kmap, row, full);
+                    }
+                    ++uses;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        ec[k] = en[k];
+                }
+                it += (uint32_t)nb;
+            });
+        }
+        // this warp's copies have landed before the CTA can finish (they complete
+        // whether or not the MMA consumes them)
+        if (uses > 0)
+            (void)__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_k_full[gw]), (uses - 1u) & 1u));
+    } else {
+        // ---------------- epilogue: four groups, group g the blocks in accumulator g ----------------
+        const int grp = (warp - 9) >> 2;            // takes the blocks with item index grp mod 4
+        const int et = tid - (9 + 4 * grp) * 32;    // 0..127 within the group
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;          // the query-tile row of this thread
+        const int q = r / HP, h = r % HP;
+        const uint32_t d_lane = (uint32_t)(quarter * 32) << 16;
+        const float kscale = __ldg(p.k_scale);
+        auto group_sync = [&]() {
+            if (grp == 0)
+                asm volatile("bar.sync 2, 128;" ::: "memory");
+            else if (grp == 1)
+                asm volatile("bar.sync 3, 128;" ::: "memory");
+            else if (grp == 2)
+                asm volatile("bar.sync 4, 128;" ::: "memory");
+            else
+                asm volatile("bar.sync 5, 128;" ::: "memory");
+        };
+        uint32_t it = 0, tile_it = 0;
+        bool aborted = false;
+        for (int64_t ti = blockIdx.x; ti < num_tiles; ti += gridDim.x, ++tile_it) {
+            const uint32_t tb = tile_it & 1;
+            const int64_t t0 = ti * QT;
+            int32_t *elen = e_len[grp][tb];
+            int64_t *etoff = e_toff[grp][tb];
+            if (et < QT) {
+                const int64_t t = t0 + et;
+                const int32_t len = t < p.num_queries ? __ldg(p.kv_len + t) : 0;
+                elen[et] = len > 0 ? len : 0;
+                etoff[et] = t < p.num_queries ? __ldg(p.table_offset + t) : INT64_MIN;
+            }
+            if (!aborted) {
+                // the query scales s_qinv[tb] are written before the gather releases the
+                // tile; the tile is not reused before this group releases it
+                const uint32_t par = (tile_it >> 1) & 1;
+                bool ok = __all_sync(0xffffffffu, mbar_try(smem_u32(&bar_tile_full[tb]), par));
+                if (!ok && !__any_sync(0xffffffffu, *abort_flag != 0))
+                    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_tile_full[tb]), par));
+                if (!ok) {
+                    aborted = true;
+                    *abort_flag = 1;
+                }
+            }
+            group_sync();
+            const float qscale = kscale * s_qinv[tb][q];
+            for_each_segment<QT>(elen, etoff, p.max_blocks,
+                                 [&](uint32_t seg, int64_t toff, int32_t, int nb) {
+                const bool mine = ((seg >> q) & 1) && t0 + q < p.num_queries;
+                const int32_t lenq = elen[q];
+                // the page entries of keys 4 lane .. 4 lane + 3 of block bb (-1: none)
+                auto kload = [&](int bb, int32_t (&e)[4]) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int64_t j = (int64_t)bb * kTileKeys + 4 * lane + k;
+                        const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
+                        const int64_t ti2 = toff + blk;
+                        e[k] = (bb < nb && ti2 >= 0 && ti2 < p.page_table_len) ? __ldg(p.page_table + ti2) : -1;
+                    }
+                };
+                int b = (int)(((uint32_t)grp - it) & 3u);         // this group's first block
+                int32_t ec[4];
+                kload(b, ec);
+                for (; b < nb; b += 4) {
+                    const uint32_t its = it + (uint32_t)b;          // global item index
+                    const uint32_t acc = (uint32_t)grp, pa = (its / (uint32_t)NACC) & 1u;
+                    int32_t en[4];
+                    kload(b + 4, en);                               // in flight meanwhile
+                    // bit `lane` of word k: key 4 lane + k has a page
+                    uint32_t km[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        km[k] = __ballot_sync(0xffffffffu, ec[k] >= 0 && (int64_t)ec[k] < p.num_pages);
+                    // the abort flag is read only when the accumulator is not ready yet
+                    bool got = false;
+                    if (!aborted) {
+                        got = __all_sync(0xffffffffu, mbar_try(smem_u32(&bar_acc_full[acc]), pa));
+                        if (!got && !__any_sync(0xffffffffu, *abort_flag != 0))
+                            got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_acc_full[acc]), pa));
+                        if (!got) {
+                            aborted = true;
+                            *abort_flag = 1;
+                        }
+                    }
+                    float m = -INFINITY;
+                    if (got) {
+                        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                        // keys of this block inside the query's history
+                        const int cut = lenq - b * kTileKeys;
+                        const bool all_pages = (km[0] & km[1] & km[2] & km[3]) == 0xffffffffu;
+                        const bool plain = all_pages && cut >= kTileKeys;
+#pragma unroll
+                        for (int c0 = 0; c0 < 128; c0 += 32) {
+                            uint32_t v[32];
+                            tmem_ld32_nowait(tmem + d_lane + acc * kAccCols + (uint32_t)c0, v);
+                            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                            if (plain) {
+                                float m2[4] = {m, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    m2[i & 3] = fmaxf(m2[i & 3], __uint_as_float(v[i]));
+                                m = fmaxf(fmaxf(m2[0], m2[1]), fmaxf(m2[2], m2[3]));
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) {
+                                    const int c = c0 + i;   // key c: word c % 4, bit c / 4
+                                    if (c < cut && ((km[c & 3] >> (c >> 2)) & 1u))
+                                        m = fmaxf(m, __uint_as_float(v[i]));
+                                }
+                            }
+                        }
+                    }
+                    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive_local(smem_u32(&bar_acc_empty[acc]));
+#pragma unroll
+                    for (int o = 1; o < HP; o <<= 1)   // over the query's heads
+                        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                    if (h == 0 && mine)
+                        p.block_scores[(t0 + q) * p.max_blocks + b] =
+                            got ? (m > -INFINITY ? m * qscale : -INFINITY) : __int_as_float(0x7fc00000);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        ec[k] = en[k];
+                }
+                it += (uint32_t)nb;
+                // blocks the segment's queries do not reach (the four groups share them)
+                const int rest = p.max_blocks - nb;
+                for (int idx = et + 128 * grp; idx < QT * rest; idx += 512) {
+                    const int qq = idx / rest, bb = nb + idx % rest;
+                    if ((seg >> qq) & 1 && t0 + qq < p.num_queries)
+                        p.block_scores[(t0 + qq) * p.max_blocks + bb] = -INFINITY;
                 }
             });
             __syncwarp();
@@ -1547,27 +1985,31 @@ msa_status indexer_launch(const msa_indexer_cfg *cfg, int64_t num_queries, const
             (reinterpret_cast<uintptr_t>(p.kdata) & 15u) == 0) {
             const int64_t rpp = p.stride_page / p.stride_token;
             const int64_t rows = (p.num_pages - 1) * rpp + cfg->page_size;
-            if (rpp >= cfg->page_size && rows < ((int64_t)1 << 31) &&
-                msa_internal_encode_byte_rows(&kmap, p.kdata, rows, p.stride_token)) {
+            const int P = cfg->page_size;
+            // whole pages per copy where a page is a box (at most 16 copies a block)
+            const int br = (kTileKeys % P == 0 && P >= 8) ? P : (P % kTileKeys == 0 ? kTileKeys : 1);
+            if (rpp >= P && rows < ((int64_t)1 << 31) &&
+                msa_internal_encode_byte_rows(&kmap, p.kdata, rows, p.stride_token, br)) {
                 tma = true;
                 p.rows_per_page = rpp;
+                p.box_rows = br;
             }
         }
         const int smem = tma ? kRunsDynSmemTma : kRunsDynSmem;
         const void *fns[10] = {
-            reinterpret_cast<const void *>(&msa_index_runs_kernel<64, false, 8, false>),
-            reinterpret_cast<const void *>(&msa_index_runs_kernel<64, false, 16, false>),
-            reinterpret_cast<const void *>(&msa_index_runs_kernel<64, true, 8, false>),
-            reinterpret_cast<const void *>(&msa_index_runs_kernel<64, true, 16, false>),
-            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, false, 8, false>),
-            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, false, 16, false>),
-            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, true, 8, false>),
-            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, true, 16, false>),
-            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, true, 8, true>),
-            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, true, 16, true>)};
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<64, false, 8>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<64, false, 16>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<64, true, 8>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<64, true, 16>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, false, 8>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, false, 16>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, true, 8>),
+            reinterpret_cast<const void *>(&msa_index_runs_kernel<128, true, 16>),
+            reinterpret_cast<const void *>(&msa_index_runs_tma_kernel<8>),
+            reinterpret_cast<const void *>(&msa_index_runs_tma_kernel<16>)};
         score_fn = tma ? fns[8 + (hp8 ? 0 : 1)] : fns[(D == 128 ? 4 : 0) + (p.fp8 ? 2 : 0) + (hp8 ? 0 : 1)];
         sc.gridDim = dim3((unsigned)(tiles < sms ? tiles : sms));   // persistent, one CTA per SM
-        sc.blockDim = dim3(kRunsThreads);
+        sc.blockDim = dim3(tma ? kRunsTmaThreads : kRunsThreads);
         if (cudaFuncSetAttribute(score_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
             cudaSuccess)
             return fail(MSA_ERR_CUDA, "cudaFuncSetAttribute failed");
@@ -1582,7 +2024,7 @@ msa_status indexer_launch(const msa_indexer_cfg *cfg, int64_t num_queries, const
     }
     if (!tiled)
         p.counters = counters;
-    void *sargs[] = {&p, &kmap};   // the per-query kernel takes p alone
+    void *sargs[] = {&p, &kmap};   // the kernels without the map take p alone
     cudaError_t e = cudaLaunchKernelExC(&sc, score_fn, sargs);
     if (e != cudaSuccess)
         return fail(MSA_ERR_CUDA, "score kernel launch failed: %s", cudaGetErrorString(e));

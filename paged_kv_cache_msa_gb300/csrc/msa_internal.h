@@ -51,6 +51,7 @@ const uint8_t *msa_internal_cache_end(uint8_t *const *data, int64_t heads, int64
 msa_status msa_internal_projection_violations(uint64_t *count, int32_t reset);
 
 // A TMA tensor map over `rows` rows of 128 bytes (8-bit elements) that start
-// `stride_bytes` apart from `base`, copied one row per box with the 128-byte
+// `stride_bytes` apart from `base`, copied `box_rows` rows per box with the 128-byte
 // swizzle.  False when the driver's encoder is unavailable or rejects the layout.
-bool msa_internal_encode_byte_rows(CUtensorMap *m, const void *base, int64_t rows, int64_t stride_bytes);
+bool msa_internal_encode_byte_rows(CUtensorMap *m, const void *base, int64_t rows, int64_t stride_bytes,
+                                   int box_rows);

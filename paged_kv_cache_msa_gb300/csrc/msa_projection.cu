@@ -1673,9 +1673,10 @@ msa_status validate(const msa_producer_cfg *cfg, int64_t num_tokens, const void 
 
 }  // namespace
 
-bool msa_internal_encode_byte_rows(CUtensorMap *m, const void *base, int64_t rows, int64_t stride_bytes)
+bool msa_internal_encode_byte_rows(CUtensorMap *m, const void *base, int64_t rows, int64_t stride_bytes,
+                                   int box_rows)
 {
-    return encode_map(m, base, rows, kBKBytes, stride_bytes, 1, 1);
+    return encode_map(m, base, rows, kBKBytes, stride_bytes, box_rows, 1);
 }
 
 extern "C" msa_status msa_projection_validate(
