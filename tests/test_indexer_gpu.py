@@ -157,6 +157,42 @@ def test_query_runs_key_row_layouts(P, pad):
     _check(w, flags=_runs())
 
 
+def test_query_runs_in_a_graph_with_two_caches():
+    """Query-run calls on two batches with different caches (one on the row grid, one
+    off it) captured in one CUDA graph with programmatic dependent launch, replayed
+    twice: each call keeps its own key-row tensor map (a by-value kernel argument) and
+    equals a plain call bit for bit."""
+    from paged_kv_cache_msa_gb300 import binding as B
+    ws = [wl.make_indexer_prefill("graph_grid", 571, [300, 129], page_size=64),
+          wl.make_indexer_prefill("graph_offgrid", 572, [200, 90], page_size=64, page_pad_bytes=16)]
+    flags = _runs()
+    ref = []
+    for w in ws:
+        dv = DeviceIndexer(w)
+        dv.run(launch_flags=flags)
+        torch.cuda.synchronize()
+        ref.append((dv.block_scores.clone(), dv.topk_ids.clone()))
+    dvs = [DeviceIndexer(w) for w in ws]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for dv in dvs:
+            dv.run(stream=s, launch_flags=flags)
+        s.synchronize()
+        for dv in dvs:
+            dv.block_scores.fill_(float("nan"))
+            dv.topk_ids.fill_(-7)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for dv in dvs:
+                dv.run(stream=s, launch_flags=flags | B.MSA_LAUNCH_PDL)
+        for _ in range(2):
+            g.replay()
+        s.synchronize()
+    for dv, (rs, rt) in zip(dvs, ref):
+        assert torch.equal(dv.block_scores, rs)
+        assert torch.equal(dv.topk_ids, rt)
+
+
 def test_query_runs_table_holes_and_topk_sizes():
     w = wl.make_indexer_prefill("holes_runs", 501, [700, 260], topk=3)
     pt = np.array(w.page_table, copy=True)

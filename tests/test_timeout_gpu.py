@@ -65,10 +65,13 @@ def test_projection_stops_and_reports(libs, T, hidden, heads):
     check_projection(pw)
 
 
-def test_query_run_indexer_scores_nan_and_selects_nothing(libs):
+@pytest.mark.parametrize("pad", [0, 16], ids=["tma_key_rows", "register_gather"])
+def test_query_run_indexer_scores_nan_and_selects_nothing(libs, pad):
+    """Both query-run kernels: E4M3 keys on one row grid (TMA key copies) and off it
+    (the register gather)."""
     from test_indexer_gpu import _check
     normal, starved = libs
-    w = wl.make_indexer_prefill("starved_runs", 901, [40, 200, 7])
+    w = wl.make_indexer_prefill(f"starved_runs_{pad}", 901, [40, 200, 7], page_pad_bytes=pad)
     _use(starved)
     dv = DeviceIndexer(w)
     dv.run(launch_flags=B.MSA_LAUNCH_QUERY_RUNS)
