@@ -144,14 +144,15 @@ def test_query_runs_interleaved_sequences_and_pages(P):
     _check(w, flags=_runs())
 
 
-@pytest.mark.parametrize("P,pad", [(64, 128), (96, 0), (16, 384), (256, 0), (64, 16)],
+@pytest.mark.parametrize("P,pad", [(64, 128), (96, 0), (16, 384), (256, 0), (8, 0), (32, 0), (128, 0),
+                                   (64, 16)],
                          ids=["unused_rows_between_pages", "page_96", "page_16_padded", "page_256",
-                              "off_the_row_grid"])
+                              "page_8", "page_32", "page_128", "off_the_row_grid"])
 def test_query_runs_key_row_layouts(P, pad):
     """E4M3 keys of 128 dims: pages that span a whole number of token rows take the
-    TMA key copies (whole pages as boxes for page sizes 16, 64 and 256, with unused
-    rows between pages; row gathers for page size 96); padding off the row grid takes
-    the register gather.  All against the oracle."""
+    TMA key copies (whole pages as boxes for page sizes 8 to 128, 128-row boxes inside
+    256-row pages, with unused rows between pages; row gathers for page size 96);
+    padding off the row grid takes the register gather.  All against the oracle."""
     w = wl.make_indexer_prefill(f"rows{P}_{pad}", 560 + P + pad, [700, 333, 129], page_size=P,
                                 page_pad_bytes=pad)
     _check(w, flags=_runs())
