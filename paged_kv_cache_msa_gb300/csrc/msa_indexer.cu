@@ -1781,82 +1781,6 @@ constexpr int64_t kTopkRowsMinQueries = 2048;  // batches that take it (each CTA
 // finite entry counts the entries of its row ranked before it, all rows at once --
 // the rule of topk_row; ranks past a row's finite entries take -1.  One CTA per
 // query would leave each of them mostly waiting on its loads, in dozens of waves.
-// Top-k of rows of at most 64 block scores, one warp per row (large batches): a
-// bitonic sort of the row's (score, id) pairs in registers, two per lane, best first
-// (higher score, then lower id: the order of ranks_before).  Entries that are not
-// candidates (NaN, -inf, past the row's history, past the row) sort last and give
-// id -1.  Entries past the history are written -inf first, as by the other top-k
-// kernels.
-constexpr int kTopkWarpMaxBlocks = 64;
-constexpr int kTopkWarpRowsPerCta = 8;
-
-__global__ void __launch_bounds__(kTopkWarpRowsPerCta * 32) msa_index_topk_warp_kernel(const __grid_constant__ IndexerParams p)
-{
-    const int lane = threadIdx.x & 31;
-    const int64_t t = (int64_t)blockIdx.x * kTopkWarpRowsPerCta + (threadIdx.x >> 5);
-    const int32_t len_raw = t < p.num_queries ? __ldg(p.kv_len + t) : 0;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" :::);
-    if (t >= p.num_queries)
-        return;
-    const int n = p.max_blocks, topk = p.topk;
-    const int64_t L = len_raw > 0 ? (int64_t)len_raw : 0;
-    const int64_t nb64 = (L + p.block_tokens - 1) / p.block_tokens;
-    const int nb = nb64 < n ? (int)nb64 : n;
-    float *row = p.block_scores + t * n;
-    float v[2];
-    int id[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const int b = lane + 32 * e;
-        float x = -INFINITY;
-        if (b < nb)
-            x = row[b];
-        else if (b < n)
-            row[b] = -INFINITY;
-        v[e] = (x > -INFINITY) ? x : -INFINITY;   // NaN and -inf are not candidates
-        id[e] = b < n ? b : 0x7fffffff;
-    }
-#pragma unroll
-    for (int k = 2; k <= 64; k <<= 1) {
-#pragma unroll
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            float pv[2];
-            int pid[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                if (j == 32) {
-                    pv[e] = v[e ^ 1];
-                    pid[e] = id[e ^ 1];
-                } else {
-                    pv[e] = __shfl_xor_sync(0xffffffffu, v[e], j);
-                    pid[e] = __shfl_xor_sync(0xffffffffu, id[e], j);
-                }
-            }
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int i = lane + 32 * e;
-                const bool lower = (i & j) == 0;    // the pair's first index
-                const bool up = (i & k) == 0;       // this run sorts best first
-                const bool partner_better = ranks_before(pv[e], pid[e], v[e], id[e]);
-                if ((lower == up) ? partner_better : !partner_better) {
-                    v[e] = pv[e];
-                    id[e] = pid[e];
-                }
-            }
-        }
-    }
-    int32_t *out = p.topk_ids + t * topk;
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const int r = lane + 32 * e;
-        if (r < topk)
-            out[r] = v[e] > -INFINITY ? id[e] : -1;
-    }
-    for (int r = 64 + lane; r < topk; r += 32)
-        out[r] = -1;
-}
-
 __global__ void __launch_bounds__(kTopkThreads) msa_index_topk_rows_kernel(const __grid_constant__ IndexerParams p)
 {
     __shared__ __align__(16) float s_row[kRankMaxBlocks];
@@ -2109,8 +2033,7 @@ msa_status indexer_launch(const msa_indexer_cfg *cfg, int64_t num_queries, const
     // top-k: one CTA per query (several short rows per CTA in large batches),
     // launched programmatically dependent on the scores
     int rows = 1;
-    const bool warp_rows = num_queries >= kTopkRowsMinQueries && cfg->max_blocks <= kTopkWarpMaxBlocks;
-    if (!warp_rows && num_queries >= kTopkRowsMinQueries && 2 * cfg->max_blocks <= kRankMaxBlocks) {
+    if (num_queries >= kTopkRowsMinQueries && 2 * cfg->max_blocks <= kRankMaxBlocks) {
         rows = kRankMaxBlocks / cfg->max_blocks;
         rows = rows > kTopkRowsMax ? kTopkRowsMax : rows;
     }
@@ -2119,10 +2042,6 @@ msa_status indexer_launch(const msa_indexer_cfg *cfg, int64_t num_queries, const
     memset(&lc, 0, sizeof lc);
     lc.gridDim = dim3((unsigned)((num_queries + rows - 1) / rows));
     lc.blockDim = dim3(kTopkThreads);
-    if (warp_rows) {   // a warp per row
-        lc.gridDim = dim3((unsigned)((num_queries + kTopkWarpRowsPerCta - 1) / kTopkWarpRowsPerCta));
-        lc.blockDim = dim3(kTopkWarpRowsPerCta * 32);
-    }
     lc.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -2130,9 +2049,8 @@ msa_status indexer_launch(const msa_indexer_cfg *cfg, int64_t num_queries, const
     lc.attrs = attr;
     lc.numAttrs = 1;
     void *args[] = {&p};
-    e = cudaLaunchKernelExC(&lc, warp_rows  ? reinterpret_cast<const void *>(&msa_index_topk_warp_kernel)
-                                 : rows > 1 ? reinterpret_cast<const void *>(&msa_index_topk_rows_kernel)
-                                            : reinterpret_cast<const void *>(&msa_index_topk_kernel),
+    e = cudaLaunchKernelExC(&lc, rows > 1 ? reinterpret_cast<const void *>(&msa_index_topk_rows_kernel)
+                                          : reinterpret_cast<const void *>(&msa_index_topk_kernel),
                             args);
     if (e != cudaSuccess)
         return fail(MSA_ERR_CUDA, "top-k kernel launch failed: %s", cudaGetErrorString(e));
