@@ -20,8 +20,20 @@
 //     score kernel.  Rows up to 1024 blocks are staged in shared memory and every
 //     finite entry counts the entries ranked before it (score descending, id
 //     ascending), all in parallel.  Longer rows take topk rounds of warp-wide
-//     arg-max over the entries ranked after the last pick.
+//     arg-max over the entries ranked after the last pick.  Large batches of short
+//     rows rank up to 16 rows per CTA.
 //   * No scratch memory: block_scores is an output of the call.
+//
+// Design (prefill, MSA_LAUNCH_QUERY_RUNS): consecutive queries of a sequence see
+// the same blocks, so tiles of 16 queries (8 for more than 8 heads) are scored
+// against each 128-token block on the tcgen05 tensor cores by warp-specialised
+// persistent kernels with mbarrier hand-offs and bounded waits:
+//   * msa_index_runs_tma_kernel (E4M3 keys of 128 dims whose pages lie on one row
+//     grid): the query tile, split into E4M3 halves hi | lo, is A and the block's
+//     key rows, copied by TMA (whole pages as boxes, or tile::gather4 rows), are B,
+//     both in shared memory; four accumulators, two MMA warps, four epilogue groups.
+//   * msa_index_runs_kernel (every other layout): the block's keys are written into
+//     tensor memory from registers as A, the query tile is B in shared memory.
 
 #include "msa_internal.h"
 #include "msa_producer.h"
