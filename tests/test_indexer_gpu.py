@@ -243,9 +243,11 @@ def test_query_runs_match_the_per_query_kernel():
 
 def test_query_runs_prefill_65536_sampled():
     """The prefill batch (8 x 8192 causal queries, 8 heads x 128, fp8 index-K):
-    block scores and top-k of sampled queries (sequence starts and ends, tile edges,
-    random) against the oracle; every row's ids a valid ranking of its scores."""
+    block scores and top-k of sampled queries -- a random one from every 16-query
+    tile, sequence starts and ends, tile edges -- against the oracle (run over a
+    process pool); every row's ids a valid ranking of its scores."""
     from dataclasses import replace
+    from oracle_pool import indexer_rows
     w = wl.indexer_prefill()
     dv = DeviceIndexer(w)
     dv.run(launch_flags=_runs())
@@ -254,13 +256,13 @@ def test_query_runs_prefill_65536_sampled():
     top_all = dv.topk_ids.cpu().numpy()
     T = w.kv_len.shape[0]
     rng = np.random.default_rng(5)
+    tiles = np.arange(0, T, 16)
+    per_tile = np.minimum(tiles + rng.integers(0, 16, size=tiles.size), T - 1)
     idx = np.unique(np.concatenate([[0, 1, 15, 16, 17, 8191, 8192, 8193, T - 17, T - 16, T - 1],
-                                    rng.integers(0, T, size=37)]))
+                                    rng.integers(0, T, size=37), per_tile]))
     sub = replace(w, idx_q=np.ascontiguousarray(w.idx_q[idx]), kv_len=w.kv_len[idx].copy(),
                   table_offset=w.table_offset[idx].copy())
-    ref_s, ref_top = oracle.indexer(sub.idx_q, sub.kv_len, sub.table_offset, sub.page_table,
-                                    wl.indexer_cache_arg(sub, sub.pool_fill), sub.k_scale,
-                                    sub.page_size, sub.block_tokens, sub.topk, sub.max_blocks)
+    ref_s, ref_top = indexer_rows(w, idx, wl.indexer_cache_arg(w, w.pool_fill))
     check_indexer_against_reference(sub, s_all[idx], top_all[idx], ref_s.astype(np.float64), ref_top)
     fin = np.isfinite(s_all)
     nfin = fin.sum(axis=1)
