@@ -1751,6 +1751,437 @@ msa_index_runs_tma_kernel(const __grid_constant__ IndexerParams p, const __grid_
 }
 
 // ---------------------------------------------------------------------------
+// decode block scores on the tensor cores over a flat list of (query, block) items
+// ---------------------------------------------------------------------------
+//
+// For E4M3 keys of 128 dims whose pages are whole TMA boxes, and batches of up to
+// kDecMaxQueries queries of up to 16 index heads: one persistent CTA per SM takes an
+// equal share of the batch's (query, block) items, the queries' visible blocks laid
+// end to end.  Per item the MMA takes
+//   A (M = 128)  the block's key rows as stored, copied by TMA into a 16 KB stage
+//                (one box per page, 128-byte swizzle; a box without a page, or past
+//                the history, from row 0 and masked);
+//   B (N = 16)   the query's heads (rows past num_heads repeat head 0), split into
+//                E4M3 halves hi | lo under a power-of-two scale as in the query-run
+//                kernel: K steps 0-3 read hi, 4-7 lo;
+//   D            fp32 [key, head] in 16 tensor-memory columns, eight accumulators.
+// Warps: 0 copies the keys (page entries of up to 32 boxes looked up together);
+// 1 builds the query tiles (three slots, one query ahead) and issues the MMAs; 2-9
+// are two epilogue groups taking alternate items: a thread holds one key's row of
+// 16 heads, its max masked by the key's page and the query's length, then the max
+// over the block's keys by shuffles and across the group's four warps through
+// shared memory.  Each barrier phase is waited on by one warp or group that also
+// waited on the phase before it.  A wait that runs out scores the CTA's remaining
+// items NaN.
+constexpr int kDecStages = 8;
+constexpr int kDecAcc = 8;
+constexpr int kDecQSlots = 3;
+constexpr int kDecThreads = 10 * 32;
+constexpr int kDecMaxQueries = 1024;
+constexpr uint32_t kDecTmemCols = 128;
+constexpr int kDecQBytes = 2 * 16 * 128;   // one query tile: hi rows | lo rows
+constexpr int kDecDynSmem = 1024 + kDecStages * 128 * 128 + kDecQSlots * kDecQBytes;
+
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(kDecThreads, 1)
+msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid_constant__ CUtensorMap kmap)
+{
+    constexpr int S = kDecStages, NA = kDecAcc, QS = kDecQSlots;
+    // E4M3 x E4M3 -> fp32, both K-major, N = 16, M = 128
+    constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(16 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_k_full[S], bar_k_empty[S];
+    __shared__ __align__(8) uint64_t bar_acc_full[NA], bar_acc_empty[NA];
+    __shared__ __align__(8) uint64_t bar_q_ready[QS], bar_q_free[QS];
+    __shared__ __align__(8) uint64_t bar_drain;
+    __shared__ int32_t s_pre[kDecMaxQueries + 1];   // items of the queries before q
+    __shared__ float s_qinv[QS];
+    __shared__ float s_part[2][2][4];               // [group][item parity][warp of the group]
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t kbase = (smem_u32(smem_raw) + 1023u) & ~1023u;          // key stages
+    const uint32_t qbase = kbase + (uint32_t)(S * kRunsStageBytes);          // query slots
+    const int nq = (int)p.num_queries;                                       // <= kDecMaxQueries
+    const int n = p.max_blocks;
+    volatile int *abort_flag = &s_abort;
+
+    if (tid == 0) {
+        for (int i = 0; i < S; ++i) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_k_full[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_k_empty[i])));
+        }
+        for (int i = 0; i < NA; ++i) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_acc_full[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(smem_u32(&bar_acc_empty[i])));
+        }
+        for (int i = 0; i < QS; ++i) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_q_ready[i])));
+            // released by the eight epilogue warps
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(smem_u32(&bar_q_free[i])));
+        }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_drain)));
+        s_abort = 0;
+        s_pre[0] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&s_tmem)),
+                     "r"(kDecTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // blocks per query (the lengths are read before waiting on the previous kernel)
+    for (int q = tid; q < nq; q += kDecThreads) {
+        const int32_t len = __ldg(p.kv_len + q);
+        const int64_t nb64 = len > 0 ? ((int64_t)len + kTileKeys - 1) / kTileKeys : 0;
+        s_pre[q + 1] = (int32_t)(nb64 < n ? nb64 : n);
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (warp == 0) {   // s_pre[q] = items of the queries before q: lane l scans a chunk
+        const int per = (nq + 31) / 32;
+        const int a = 1 + lane * per, e = a + per < nq + 1 ? a + per : nq + 1;
+        int sum = 0;
+        for (int q = a; q < e; ++q)
+            sum += s_pre[q];
+        int ex = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, ex, o);
+            if (lane >= o)
+                ex += v;
+        }
+        int run = ex - sum;
+        for (int q = a; q < e; ++q) {
+            run += s_pre[q];
+            s_pre[q] = run;
+        }
+    }
+    __syncthreads();
+    const uint32_t tmem = s_tmem;
+    const int64_t total = s_pre[nq];
+    const int64_t i0 = total * blockIdx.x / gridDim.x, i1 = total * (blockIdx.x + 1) / gridDim.x;
+    // the last query q with s_pre[q] <= it
+    auto query_of = [&](int64_t it) -> int {
+        int lo = 0, hi = nq;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_pre[mid] <= it)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        return lo;
+    };
+    const int q_lo = i1 > i0 ? query_of(i0) : 0, q_hi = i1 > i0 ? query_of(i1 - 1) : -1;
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // keys and queries are written before
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+
+    if (warp == 0) {
+        // ---------------- key copies ----------------
+        // The page entries of a chunk of items are looked up together, one box per lane
+        // (lane l: item l / nbox of the chunk, box l mod nbox).
+        const int BR = p.box_rows, nbox = kTileKeys / BR, ipc = 32 / nbox;
+        uint32_t k = 0;
+        bool stop = false;
+        for (int64_t c0 = i0; c0 < i1 && !stop; c0 += ipc) {
+            const int64_t itl = c0 + lane / nbox;
+            const int bx = lane % nbox;
+            int32_t rowl = 0;
+            if (itl < i1) {
+                const int q = query_of(itl), b = (int)(itl - s_pre[q]);
+                const int32_t len = __ldg(p.kv_len + q);
+                const int64_t j = (int64_t)b * kTileKeys + (int64_t)bx * BR;
+                if (j < len) {
+                    const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
+                    const int64_t off = p.page_shift >= 0 ? (j & (p.page_size - 1)) : j % p.page_size;
+                    const int64_t ti2 = __ldg(p.table_offset + q) + blk;
+                    if (ti2 >= 0 && ti2 < p.page_table_len) {
+                        const int64_t pg = __ldg(p.page_table + ti2);
+                        if (pg >= 0 && pg < p.num_pages)
+                            rowl = (int32_t)(pg * p.rows_per_page + off);
+                    }
+                }
+            }
+            for (int x = 0; x < ipc && c0 + x < i1; ++x, ++k) {
+                const uint32_t s = k % S, par = ((k / S) & 1u) ^ 1u;
+                const int32_t row = __shfl_sync(0xffffffffu, rowl, (x * nbox + lane) & 31);
+                const uint32_t empty = smem_u32(&bar_k_empty[s]), full = smem_u32(&bar_k_full[s]);
+                if (!__all_sync(0xffffffffu, mbar_try(empty, par)) &&
+                    (__any_sync(0xffffffffu, *abort_flag != 0) ||
+                     !__all_sync(0xffffffffu, mbar_wait(empty, par)))) {
+                    *abort_flag = 1;
+                    stop = true;
+                    break;
+                }
+                if (lane == 0)
+                    mbar_expect_tx(full, (uint32_t)kRunsStageBytes);
+                __syncwarp();
+                if (lane < nbox)
+                    tma_load_rows(kbase + s * (uint32_t)kRunsStageBytes + (uint32_t)(lane * BR) * 128u, &kmap,
+                                  row, full);
+            }
+        }
+        // every copy issued has landed before the CTA finishes
+        for (uint32_t s = 0; s < (uint32_t)S && s < k; ++s) {
+            const uint32_t uses = (k - s + S - 1) / S;   // items issued to stage s
+            (void)__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_k_full[s]), (uses - 1u) & 1u));
+        }
+    } else if (warp == 1) {
+        // ---------------- query tiles and MMAs ----------------
+        const int H = p.heads;
+        bool ok = true;
+        // the tile of the qi-th query with items (query q) into slot qi mod 3: row r =
+        // head r (rows past num_heads repeat head 0), lane (r, half) the dims
+        // 64 half .. 64 half + 63
+        auto build = [&](int q, int qi) {
+            const int x = qi % QS;
+            if (qi >= QS) {   // the query that last used the slot has left every epilogue warp
+                const uint32_t par = (uint32_t)((qi / QS - 1) & 1);
+                if (!__all_sync(0xffffffffu, mbar_wait_fast(smem_u32(&bar_q_free[x]), par))) {
+                    ok = false;
+                    return;
+                }
+            }
+            const int r = lane >> 1, half = lane & 1;
+            const int h = r < H ? r : 0;
+            const uint16_t *src = p.idx_q + ((int64_t)q * H + h) * 128 + half * 64;
+            uint4 v[8];
+            float amax = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                v[c] = ldg16(src + 8 * c);
+                const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[j] << 16)),
+                                             fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+            }
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            int e = 0;
+            if (amax > 0.0f) {
+                e = 7 - ((int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127);   // 7 - floor(log2 amax)
+                e = e > 126 ? 126 : e;
+            }
+            const float sc = __int_as_float((e + 127) << 23);   // 2^e, e in [-120, 126]
+            uint32_t hw[16], lw[16];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {   // 8 dims -> 2 words of hi, 2 of lo
+                const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+                for (int j = 0; j < 4; j += 2) {
+                    const float x0 = __uint_as_float(w[j] << 16) * sc, x1 = __uint_as_float(w[j] & 0xFFFF0000u) * sc;
+                    const float x2 = __uint_as_float(w[j + 1] << 16) * sc,
+                                x3 = __uint_as_float(w[j + 1] & 0xFFFF0000u) * sc;
+                    const uint32_t h01 = e4m3x2_from_f32(x0, x1), h23 = e4m3x2_from_f32(x2, x3);
+                    const float2 d01 = f16x2_to_f2(e4m3x2_to_f16x2(h01)), d23 = f16x2_to_f2(e4m3x2_to_f16x2(h23));
+                    hw[2 * c + j / 2] = h01 | (h23 << 16);
+                    lw[2 * c + j / 2] = e4m3x2_from_f32(x0 - d01.x, x1 - d01.y) |
+                                        (e4m3x2_from_f32(x2 - d23.x, x3 - d23.y) << 16);
+                }
+            }
+            const uint32_t tile = qbase + (uint32_t)x * (uint32_t)kDecQBytes;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {   // chunks 4 half + m of row r (128-byte swizzle)
+                const uint32_t off = (uint32_t)r * 128u + ((uint32_t)((4 * half + m) ^ (r & 7)) << 4);
+                sts128(tile + off, hw[4 * m], hw[4 * m + 1], hw[4 * m + 2], hw[4 * m + 3]);
+                sts128(tile + 2048u + off, lw[4 * m], lw[4 * m + 1], lw[4 * m + 2], lw[4 * m + 3]);
+            }
+            if (lane == 0)
+                s_qinv[x] = __int_as_float((127 - e) << 23);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_local(smem_u32(&bar_q_ready[x]));
+        };
+        // the queries with items in this CTA's range, in order
+        auto next_query = [&](int q) {
+            ++q;
+            while (q <= q_hi && s_pre[q + 1] == s_pre[q])
+                ++q;
+            return q;
+        };
+        int qi = 0;
+        if (q_hi >= q_lo)
+            build(q_lo, 0);
+        for (int q = q_lo; q <= q_hi && ok; q = next_query(q), ++qi) {
+            const int qn = next_query(q);
+            if (qn <= q_hi)
+                build(qn, qi + 1);
+            if (!ok)
+                break;
+            const uint32_t tile = qbase + (uint32_t)(qi % QS) * (uint32_t)kDecQBytes;
+            const int64_t a0 = s_pre[q] > i0 ? s_pre[q] : i0;
+            const int64_t a1 = s_pre[q + 1] < i1 ? s_pre[q + 1] : i1;
+            for (int64_t it = a0; it < a1 && ok; ++it) {
+                const uint32_t k = (uint32_t)(it - i0);
+                const uint32_t s = k % S, ph = (k / S) & 1u, a = k % NA, pa = (k / NA) & 1u;
+                if (!__all_sync(0xffffffffu, mbar_try(smem_u32(&bar_k_full[s]), ph) &&
+                                                 mbar_try(smem_u32(&bar_acc_empty[a]), pa ^ 1)) &&
+                    (__any_sync(0xffffffffu, *abort_flag != 0) ||
+                     !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_k_full[s]), ph) &&
+                                                  mbar_wait(smem_u32(&bar_acc_empty[a]), pa ^ 1)))) {
+                    ok = false;
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t d = tmem + a * 16u;
+#ifndef MSA_STARVE
+                const uint64_t kd = sw128_desc(kbase + s * (uint32_t)kRunsStageBytes);
+                const uint64_t qd = sw128_desc(tile);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)   // K steps 0-3: keys x hi, 4-7: keys x lo (32 bytes each)
+                    asm volatile(
+                        "{\n\t.reg .pred pp, pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
+                        "setp.ne.b32 pp, %4, 0;\n\t"
+                        "@pe tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, pp;\n\t}" ::"r"(d),
+                        "l"(kd + (uint64_t)((ks & 3) * 2)), "l"(qd + (uint64_t)((ks >> 2) * 128 + (ks & 3) * 2)),
+                        "r"(kIdesc), "r"((uint32_t)ks)
+                        : "memory");
+                asm volatile(
+                    "{\n\t.reg .pred pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
+                    "@pe tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t"
+                    "@pe tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];\n\t}" ::"r"(
+                        smem_u32(&bar_k_empty[s])),
+                    "r"(smem_u32(&bar_acc_full[a]))
+                    : "memory");
+#else
+                (void)d;
+                (void)tile;
+#endif
+            }
+        }
+        if (!ok && lane == 0)
+            *abort_flag = 1;
+        // every MMA has completed before tensor memory is released
+        asm volatile(
+            "{\n\t.reg .pred pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
+            "@pe tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+                smem_u32(&bar_drain))
+            : "memory");
+        (void)mbar_wait_fast(smem_u32(&bar_drain), 0);
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: group g takes the items k with k mod 2 == g ----------------
+        const int grp = (warp - 2) >> 2, quarter = warp & 3;
+        const int key = quarter * 32 + lane;        // tensor-memory lane = key of the block
+        const uint32_t d_lane = (uint32_t)(quarter * 32) << 16;
+        const float kscale = __ldg(p.k_scale);
+        auto group_sync = [&]() {
+            if (grp == 0)
+                asm volatile("bar.sync 2, 128;" ::: "memory");
+            else
+                asm volatile("bar.sync 3, 128;" ::: "memory");
+        };
+        bool aborted = false;
+        int qi = 0;
+        for (int q = q_lo; q <= q_hi; ++q) {
+            if (s_pre[q + 1] == s_pre[q])
+                continue;   // no items (an empty history)
+            const int x = qi % QS;
+            bool qok = false;
+            if (!aborted) {
+                const uint32_t par = (uint32_t)((qi / QS) & 1);
+                qok = __all_sync(0xffffffffu, mbar_try(smem_u32(&bar_q_ready[x]), par));
+                if (!qok && !__any_sync(0xffffffffu, *abort_flag != 0))
+                    qok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_q_ready[x]), par));
+                if (!qok) {
+                    aborted = true;
+                    *abort_flag = 1;
+                }
+            }
+            const float qscale = qok ? kscale * s_qinv[x] : 0.0f;
+            const int32_t len = __ldg(p.kv_len + q);
+            const int64_t toff = __ldg(p.table_offset + q);
+            const int64_t a0 = s_pre[q] > i0 ? s_pre[q] : i0;
+            const int64_t a1 = s_pre[q + 1] < i1 ? s_pre[q + 1] : i1;
+            for (int64_t it = a0 + (((a0 - i0) & 1) != grp ? 1 : 0); it < a1; it += 2) {
+                const uint32_t k = (uint32_t)(it - i0);
+                const uint32_t a = k % NA, pa = (k / NA) & 1u;
+                const int b = (int)(it - s_pre[q]);
+                // this key's page, requested before the accumulator wait
+                const int64_t j = (int64_t)b * kTileKeys + key;
+                bool kvalid = false;
+                if (j < len) {
+                    const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
+                    const int64_t ti2 = toff + blk;
+                    const int64_t pg = (ti2 >= 0 && ti2 < p.page_table_len) ? (int64_t)__ldg(p.page_table + ti2) : -1;
+                    kvalid = pg >= 0 && pg < p.num_pages;
+                }
+                bool got = false;
+                if (!aborted) {
+                    got = __all_sync(0xffffffffu, mbar_try(smem_u32(&bar_acc_full[a]), pa));
+                    if (!got && !__any_sync(0xffffffffu, *abort_flag != 0))
+                        got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_acc_full[a]), pa));
+                    if (!got) {
+                        aborted = true;
+                        *abort_flag = 1;
+                    }
+                }
+                float m = -INFINITY;
+                if (got) {
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    uint32_t v[16];
+                    tmem_ld16_nowait(tmem + d_lane + a * 16u, v);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                    float m2[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)   // the max over the heads (rows past them repeat head 0)
+                        m2[c & 3] = fmaxf(m2[c & 3], __uint_as_float(v[c]));
+                    m = kvalid ? fmaxf(fmaxf(m2[0], m2[1]), fmaxf(m2[2], m2[3])) : -INFINITY;
+                }
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_local(smem_u32(&bar_acc_empty[a]));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                const int buf = (int)((k >> 1) & 1u);
+                if (lane == 0)
+                    s_part[grp][buf][quarter] = got ? m : __int_as_float(0x7fc00000);
+                group_sync();
+                if (quarter == 0 && lane == 0) {
+                    const float *pp = s_part[grp][buf];
+                    const bool bad = isnan(pp[0]) || isnan(pp[1]) || isnan(pp[2]) || isnan(pp[3]);
+                    const float vmax = fmaxf(fmaxf(pp[0], pp[1]), fmaxf(pp[2], pp[3]));
+                    p.block_scores[(int64_t)q * n + b] =
+                        bad ? __int_as_float(0x7fc00000) : (vmax > -INFINITY ? vmax * qscale : -INFINITY);
+                }
+            }
+            __syncwarp();
+            if (lane == 0)   // this warp is done with the query's tile
+                mbar_arrive_local(smem_u32(&bar_q_free[x]));
+            ++qi;
+        }
+    }
+
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 1) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kDecTmemCols)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
 // top-k block ids
 // ---------------------------------------------------------------------------
 // One CTA per query, after a score kernel; under programmatic dependent launch it
@@ -1971,8 +2402,26 @@ msa_status indexer_launch(const msa_indexer_cfg *cfg, int64_t num_queries, const
                      : reinterpret_cast<const void *>(&msa_index_score_kernel<128, false>))
             : (p.fp8 ? reinterpret_cast<const void *>(&msa_index_score_kernel<64, true>)
                      : reinterpret_cast<const void *>(&msa_index_score_kernel<64, false>));
-    alignas(64) CUtensorMap kmap;   // the key rows, for query runs on E4M3 keys of 128 dims
+    alignas(64) CUtensorMap kmap;   // the key rows, for E4M3 keys of 128 dims copied by TMA
     memset(&kmap, 0, sizeof kmap);
+    // E4M3 keys of 128 dims whose rows lie on one grid (each page a whole number of
+    // token strides, 16-byte aligned): encode the map, whole pages per box where a page
+    // is a box (at most 16 boxes a block), else one row per box
+    auto encode_key_rows = [&]() -> bool {
+        if (!(p.fp8 && cfg->head_dim == 128 && p.num_pages >= 1 && p.stride_token > 0 &&
+              p.stride_page % p.stride_token == 0 && (reinterpret_cast<uintptr_t>(p.kdata) & 15u) == 0))
+            return false;
+        const int64_t rpp = p.stride_page / p.stride_token;
+        const int64_t rows = (p.num_pages - 1) * rpp + cfg->page_size;
+        const int P = cfg->page_size;
+        const int br = (kTileKeys % P == 0 && P >= 8) ? P : (P % kTileKeys == 0 ? kTileKeys : 1);
+        if (rpp < P || rows >= ((int64_t)1 << 31) ||
+            !msa_internal_encode_byte_rows(&kmap, p.kdata, rows, p.stride_token, br))
+            return false;
+        p.rows_per_page = rpp;
+        p.box_rows = br;
+        return true;
+    };
     cudaLaunchConfig_t sc;
     memset(&sc, 0, sizeof sc);
     sc.gridDim = dim3((unsigned)(num_queries * cpq));
@@ -1990,23 +2439,8 @@ msa_status indexer_launch(const msa_indexer_cfg *cfg, int64_t num_queries, const
         if (major != 10)
             return fail(MSA_ERR_UNSUPPORTED, "query runs need tcgen05 tensor cores (compute capability 10.x)");
         const int64_t tiles = (num_queries + qt - 1) / qt;
-        // E4M3 keys of 128 dims whose rows lie on one grid (each page a whole number of
-        // token strides, 16-byte aligned): the key rows are gathered by TMA
-        bool tma = false;
-        if (p.fp8 && D == 128 && p.num_pages >= 1 && p.stride_token > 0 && p.stride_page % p.stride_token == 0 &&
-            (reinterpret_cast<uintptr_t>(p.kdata) & 15u) == 0) {
-            const int64_t rpp = p.stride_page / p.stride_token;
-            const int64_t rows = (p.num_pages - 1) * rpp + cfg->page_size;
-            const int P = cfg->page_size;
-            // whole pages per copy where a page is a box (at most 16 copies a block)
-            const int br = (kTileKeys % P == 0 && P >= 8) ? P : (P % kTileKeys == 0 ? kTileKeys : 1);
-            if (rpp >= P && rows < ((int64_t)1 << 31) &&
-                msa_internal_encode_byte_rows(&kmap, p.kdata, rows, p.stride_token, br)) {
-                tma = true;
-                p.rows_per_page = rpp;
-                p.box_rows = br;
-            }
-        }
+        // E4M3 keys of 128 dims on one row grid: the key rows are copied by TMA
+        const bool tma = D == 128 && encode_key_rows();
         const int smem = tma ? kRunsDynSmemTma : kRunsDynSmem;
         const void *fns[10] = {
             reinterpret_cast<const void *>(&msa_index_runs_kernel<64, false, 8>),
@@ -2026,6 +2460,24 @@ msa_status indexer_launch(const msa_indexer_cfg *cfg, int64_t num_queries, const
             cudaSuccess)
             return fail(MSA_ERR_CUDA, "cudaFuncSetAttribute failed");
         sc.dynamicSmemBytes = (size_t)smem;
+    } else if (!counters && cfg->block_tokens == kTileKeys && cfg->num_heads <= 16 && num_queries <= kDecMaxQueries &&
+               encode_key_rows() && p.box_rows > 1) {
+        // decode batches of E4M3 keys in whole-page boxes: the flat item list on the
+        // tcgen05 tensor cores
+        int major = 0, dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return fail(MSA_ERR_CUDA, "device query failed");
+        if (major == 10) {
+            score_fn = reinterpret_cast<const void *>(&msa_index_decode_tc_kernel);
+            sc.gridDim = dim3((unsigned)sms);   // persistent, one CTA per SM
+            sc.blockDim = dim3(kDecThreads);
+            if (cudaFuncSetAttribute(score_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecDynSmem) !=
+                cudaSuccess)
+                return fail(MSA_ERR_CUDA, "cudaFuncSetAttribute failed");
+            sc.dynamicSmemBytes = (size_t)kDecDynSmem;
+        }
     }
     cudaLaunchAttribute sattr[1];
     if (p.pdl) {

@@ -467,6 +467,16 @@ def check_indexer_against_reference(w, s, top, ref_s, ref_top):
             assert abs(ref_s[t, a] - ref_s[t, b]) <= 2 * tol, (t, r, a, b)
 
 
+def same_indexer_results(w, a_scores, a_ids, b_scores, b_ids):
+    """Two indexer entries agree: bit for bit, or (one of them on the tensor-core
+    decode kernel, whose E4M3 query halves round differently) within the scores'
+    tolerance, with the ids equal wherever the scores separate them."""
+    if torch.equal(a_scores, b_scores) and torch.equal(a_ids, b_ids):
+        return
+    check_indexer_against_reference(w, a_scores.cpu().numpy(), a_ids.cpu().numpy(),
+                                    b_scores.cpu().numpy().astype(np.float64), b_ids.cpu().numpy())
+
+
 def pin_indexer_hand_worked():
     """H = 2 heads, D = 2, q = identity rows; bf16 cache of 2-token pages with the
     table [1, 0]; rows j0 = (3, -1), j1 = (-2, 5), j2 = (0.5, 0.5).  Token scores

@@ -1,10 +1,13 @@
 """The single-launch indexer (msa_indexer_forward_fused) against the two-kernel one
 and the oracle, through the C ABI (GPU).
 
-The fused entry runs the same score kernel, with the top-k taken by the last CTA of
-each query: block scores and ids must equal the two-kernel path's bit for bit, the
-ids must pass the oracle check of the two-kernel tests, and the per-query counters
-must be zero again after every launch."""
+The fused entry runs the per-query score kernel with the top-k taken by the last CTA
+of each query.  The two-kernel path runs the same kernel, except for decode batches
+of E4M3 keys in whole-page boxes, which take the tensor-core kernel over a flat item
+list (E4M3 query halves, so its scores differ within the oracle tolerance).  So the
+two entries must agree bit for bit, or within that tolerance with the same ids
+wherever the scores separate them; both must pass the oracle check, and the
+per-query counters must be zero again after every launch."""
 import numpy as np
 import pytest
 import torch
@@ -15,7 +18,7 @@ from paged_kv_cache_msa_gb300 import build as build_mod
 from paged_kv_cache_msa_gb300 import workloads as wl
 from paged_kv_cache_msa_gb300.device import DeviceIndexer
 
-from oracle_pins import check_indexer_against_reference
+from oracle_pins import check_indexer_against_reference, same_indexer_results as same_results
 
 pytestmark = pytest.mark.gpu
 
@@ -35,8 +38,7 @@ def _both(w, pool=None, flags=0):
 
 def _check(w, pool=None, flags=0):
     two, fused = _both(w, pool, flags)
-    assert torch.equal(two.block_scores, fused.block_scores)
-    assert torch.equal(two.topk_ids, fused.topk_ids)
+    same_results(w, fused.block_scores, fused.topk_ids, two.block_scores, two.topk_ids)
     assert int(fused.counters.abs().sum().item()) == 0
     pool = w.pool_fill if pool is None else pool
     ref_s, ref_top = oracle.indexer(w.idx_q, w.kv_len, w.table_offset, w.page_table,
@@ -126,7 +128,7 @@ def test_fused_entry_with_query_runs_leaves_the_counters_alone():
 
 def test_fused_decode_layer_in_a_graph():
     """Producer then the single-launch indexer, 4 layers in one graph with PDL: every
-    layer's ids and scores equal the two-kernel path's."""
+    layer's ids and scores agree with the two-kernel path's (see same_results)."""
     from paged_kv_cache_msa_gb300.device import DecodeLayer, DeviceWorkload
     build_mod.build()
     w = wl.config2_decode64()
@@ -147,7 +149,7 @@ def test_fused_decode_layer_in_a_graph():
         for _ in range(2):
             g.replay()
         s.synchronize()
+    from types import SimpleNamespace
     for l, (rs, rt) in zip(layers, ref):
-        assert torch.equal(rs, l.block_scores)
-        assert torch.equal(rt, l.topk_ids)
+        same_results(SimpleNamespace(topk=int(rt.shape[1])), l.block_scores, l.topk_ids, rs, rt)
         assert int(l.counters.abs().sum().item()) == 0
