@@ -1765,18 +1765,19 @@ msa_index_runs_tma_kernel(const __grid_constant__ IndexerParams p, const __grid_
 //                E4M3 halves hi | lo under a power-of-two scale as in the query-run
 //                kernel: K steps 0-3 read hi, 4-7 lo;
 //   D            fp32 [key, head] in 16 tensor-memory columns, eight accumulators.
-// Warps: 0 copies the keys (page entries of up to 32 boxes looked up together);
-// 1 builds the query tiles (three slots, one query ahead) and issues the MMAs; 2-9
-// are two epilogue groups taking alternate items: a thread holds one key's row of
-// 16 heads, its max masked by the key's page and the query's length, then the max
-// over the block's keys by shuffles and across the group's four warps through
-// shared memory.  Each barrier phase is waited on by one warp or group that also
+// Warps: 0 copies the keys (page entries of up to 32 boxes looked up together, the
+// first chunk's before waiting on the previous kernel); 1 builds the query tiles
+// (three slots, one query ahead); 2 and 3 issue the MMAs of the even and the odd
+// items; 4-11 are two epilogue groups taking alternate items: a thread holds one
+// key's row of 16 heads, its max masked by the key's page and the query's length,
+// then the max over the block's keys by shuffles and across the group's four warps
+// through shared memory.  Each barrier phase is waited on by one warp or group that also
 // waited on the phase before it.  A wait that runs out scores the CTA's remaining
 // items NaN.
 constexpr int kDecStages = 8;
 constexpr int kDecAcc = 8;
 constexpr int kDecQSlots = 3;
-constexpr int kDecThreads = 10 * 32;
+constexpr int kDecThreads = 12 * 32;
 constexpr int kDecMaxQueries = 1024;
 constexpr uint32_t kDecTmemCols = 128;
 constexpr int kDecQBytes = 2 * 16 * 128;   // one query tile: hi rows | lo rows
@@ -1827,15 +1828,16 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
         }
         for (int i = 0; i < QS; ++i) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_q_ready[i])));
-            // released by the eight epilogue warps
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(smem_u32(&bar_q_free[i])));
+            // released by the eight epilogue warps and the two MMA warps (every waiter of
+            // the slot's ready phase is past it before the slot is rebuilt)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 10;" ::"r"(smem_u32(&bar_q_free[i])));
         }
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_drain)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 2;" ::"r"(smem_u32(&bar_drain)));
         s_abort = 0;
         s_pre[0] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) {
+    if (warp == 2) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(&s_tmem)),
                      "r"(kDecTmemCols)
@@ -1887,17 +1889,20 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
         return lo;
     };
     const int q_lo = i1 > i0 ? query_of(i0) : 0, q_hi = i1 > i0 ? query_of(i1 - 1) : -1;
-    asm volatile("griddepcontrol.wait;" ::: "memory");   // keys and queries are written before
-    asm volatile("griddepcontrol.launch_dependents;" :::);
+    // Every role waits on the previous kernel (which writes the keys and the queries)
+    // before touching them; lengths, table offsets and page entries may be read before.
+    auto wait_previous = [&]() {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" :::);
+    };
 
     if (warp == 0) {
         // ---------------- key copies ----------------
         // The page entries of a chunk of items are looked up together, one box per lane
         // (lane l: item l / nbox of the chunk, box l mod nbox).
         const int BR = p.box_rows, nbox = kTileKeys / BR, ipc = 32 / nbox;
-        uint32_t k = 0;
-        bool stop = false;
-        for (int64_t c0 = i0; c0 < i1 && !stop; c0 += ipc) {
+        // the rows of this lane's box in the chunk of items starting at c0
+        auto chunk_rows = [&](int64_t c0) -> int32_t {
             const int64_t itl = c0 + lane / nbox;
             const int bx = lane % nbox;
             int32_t rowl = 0;
@@ -1916,6 +1921,15 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
                     }
                 }
             }
+            return rowl;
+        };
+        int32_t rowl = chunk_rows(i0);
+        wait_previous();
+        uint32_t k = 0;
+        bool stop = false;
+        for (int64_t c0 = i0; c0 < i1 && !stop; c0 += ipc) {
+            if (c0 != i0)
+                rowl = chunk_rows(c0);
             for (int x = 0; x < ipc && c0 + x < i1; ++x, ++k) {
                 const uint32_t s = k % S, par = ((k / S) & 1u) ^ 1u;
                 const int32_t row = __shfl_sync(0xffffffffu, rowl, (x * nbox + lane) & 31);
@@ -1941,19 +1955,24 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
             (void)__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_k_full[s]), (uses - 1u) & 1u));
         }
     } else if (warp == 1) {
-        // ---------------- query tiles and MMAs ----------------
+        // ---------------- query tiles ----------------
+        wait_previous();
         const int H = p.heads;
-        bool ok = true;
         // the tile of the qi-th query with items (query q) into slot qi mod 3: row r =
         // head r (rows past num_heads repeat head 0), lane (r, half) the dims
         // 64 half .. 64 half + 63
-        auto build = [&](int q, int qi) {
+        int qi = 0;
+        for (int q = q_lo; q <= q_hi; ++q) {
+            if (s_pre[q + 1] == s_pre[q])
+                continue;   // no items (an empty history)
             const int x = qi % QS;
-            if (qi >= QS) {   // the query that last used the slot has left every epilogue warp
+            if (qi >= QS) {   // the query that last used the slot has left the MMA and epilogue warps
                 const uint32_t par = (uint32_t)((qi / QS - 1) & 1);
-                if (!__all_sync(0xffffffffu, mbar_wait_fast(smem_u32(&bar_q_free[x]), par))) {
-                    ok = false;
-                    return;
+                if (__any_sync(0xffffffffu, *abort_flag != 0) ||
+                    !__all_sync(0xffffffffu, mbar_wait_fast(smem_u32(&bar_q_free[x]), par))) {
+                    if (lane == 0)
+                        *abort_flag = 1;
+                    break;
                 }
             }
             const int r = lane >> 1, half = lane & 1;
@@ -2008,27 +2027,28 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
             __syncwarp();
             if (lane == 0)
                 mbar_arrive_local(smem_u32(&bar_q_ready[x]));
-        };
-        // the queries with items in this CTA's range, in order
-        auto next_query = [&](int q) {
-            ++q;
-            while (q <= q_hi && s_pre[q + 1] == s_pre[q])
-                ++q;
-            return q;
-        };
+            ++qi;
+        }
+    } else if (warp <= 3) {
+        // ---------------- MMAs: warp 2 the even items, warp 3 the odd ones ----------------
+        wait_previous();
+        const uint32_t g = (uint32_t)(warp - 2);
+        bool ok = true;
         int qi = 0;
-        if (q_hi >= q_lo)
-            build(q_lo, 0);
-        for (int q = q_lo; q <= q_hi && ok; q = next_query(q), ++qi) {
-            const int qn = next_query(q);
-            if (qn <= q_hi)
-                build(qn, qi + 1);
-            if (!ok)
+        for (int q = q_lo; q <= q_hi && ok; ++q) {
+            if (s_pre[q + 1] == s_pre[q])
+                continue;   // no items (an empty history)
+            const int x = qi % QS;
+            // the query's tile (every query in order, so that no phase is skipped)
+            if (__any_sync(0xffffffffu, *abort_flag != 0) ||
+                !__all_sync(0xffffffffu, mbar_wait_fast(smem_u32(&bar_q_ready[x]), (uint32_t)((qi / QS) & 1)))) {
+                ok = false;
                 break;
-            const uint32_t tile = qbase + (uint32_t)(qi % QS) * (uint32_t)kDecQBytes;
+            }
+            const uint32_t tile = qbase + (uint32_t)x * (uint32_t)kDecQBytes;
             const int64_t a0 = s_pre[q] > i0 ? s_pre[q] : i0;
             const int64_t a1 = s_pre[q + 1] < i1 ? s_pre[q + 1] : i1;
-            for (int64_t it = a0; it < a1 && ok; ++it) {
+            for (int64_t it = a0 + ((uint32_t)((a0 - i0) & 1) != g ? 1 : 0); it < a1 && ok; it += 2) {
                 const uint32_t k = (uint32_t)(it - i0);
                 const uint32_t s = k % S, ph = (k / S) & 1u, a = k % NA, pa = (k / NA) & 1u;
                 if (!__all_sync(0xffffffffu, mbar_try(smem_u32(&bar_k_full[s]), ph) &&
@@ -2065,10 +2085,14 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
                 (void)tile;
 #endif
             }
+            __syncwarp();
+            if (ok && lane == 0)   // this warp is done with the query's tile (its MMAs may still run)
+                mbar_arrive_local(smem_u32(&bar_q_free[x]));
+            ++qi;
         }
         if (!ok && lane == 0)
             *abort_flag = 1;
-        // every MMA has completed before tensor memory is released
+        // every MMA of both warps has completed before tensor memory is released
         asm volatile(
             "{\n\t.reg .pred pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
             "@pe tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
@@ -2078,7 +2102,8 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
         __syncwarp();
     } else {
         // ---------------- epilogue: group g takes the items k with k mod 2 == g ----------------
-        const int grp = (warp - 2) >> 2, quarter = warp & 3;
+        wait_previous();
+        const int grp = (warp - 4) >> 2, quarter = warp & 3;
         const int key = quarter * 32 + lane;        // tensor-memory lane = key of the block
         const uint32_t d_lane = (uint32_t)(quarter * 32) << 16;
         const float kscale = __ldg(p.k_scale);
@@ -2173,7 +2198,7 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
 
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 2) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kDecTmemCols)
