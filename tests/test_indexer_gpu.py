@@ -117,6 +117,41 @@ def test_indexer_pdl_back_to_back_in_a_graph():
 
 
 # ---------------------------------------------------------------------------
+# decode batches on the tensor-core kernel over a flat (query, block) list
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("case", ["many_short", "limit_1024", "over_limit_1025", "heads_16",
+                                  "empty_between"])
+def test_decode_flat_list_batches(case):
+    """E4M3 keys of 128 dims in whole-page boxes: batch shapes that stress the flat item
+    list (a CTA's share spanning many queries, the 1,024-query limit and one past it,
+    which takes the per-query kernel, 16 heads, histories without a token between
+    others), against the oracle."""
+    rng = np.random.default_rng(700 + len(case))
+    heads = 8
+    if case == "many_short":
+        lens = rng.integers(1, 300, size=600)
+    elif case == "limit_1024":
+        lens = rng.integers(1, 1200, size=1024)
+    elif case == "over_limit_1025":
+        lens = rng.integers(1, 1200, size=1025)
+    elif case == "heads_16":
+        lens = rng.integers(1, 9216, size=48)
+        heads = 16
+    else:
+        lens = rng.integers(1, 4000, size=64)
+        lens[::5] = 0
+    _check(wl.make_indexer_batch(f"flat_{case}", 710 + len(case), lens, heads=heads, topk=16))
+
+
+@pytest.mark.parametrize("P", [8, 32, 128, 256])
+def test_decode_flat_list_page_sizes(P):
+    """The flat decode kernel with one TMA box per page for page sizes 8 to 128 and
+    128-row boxes inside 256-row pages, against the oracle."""
+    _check(wl.make_indexer_batch(f"flat_p{P}", 730 + P, [1, 127, 128, 129, 700, 3000, 9216, 0], page_size=P))
+
+
+# ---------------------------------------------------------------------------
 # query runs (prefill): tiles of consecutive queries on the tcgen05 tensor cores
 # ---------------------------------------------------------------------------
 
