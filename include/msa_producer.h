@@ -253,6 +253,14 @@ typedef struct {
  *                The indexer's kernels let the next kernel on the stream start only
  *                after their own wait.
  *                MSA_LAUNCH_QUERY_RUNS: see its definition.
+ * Arithmetic: an FP8 cache's codes are exact in every kernel, and scores accumulate
+ * in fp32.  The query is rounded to f16 by the per-query kernel; where the keys are
+ * multiplied as stored on the tensor cores (E4M3 keys of 128 dims on the query-run
+ * kernels, and decode batches of up to 1,024 queries of up to 16 heads whose index-K
+ * pages are whole TMA boxes), each query is split into two E4M3 halves hi + lo under
+ * a power-of-two scale, which reproduces its bf16 values exactly except elements
+ * below 2^-9 of the query's largest magnitude.  Which kernel runs depends only on
+ * the arguments, so a call is deterministic.
  * Errors as for msa_producer_forward; num_queries == 0 launches nothing.
  */
 msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t num_queries, const void *idx_q,
@@ -263,9 +271,11 @@ msa_status msa_indexer_forward(const msa_indexer_cfg *cfg, int64_t num_queries, 
                                cudaStream_t stream);
 
 /*
- * msa_indexer_forward in a single launch: the same scores, block scores and top-k
- * ids (bit for bit), with the top-k taken inside the per-query score kernel instead
- * of a second kernel.  Each of the query's CTAs that scores blocks counts itself in
+ * msa_indexer_forward in a single launch, with the top-k taken inside the per-query
+ * score kernel instead of a second kernel.  The block scores and ids equal
+ * msa_indexer_forward's bit for bit, except where that entry takes the tensor-core
+ * decode kernel (see its arithmetic note): there the scores agree within the query
+ * split's rounding, and the ids wherever the scores separate them.  Each of the query's CTAs that scores blocks counts itself in
  * counters[t] once its block scores are stored; the CTA that arrives last resets
  * counters[t] to zero and ranks the query's row.
  *
