@@ -1765,8 +1765,9 @@ msa_index_runs_tma_kernel(const __grid_constant__ IndexerParams p, const __grid_
 //                E4M3 halves hi | lo under a power-of-two scale as in the query-run
 //                kernel: K steps 0-3 read hi, 4-7 lo;
 //   D            fp32 [key, head] in 16 tensor-memory columns, eight accumulators.
-// Warps: 0 copies the keys (page entries of up to 32 boxes looked up together, the
-// first chunk's before waiting on the previous kernel); 1 builds the query tiles
+// Warps: 0 and 12 copy the keys of the even and the odd items (page entries of up to
+// 32 boxes looked up together, the first chunk's before waiting on the previous
+// kernel); 1 builds the query tiles
 // (three slots, one query ahead); 2 and 3 issue the MMAs of the even and the odd
 // items; 4-11 are two epilogue groups taking alternate items: a thread holds one
 // key's row of 16 heads, its max masked by the key's page and the query's length,
@@ -1777,7 +1778,7 @@ msa_index_runs_tma_kernel(const __grid_constant__ IndexerParams p, const __grid_
 constexpr int kDecStages = 8;
 constexpr int kDecAcc = 8;
 constexpr int kDecQSlots = 3;
-constexpr int kDecThreads = 12 * 32;
+constexpr int kDecThreads = 13 * 32;   // 2 key-copy, 1 query-tile, 2 MMA, 2 x 4 epilogue warps
 constexpr int kDecMaxQueries = 1024;
 constexpr uint32_t kDecTmemCols = 128;
 constexpr int kDecQBytes = 2 * 16 * 128;   // one query tile: hi rows | lo rows
@@ -1896,8 +1897,9 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
         asm volatile("griddepcontrol.launch_dependents;" :::);
     };
 
-    if (warp == 0) {
-        // ---------------- key copies ----------------
+    if (warp == 0 || warp == 12) {
+        // ---------------- key copies: warp 0 the even items, warp 12 the odd ones ----------------
+        const uint32_t pw = warp == 0 ? 0u : 1u;
         // The page entries of a chunk of items are looked up together, one box per lane
         // (lane l: item l / nbox of the chunk, box l mod nbox).
         const int BR = p.box_rows, nbox = kTileKeys / BR, ipc = 32 / nbox;
@@ -1931,6 +1933,8 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
             if (c0 != i0)
                 rowl = chunk_rows(c0);
             for (int x = 0; x < ipc && c0 + x < i1; ++x, ++k) {
+                if ((k & 1u) != pw)
+                    continue;
                 const uint32_t s = k % S, par = ((k / S) & 1u) ^ 1u;
                 const int32_t row = __shfl_sync(0xffffffffu, rowl, (x * nbox + lane) & 31);
                 const uint32_t empty = smem_u32(&bar_k_empty[s]), full = smem_u32(&bar_k_full[s]);
@@ -1949,8 +1953,8 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
                                   row, full);
             }
         }
-        // every copy issued has landed before the CTA finishes
-        for (uint32_t s = 0; s < (uint32_t)S && s < k; ++s) {
+        // every copy this warp issued has landed before the CTA finishes
+        for (uint32_t s = pw; s < (uint32_t)S && s < k; s += 2) {
             const uint32_t uses = (k - s + S - 1) / S;   // items issued to stage s
             (void)__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_k_full[s]), (uses - 1u) & 1u));
         }
@@ -2135,19 +2139,24 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
             const int64_t toff = __ldg(p.table_offset + q);
             const int64_t a0 = s_pre[q] > i0 ? s_pre[q] : i0;
             const int64_t a1 = s_pre[q + 1] < i1 ? s_pre[q + 1] : i1;
-            for (int64_t it = a0 + (((a0 - i0) & 1) != grp ? 1 : 0); it < a1; it += 2) {
+            // this key's page entry in item itx of the query (-1: none), one item ahead
+            auto page_of = [&](int64_t itx) -> int32_t {
+                if (itx >= a1)
+                    return -1;
+                const int64_t j = (itx - s_pre[q]) * kTileKeys + key;
+                if (j >= len)
+                    return -1;
+                const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
+                const int64_t ti2 = toff + blk;
+                return (ti2 >= 0 && ti2 < p.page_table_len) ? __ldg(p.page_table + ti2) : -1;
+            };
+            int64_t it = a0 + (((a0 - i0) & 1) != grp ? 1 : 0);
+            int32_t pgc = page_of(it);
+            for (; it < a1; it += 2) {
                 const uint32_t k = (uint32_t)(it - i0);
                 const uint32_t a = k % NA, pa = (k / NA) & 1u;
                 const int b = (int)(it - s_pre[q]);
-                // this key's page, requested before the accumulator wait
-                const int64_t j = (int64_t)b * kTileKeys + key;
-                bool kvalid = false;
-                if (j < len) {
-                    const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
-                    const int64_t ti2 = toff + blk;
-                    const int64_t pg = (ti2 >= 0 && ti2 < p.page_table_len) ? (int64_t)__ldg(p.page_table + ti2) : -1;
-                    kvalid = pg >= 0 && pg < p.num_pages;
-                }
+                const int32_t pgn = page_of(it + 2);   // in flight meanwhile
                 bool got = false;
                 if (!aborted) {
                     got = __all_sync(0xffffffffu, mbar_try(smem_u32(&bar_acc_full[a]), pa));
@@ -2168,6 +2177,7 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
 #pragma unroll
                     for (int c = 0; c < 16; ++c)   // the max over the heads (rows past them repeat head 0)
                         m2[c & 3] = fmaxf(m2[c & 3], __uint_as_float(v[c]));
+                    const bool kvalid = pgc >= 0 && (int64_t)pgc < p.num_pages;
                     m = kvalid ? fmaxf(fmaxf(m2[0], m2[1]), fmaxf(m2[2], m2[3])) : -INFINITY;
                 }
                 asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -2188,6 +2198,7 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
                     p.block_scores[(int64_t)q * n + b] =
                         bad ? __int_as_float(0x7fc00000) : (vmax > -INFINITY ? vmax * qscale : -INFINITY);
                 }
+                pgc = pgn;
             }
             __syncwarp();
             if (lane == 0)   // this warp is done with the query's tile
