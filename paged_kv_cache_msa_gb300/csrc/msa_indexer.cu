@@ -1765,20 +1765,19 @@ msa_index_runs_tma_kernel(const __grid_constant__ IndexerParams p, const __grid_
 //                E4M3 halves hi | lo under a power-of-two scale as in the query-run
 //                kernel: K steps 0-3 read hi, 4-7 lo;
 //   D            fp32 [key, head] in 16 tensor-memory columns, eight accumulators.
-// Warps: 0 and 12 copy the keys of the even and the odd items (page entries of up to
-// 32 boxes looked up together, the first chunk's before waiting on the previous
-// kernel); 1 builds the query tiles
+// Warps: 0 copies the keys (page entries of up to 32 boxes looked up together, the
+// first chunk's before waiting on the previous kernel); 1 builds the query tiles
 // (three slots, one query ahead); 2 and 3 issue the MMAs of the even and the odd
-// items; 4-11 are two epilogue groups taking alternate items: a thread holds one
-// key's row of 16 heads, its max masked by the key's page and the query's length,
-// then the max over the block's keys by shuffles and across the group's four warps
-// through shared memory.  Each barrier phase is waited on by one warp or group that also
+// items; 4-19 are four epilogue groups, group g taking the items k with k mod 4 == g
+// (and so the accumulators g and g + 4): a thread holds one key's row of 16 heads,
+// its max masked by the key's page and the query's length, then the max over the
+// block's keys by shuffles and across the group's four warps through shared memory.  Each barrier phase is waited on by one warp or group that also
 // waited on the phase before it.  A wait that runs out scores the CTA's remaining
 // items NaN.
 constexpr int kDecStages = 8;
 constexpr int kDecAcc = 8;
 constexpr int kDecQSlots = 3;
-constexpr int kDecThreads = 13 * 32;   // 2 key-copy, 1 query-tile, 2 MMA, 2 x 4 epilogue warps
+constexpr int kDecThreads = 20 * 32;   // key-copy, query-tile, 2 MMA, 4 x 4 epilogue warps
 constexpr int kDecMaxQueries = 1024;
 constexpr uint32_t kDecTmemCols = 128;
 constexpr int kDecQBytes = 2 * 16 * 128;   // one query tile: hi rows | lo rows
@@ -1808,7 +1807,7 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
     __shared__ __align__(8) uint64_t bar_drain;
     __shared__ int32_t s_pre[kDecMaxQueries + 1];   // items of the queries before q
     __shared__ float s_qinv[QS];
-    __shared__ float s_part[2][2][4];               // [group][item parity][warp of the group]
+    __shared__ float s_part[4][2][4];               // [group][item parity][warp of the group]
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1829,9 +1828,9 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
         }
         for (int i = 0; i < QS; ++i) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_q_ready[i])));
-            // released by the eight epilogue warps and the two MMA warps (every waiter of
-            // the slot's ready phase is past it before the slot is rebuilt)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 10;" ::"r"(smem_u32(&bar_q_free[i])));
+            // released by the sixteen epilogue warps and the two MMA warps (every waiter
+            // of the slot's ready phase is past it before the slot is rebuilt)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 18;" ::"r"(smem_u32(&bar_q_free[i])));
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 2;" ::"r"(smem_u32(&bar_drain)));
         s_abort = 0;
@@ -1897,9 +1896,8 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
         asm volatile("griddepcontrol.launch_dependents;" :::);
     };
 
-    if (warp == 0 || warp == 12) {
-        // ---------------- key copies: warp 0 the even items, warp 12 the odd ones ----------------
-        const uint32_t pw = warp == 0 ? 0u : 1u;
+    if (warp == 0) {
+        // ---------------- key copies ----------------
         // The page entries of a chunk of items are looked up together, one box per lane
         // (lane l: item l / nbox of the chunk, box l mod nbox).
         const int BR = p.box_rows, nbox = kTileKeys / BR, ipc = 32 / nbox;
@@ -1933,8 +1931,6 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
             if (c0 != i0)
                 rowl = chunk_rows(c0);
             for (int x = 0; x < ipc && c0 + x < i1; ++x, ++k) {
-                if ((k & 1u) != pw)
-                    continue;
                 const uint32_t s = k % S, par = ((k / S) & 1u) ^ 1u;
                 const int32_t row = __shfl_sync(0xffffffffu, rowl, (x * nbox + lane) & 31);
                 const uint32_t empty = smem_u32(&bar_k_empty[s]), full = smem_u32(&bar_k_full[s]);
@@ -1954,7 +1950,7 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
             }
         }
         // every copy this warp issued has landed before the CTA finishes
-        for (uint32_t s = pw; s < (uint32_t)S && s < k; s += 2) {
+        for (uint32_t s = 0; s < (uint32_t)S && s < k; ++s) {
             const uint32_t uses = (k - s + S - 1) / S;   // items issued to stage s
             (void)__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_k_full[s]), (uses - 1u) & 1u));
         }
@@ -2105,7 +2101,7 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
         (void)mbar_wait_fast(smem_u32(&bar_drain), 0);
         __syncwarp();
     } else {
-        // ---------------- epilogue: group g takes the items k with k mod 2 == g ----------------
+        // ---------------- epilogue: group g takes the items k with k mod 4 == g ----------------
         wait_previous();
         const int grp = (warp - 4) >> 2, quarter = warp & 3;
         const int key = quarter * 32 + lane;        // tensor-memory lane = key of the block
@@ -2114,8 +2110,12 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
         auto group_sync = [&]() {
             if (grp == 0)
                 asm volatile("bar.sync 2, 128;" ::: "memory");
-            else
+            else if (grp == 1)
                 asm volatile("bar.sync 3, 128;" ::: "memory");
+            else if (grp == 2)
+                asm volatile("bar.sync 4, 128;" ::: "memory");
+            else
+                asm volatile("bar.sync 5, 128;" ::: "memory");
         };
         bool aborted = false;
         int qi = 0;
@@ -2150,13 +2150,13 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
                 const int64_t ti2 = toff + blk;
                 return (ti2 >= 0 && ti2 < p.page_table_len) ? __ldg(p.page_table + ti2) : -1;
             };
-            int64_t it = a0 + (((a0 - i0) & 1) != grp ? 1 : 0);
+            int64_t it = a0 + (int64_t)(((uint32_t)grp - (uint32_t)(a0 - i0)) & 3u);
             int32_t pgc = page_of(it);
-            for (; it < a1; it += 2) {
+            for (; it < a1; it += 4) {
                 const uint32_t k = (uint32_t)(it - i0);
                 const uint32_t a = k % NA, pa = (k / NA) & 1u;
                 const int b = (int)(it - s_pre[q]);
-                const int32_t pgn = page_of(it + 2);   // in flight meanwhile
+                const int32_t pgn = page_of(it + 4);   // in flight meanwhile
                 bool got = false;
                 if (!aborted) {
                     got = __all_sync(0xffffffffu, mbar_try(smem_u32(&bar_acc_full[a]), pa));
@@ -2187,7 +2187,7 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1)
                     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                const int buf = (int)((k >> 1) & 1u);
+                const int buf = (int)((k >> 2) & 1u);
                 if (lane == 0)
                     s_part[grp][buf][quarter] = got ? m : __int_as_float(0x7fc00000);
                 group_sync();
