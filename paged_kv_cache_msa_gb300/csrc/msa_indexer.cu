@@ -1806,6 +1806,10 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
     __shared__ __align__(8) uint64_t bar_q_ready[QS], bar_q_free[QS];
     __shared__ __align__(8) uint64_t bar_drain;
     __shared__ int32_t s_pre[kDecMaxQueries + 1];   // items of the queries before q
+    __shared__ int32_t s_len[kDecMaxQueries];       // kv_len, table_offset: read once, together
+    __shared__ int64_t s_toff[kDecMaxQueries];
+    __shared__ int64_t s_irange[2];                 // this CTA's items [i0, i1)
+    __shared__ int s_qrange[2];                     // the queries of its first and last item
     __shared__ float s_qinv[QS];
     __shared__ float s_part[4][2][4];               // [group][item parity][warp of the group]
     __shared__ uint32_t s_tmem;
@@ -1818,6 +1822,8 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
     volatile int *abort_flag = &s_abort;
 
     if (tid == 0) {
+        // the key map's descriptor is fetched while the lengths are read
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&kmap) : "memory");
         for (int i = 0; i < S; ++i) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_k_full[i])));
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar_k_empty[i])));
@@ -1835,6 +1841,8 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 2;" ::"r"(smem_u32(&bar_drain)));
         s_abort = 0;
         s_pre[0] = 0;
+        s_qrange[0] = 0;
+        s_qrange[1] = -1;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 2) {
@@ -1844,9 +1852,12 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    // blocks per query (the lengths are read before waiting on the previous kernel)
+    // blocks per query (the lengths and table offsets are read before waiting on the
+    // previous kernel, in one round of loads: every page lookup after this is one load)
     for (int q = tid; q < nq; q += kDecThreads) {
         const int32_t len = __ldg(p.kv_len + q);
+        s_toff[q] = __ldg(p.table_offset + q);
+        s_len[q] = len;
         const int64_t nb64 = len > 0 ? ((int64_t)len + kTileKeys - 1) / kTileKeys : 0;
         s_pre[q + 1] = (int32_t)(nb64 < n ? nb64 : n);
     }
@@ -1871,24 +1882,30 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
             run += s_pre[q];
             s_pre[q] = run;
         }
+        // this CTA's equal share of the items, and the queries holding its first and
+        // last item (query q holds item it when s_pre[q] <= it < s_pre[q + 1]): each
+        // lane tests the queries a - 1 .. e - 2, whose bounds it has just written
+        const int64_t total = __shfl_sync(0xffffffffu, ex, 31);
+        const int64_t c0 = total * blockIdx.x / gridDim.x, c1 = total * (blockIdx.x + 1) / gridDim.x;
+        __syncwarp();
+        if (c1 > c0) {
+            for (int q = a - 1; q < e - 1; ++q) {
+                const int lo = s_pre[q], hi = s_pre[q + 1];
+                if (lo <= c0 && c0 < hi)
+                    s_qrange[0] = q;
+                if (lo <= c1 - 1 && c1 - 1 < hi)
+                    s_qrange[1] = q;
+            }
+        }
+        if (lane == 0) {
+            s_irange[0] = c0;
+            s_irange[1] = c1;
+        }
     }
     __syncthreads();
     const uint32_t tmem = s_tmem;
-    const int64_t total = s_pre[nq];
-    const int64_t i0 = total * blockIdx.x / gridDim.x, i1 = total * (blockIdx.x + 1) / gridDim.x;
-    // the last query q with s_pre[q] <= it
-    auto query_of = [&](int64_t it) -> int {
-        int lo = 0, hi = nq;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (s_pre[mid] <= it)
-                lo = mid;
-            else
-                hi = mid;
-        }
-        return lo;
-    };
-    const int q_lo = i1 > i0 ? query_of(i0) : 0, q_hi = i1 > i0 ? query_of(i1 - 1) : -1;
+    const int64_t i0 = s_irange[0], i1 = s_irange[1];
+    const int q_lo = s_qrange[0], q_hi = s_qrange[1];
     // Every role waits on the previous kernel (which writes the keys and the queries)
     // before touching them; lengths, table offsets and page entries may be read before.
     auto wait_previous = [&]() {
@@ -1901,19 +1918,25 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
         // The page entries of a chunk of items are looked up together, one box per lane
         // (lane l: item l / nbox of the chunk, box l mod nbox).
         const int BR = p.box_rows, nbox = kTileKeys / BR, ipc = 32 / nbox;
+        int qc = q_lo;   // the query of the chunk's first item (items run in query order)
         // the rows of this lane's box in the chunk of items starting at c0
         auto chunk_rows = [&](int64_t c0) -> int32_t {
+            while (qc + 1 < nq && s_pre[qc + 1] <= c0)
+                ++qc;
             const int64_t itl = c0 + lane / nbox;
             const int bx = lane % nbox;
             int32_t rowl = 0;
             if (itl < i1) {
-                const int q = query_of(itl), b = (int)(itl - s_pre[q]);
-                const int32_t len = __ldg(p.kv_len + q);
+                int q = qc;
+                while (q + 1 < nq && s_pre[q + 1] <= itl)
+                    ++q;
+                const int b = (int)(itl - s_pre[q]);
+                const int32_t len = s_len[q];
                 const int64_t j = (int64_t)b * kTileKeys + (int64_t)bx * BR;
                 if (j < len) {
                     const int64_t blk = p.page_shift >= 0 ? (j >> p.page_shift) : j / p.page_size;
                     const int64_t off = p.page_shift >= 0 ? (j & (p.page_size - 1)) : j % p.page_size;
-                    const int64_t ti2 = __ldg(p.table_offset + q) + blk;
+                    const int64_t ti2 = s_toff[q] + blk;
                     if (ti2 >= 0 && ti2 < p.page_table_len) {
                         const int64_t pg = __ldg(p.page_table + ti2);
                         if (pg >= 0 && pg < p.num_pages)
@@ -2135,8 +2158,8 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
                 }
             }
             const float qscale = qok ? kscale * s_qinv[x] : 0.0f;
-            const int32_t len = __ldg(p.kv_len + q);
-            const int64_t toff = __ldg(p.table_offset + q);
+            const int32_t len = s_len[q];
+            const int64_t toff = s_toff[q];
             const int64_t a0 = s_pre[q] > i0 ? s_pre[q] : i0;
             const int64_t a1 = s_pre[q + 1] < i1 ? s_pre[q + 1] : i1;
             // this key's page entry in item itx of the query (-1: none), one item ahead
