@@ -1886,7 +1886,15 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
         // last item (query q holds item it when s_pre[q] <= it < s_pre[q + 1]): each
         // lane tests the queries a - 1 .. e - 2, whose bounds it has just written
         const int64_t total = __shfl_sync(0xffffffffu, ex, 31);
-        const int64_t c0 = total * blockIdx.x / gridDim.x, c1 = total * (blockIdx.x + 1) / gridDim.x;
+        const uint64_t m0 = (uint64_t)total * blockIdx.x, m1 = m0 + (uint64_t)total;
+        int64_t c0, c1;
+        if (m1 <= 0xffffffffull) {   // the common case, in 32-bit arithmetic
+            c0 = (uint32_t)m0 / gridDim.x;
+            c1 = (uint32_t)m1 / gridDim.x;
+        } else {
+            c0 = (int64_t)(m0 / gridDim.x);
+            c1 = (int64_t)(m1 / gridDim.x);
+        }
         __syncwarp();
         if (c1 > c0) {
             for (int q = a - 1; q < e - 1; ++q) {
@@ -1917,14 +1925,15 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
         // ---------------- key copies ----------------
         // The page entries of a chunk of items are looked up together, one box per lane
         // (lane l: item l / nbox of the chunk, box l mod nbox).
-        const int BR = p.box_rows, nbox = kTileKeys / BR, ipc = 32 / nbox;
+        // a box is a whole page whose rows divide 128, or 128 rows: BR is a power of two
+        const int BR = p.box_rows, lb = __ffs(BR) - 1, nbox = kTileKeys >> lb, ipc = 32 >> (7 - lb);
         int qc = q_lo;   // the query of the chunk's first item (items run in query order)
         // the rows of this lane's box in the chunk of items starting at c0
         auto chunk_rows = [&](int64_t c0) -> int32_t {
             while (qc + 1 < nq && s_pre[qc + 1] <= c0)
                 ++qc;
-            const int64_t itl = c0 + lane / nbox;
-            const int bx = lane % nbox;
+            const int64_t itl = c0 + (lane >> (7 - lb));
+            const int bx = lane & (nbox - 1);
             int32_t rowl = 0;
             if (itl < i1) {
                 int q = qc;
