@@ -1808,6 +1808,7 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
     __shared__ int32_t s_pre[kDecMaxQueries + 1];   // items of the queries before q
     __shared__ int32_t s_len[kDecMaxQueries];       // kv_len, table_offset: read once, together
     __shared__ int64_t s_toff[kDecMaxQueries];
+    __shared__ int32_t s_csum[2 * kDecThreads / 32];   // items of each chunk of 32 queries
     __shared__ int64_t s_irange[2];                 // this CTA's items [i0, i1)
     __shared__ int s_qrange[2];                     // the queries of its first and last item
     __shared__ float s_qinv[QS];
@@ -1852,40 +1853,55 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    // blocks per query (the lengths and table offsets are read before waiting on the
-    // previous kernel, in one round of loads: every page lookup after this is one load)
-    for (int q = tid; q < nq; q += kDecThreads) {
-        const int32_t len = __ldg(p.kv_len + q);
-        s_toff[q] = __ldg(p.table_offset + q);
-        s_len[q] = len;
-        const int64_t nb64 = len > 0 ? ((int64_t)len + kTileKeys - 1) / kTileKeys : 0;
-        s_pre[q + 1] = (int32_t)(nb64 < n ? nb64 : n);
+    // Blocks per query and their prefix sums s_pre, in registers: thread t holds the
+    // queries t and t + kDecThreads, so each warp scans 32 consecutive queries per pass
+    // with shuffles and publishes the total of its chunk (chunk c = queries 32c ..
+    // 32c + 31).  Lengths and table offsets are read before waiting on the previous
+    // kernel, in one round of loads: every page lookup after this is one load.
+    constexpr int kPasses = (kDecMaxQueries + kDecThreads - 1) / kDecThreads;
+    constexpr int kWarps = kDecThreads / 32;
+    int32_t nbq[kPasses], inc[kPasses];
+#pragma unroll
+    for (int r = 0; r < kPasses; ++r) {
+        const int q = tid + r * kDecThreads;
+        int32_t nb = 0;
+        if (q < nq) {
+            const int32_t len = __ldg(p.kv_len + q);
+            s_toff[q] = __ldg(p.table_offset + q);
+            s_len[q] = len;
+            const int64_t nb64 = len > 0 ? ((int64_t)len + kTileKeys - 1) / kTileKeys : 0;
+            nb = (int32_t)(nb64 < n ? nb64 : n);
+        }
+        int32_t x = nb;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t v = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o)
+                x += v;
+        }
+        nbq[r] = nb;
+        inc[r] = x;
+        if (lane == 31)
+            s_csum[r * kWarps + warp] = x;
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (warp == 0) {   // s_pre[q] = items of the queries before q: lane l scans a chunk
-        const int per = (nq + 31) / 32;
-        const int a = 1 + lane * per, e = a + per < nq + 1 ? a + per : nq + 1;
-        int sum = 0;
-        for (int q = a; q < e; ++q)
-            sum += s_pre[q];
-        int ex = sum;
+    {
+        // every warp: the chunks' prefix (lane c holds chunk c, at most 32 chunks), the
+        // total, this CTA's equal share [c0, c1) of the items; then each thread's
+        // queries' bounds, and the queries holding the share's first and last item
+        // (query q holds item it when s_pre[q] <= it < s_pre[q + 1])
+        const int nch = (nq + 31) >> 5;
+        const int32_t cs = lane < nch ? s_csum[lane] : 0;
+        int32_t cinc = cs;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, ex, o);
+            const int32_t v = __shfl_up_sync(0xffffffffu, cinc, o);
             if (lane >= o)
-                ex += v;
+                cinc += v;
         }
-        int run = ex - sum;
-        for (int q = a; q < e; ++q) {
-            run += s_pre[q];
-            s_pre[q] = run;
-        }
-        // this CTA's equal share of the items, and the queries holding its first and
-        // last item (query q holds item it when s_pre[q] <= it < s_pre[q + 1]): each
-        // lane tests the queries a - 1 .. e - 2, whose bounds it has just written
-        const int64_t total = __shfl_sync(0xffffffffu, ex, 31);
+        const int64_t total = __shfl_sync(0xffffffffu, cinc, 31);
         const uint64_t m0 = (uint64_t)total * blockIdx.x, m1 = m0 + (uint64_t)total;
         int64_t c0, c1;
         if (m1 <= 0xffffffffull) {   // the common case, in 32-bit arithmetic
@@ -1895,17 +1911,22 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
             c0 = (int64_t)(m0 / gridDim.x);
             c1 = (int64_t)(m1 / gridDim.x);
         }
-        __syncwarp();
-        if (c1 > c0) {
-            for (int q = a - 1; q < e - 1; ++q) {
-                const int lo = s_pre[q], hi = s_pre[q + 1];
-                if (lo <= c0 && c0 < hi)
-                    s_qrange[0] = q;
-                if (lo <= c1 - 1 && c1 - 1 < hi)
-                    s_qrange[1] = q;
+#pragma unroll
+        for (int r = 0; r < kPasses; ++r) {
+            const int q = tid + r * kDecThreads;
+            const int32_t pc = __shfl_sync(0xffffffffu, cinc - cs, (r * kWarps + warp) & 31);
+            if (q < nq) {   // then its chunk is below nch <= 32
+                const int32_t hi = pc + inc[r], lo = hi - nbq[r];
+                s_pre[q + 1] = hi;
+                if (c1 > c0) {
+                    if (lo <= c0 && c0 < hi)
+                        s_qrange[0] = q;
+                    if (lo <= c1 - 1 && c1 - 1 < hi)
+                        s_qrange[1] = q;
+                }
             }
         }
-        if (lane == 0) {
+        if (tid == 0) {
             s_irange[0] = c0;
             s_irange[1] = c1;
         }
