@@ -1782,6 +1782,11 @@ constexpr int kDecMaxQueries = 1024;
 constexpr uint32_t kDecTmemCols = 128;
 constexpr int kDecQBytes = 2 * 16 * 128;   // one query tile: hi rows | lo rows
 constexpr int kDecDynSmem = 1024 + kDecStages * 128 * 128 + kDecQSlots * kDecQBytes;
+// the prefix scan: each thread holds kDecPasses queries, each warp scans 32 of them per pass
+constexpr int kDecPasses = (kDecMaxQueries + kDecThreads - 1) / kDecThreads;
+constexpr int kDecWarps = kDecThreads / 32;
+static_assert(kDecThreads % 32 == 0, "whole warps");
+static_assert(kDecMaxQueries <= 32 * 32, "one warp scans the chunk totals, one chunk a lane");
 
 __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16])
 {
@@ -1808,7 +1813,7 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
     __shared__ int32_t s_pre[kDecMaxQueries + 1];   // items of the queries before q
     __shared__ int32_t s_len[kDecMaxQueries];       // kv_len, table_offset: read once, together
     __shared__ int64_t s_toff[kDecMaxQueries];
-    __shared__ int32_t s_csum[2 * kDecThreads / 32];   // items of each chunk of 32 queries
+    __shared__ int32_t s_csum[kDecPasses * kDecWarps];   // items of each chunk of 32 queries
     __shared__ int64_t s_irange[2];                 // this CTA's items [i0, i1)
     __shared__ int s_qrange[2];                     // the queries of its first and last item
     __shared__ float s_qinv[QS];
@@ -1858,8 +1863,7 @@ msa_index_decode_tc_kernel(const __grid_constant__ IndexerParams p, const __grid
     // with shuffles and publishes the total of its chunk (chunk c = queries 32c ..
     // 32c + 31).  Lengths and table offsets are read before waiting on the previous
     // kernel, in one round of loads: every page lookup after this is one load.
-    constexpr int kPasses = (kDecMaxQueries + kDecThreads - 1) / kDecThreads;
-    constexpr int kWarps = kDecThreads / 32;
+    constexpr int kPasses = kDecPasses, kWarps = kDecWarps;
     int32_t nbq[kPasses], inc[kPasses];
 #pragma unroll
     for (int r = 0; r < kPasses; ++r) {
