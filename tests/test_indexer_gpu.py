@@ -121,12 +121,13 @@ def test_indexer_pdl_back_to_back_in_a_graph():
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("case", ["many_short", "limit_1024", "over_limit_1025", "heads_16",
-                                  "empty_between"])
+                                  "empty_between", "all_empty", "one_item"])
 def test_decode_flat_list_batches(case):
     """E4M3 keys of 128 dims in whole-page boxes: batch shapes that stress the flat item
     list (a CTA's share spanning many queries, the 1,024-query limit and one past it,
     which takes the per-query kernel, 16 heads, histories without a token between
-    others), against the oracle."""
+    others, a batch with no item at all and one with a single item, where every CTA or
+    all CTAs but one have nothing to score), against the oracle."""
     rng = np.random.default_rng(700 + len(case))
     heads = 8
     if case == "many_short":
@@ -138,6 +139,10 @@ def test_decode_flat_list_batches(case):
     elif case == "heads_16":
         lens = rng.integers(1, 9216, size=48)
         heads = 16
+    elif case == "all_empty":
+        lens = np.zeros(40, dtype=np.int64)
+    elif case == "one_item":
+        lens = np.array([1])
     else:
         lens = rng.integers(1, 4000, size=64)
         lens[::5] = 0
